@@ -1,0 +1,461 @@
+// gemm_tc.cu - K2: the sharded, batched bf16 GEMM on the sm_103a tensor cores.
+//
+// Persistent, warp-specialised kernel, one CTA per SM:
+//   warp 0      TMA producer: 3-D tensor maps (shard column, shard row,
+//               shard number) read each operand tile straight out of the shard
+//               that holds it - the all-gathers of "Maximizing Parallelism in
+//               Distributed Training for Huge Neural Networks", Algorithm 1,
+//               become coordinates.  128-byte swizzle, STAGES-deep ring.
+//   warp 1      MMA issuer: tcgen05.mma kind::f16 (bf16 x bf16 -> fp32) with
+//               the accumulator in tensor memory; the contraction loop runs
+//               over every depth index l in ascending order into the same
+//               accumulator (the reduce-scatter over z of Algorithm 1).
+//               Two accumulators alternate so the epilogue of one tile
+//               overlaps the products of the next.  Also owns TMEM alloc.
+//   warps 2-5   epilogue: tcgen05.ld of the 128 x BN fp32 tile, scale, bias
+//               (Algorithm 7's b_j), GELU / GELU-backward, residual, bf16 or
+//               fp32 stores into the output's shards.
+// Every mbarrier wait is bounded (see common.cuh); a wait that runs out sets
+// the context's error word, the CTA drains what it issued and returns.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "gemm.cuh"
+
+namespace tp3d {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int kThreads = 192;
+
+template <int BN>
+struct TcCfg {
+  static constexpr int STAGES = (BN == 256) ? 4 : 6;
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+};
+
+struct TileInfo {
+  int32_t z;
+  int64_t m0, n0, m_end, n_end;  // per-batch logical coordinates; *_end = segment end
+};
+
+__device__ __forceinline__ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+template <int BN>
+__device__ __forceinline__ void decode_tile(const GemmProblem& P, int64_t t, TileInfo& T) {
+  const int64_t tpsM = ceil_div(P.segM, BM), tpsN = ceil_div(P.segN, BN);
+  const int64_t tiles_m = (P.M / P.segM) * tpsM, tiles_n = (P.N / P.segN) * tpsN;
+  const int64_t per_z = tiles_m * tiles_n;
+  T.z = (int32_t)(t / per_z);
+  const int64_t r = t - (int64_t)T.z * per_z;
+  const int64_t tn = r / tiles_m, tm = r - tn * tiles_m;
+  const int64_t sm = tm / tpsM, sn = tn / tpsN;
+  T.m0 = sm * P.segM + (tm - sm * tpsM) * BM;
+  T.n0 = sn * P.segN + (tn - sn * tpsN) * BN;
+  T.m_end = sm * P.segM + P.segM;
+  T.n_end = sn * P.segN + P.segN;
+}
+
+template <int BN>
+__device__ __forceinline__ int64_t total_tiles(const GemmProblem& P) {
+  return (int64_t)P.Z * (P.M / P.segM) * ceil_div(P.segM, BM) * (P.N / P.segN) * ceil_div(P.segN, BN);
+}
+
+template <int BN>
+__device__ __forceinline__ bool tile_skipped(const GemmProblem& P, const TileInfo& T) {
+  return P.causal == CAUSAL_SKIP_UPPER && T.n0 > T.m0 + BM - 1;
+}
+
+__device__ __forceinline__ int64_t num_k_iters(const GemmProblem& P) {
+  return (P.K / P.segK) * ceil_div(P.segK, BK);
+}
+
+__device__ __forceinline__ int64_t k_of(const GemmProblem& P, int64_t kk) {
+  const int64_t tps = ceil_div(P.segK, BK);
+  const int64_t s = kk / tps;
+  return s * P.segK + (kk - s * tps) * BK;
+}
+
+__device__ __forceinline__ bool k_needed(const GemmProblem& P, const TileInfo& T, int64_t k0) {
+  if (P.causal == CAUSAL_K_LE_M) return k0 <= T.m0 + BM - 1;
+  if (P.causal == CAUSAL_K_GE_M) return k0 + BK - 1 >= T.m0;
+  return true;
+}
+
+// stored (row, col) of an operand -> TMA coordinates (col in shard, row in shard, shard)
+__device__ __forceinline__ void tma_coords(const Grid& g, int64_t row, int64_t col, int& c0, int& c1, int& c2) {
+  const int64_t br = row / g.bh, bc = col / g.bw;
+  c2 = (br < g.rb && bc < g.cb) ? g.shard((int32_t)br, (int32_t)bc) : g.nshards();  // past the end: zero fill
+  c1 = (int)(row - br * g.bh);
+  c0 = (int)(col - bc * g.bw);
+}
+
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ float gelu_f(float x) { return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f)); }
+__device__ __forceinline__ float gelu_grad_f(float x) {
+  const float cdf = 0.5f * (1.0f + erff(x * 0.70710678118654752f));
+  const float pdf = 0.39894228040143268f * expf(-0.5f * x * x);
+  return cdf + x * pdf;
+}
+
+__device__ __forceinline__ void unpack8(const uint4& v, float* f) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 t = __bfloat1622float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+__device__ __forceinline__ uint4 pack8(const float* f) {
+  uint4 v;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+  return v;
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                   const GemmProblem P) {
+  using Cfg = TcCfg<BN>;
+  constexpr int S = Cfg::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + S * Cfg::STAGE_BYTES);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * S + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * S + 2 + b); };
+  const uint32_t final_bar = bar0 + 8u * (2 * S + 4);
+  auto a_stage = [&](int s) { return base + (uint32_t)(s * Cfg::A_BYTES); };
+  auto b_stage = [&](int s) { return base + (uint32_t)(S * Cfg::A_BYTES + s * Cfg::B_BYTES); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 4);
+    }
+    mbar_init(final_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&mapA);
+    tma_prefetch_map(&mapB);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  const int64_t ntiles = total_tiles<BN>(P);
+  const int64_t nk = num_k_iters(P);
+  const bool a_mn = P.a.mn_major != 0, b_mn = P.b.mn_major != 0;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      uint32_t it = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        TileInfo T;
+        decode_tile<BN>(P, t, T);
+        if (tile_skipped<BN>(P, T)) continue;
+        const int64_t am = T.m0 + op_off(P.a.hi1, P.a.lo1, P.a.base1, T.z, P.Hz);
+        const int64_t ak = op_off(P.a.hi2, P.a.lo2, P.a.base2, T.z, P.Hz);
+        const int64_t bk = op_off(P.b.hi1, P.b.lo1, P.b.base1, T.z, P.Hz);
+        const int64_t bn = T.n0 + op_off(P.b.hi2, P.b.lo2, P.b.base2, T.z, P.Hz);
+        for (int64_t kk = 0; kk < nk; ++kk) {
+          const int64_t k0 = k_of(P, kk);
+          if (!k_needed(P, T, k0)) continue;
+          const int s = (int)(it % S);
+          const uint32_t ph = (it / S) & 1u;
+          if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, P.err)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full_bar(s), Cfg::STAGE_BYTES);
+          int c0, c1, c2;
+          if (!a_mn) {
+            tma_coords(P.a.g, am, ak + k0, c0, c1, c2);
+            tma_load_3d(a_stage(s), &mapA, full_bar(s), c0, c1, c2);
+          } else {
+#pragma unroll
+            for (int h = 0; h < BM / 64; ++h) {
+              tma_coords(P.a.g, ak + k0, am + 64 * h, c0, c1, c2);
+              tma_load_3d(a_stage(s) + h * 8192u, &mapA, full_bar(s), c0, c1, c2);
+            }
+          }
+          if (!b_mn) {
+            tma_coords(P.b.g, bn, bk + k0, c0, c1, c2);
+            tma_load_3d(b_stage(s), &mapB, full_bar(s), c0, c1, c2);
+          } else {
+#pragma unroll
+            for (int h = 0; h < BN / 64; ++h) {
+              tma_coords(P.b.g, bk + k0, bn + 64 * h, c0, c1, c2);
+              tma_load_3d(b_stage(s) + h * 8192u, &mapB, full_bar(s), c0, c1, c2);
+            }
+          }
+          ++it;
+        }
+      }
+      if (!ok) {
+        // drain: let every load this thread issued land before the CTA exits
+        const uint32_t first = it > (uint32_t)S ? it - S : 0u;
+        for (uint32_t j = first; j < it; ++j) mbar_wait_drain(full_bar((int)(j % S)), (j / S) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      const uint32_t idesc = idesc_bf16_f32(BM, BN, a_mn ? 1 : 0, b_mn ? 1 : 0);
+      uint32_t it = 0, tc = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        TileInfo T;
+        decode_tile<BN>(P, t, T);
+        if (tile_skipped<BN>(P, T)) continue;
+        const int buf = (int)(tc & 1u);
+        const uint32_t tph = (tc >> 1) & 1u;
+        if (!mbar_wait(tempty_bar(buf), tph ^ 1u, abort_flag, P.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+        bool first = true;
+        for (int64_t kk = 0; kk < nk; ++kk) {
+          const int64_t k0 = k_of(P, kk);
+          if (!k_needed(P, T, k0)) continue;
+          const int s = (int)(it % S);
+          const uint32_t ph = (it / S) & 1u;
+          if (!mbar_wait(full_bar(s), ph, abort_flag, P.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int k16 = 0; k16 < BK / 16; ++k16) {
+            const uint64_t ad = a_mn ? smem_desc_sw128(a_stage(s) + k16 * 2048u, 8192u, 1024u)
+                                     : smem_desc_sw128(a_stage(s) + k16 * 32u, 16u, 1024u);
+            const uint64_t bd = b_mn ? smem_desc_sw128(b_stage(s) + k16 * 2048u, 8192u, 1024u)
+                                     : smem_desc_sw128(b_stage(s) + k16 * 32u, 16u, 1024u);
+            umma_bf16(d_tmem, ad, bd, idesc, (first && k16 == 0) ? 0u : 1u);
+          }
+          first = false;
+          umma_commit(empty_bar(s));
+          ++it;
+        }
+        if (!ok) break;
+        umma_commit(tfull_bar(buf));
+        ++tc;
+      }
+      // wait until every product this thread issued has finished before TMEM is freed
+      umma_commit(final_bar);
+      mbar_wait_drain(final_bar, 0);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    uint32_t tc = 0;
+    const Grid& cg = P.c.g;
+    const int esz = P.epi.out_f32 ? 4 : 2;
+    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+      TileInfo T;
+      decode_tile<BN>(P, t, T);
+      if (tile_skipped<BN>(P, T)) continue;
+      bool any_k = false;
+      for (int64_t kk = 0; kk < nk && !any_k; ++kk) any_k = k_needed(P, T, k_of(P, kk));
+      const int buf = (int)(tc & 1u);
+      const uint32_t tph = (tc >> 1) & 1u;
+      // one lane waits and the warp follows it, so the warp stays converged
+      // for the .sync.aligned tensor-memory loads below
+      bool ok = lane == 0 ? mbar_wait(tfull_bar(buf), tph, abort_flag, P.err) : false;
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      tc_fence_after();
+
+      const int64_t m = T.m0 + row;
+      const bool row_ok = m < T.m_end;
+      const int64_t gm = m + op_off(P.c.hi1, P.c.lo1, P.c.base1, T.z, P.Hz);
+      const int64_t gn0 = T.n0 + op_off(P.c.hi2, P.c.lo2, P.c.base2, T.z, P.Hz);
+      int64_t row_base = 0;
+      if (row_ok) {
+        const int64_t br = gm / cg.bh, bc = gn0 / cg.bw;
+        row_base = cg.block_base((int32_t)br, (int32_t)bc) + (gm - br * cg.bh) * cg.bw + (gn0 - bc * cg.bw);
+      }
+#pragma unroll 1
+      for (int ch = 0; ch < BN / 32; ++ch) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * BN + ch * 32), r);
+        tmem_ld_wait();
+        if (ch == BN / 32 - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty_bar(buf));
+        }
+        const int64_t n = T.n0 + ch * 32;
+        if (!row_ok || n >= T.n_end) continue;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const int64_t nv = n + v * 8;
+          if (nv >= T.n_end) break;
+          const int64_t off = row_base + (nv - T.n0);
+          float x[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = any_k ? __uint_as_float(r[v * 8 + e]) * P.epi.alpha : 0.0f;
+          if (P.epi.bias) {
+            float bb[8];
+            unpack8(*reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(P.epi.bias) + (gn0 + (nv - T.n0))), bb);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] += bb[e];
+          }
+          if (P.epi.zsave) *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(P.epi.zsave) + off) = pack8(x);
+          if (P.epi.act == EPI_GELU) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = gelu_f(x[e]);
+          } else if (P.epi.act == EPI_GELU_BWD) {
+            float zz[8];
+            unpack8(*reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(P.epi.gin) + off), zz);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] *= gelu_grad_f(zz[e]);
+          }
+          if (P.epi.resid) {
+            float rr[8];
+            unpack8(*reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(P.epi.resid) + off), rr);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] += rr[e];
+          }
+          if (esz == 2) {
+            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(const_cast<void*>(P.c.ptr)) + off) = pack8(x);
+          } else {
+            float4* o = reinterpret_cast<float4*>(static_cast<float*>(const_cast<void*>(P.c.ptr)) + off);
+            o[0] = make_float4(x[0], x[1], x[2], x[3]);
+            o[1] = make_float4(x[4], x[5], x[6], x[7]);
+          }
+        }
+      }
+      ++tc;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 3-D map over a stored bf16 matrix: (column in shard, row in shard, shard).
+tp3d_status make_map(CUtensorMap* m, const Grid& g, const void* ptr, uint32_t box_inner, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return TP3D_ECUDA;
+  cuuint64_t dims[3] = {(cuuint64_t)g.bw, (cuuint64_t)g.bh, (cuuint64_t)g.nshards()};
+  cuuint64_t strides[2] = {(cuuint64_t)g.bw * 2, (cuuint64_t)(g.bh * g.bw * 2)};
+  cuuint32_t box[3] = {box_inner, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? TP3D_OK : TP3D_ECUDA;
+}
+
+template <int BN>
+tp3d_status launch(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t s) {
+  using Cfg = TcCfg<BN>;
+  CUtensorMap ma, mb;
+  TP3D_TRY(make_map(&ma, P.a.g, P.a.ptr, 64, P.a.mn_major ? 64 : BM));
+  TP3D_TRY(make_map(&mb, P.b.g, P.b.ptr, 64, P.b.mn_major ? 64 : BN));
+  TP3D_CUDA_TRY(cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM));
+  const int64_t tpsM = (P.segM + BM - 1) / BM, tpsN = (P.segN + BN - 1) / BN;
+  const int64_t ntiles = (int64_t)P.Z * (P.M / P.segM) * tpsM * (P.N / P.segN) * tpsN;
+  if (ntiles <= 0) return TP3D_OK;
+  const int grid = (int)(ntiles < ctx->num_sms ? ntiles : ctx->num_sms);
+  gemm_tc_kernel<BN><<<grid, kThreads, Cfg::SMEM, s>>>(ma, mb, P);
+  return cudaGetLastError() == cudaSuccess ? TP3D_OK : TP3D_ECUDA;
+}
+
+}  // namespace
+
+tp3d_status gemm_bf16_tc(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t s) {
+  // every operand block must be at least one TMA box wide and tall enough
+  // for its 16-byte row pitch; the tile shape is picked per problem.
+  const Grid* gs[3] = {&P.a.g, &P.b.g, &P.c.g};
+  for (const Grid* g : gs)
+    if (g->bw % 8 != 0) return TP3D_EALIGN;
+  if (P.segM % 8 || P.segN % 8) return TP3D_EUNSUPPORTED;
+  // a ragged contraction tile is exact only if one operand's block ends at the segment end
+  if (P.segK % BK != 0) {
+    const int64_t ka = P.a.mn_major ? P.a.g.bh : P.a.g.bw;
+    const int64_t kb = P.b.mn_major ? P.b.g.bh : P.b.g.bw;
+    if (ka != P.segK && kb != P.segK) return TP3D_EUNSUPPORTED;
+  }
+  const int64_t tiles256 = (int64_t)P.Z * (P.M / P.segM) * ((P.segM + BM - 1) / BM) * (P.N / P.segN) * ((P.segN + 255) / 256);
+  const bool narrow = P.segN <= 128 || tiles256 < ctx->num_sms;
+  return narrow ? launch<128>(ctx, P, s) : launch<256>(ctx, P, s);
+}
+
+tp3d_status plan_segments(GemmProblem& P) {
+  auto g = [](std::initializer_list<int64_t> xs) {
+    int64_t r = 0;
+    for (int64_t x : xs) r = gcd64(r, x < 0 ? -x : x);
+    return r;
+  };
+  const int64_t aM = P.a.mn_major ? P.a.g.bw : P.a.g.bh, aK = P.a.mn_major ? P.a.g.bh : P.a.g.bw;
+  const int64_t bK = P.b.mn_major ? P.b.g.bh : P.b.g.bw, bN = P.b.mn_major ? P.b.g.bw : P.b.g.bh;
+  P.segM = g({aM, P.c.g.bh, P.M, P.a.hi1, P.a.lo1, P.a.base1, P.c.hi1, P.c.lo1, P.c.base1});
+  P.segN = g({bN, P.c.g.bw, P.N, P.b.hi2, P.b.lo2, P.b.base2, P.c.hi2, P.c.lo2, P.c.base2});
+  P.segK = g({aK, bK, P.K, P.a.hi2, P.a.lo2, P.a.base2, P.b.hi1, P.b.lo1, P.b.base1});
+  if (P.segM <= 0 || P.segN <= 0 || P.segK <= 0) return TP3D_ESHAPE;
+  return TP3D_OK;
+}
+
+}  // namespace tp3d
