@@ -12,7 +12,7 @@
 //               accumulator (the reduce-scatter over z of Algorithm 1).
 //               Two accumulators alternate so the epilogue of one tile
 //               overlaps the products of the next.  Also owns TMEM alloc.
-//   warps 2-5   epilogue: tcgen05.ld of the 128 x BN fp32 tile, scale, bias
+//   warps 2-9   epilogue: tcgen05.ld of the 128 x BN fp32 tile, scale, bias
 //               (Algorithm 7's b_j), GELU / GELU-backward, residual, bf16 or
 //               fp32 stores into the output's shards.
 // Every mbarrier wait is bounded (see common.cuh); a wait that runs out sets
@@ -29,7 +29,8 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;                      // two per TMEM lane quarter
+constexpr int kThreads = 32 * (2 + kEpiWarps);
 
 template <int BN>
 struct TcCfg {
@@ -74,28 +75,29 @@ __device__ __forceinline__ bool tile_skipped(const GemmProblem& P, const TileInf
   return P.causal == CAUSAL_SKIP_UPPER && T.n0 > T.m0 + BM - 1;
 }
 
-__device__ __forceinline__ int64_t num_k_iters(const GemmProblem& P) {
-  return (P.K / P.segK) * ceil_div(P.segK, BK);
+// Contraction tiles start at k0 = segment * segK + kt * BK (kt < ceil(segK / BK)).
+// A tile needs the k0 in [klo, khi): all of them, or the causal part.
+__device__ __forceinline__ void k_bounds(const GemmProblem& P, const TileInfo& T, int64_t& klo, int64_t& khi) {
+  klo = 0;
+  khi = P.K;
+  if (P.causal == CAUSAL_K_LE_M) khi = T.m0 + BM < P.K ? T.m0 + BM : P.K;
+  if (P.causal == CAUSAL_K_GE_M) klo = T.m0 - BK + 1;
 }
 
-__device__ __forceinline__ int64_t k_of(const GemmProblem& P, int64_t kk) {
-  const int64_t tps = ceil_div(P.segK, BK);
-  const int64_t s = kk / tps;
-  return s * P.segK + (kk - s * tps) * BK;
+__device__ __forceinline__ bool tile_has_k(const GemmProblem& P, int64_t klo, int64_t khi, int32_t nsegK,
+                                           int32_t tpsK) {
+  for (int32_t sg = 0; sg < nsegK; ++sg) {
+    const int64_t ks = (int64_t)sg * P.segK;
+    const int64_t kt0 = klo > ks ? (klo - ks + BK - 1) / BK : 0;
+    if (kt0 < tpsK && ks + kt0 * BK < khi) return true;
+  }
+  return false;
 }
 
-__device__ __forceinline__ bool k_needed(const GemmProblem& P, const TileInfo& T, int64_t k0) {
-  if (P.causal == CAUSAL_K_LE_M) return k0 <= T.m0 + BM - 1;
-  if (P.causal == CAUSAL_K_GE_M) return k0 + BK - 1 >= T.m0;
-  return true;
-}
-
-// stored (row, col) of an operand -> TMA coordinates (col in shard, row in shard, shard)
-__device__ __forceinline__ void tma_coords(const Grid& g, int64_t row, int64_t col, int& c0, int& c1, int& c2) {
-  const int64_t br = row / g.bh, bc = col / g.bw;
-  c2 = (br < g.rb && bc < g.cb) ? g.shard((int32_t)br, (int32_t)bc) : g.nshards();  // past the end: zero fill
-  c1 = (int)(row - br * g.bh);
-  c0 = (int)(col - bc * g.bw);
+// block (br, bc) of an operand -> shard number, or one past the last shard
+// (a TMA coordinate that reads zeros) when the block lies outside the matrix
+__device__ __forceinline__ int shard_or_oob(const Grid& g, int64_t br, int64_t bc) {
+  return (br < g.rb && bc < g.cb) ? g.shard((int32_t)br, (int32_t)bc) : g.nshards();
 }
 
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
@@ -162,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), 4);
+      mbar_init(tempty_bar(b), kEpiWarps);
     }
     mbar_init(final_bar, 1);
     *abort_flag = 0;
@@ -182,54 +184,108 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_holder;
 
   const int64_t ntiles = total_tiles<BN>(P);
-  const int64_t nk = num_k_iters(P);
+  const int32_t segK = (int32_t)P.segK;
+  const int32_t tpsK = (segK + BK - 1) / BK;
+  const int32_t nsegK = (int32_t)(P.K / P.segK);
   const bool a_mn = P.a.mn_major != 0, b_mn = P.b.mn_major != 0;
 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
+      // Shard coordinates change only at contraction-segment boundaries, so
+      // they are computed once per tile (the M / N side) and once per
+      // segment (the K side); the inner loop only adds BK.
       uint32_t it = 0;
       bool ok = true;
       for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
         TileInfo T;
         decode_tile<BN>(P, t, T);
         if (tile_skipped<BN>(P, T)) continue;
+        int64_t klo, khi;
+        k_bounds(P, T, klo, khi);
         const int64_t am = T.m0 + op_off(P.a.hi1, P.a.lo1, P.a.base1, T.z, P.Hz);
         const int64_t ak = op_off(P.a.hi2, P.a.lo2, P.a.base2, T.z, P.Hz);
         const int64_t bk = op_off(P.b.hi1, P.b.lo1, P.b.base1, T.z, P.Hz);
         const int64_t bn = T.n0 + op_off(P.b.hi2, P.b.lo2, P.b.base2, T.z, P.Hz);
-        for (int64_t kk = 0; kk < nk; ++kk) {
-          const int64_t k0 = k_of(P, kk);
-          if (!k_needed(P, T, k0)) continue;
-          const int s = (int)(it % S);
-          const uint32_t ph = (it / S) & 1u;
-          if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, P.err)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(full_bar(s), Cfg::STAGE_BYTES);
-          int c0, c1, c2;
-          if (!a_mn) {
-            tma_coords(P.a.g, am, ak + k0, c0, c1, c2);
-            tma_load_3d(a_stage(s), &mapA, full_bar(s), c0, c1, c2);
-          } else {
+        // M / N side, fixed for the tile
+        int64_t a_br = 0, b_br = 0;
+        int a_c1 = 0, b_c1 = 0;
+        int64_t a_bc[BM / 64], b_bc[BN / 64];
+        int a_c0[BM / 64], b_c0[BN / 64];
+        if (!a_mn) {
+          a_br = am / P.a.g.bh;
+          a_c1 = (int)(am - a_br * P.a.g.bh);
+        } else {
 #pragma unroll
-            for (int h = 0; h < BM / 64; ++h) {
-              tma_coords(P.a.g, ak + k0, am + 64 * h, c0, c1, c2);
-              tma_load_3d(a_stage(s) + h * 8192u, &mapA, full_bar(s), c0, c1, c2);
-            }
+          for (int h = 0; h < BM / 64; ++h) {
+            a_bc[h] = (am + 64 * h) / P.a.g.bw;
+            a_c0[h] = (int)(am + 64 * h - a_bc[h] * P.a.g.bw);
+          }
+        }
+        if (!b_mn) {
+          b_br = bn / P.b.g.bh;
+          b_c1 = (int)(bn - b_br * P.b.g.bh);
+        } else {
+#pragma unroll
+          for (int h = 0; h < BN / 64; ++h) {
+            b_bc[h] = (bn + 64 * h) / P.b.g.bw;
+            b_c0[h] = (int)(bn + 64 * h - b_bc[h] * P.b.g.bw);
+          }
+        }
+        for (int32_t sg = 0; sg < nsegK && ok; ++sg) {
+          const int64_t ks = (int64_t)sg * segK;
+          if (ks >= khi) break;
+          if (ks + segK <= klo) continue;
+          // K side, fixed for the segment
+          int a_k = 0, b_k = 0, a_sh = 0, b_sh = 0;
+          int a_shh[BM / 64], b_shh[BN / 64];
+          if (!a_mn) {
+            const int64_t bc = (ak + ks) / P.a.g.bw;
+            a_k = (int)(ak + ks - bc * P.a.g.bw);
+            a_sh = shard_or_oob(P.a.g, a_br, bc);
+          } else {
+            const int64_t br = (ak + ks) / P.a.g.bh;
+            a_k = (int)(ak + ks - br * P.a.g.bh);
+#pragma unroll
+            for (int h = 0; h < BM / 64; ++h) a_shh[h] = shard_or_oob(P.a.g, br, a_bc[h]);
           }
           if (!b_mn) {
-            tma_coords(P.b.g, bn, bk + k0, c0, c1, c2);
-            tma_load_3d(b_stage(s), &mapB, full_bar(s), c0, c1, c2);
+            const int64_t bc = (bk + ks) / P.b.g.bw;
+            b_k = (int)(bk + ks - bc * P.b.g.bw);
+            b_sh = shard_or_oob(P.b.g, b_br, bc);
           } else {
+            const int64_t br = (bk + ks) / P.b.g.bh;
+            b_k = (int)(bk + ks - br * P.b.g.bh);
 #pragma unroll
-            for (int h = 0; h < BN / 64; ++h) {
-              tma_coords(P.b.g, bk + k0, bn + 64 * h, c0, c1, c2);
-              tma_load_3d(b_stage(s) + h * 8192u, &mapB, full_bar(s), c0, c1, c2);
-            }
+            for (int h = 0; h < BN / 64; ++h) b_shh[h] = shard_or_oob(P.b.g, br, b_bc[h]);
           }
-          ++it;
+          for (int32_t kt = 0; kt < tpsK; ++kt) {
+            const int64_t k0 = ks + (int64_t)kt * BK;
+            if (k0 < klo || k0 >= khi) continue;
+            const int s = (int)(it % S);
+            const uint32_t ph = (it / S) & 1u;
+            if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, P.err)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(full_bar(s), Cfg::STAGE_BYTES);
+            const int kofs = kt * BK;
+            if (!a_mn) {
+              tma_load_3d(a_stage(s), &mapA, full_bar(s), a_k + kofs, a_c1, a_sh);
+            } else {
+#pragma unroll
+              for (int h = 0; h < BM / 64; ++h)
+                tma_load_3d(a_stage(s) + h * 8192u, &mapA, full_bar(s), a_c0[h], a_k + kofs, a_shh[h]);
+            }
+            if (!b_mn) {
+              tma_load_3d(b_stage(s), &mapB, full_bar(s), b_k + kofs, b_c1, b_sh);
+            } else {
+#pragma unroll
+              for (int h = 0; h < BN / 64; ++h)
+                tma_load_3d(b_stage(s) + h * 8192u, &mapB, full_bar(s), b_c0[h], b_k + kofs, b_shh[h]);
+            }
+            ++it;
+          }
         }
       }
       if (!ok) {
@@ -248,6 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         TileInfo T;
         decode_tile<BN>(P, t, T);
         if (tile_skipped<BN>(P, T)) continue;
+        int64_t klo, khi;
+        k_bounds(P, T, klo, khi);
         const int buf = (int)(tc & 1u);
         const uint32_t tph = (tc >> 1) & 1u;
         if (!mbar_wait(tempty_bar(buf), tph ^ 1u, abort_flag, P.err)) {
@@ -257,27 +315,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
         bool first = true;
-        for (int64_t kk = 0; kk < nk; ++kk) {
-          const int64_t k0 = k_of(P, kk);
-          if (!k_needed(P, T, k0)) continue;
-          const int s = (int)(it % S);
-          const uint32_t ph = (it / S) & 1u;
-          if (!mbar_wait(full_bar(s), ph, abort_flag, P.err)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+        for (int32_t sg = 0; sg < nsegK && ok; ++sg) {
+          const int64_t ks = (int64_t)sg * segK;
+          if (ks >= khi) break;
+          if (ks + segK <= klo) continue;
+          for (int32_t kt = 0; kt < tpsK; ++kt) {
+            const int64_t k0 = ks + (int64_t)kt * BK;
+            if (k0 < klo || k0 >= khi) continue;
+            const int s = (int)(it % S);
+            const uint32_t ph = (it / S) & 1u;
+            if (!mbar_wait(full_bar(s), ph, abort_flag, P.err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
 #pragma unroll
-          for (int k16 = 0; k16 < BK / 16; ++k16) {
-            const uint64_t ad = a_mn ? smem_desc_sw128(a_stage(s) + k16 * 2048u, 8192u, 1024u)
-                                     : smem_desc_sw128(a_stage(s) + k16 * 32u, 16u, 1024u);
-            const uint64_t bd = b_mn ? smem_desc_sw128(b_stage(s) + k16 * 2048u, 8192u, 1024u)
-                                     : smem_desc_sw128(b_stage(s) + k16 * 32u, 16u, 1024u);
-            umma_bf16(d_tmem, ad, bd, idesc, (first && k16 == 0) ? 0u : 1u);
+            for (int k16 = 0; k16 < BK / 16; ++k16) {
+              const uint64_t ad = a_mn ? smem_desc_sw128(a_stage(s) + k16 * 2048u, 8192u, 1024u)
+                                       : smem_desc_sw128(a_stage(s) + k16 * 32u, 16u, 1024u);
+              const uint64_t bd = b_mn ? smem_desc_sw128(b_stage(s) + k16 * 2048u, 8192u, 1024u)
+                                       : smem_desc_sw128(b_stage(s) + k16 * 32u, 16u, 1024u);
+              umma_bf16(d_tmem, ad, bd, idesc, (first && k16 == 0) ? 0u : 1u);
+            }
+            first = false;
+            umma_commit(empty_bar(s));
+            ++it;
           }
-          first = false;
-          umma_commit(empty_bar(s));
-          ++it;
         }
         if (!ok) break;
         umma_commit(tfull_bar(buf));
@@ -289,8 +352,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // -------------------------------------------------------------- epilogue
+    // warp w may read TMEM lanes 32*(w%4) .. +31 only: two warps share each
+    // lane quarter (= 32 rows of the tile) and split its columns in halves
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
+    constexpr int CH = BN / 64;  // 32-column chunks per warp
     uint32_t tc = 0;
     const Grid& cg = P.c.g;
     const int esz = P.epi.out_f32 ? 4 : 2;
@@ -298,8 +365,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       TileInfo T;
       decode_tile<BN>(P, t, T);
       if (tile_skipped<BN>(P, T)) continue;
-      bool any_k = false;
-      for (int64_t kk = 0; kk < nk && !any_k; ++kk) any_k = k_needed(P, T, k_of(P, kk));
+      int64_t klo, khi;
+      k_bounds(P, T, klo, khi);
+      const bool any_k = tile_has_k(P, klo, khi, nsegK, tpsK);
       const int buf = (int)(tc & 1u);
       const uint32_t tph = (tc >> 1) & 1u;
       // one lane waits and the warp follows it, so the warp stays converged
@@ -319,11 +387,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         row_base = cg.block_base((int32_t)br, (int32_t)bc) + (gm - br * cg.bh) * cg.bw + (gn0 - bc * cg.bw);
       }
 #pragma unroll 1
-      for (int ch = 0; ch < BN / 32; ++ch) {
+      for (int cc = 0; cc < CH; ++cc) {
+        const int ch = half * CH + cc;
         uint32_t r[32];
         tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * BN + ch * 32), r);
         tmem_ld_wait();
-        if (ch == BN / 32 - 1) {
+        if (cc == CH - 1) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(tempty_bar(buf));
