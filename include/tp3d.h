@@ -141,6 +141,28 @@ tp3d_status tp3d_mlp(tp3d_ctx* ctx, int q, int64_t M, int64_t h, int64_t f, tp3d
                      const void* X, const void* W1, const void* b1, const void* W2,
                      const void* b2, void* Y1, void* Y, void* stream);
 
+/* tp3d_mlp without the hidden-activation argument, for callers that cannot
+ * allocate device memory: code that must not call cudaMalloc (it would
+ * synchronise the device, or the process's memory is all handed to another
+ * pool), or that is given only the tensors it reads and writes.  The paper
+ * has no counterpart; this is a convenience of this library.
+ *
+ * Same computation, kernels and order as tp3d_mlp.  The hidden activation
+ * Y1 lives in a fixed array of 8 Mi bf16 elements (16 MiB) in this
+ * library's device memory, which every GPU that loads the library keeps
+ * until the process exits; M * f must be <= 8388608, else TP3D_EUNSUPPORTED
+ * and nothing is launched.  The call allocates nothing.
+ *   - The first call on a device looks up the array's device address (one
+ *     cudaGetSymbolAddress with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - Every call, on every stream, shares the one array, which keeps the last
+ *     call's contents; calls that overlap on the GPU race.  Y1 is fully
+ *     written before it is read, so nothing needs clearing between calls.
+ * Other arguments, layouts and errors as tp3d_mlp.                           */
+tp3d_status tp3d_mlp_noalloc(tp3d_ctx* ctx, int q, int64_t M, int64_t h, int64_t f, tp3d_dtype dtype,
+                             const void* X, const void* W1, const void* b1, const void* W2,
+                             const void* b2, void* Y, void* stream);
+
 /* GPT decoder layer (MP3D §3.2), pre-LN:
  *   H = X + Attn(LN1(X)),  Y = H + MLP(LN2(H))
  * LN: biased variance, eps; attention: causal, `heads` heads of

@@ -25,7 +25,7 @@ from .build import build
 __all__ = [
     "build", "lib", "Tp3dError", "check", "STATUS", "layout",
     "tp3d_create", "tp3d_destroy", "tp3d_status_string", "tp3d_sync_status", "tp3d_reshard",
-    "tp3d_linear", "tp3d_mlp", "tp3d_layer_workspace_bytes", "tp3d_layer_fwd", "tp3d_layer_bwd",
+    "tp3d_linear", "tp3d_mlp", "tp3d_mlp_noalloc", "tp3d_layer_workspace_bytes", "tp3d_layer_fwd", "tp3d_layer_bwd",
     "tp3d_layout", "tp3d_layer_cfg", "tp3d_layer_params", "tp3d_layer_grads",
     "TP3D_F32", "TP3D_BF16", "CUBE_A", "CUBE_B", "CUBE_C", "CUBE_B_SWAP", "ROW", "COL", "BLOCK2D", "REPLICATED",
 ]
@@ -87,6 +87,10 @@ _SIGS = {
     "tp3d_mlp": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                 ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "tp3d_mlp_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                        ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                        ctypes.c_void_p]),
     "tp3d_layer_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(tp3d_layer_cfg)]),
     "tp3d_layer_fwd": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(tp3d_layer_cfg),
                                       ctypes.POINTER(tp3d_layer_params), ctypes.c_void_p, ctypes.c_void_p,
@@ -161,6 +165,12 @@ def tp3d_linear(ctx, q, y, M, N, K, dtype, A, B, bias, act, C, stream=None) -> i
 
 def tp3d_mlp(ctx, q, M, h, f, dtype, X, W1, b1, W2, b2, Y1, Y, stream=None) -> int:
     return lib().tp3d_mlp(ctx, q, M, h, f, dtype, _p(X), _p(W1), _p(b1), _p(W2), _p(b2), _p(Y1), _p(Y), _s(stream))
+
+
+def tp3d_mlp_noalloc(ctx, q, M, h, f, dtype, X, W1, b1, W2, b2, Y, stream=None) -> int:
+    """tp3d_mlp for callers that cannot allocate: the hidden activation lives
+    in the library's own fixed 16 MiB device array (M * f <= 8388608)."""
+    return lib().tp3d_mlp_noalloc(ctx, q, M, h, f, dtype, _p(X), _p(W1), _p(b1), _p(W2), _p(b2), _p(Y), _s(stream))
 
 
 def tp3d_layer_workspace_bytes(cfg: tp3d_layer_cfg) -> int:
