@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(T * T) gemm_simt_kernel(const GemmProblem P) {
 }  // namespace
 
 tp3d_status gemm_f32_simt(const tp3d_ctx*, const GemmProblem& P, cudaStream_t s) {
-  if (P.Z <= 0 || P.M <= 0 || P.N <= 0) return TP3D_OK;
+  if (P.Z < 1 || P.Hz < 1 || P.M < 1 || P.N < 1 || P.K < 1) return TP3D_EINVAL;
   dim3 grid((unsigned)((P.N + T - 1) / T), (unsigned)((P.M + T - 1) / T), (unsigned)P.Z);
   if (grid.y > 65535u || grid.z > 65535u) return TP3D_EUNSUPPORTED;
   gemm_simt_kernel<<<grid, dim3(T, T), 0, s>>>(P);

@@ -495,6 +495,8 @@ tp3d_status launch(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t s) {
 }  // namespace
 
 tp3d_status gemm_bf16_tc(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t s) {
+  if (P.Z < 1 || P.Hz < 1 || P.M < 1 || P.N < 1 || P.K < 1) return TP3D_EINVAL;
+  if (P.segM < 1 || P.segN < 1 || P.segK < 1 || P.M % P.segM || P.N % P.segN || P.K % P.segK) return TP3D_EINVAL;
   // every operand block must be at least one TMA box wide and tall enough
   // for its 16-byte row pitch; the tile shape is picked per problem.
   const Grid* gs[3] = {&P.a.g, &P.b.g, &P.c.g};

@@ -1,25 +1,377 @@
-// layer.cu - the GPT decoder layer on the cube (forward and backward).
+// layer.cu - the pre-LN GPT decoder layer on the cube, forward and backward
+// ("Maximizing Parallelism in Distributed Training for Huge Neural
+// Networks", §3.2): a Self-Attention block and an MLP block, each two 3-D
+// linears - the first with input group y = 0 (input CUBE_A, output CUBE_C),
+// the second with y and z exchanged (input CUBE_C, output CUBE_A) - so the
+// layer's output has its input's layout.  LayerNorm is the matrix-vector
+// scaling and shift of §3.1.3 with whole-row statistics.  Backward follows
+// the differentiation formulas of §3.1.2 (dA = dC B^T, dB = A^T dC; the
+// attention products are the C = A B^T and C = A^T B forms), Algorithm 8
+// read by its definition (bias gradient = column sums over every row) and
+// §3.1.3's gamma gradient sum(dC * A-hat).
+//
+// Everything runs on the caller's stream: LayerNorm, the six forward GEMMs
+// (QKV, Q K^T, P V, output projection + residual, W1 + GELU, W2 + residual)
+// and the causal softmax; the backward's twelve GEMMs, softmax backward,
+// LayerNorm backward and the column sums of the bias / gamma / beta
+// gradients.  Attention runs per (batch, head) as batched GEMMs whose
+// windows sit at (batch * seq, head * d) of the QKV and O matrices, so the
+// heads are read in place from their CUBE_C shards.
+#include <math.h>
+
 #include "gemm.cuh"
+#include "layer_kernels.cuh"
+
+namespace tp3d {
+
+tp3d_status plan_linear(const tp3d_ctx* ctx, int q, int y, int64_t M, int64_t N, int64_t K, const void* A,
+                        const void* B, const void* bias, int act, void* C, GemmProblem* out);
+
+namespace {
+
+using bf16 = __nv_bfloat16;
+
+struct Plan {
+  int q, b, s, h, H, d, f;
+  int64_t M, Z;
+  float eps;
+  // workspace offsets (bytes)
+  size_t xn1, mean1, rstd1, qkv, P, O, Hres, xn2, mean2, rstd2, z1, y1;  // saved by the forward
+  size_t S, dS, dz1, dxn, dH, dO, dqkv, part;                           // scratch
+  size_t part_floats, total;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+tp3d_status make_plan(const tp3d_layer_cfg* c, Plan* p) {
+  if (!c) return TP3D_EINVAL;
+  if (c->q < 1 || c->q > 16 || c->batch < 1 || c->seq < 1 || c->hidden < 1 || c->heads < 1 || c->ffn < 1)
+    return TP3D_EINVAL;
+  if (c->dtype != TP3D_BF16) return TP3D_EDTYPE;
+  if (!(c->eps > 0.0f)) return TP3D_EINVAL;
+  Plan x{};
+  x.q = c->q;
+  x.b = c->batch;
+  x.s = c->seq;
+  x.h = c->hidden;
+  x.H = c->heads;
+  x.f = c->ffn;
+  x.eps = c->eps;
+  if (x.h % x.H) return TP3D_ESHAPE;
+  x.d = x.h / x.H;
+  x.M = (int64_t)x.b * x.s;
+  x.Z = (int64_t)x.b * x.H;
+  const int64_t q2 = (int64_t)x.q * x.q;
+  if (x.M % q2 || x.h % q2 || x.f % q2 || (3 * (int64_t)x.h) % q2) return TP3D_ESHAPE;
+  // every shard row a whole number of 16-byte vectors, heads and query tiles
+  // inside shards (the causal tiles of the attention products are 128 rows)
+  const int64_t m = x.M / q2;
+  if ((x.h / q2) % 8 || (x.f / q2) % 8) return TP3D_ESHAPE;
+  if (x.d % 64 || x.s % 128 || gcd64(m, x.s) % 128 || ((3 * (int64_t)x.h / x.q) % x.d)) return TP3D_EUNSUPPORTED;
+  if ((int64_t)x.h * 8 > 200 * 1024) return TP3D_EUNSUPPORTED;  // LayerNorm backward's shared-memory partials
+  const int64_t M = x.M, h = x.h, f = x.f, Z = x.Z, s = x.s;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align256(o + bytes);
+    return at;
+  };
+  x.xn1 = take(M * h * 2);
+  x.mean1 = take(M * 4);
+  x.rstd1 = take(M * 4);
+  x.qkv = take(M * 3 * h * 2);
+  x.P = take(Z * s * s * 2);
+  x.O = take(M * h * 2);
+  x.Hres = take(M * h * 2);
+  x.xn2 = take(M * h * 2);
+  x.mean2 = take(M * 4);
+  x.rstd2 = take(M * 4);
+  x.z1 = take(M * f * 2);
+  x.y1 = take(M * f * 2);
+  x.S = take(Z * s * s * 4);
+  x.dS = take(Z * s * s * 2);
+  x.dz1 = take(M * f * 2);
+  x.dxn = take(M * h * 2);
+  x.dH = take(M * h * 2);
+  x.dO = take(M * h * 2);
+  x.dqkv = take(M * 3 * h * 2);
+  // column-sum partials: the largest of the bias sums and the two LayerNorm sums
+  Grid gc;
+  TP3D_TRY(make_grid(cube(TP3D_CUBE_C, x.q), M, f, &gc));
+  const int64_t pc = colsum_parts(gc) * (f > 3 * h ? f : 3 * h);
+  const int64_t pl = (int64_t)ln_bwd_parts(M) * 2 * h;
+  x.part_floats = (size_t)(pc > pl ? pc : pl);
+  x.part = take(x.part_floats * 4);
+  x.total = o;
+  *p = x;
+  return TP3D_OK;
+}
+
+// The attention products per (batch, head) z = b * heads + t.
+// Windows: Q_z rows [b*s, +s) cols [t*d, +d) of QKV, K_z at cols h + t*d,
+// V_z at 2h + t*d; O_z and dO_z at cols t*d of O / dO; S_z, P_z, dS_z are the
+// z-th s x s block of a dense buffer (layout ROW with Z blocks).
+GemmProblem att_base(const Plan& p, int64_t M, int64_t N, int64_t K, int* err) {
+  GemmProblem P{};
+  P.Z = (int32_t)p.Z;
+  P.Hz = p.H;
+  P.M = M;
+  P.N = N;
+  P.K = K;
+  P.epi.alpha = 1.0f;
+  P.err = err;
+  return P;
+}
+
+tp3d_status run(const tp3d_ctx* ctx, GemmProblem& P, cudaStream_t s) {
+  TP3D_TRY(plan_segments(P));
+  return gemm_bf16_tc(ctx, P, s);
+}
+
+// dA = dC . W^T for a 3-D linear with input group y (MP3D Algorithm 2, first line)
+tp3d_status plan_dgrad(const tp3d_ctx* ctx, int q, int y, int64_t M, int64_t Nin, int64_t Kout, const void* dC,
+                       const void* W, void* dA, GemmProblem* out) {
+  GemmProblem P{};
+  TP3D_TRY(make_grid(cube(y ? TP3D_CUBE_A : TP3D_CUBE_C, q), M, Kout, &P.a.g));
+  TP3D_TRY(make_grid(cube(y ? TP3D_CUBE_B_SWAP : TP3D_CUBE_B, q), Nin, Kout, &P.b.g));
+  TP3D_TRY(make_grid(cube(y ? TP3D_CUBE_C : TP3D_CUBE_A, q), M, Nin, &P.c.g));
+  P.Z = 1;
+  P.Hz = 1;
+  P.M = M;
+  P.N = Nin;
+  P.K = Kout;
+  P.a.ptr = dC;
+  P.a.mn_major = 0;
+  P.b.ptr = W;  // stored Nin x Kout = n x k: K-major
+  P.b.mn_major = 0;
+  P.c.ptr = dA;
+  P.epi.alpha = 1.0f;
+  P.err = ctx->d_err;
+  *out = P;
+  return TP3D_OK;
+}
+
+// dW = A^T . dC for a 3-D linear with input group y (MP3D Algorithm 2, second line)
+tp3d_status plan_wgrad(const tp3d_ctx* ctx, int q, int y, int64_t M, int64_t Nin, int64_t Kout, const void* A,
+                       const void* dC, void* dW, GemmProblem* out) {
+  GemmProblem P{};
+  TP3D_TRY(make_grid(cube(y ? TP3D_CUBE_C : TP3D_CUBE_A, q), M, Nin, &P.a.g));
+  TP3D_TRY(make_grid(cube(y ? TP3D_CUBE_A : TP3D_CUBE_C, q), M, Kout, &P.b.g));
+  TP3D_TRY(make_grid(cube(y ? TP3D_CUBE_B_SWAP : TP3D_CUBE_B, q), Nin, Kout, &P.c.g));
+  P.Z = 1;
+  P.Hz = 1;
+  P.M = Nin;
+  P.N = Kout;
+  P.K = M;
+  P.a.ptr = A;  // stored M x Nin = k x m: MN-major
+  P.a.mn_major = 1;
+  P.b.ptr = dC;  // stored M x Kout = k x n: MN-major
+  P.b.mn_major = 1;
+  P.c.ptr = dW;
+  P.epi.alpha = 1.0f;
+  P.err = ctx->d_err;
+  *out = P;
+  return TP3D_OK;
+}
+
+tp3d_status colsum(const tp3d_ctx* ctx, int kind, int q, int64_t R, int64_t C, const void* x, float* part, void* out,
+                   cudaStream_t s) {
+  Grid g;
+  TP3D_TRY(make_grid(cube(kind, q), R, C, &g));
+  TP3D_TRY(launch_colsum(ctx, g, x, part, s));
+  return launch_reduce_parts(part, colsum_parts(g), C, out, s);
+}
+
+}  // namespace
+
+}  // namespace tp3d
 
 using namespace tp3d;
 
 extern "C" {
 
 size_t tp3d_layer_workspace_bytes(const tp3d_layer_cfg* cfg) {
-  (void)cfg;
-  return 0;
+  Plan p;
+  if (make_plan(cfg, &p) != TP3D_OK) return 0;
+  return p.total;
 }
 
-tp3d_status tp3d_layer_fwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_layer_params* p, const void* X,
+tp3d_status tp3d_layer_fwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_layer_params* w, const void* X,
                            void* Y, void* workspace, void* stream) {
-  (void)ctx; (void)cfg; (void)p; (void)X; (void)Y; (void)workspace; (void)stream;
-  return TP3D_EUNSUPPORTED;
+  if (!ctx || !cfg || !w || !X || !Y || !workspace) return TP3D_EINVAL;
+  Plan p;
+  TP3D_TRY(make_plan(cfg, &p));
+  const void* need[] = {w->ln1_g, w->ln1_b, w->w_qkv, w->b_qkv, w->w_o, w->b_o,
+                        w->ln2_g, w->ln2_b, w->w_1, w->b_1, w->w_2, w->b_2};
+  for (const void* ptr : need)
+    if (!ptr) return TP3D_EINVAL;
+  for (const void* ptr : need)
+    if (!aligned16(ptr)) return TP3D_EALIGN;
+  if (!aligned16(X) || !aligned16(Y) || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return TP3D_EALIGN;
+  const int64_t M = p.M, h = p.h, f = p.f, s = p.s;
+  if (overlaps(Y, M * h * 2, X, M * h * 2) || overlaps(workspace, p.total, X, M * h * 2) ||
+      overlaps(workspace, p.total, Y, M * h * 2))
+    return TP3D_EOVERLAP;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  auto W = [&](size_t off) { return static_cast<void*>(ws + off); };
+  const cudaStream_t st = as_stream(stream);
+  const int q = p.q;
+
+  Grid gA;
+  TP3D_TRY(make_grid(cube(TP3D_CUBE_A, q), M, h, &gA));
+  // LN1
+  TP3D_TRY(launch_ln_fwd(ctx, gA, X, w->ln1_g, w->ln1_b, W(p.xn1), (float*)W(p.mean1), (float*)W(p.rstd1), p.eps, st));
+  // QKV = LN1(X) W_qkv + b_qkv   (y = 0: CUBE_A -> CUBE_C)
+  GemmProblem G;
+  TP3D_TRY(plan_linear(ctx, q, 0, M, h, 3 * h, W(p.xn1), w->w_qkv, w->b_qkv, 0, W(p.qkv), &G));
+  TP3D_TRY(gemm_bf16_tc(ctx, G, st));
+  // S_z = Q_z K_z^T / sqrt(d)  (MP3D's C = A B^T form), causal tiles only
+  Grid gQKV, gO, gD;
+  TP3D_TRY(make_grid(cube(TP3D_CUBE_C, q), M, 3 * h, &gQKV));
+  TP3D_TRY(make_grid(cube(TP3D_CUBE_C, q), M, h, &gO));
+  tp3d_layout rowZ{TP3D_ROW, 0, (int32_t)p.Z, 0};
+  TP3D_TRY(make_grid(rowZ, p.Z * s, s, &gD));
+  {
+    GemmProblem P = att_base(p, s, s, p.d, ctx->d_err);
+    P.a = Operand{gQKV, W(p.qkv), 0, s, 0, 0, 0, p.d, 0};          // Q_z: m = b*s, k = t*d
+    P.b = Operand{gQKV, W(p.qkv), 0, 0, p.d, h, s, 0, 0};          // K_z (stored keys x d): k = h + t*d, n = b*s
+    P.c = Operand{gD, W(p.S), 0, (int64_t)p.H * s, s, 0, 0, 0, 0};  // S block z
+    P.causal = CAUSAL_SKIP_UPPER;
+    P.epi.alpha = 1.0f / sqrtf((float)p.d);
+    P.epi.out_f32 = 1;
+    TP3D_TRY(run(ctx, P, st));
+  }
+  TP3D_TRY(launch_softmax_fwd(ctx, (const float*)W(p.S), W(p.P), p.Z, s, st));
+  {
+    // O_z = P_z V_z, keys <= query only
+    GemmProblem P = att_base(p, s, p.d, s, ctx->d_err);
+    P.a = Operand{gD, W(p.P), 0, (int64_t)p.H * s, s, 0, 0, 0, 0};
+    P.b = Operand{gQKV, W(p.qkv), 1, s, 0, 0, 0, p.d, 2 * h};  // V_z stored keys x d: k = b*s, n = 2h + t*d
+    P.c = Operand{gO, W(p.O), 0, s, 0, 0, 0, p.d, 0};
+    P.causal = CAUSAL_K_LE_M;
+    TP3D_TRY(run(ctx, P, st));
+  }
+  // H = X + O W_o + b_o   (y = 1: CUBE_C -> CUBE_A)
+  TP3D_TRY(plan_linear(ctx, q, 1, M, h, h, W(p.O), w->w_o, w->b_o, 0, W(p.Hres), &G));
+  G.epi.resid = X;
+  TP3D_TRY(gemm_bf16_tc(ctx, G, st));
+  // LN2, then Y1 = GELU(Z1), Z1 = LN2(H) W_1 + b_1 saved
+  TP3D_TRY(launch_ln_fwd(ctx, gA, W(p.Hres), w->ln2_g, w->ln2_b, W(p.xn2), (float*)W(p.mean2), (float*)W(p.rstd2),
+                         p.eps, st));
+  TP3D_TRY(plan_linear(ctx, q, 0, M, h, f, W(p.xn2), w->w_1, w->b_1, 1, W(p.y1), &G));
+  G.epi.zsave = W(p.z1);
+  TP3D_TRY(gemm_bf16_tc(ctx, G, st));
+  // Y = H + Y1 W_2 + b_2
+  TP3D_TRY(plan_linear(ctx, q, 1, M, f, h, W(p.y1), w->w_2, w->b_2, 0, Y, &G));
+  G.epi.resid = W(p.Hres);
+  return gemm_bf16_tc(ctx, G, st);
 }
 
-tp3d_status tp3d_layer_bwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_layer_params* p, const void* X,
+tp3d_status tp3d_layer_bwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_layer_params* w, const void* X,
                            void* workspace, const void* dY, void* dX, const tp3d_layer_grads* g, void* stream) {
-  (void)ctx; (void)cfg; (void)p; (void)X; (void)workspace; (void)dY; (void)dX; (void)g; (void)stream;
-  return TP3D_EUNSUPPORTED;
+  if (!ctx || !cfg || !w || !g || !X || !dY || !dX || !workspace) return TP3D_EINVAL;
+  Plan p;
+  TP3D_TRY(make_plan(cfg, &p));
+  const void* need[] = {w->ln1_g, w->ln1_b, w->w_qkv, w->b_qkv, w->w_o, w->b_o, w->ln2_g, w->ln2_b, w->w_1,
+                        w->b_1, w->w_2, w->b_2, g->ln1_g, g->ln1_b, g->w_qkv, g->b_qkv, g->w_o, g->b_o,
+                        g->ln2_g, g->ln2_b, g->w_1, g->b_1, g->w_2, g->b_2};
+  for (const void* ptr : need)
+    if (!ptr) return TP3D_EINVAL;
+  for (const void* ptr : need)
+    if (!aligned16(ptr)) return TP3D_EALIGN;
+  if (!aligned16(X) || !aligned16(dY) || !aligned16(dX) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return TP3D_EALIGN;
+  const int64_t M = p.M, h = p.h, f = p.f, s = p.s;
+  if (overlaps(dX, M * h * 2, dY, M * h * 2) || overlaps(dX, M * h * 2, X, M * h * 2) ||
+      overlaps(workspace, p.total, dX, M * h * 2) || overlaps(workspace, p.total, dY, M * h * 2))
+    return TP3D_EOVERLAP;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  auto W = [&](size_t off) { return static_cast<void*>(ws + off); };
+  float* part = (float*)W(p.part);
+  const cudaStream_t st = as_stream(stream);
+  const int q = p.q;
+  GemmProblem G;
+  Grid gA;
+  TP3D_TRY(make_grid(cube(TP3D_CUBE_A, q), M, h, &gA));
+
+  // ---- MLP block
+  TP3D_TRY(colsum(ctx, TP3D_CUBE_A, q, M, h, dY, part, g->b_2, st));                      // db2
+  TP3D_TRY(plan_wgrad(ctx, q, 1, M, f, h, W(p.y1), dY, g->w_2, &G));                       // dW2 = Y1^T dY
+  TP3D_TRY(run(ctx, G, st));
+  TP3D_TRY(plan_dgrad(ctx, q, 1, M, f, h, dY, w->w_2, W(p.dz1), &G));                      // dZ1 = (dY W2^T) GELU'(Z1)
+  G.epi.act = EPI_GELU_BWD;
+  G.epi.gin = W(p.z1);
+  TP3D_TRY(run(ctx, G, st));
+  TP3D_TRY(colsum(ctx, TP3D_CUBE_C, q, M, f, W(p.dz1), part, g->b_1, st));                // db1
+  TP3D_TRY(plan_wgrad(ctx, q, 0, M, h, f, W(p.xn2), W(p.dz1), g->w_1, &G));                // dW1 = LN2(H)^T dZ1
+  TP3D_TRY(run(ctx, G, st));
+  TP3D_TRY(plan_dgrad(ctx, q, 0, M, h, f, W(p.dz1), w->w_1, W(p.dxn), &G));                // dLN2 = dZ1 W1^T
+  TP3D_TRY(run(ctx, G, st));
+  int np = 0;
+  TP3D_TRY(launch_ln_bwd(ctx, gA, W(p.dxn), W(p.Hres), (const float*)W(p.mean2), (const float*)W(p.rstd2),
+                         w->ln2_g, dY, W(p.dH), part, part + (int64_t)ln_bwd_parts(M) * h, &np, st));  // dH
+  TP3D_TRY(launch_reduce_parts(part, np, h, g->ln2_g, st));
+  TP3D_TRY(launch_reduce_parts(part + (int64_t)np * h, np, h, g->ln2_b, st));
+
+  // ---- attention block
+  TP3D_TRY(colsum(ctx, TP3D_CUBE_A, q, M, h, W(p.dH), part, g->b_o, st));                 // dbo
+  TP3D_TRY(plan_wgrad(ctx, q, 1, M, h, h, W(p.O), W(p.dH), g->w_o, &G));                   // dWo = O^T dH
+  TP3D_TRY(run(ctx, G, st));
+  TP3D_TRY(plan_dgrad(ctx, q, 1, M, h, h, W(p.dH), w->w_o, W(p.dO), &G));                  // dO = dH Wo^T
+  TP3D_TRY(run(ctx, G, st));
+  Grid gQKV, gO, gD;
+  TP3D_TRY(make_grid(cube(TP3D_CUBE_C, q), M, 3 * h, &gQKV));
+  TP3D_TRY(make_grid(cube(TP3D_CUBE_C, q), M, h, &gO));
+  tp3d_layout rowZ{TP3D_ROW, 0, (int32_t)p.Z, 0};
+  TP3D_TRY(make_grid(rowZ, p.Z * s, s, &gD));
+  const int64_t Hs = (int64_t)p.H * s;
+  {
+    // dP_z = dO_z V_z^T (fp32, causal tiles)
+    GemmProblem P = att_base(p, s, s, p.d, ctx->d_err);
+    P.a = Operand{gO, W(p.dO), 0, s, 0, 0, 0, p.d, 0};
+    P.b = Operand{gQKV, W(p.qkv), 0, 0, p.d, 2 * h, s, 0, 0};
+    P.c = Operand{gD, W(p.S), 0, Hs, s, 0, 0, 0, 0};
+    P.causal = CAUSAL_SKIP_UPPER;
+    P.epi.out_f32 = 1;
+    TP3D_TRY(run(ctx, P, st));
+  }
+  TP3D_TRY(launch_softmax_bwd(ctx, W(p.P), (const float*)W(p.S), W(p.dS), p.Z, s, 1.0f / sqrtf((float)p.d), st));
+  {
+    // dV_z = P_z^T dO_z (contraction over queries >= key)
+    GemmProblem P = att_base(p, s, p.d, s, ctx->d_err);
+    P.a = Operand{gD, W(p.P), 1, 0, 0, 0, Hs, s, 0};
+    P.b = Operand{gO, W(p.dO), 1, s, 0, 0, 0, p.d, 0};
+    P.c = Operand{gQKV, W(p.dqkv), 0, s, 0, 0, 0, p.d, 2 * h};
+    P.causal = CAUSAL_K_GE_M;
+    TP3D_TRY(run(ctx, P, st));
+  }
+  {
+    // dQ_z = dS_z K_z (keys <= query)
+    GemmProblem P = att_base(p, s, p.d, s, ctx->d_err);
+    P.a = Operand{gD, W(p.dS), 0, Hs, s, 0, 0, 0, 0};
+    P.b = Operand{gQKV, W(p.qkv), 1, s, 0, 0, 0, p.d, h};
+    P.c = Operand{gQKV, W(p.dqkv), 0, s, 0, 0, 0, p.d, 0};
+    P.causal = CAUSAL_K_LE_M;
+    TP3D_TRY(run(ctx, P, st));
+  }
+  {
+    // dK_z = dS_z^T Q_z (queries >= key)
+    GemmProblem P = att_base(p, s, p.d, s, ctx->d_err);
+    P.a = Operand{gD, W(p.dS), 1, 0, 0, 0, Hs, s, 0};
+    P.b = Operand{gQKV, W(p.qkv), 1, s, 0, 0, 0, p.d, 0};
+    P.c = Operand{gQKV, W(p.dqkv), 0, s, 0, 0, 0, p.d, h};
+    P.causal = CAUSAL_K_GE_M;
+    TP3D_TRY(run(ctx, P, st));
+  }
+  TP3D_TRY(colsum(ctx, TP3D_CUBE_C, q, M, 3 * h, W(p.dqkv), part, g->b_qkv, st));          // dbqkv
+  TP3D_TRY(plan_wgrad(ctx, q, 0, M, h, 3 * h, W(p.xn1), W(p.dqkv), g->w_qkv, &G));         // dWqkv = LN1(X)^T dQKV
+  TP3D_TRY(run(ctx, G, st));
+  TP3D_TRY(plan_dgrad(ctx, q, 0, M, h, 3 * h, W(p.dqkv), w->w_qkv, W(p.dxn), &G));         // dLN1 = dQKV Wqkv^T
+  TP3D_TRY(run(ctx, G, st));
+  TP3D_TRY(launch_ln_bwd(ctx, gA, W(p.dxn), X, (const float*)W(p.mean1), (const float*)W(p.rstd1), w->ln1_g,
+                         W(p.dH), dX, part, part + (int64_t)ln_bwd_parts(M) * h, &np, st));   // dX
+  TP3D_TRY(launch_reduce_parts(part, np, h, g->ln1_g, st));
+  return launch_reduce_parts(part + (int64_t)np * h, np, h, g->ln1_b, st);
 }
 
 }  // extern "C"

@@ -1,0 +1,370 @@
+// layer_kernels.cu - the bandwidth-bound kernels of the GPT layer on the cube.
+//
+// "Maximizing Parallelism in Distributed Training for Huge Neural Networks"
+// §3.2 builds the 3-D LayerNorm from the matrix-vector operations of §3.1.3
+// (C = A * gamma, C = A + beta, Algorithms 7-8 and the gamma gradient
+// sum(dC * A-hat)); the row statistics and the attention core are not
+// partitioned by the page.  Here a row that the cube splits into q column
+// blocks (CUBE_A: blocks l = 0..q-1 of shard row (i, j)) is handled by one
+// warp that reads its q pieces, so the statistics are those of the whole
+// row.  All of these kernels are HBM-bound: 16-byte vector accesses, fp32
+// arithmetic, one pass over the data where possible.
+#include "layer_kernels.cuh"
+
+namespace tp3d {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ void unpack8(const uint4& v, float* f) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __bfloat1622float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+__device__ __forceinline__ uint4 pack8(const float* f) {
+  uint4 v;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+  return v;
+}
+
+using bf16 = __nv_bfloat16;
+
+// ------------------------------------------------------------------ LayerNorm
+__global__ void __launch_bounds__(kThreads) ln_fwd_kernel(const Grid g, const bf16* __restrict__ x,
+                                                          const bf16* __restrict__ gamma,
+                                                          const bf16* __restrict__ beta, bf16* __restrict__ y,
+                                                          float* __restrict__ mean, float* __restrict__ rstd,
+                                                          float eps) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * kWarps;
+  const int64_t vpb = g.bw / 8;
+  const float invC = 1.0f / (float)g.C;
+  for (int64_t r = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); r < g.R; r += nwarps) {
+    const int64_t br = r / g.bh, rr = r - br * g.bh;
+    float s1 = 0.0f;
+    for (int32_t bc = 0; bc < g.cb; ++bc) {
+      const uint4* p = reinterpret_cast<const uint4*>(x + g.block_base((int32_t)br, bc) + rr * g.bw);
+      for (int64_t v = lane; v < vpb; v += 32) {
+        float f[8];
+        unpack8(p[v], f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s1 += f[e];
+      }
+    }
+    const float mu = warp_sum(s1) * invC;
+    float s2 = 0.0f;
+    for (int32_t bc = 0; bc < g.cb; ++bc) {
+      const uint4* p = reinterpret_cast<const uint4*>(x + g.block_base((int32_t)br, bc) + rr * g.bw);
+      for (int64_t v = lane; v < vpb; v += 32) {
+        float f[8];
+        unpack8(p[v], f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s2 += (f[e] - mu) * (f[e] - mu);
+      }
+    }
+    const float rs = rsqrtf(warp_sum(s2) * invC + eps);
+    for (int32_t bc = 0; bc < g.cb; ++bc) {
+      const int64_t off = g.block_base((int32_t)br, bc) + rr * g.bw;
+      const uint4* p = reinterpret_cast<const uint4*>(x + off);
+      uint4* q = reinterpret_cast<uint4*>(y + off);
+      const uint4* gp = reinterpret_cast<const uint4*>(gamma + (int64_t)bc * g.bw);
+      const uint4* bp = reinterpret_cast<const uint4*>(beta + (int64_t)bc * g.bw);
+      for (int64_t v = lane; v < vpb; v += 32) {
+        float f[8], gg[8], bb[8], o[8];
+        unpack8(p[v], f);
+        unpack8(gp[v], gg);
+        unpack8(bp[v], bb);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = (f[e] - mu) * rs * gg[e] + bb[e];
+        q[v] = pack8(o);
+      }
+    }
+    if (lane == 0) {
+      mean[r] = mu;
+      rstd[r] = rs;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) ln_bwd_kernel(const Grid g, const bf16* __restrict__ dy,
+                                                          const bf16* __restrict__ x, const float* __restrict__ mean,
+                                                          const float* __restrict__ rstd,
+                                                          const bf16* __restrict__ gamma,
+                                                          const bf16* __restrict__ dres, bf16* __restrict__ dx,
+                                                          float* __restrict__ part_g, float* __restrict__ part_b) {
+  extern __shared__ float sm[];
+  float* sg = sm;
+  float* sb = sm + g.C;
+  for (int64_t c = threadIdx.x; c < 2 * g.C; c += kThreads) sm[c] = 0.0f;
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * kWarps;
+  const int64_t vpb = g.bw / 8;
+  const float invC = 1.0f / (float)g.C;
+  for (int64_t r = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); r < g.R; r += nwarps) {
+    const int64_t br = r / g.bh, rr = r - br * g.bh;
+    const float mu = mean[r], rs = rstd[r];
+    float a = 0.0f, b = 0.0f;
+    for (int32_t bc = 0; bc < g.cb; ++bc) {
+      const int64_t off = g.block_base((int32_t)br, bc) + rr * g.bw;
+      const uint4* dp = reinterpret_cast<const uint4*>(dy + off);
+      const uint4* xp = reinterpret_cast<const uint4*>(x + off);
+      const uint4* gp = reinterpret_cast<const uint4*>(gamma + (int64_t)bc * g.bw);
+      for (int64_t v = lane; v < vpb; v += 32) {
+        float d[8], xv[8], gg[8];
+        unpack8(dp[v], d);
+        unpack8(xp[v], xv);
+        unpack8(gp[v], gg);
+        const int64_t c0 = (int64_t)bc * g.bw + v * 8;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float xh = (xv[e] - mu) * rs;
+          const float dxh = d[e] * gg[e];
+          a += dxh;
+          b += dxh * xh;
+          atomicAdd(&sg[c0 + e], d[e] * xh);
+          atomicAdd(&sb[c0 + e], d[e]);
+        }
+      }
+    }
+    a = warp_sum(a) * invC;
+    b = warp_sum(b) * invC;
+    for (int32_t bc = 0; bc < g.cb; ++bc) {
+      const int64_t off = g.block_base((int32_t)br, bc) + rr * g.bw;
+      const uint4* dp = reinterpret_cast<const uint4*>(dy + off);
+      const uint4* xp = reinterpret_cast<const uint4*>(x + off);
+      const uint4* rp = reinterpret_cast<const uint4*>(dres + off);
+      const uint4* gp = reinterpret_cast<const uint4*>(gamma + (int64_t)bc * g.bw);
+      uint4* op = reinterpret_cast<uint4*>(dx + off);
+      for (int64_t v = lane; v < vpb; v += 32) {
+        float d[8], xv[8], gg[8], rv[8], o[8];
+        unpack8(dp[v], d);
+        unpack8(xp[v], xv);
+        unpack8(gp[v], gg);
+        unpack8(rp[v], rv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float xh = (xv[e] - mu) * rs;
+          o[e] = rv[e] + rs * (d[e] * gg[e] - a - xh * b);
+        }
+        op[v] = pack8(o);
+      }
+    }
+  }
+  __syncthreads();
+  for (int64_t c = threadIdx.x; c < g.C; c += kThreads) {
+    part_g[(int64_t)blockIdx.x * g.C + c] = sg[c];
+    part_b[(int64_t)blockIdx.x * g.C + c] = sb[c];
+  }
+}
+
+// ------------------------------------------------------------------ softmax
+// One warp per row i of one (batch, head) block; lanes take 4 consecutive
+// columns per step.  Columns past the row's last key but inside its
+// 128-column tile are written as 0 (the P.V and P^T.dO products read them).
+__global__ void __launch_bounds__(kThreads) softmax_fwd_kernel(const float* __restrict__ S, bf16* __restrict__ P,
+                                                               int64_t rows, int64_t s) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * kWarps;
+  for (int64_t row = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); row < rows; row += nwarps) {
+    const int64_t i = row % s;
+    const int64_t n = i + 1;
+    const int64_t nw = ((i >> 7) + 1) << 7;
+    const float* sr = S + row * s;
+    bf16* pr = P + row * s;
+    float mx = -INFINITY;
+    for (int64_t c = lane * 4; c < n; c += 128) {
+      const float4 v = *reinterpret_cast<const float4*>(sr + c);
+      const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (c + k < n) mx = fmaxf(mx, e[k]);
+    }
+    mx = warp_max(mx);
+    float sum = 0.0f;
+    for (int64_t c = lane * 4; c < n; c += 128) {
+      const float4 v = *reinterpret_cast<const float4*>(sr + c);
+      const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (c + k < n) sum += exp2f((e[k] - mx) * kLog2e);
+    }
+    const float inv = 1.0f / warp_sum(sum);
+    for (int64_t c = lane * 4; c < nw; c += 128) {
+      const float4 v = *reinterpret_cast<const float4*>(sr + c);
+      const float e[4] = {v.x, v.y, v.z, v.w};
+      float p[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) p[k] = (c + k < n) ? exp2f((e[k] - mx) * kLog2e) * inv : 0.0f;
+      __nv_bfloat162 h[2] = {__floats2bfloat162_rn(p[0], p[1]), __floats2bfloat162_rn(p[2], p[3])};
+      *reinterpret_cast<uint2*>(pr + c) = *reinterpret_cast<const uint2*>(h);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) softmax_bwd_kernel(const bf16* __restrict__ P,
+                                                               const float* __restrict__ dP, bf16* __restrict__ dS,
+                                                               int64_t rows, int64_t s, float scale) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * kWarps;
+  for (int64_t row = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); row < rows; row += nwarps) {
+    const int64_t i = row % s;
+    const int64_t n = i + 1;
+    const int64_t nw = ((i >> 7) + 1) << 7;
+    const bf16* pr = P + row * s;
+    const float* gr = dP + row * s;
+    bf16* orow = dS + row * s;
+    float dsum = 0.0f;
+    for (int64_t c = lane * 4; c < n; c += 128) {
+      const uint2 pv = *reinterpret_cast<const uint2*>(pr + c);
+      const float2 p01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pv.x));
+      const float2 p23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pv.y));
+      const float4 g = *reinterpret_cast<const float4*>(gr + c);
+      const float pp[4] = {p01.x, p01.y, p23.x, p23.y}, gg[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (c + k < n) dsum += pp[k] * gg[k];
+    }
+    const float D = warp_sum(dsum);
+    for (int64_t c = lane * 4; c < nw; c += 128) {
+      const uint2 pv = *reinterpret_cast<const uint2*>(pr + c);
+      const float2 p01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pv.x));
+      const float2 p23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pv.y));
+      const float4 g = *reinterpret_cast<const float4*>(gr + c);
+      const float pp[4] = {p01.x, p01.y, p23.x, p23.y}, gg[4] = {g.x, g.y, g.z, g.w};
+      float o[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) o[k] = (c + k < n) ? scale * pp[k] * (gg[k] - D) : 0.0f;
+      __nv_bfloat162 h[2] = {__floats2bfloat162_rn(o[0], o[1]), __floats2bfloat162_rn(o[2], o[3])};
+      *reinterpret_cast<uint2*>(orow + c) = *reinterpret_cast<const uint2*>(h);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ column sums
+// CTA (x, y): columns [256 x, +256) over the rows of part y (rows_per_part
+// rows inside one row block); lane l of every warp holds columns 8l..8l+7,
+// warps stride over rows; the 8 warps are summed in shared memory.
+__global__ void __launch_bounds__(kThreads) colsum_kernel(const Grid g, const bf16* __restrict__ x,
+                                                          float* __restrict__ part, int64_t rows_per_part) {
+  __shared__ float red[kWarps][257];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t c = (int64_t)blockIdx.x * 256 + lane * 8;
+  const int64_t r0 = (int64_t)blockIdx.y * rows_per_part;
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  if (c < g.C) {
+    const int64_t br = r0 / g.bh, bc = c / g.bw;
+    const bf16* base = x + g.block_base((int32_t)br, (int32_t)bc) + (r0 - br * g.bh) * g.bw + (c - bc * g.bw);
+    for (int64_t rr = w; rr < rows_per_part; rr += kWarps) {
+      float f[8];
+      unpack8(*reinterpret_cast<const uint4*>(base + rr * g.bw), f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] += f[e];
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) red[w][lane * 8 + e] = acc[e];
+  __syncthreads();
+  float s = 0.0f;
+#pragma unroll
+  for (int k = 0; k < kWarps; ++k) s += red[k][threadIdx.x];
+  const int64_t cc = (int64_t)blockIdx.x * 256 + threadIdx.x;
+  if (cc < g.C) part[(int64_t)blockIdx.y * g.C + cc] = s;
+}
+
+__global__ void __launch_bounds__(kThreads) reduce_parts_kernel(const float* __restrict__ part, int64_t nparts,
+                                                                int64_t C, bf16* __restrict__ out) {
+  for (int64_t c = (int64_t)blockIdx.x * kThreads + threadIdx.x; c < C; c += (int64_t)gridDim.x * kThreads) {
+    float s = 0.0f;
+    for (int64_t p = 0; p < nparts; ++p) s += part[p * C + c];
+    out[c] = __float2bfloat16_rn(s);
+  }
+}
+
+unsigned grid_for_rows(const tp3d_ctx* ctx, int64_t rows, int per_sm) {
+  int64_t g = (rows + kWarps - 1) / kWarps;
+  const int64_t cap = (int64_t)ctx->num_sms * per_sm;
+  return (unsigned)(g < cap ? (g > 0 ? g : 1) : cap);
+}
+
+tp3d_status last_error() { return cudaGetLastError() == cudaSuccess ? TP3D_OK : TP3D_ECUDA; }
+
+}  // namespace
+
+tp3d_status launch_ln_fwd(const tp3d_ctx* ctx, const Grid& g, const void* x, const void* gamma, const void* beta,
+                          void* y, float* mean, float* rstd, float eps, cudaStream_t s) {
+  ln_fwd_kernel<<<grid_for_rows(ctx, g.R, 16), kThreads, 0, s>>>(
+      g, static_cast<const bf16*>(x), static_cast<const bf16*>(gamma), static_cast<const bf16*>(beta),
+      static_cast<bf16*>(y), mean, rstd, eps);
+  return last_error();
+}
+
+int ln_bwd_parts(int64_t R) {
+  const int64_t g = (R + kWarps - 1) / kWarps;
+  return (int)(g < 512 ? g : 512);
+}
+
+tp3d_status launch_ln_bwd(const tp3d_ctx*, const Grid& g, const void* dy, const void* x, const float* mean,
+                          const float* rstd, const void* gamma, const void* dres, void* dx, float* part_g,
+                          float* part_b, int* nparts, cudaStream_t s) {
+  const unsigned grid = (unsigned)ln_bwd_parts(g.R);
+  const size_t smem = (size_t)g.C * 2 * sizeof(float);
+  if (smem > 200 * 1024) return TP3D_EUNSUPPORTED;
+  if (smem > 48 * 1024)
+    TP3D_CUDA_TRY(cudaFuncSetAttribute(ln_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  ln_bwd_kernel<<<grid, kThreads, smem, s>>>(g, static_cast<const bf16*>(dy), static_cast<const bf16*>(x), mean,
+                                              rstd, static_cast<const bf16*>(gamma), static_cast<const bf16*>(dres),
+                                              static_cast<bf16*>(dx), part_g, part_b);
+  *nparts = (int)grid;
+  return last_error();
+}
+
+tp3d_status launch_softmax_fwd(const tp3d_ctx* ctx, const float* S, void* P, int64_t Z, int64_t s, cudaStream_t st) {
+  softmax_fwd_kernel<<<grid_for_rows(ctx, Z * s, 16), kThreads, 0, st>>>(S, static_cast<bf16*>(P), Z * s, s);
+  return last_error();
+}
+
+tp3d_status launch_softmax_bwd(const tp3d_ctx* ctx, const void* P, const float* dP, void* dS, int64_t Z, int64_t s,
+                               float scale, cudaStream_t st) {
+  softmax_bwd_kernel<<<grid_for_rows(ctx, Z * s, 16), kThreads, 0, st>>>(
+      static_cast<const bf16*>(P), dP, static_cast<bf16*>(dS), Z * s, s, scale);
+  return last_error();
+}
+
+int64_t colsum_parts(const Grid& g) { return g.R / gcd64(g.bh, 256); }
+
+tp3d_status launch_colsum(const tp3d_ctx*, const Grid& g, const void* x, float* part, cudaStream_t s) {
+  const int64_t rpp = gcd64(g.bh, 256);
+  const dim3 grid((unsigned)((g.C + 255) / 256), (unsigned)(g.R / rpp));
+  if (grid.y > 65535u) return TP3D_EUNSUPPORTED;
+  colsum_kernel<<<grid, kThreads, 0, s>>>(g, static_cast<const bf16*>(x), part, rpp);
+  return last_error();
+}
+
+tp3d_status launch_reduce_parts(const float* part, int64_t nparts, int64_t C, void* out, cudaStream_t s) {
+  const unsigned grid = (unsigned)((C + kThreads - 1) / kThreads);
+  reduce_parts_kernel<<<grid, kThreads, 0, s>>>(part, nparts, C, static_cast<bf16*>(out));
+  return last_error();
+}
+
+}  // namespace tp3d

@@ -1,0 +1,39 @@
+// layer_kernels.cuh - host launchers of the layer's bandwidth-bound kernels
+// (layer_kernels.cu): LayerNorm forward/backward, causal softmax
+// forward/backward and column sums.  All read and write matrices through
+// their layout grid, so a row that the cube splits over q shards is read from
+// those q shards.
+#pragma once
+
+#include "common.cuh"
+
+namespace tp3d {
+
+// y = (x - mean) * rstd * gamma + beta per row of the R x C matrix x (layout g,
+// y in the same layout); mean / rstd (fp32, R each) are saved.
+tp3d_status launch_ln_fwd(const tp3d_ctx* ctx, const Grid& g, const void* x, const void* gamma, const void* beta,
+                          void* y, float* mean, float* rstd, float eps, cudaStream_t s);
+
+// dx = dres + rstd * (dxh - mean(dxh) - xh * mean(dxh * xh)), dxh = dy * gamma,
+// xh = (x - mean) * rstd.  Per-CTA column partial sums of dy * xh (gamma) and
+// dy (beta) go to part_g / part_b, ln_bwd_parts(R) rows of C floats each.
+tp3d_status launch_ln_bwd(const tp3d_ctx* ctx, const Grid& g, const void* dy, const void* x, const float* mean,
+                          const float* rstd, const void* gamma, const void* dres, void* dx, float* part_g,
+                          float* part_b, int* nparts, cudaStream_t s);
+int ln_bwd_parts(int64_t R);
+
+// Causal softmax over rows of the dense fp32 scores S (Z blocks of s x s):
+// P[i][c] = exp(S[i][c] - max) / sum for c <= i, 0 for i < c < (i/128+1)*128.
+tp3d_status launch_softmax_fwd(const tp3d_ctx* ctx, const float* S, void* P, int64_t Z, int64_t s, cudaStream_t st);
+
+// dS = scale * P * (dP - sum_c P dP) on the same causal support as P.
+tp3d_status launch_softmax_bwd(const tp3d_ctx* ctx, const void* P, const float* dP, void* dS, int64_t Z, int64_t s,
+                               float scale, cudaStream_t st);
+
+// Column sums of the R x C bf16 matrix x (layout g): partials in `part`
+// (colsum_parts(g) rows of C floats), then reduce_parts writes the bf16 vector.
+int64_t colsum_parts(const Grid& g);
+tp3d_status launch_colsum(const tp3d_ctx* ctx, const Grid& g, const void* x, float* part, cudaStream_t s);
+tp3d_status launch_reduce_parts(const float* part, int64_t nparts, int64_t C, void* out, cudaStream_t s);
+
+}  // namespace tp3d

@@ -1,0 +1,123 @@
+"""GPU parity of tp3d_layer_fwd / tp3d_layer_bwd against the oracle.
+
+The layer is the pre-LN GPT decoder layer of "Maximizing Parallelism in
+Distributed Training for Huge Neural Networks" §3.2 on the cube (readings
+in oracle/layer.py).  The oracle keeps every intermediate in float64; the GPU
+keeps bf16 intermediates with fp32 accumulation and fp32 LN / softmax
+statistics.  Bars, for the output, dX and every parameter gradient:
+max relative error max|g - o| / max|o| <= 1e-2 and Frobenius relative error
+<= 1e-2; the element-wise error with an RMS floor <= 5e-2, which bf16
+rounding of the stored activations alone can push past 1e-2 on tensors of
+1e5..1e7 elements (see oracle/metrics.py) but a localised error would not
+stay under.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth_inputs as S
+import tensor_transformer_layer_cube_gb300 as t
+from oracle import layer as OY
+from oracle import layouts as L
+from oracle.metrics import BF16_TOL, LAYER_ELEM_TOL, fro_err, max_rel_err, rel_err
+from tests.gpu_util import as_np64, device, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ctx():
+    c = t.tp3d_create(0)
+    yield c
+    t.tp3d_destroy(c)
+
+
+def _run(ctx, cfg: OY.LayerConfig, seed, perturb):
+    I = S.layer_inputs(cfg.batch, cfg.seq, cfg.hidden, cfg.heads, cfg.ffn, seed, perturb=perturb)
+    q, M, h = cfg.p, cfg.M, cfg.hidden
+    params = {}
+    for k, lay in OY.WEIGHT_LAYOUTS.items():
+        params[k] = to_dev_bf16(I[k], lay(q))
+    for k in OY.VECTORS:
+        params[k] = I[k].to(device())
+    X = to_dev_bf16(I["X"], L.CUBE_A(q))
+    dY = to_dev_bf16(I["dY"], L.CUBE_A(q))
+    c = t.tp3d_layer_cfg(q, cfg.batch, cfg.seq, h, cfg.heads, cfg.ffn, t.TP3D_BF16, cfg.eps)
+    wsb = t.tp3d_layer_workspace_bytes(c)
+    assert wsb > 0
+    ws = torch.empty(wsb, dtype=torch.uint8, device=device())
+    Y = torch.full((M * h,), float("nan"), dtype=torch.bfloat16, device=device())
+    st = t.tp3d_layer_fwd(ctx, c, params, X, Y, ws)
+    assert st == 0, t.STATUS[st]
+    assert t.tp3d_sync_status(ctx) == 0
+    grads = {k: torch.full_like(v, float("nan")) for k, v in params.items()}
+    dX = torch.full((M * h,), float("nan"), dtype=torch.bfloat16, device=device())
+    st = t.tp3d_layer_bwd(ctx, c, params, X, ws, dY, dX, grads)
+    assert st == 0, t.STATUS[st]
+    assert t.tp3d_sync_status(ctx) == 0
+    # oracle on the same bf16 values, sharded by its own layout maps
+    P64 = {k: S.as_f64(v) for k, v in I.items() if k not in ("X", "dY")}
+    Ps = OY.shard_params(P64, cfg)
+    Xb = L.to_sharded(S.as_f64(I["X"]), L.CUBE_A(q))
+    dYb = L.to_sharded(S.as_f64(I["dY"]), L.CUBE_A(q))
+    return Y, dX, grads, Xb, dYb, Ps
+
+
+def _check(ctx, cfg, seed, perturb, tol=BF16_TOL):
+    Y, dX, grads, Xb, dYb, Ps = _run(ctx, cfg, seed, perturb)
+    want_Y = OY.layer_forward(Xb, Ps, cfg)
+    want_dX, want_g = OY.layer_backward(dYb, Xb, Ps, cfg)
+    pairs = {"Y": (as_np64(Y), want_Y), "dX": (as_np64(dX), want_dX)}
+    for k in want_g:
+        pairs[k] = (as_np64(grads[k]), want_g[k])
+    report, bad = {}, {}
+    for k, (got, want) in pairs.items():
+        assert not np.isnan(got).any(), k
+        e = (max_rel_err(got, want), fro_err(got, want), rel_err(got, want))
+        report[k] = tuple(round(x, 5) for x in e)
+        if not (e[0] <= tol and e[1] <= tol and e[2] <= LAYER_ELEM_TOL):
+            bad[k] = report[k]
+    assert not bad, (bad, report)
+    return report
+
+
+def test_layer_small_perturbed(ctx):
+    cfg = OY.LayerConfig(p=2, batch=2, seq=256, hidden=256, heads=2, ffn=1024)
+    _check(ctx, cfg, 500, perturb=True)
+
+
+def test_layer_small_zero_bias(ctx):
+    cfg = OY.LayerConfig(p=2, batch=2, seq=256, hidden=512, heads=4, ffn=2048)
+    _check(ctx, cfg, 510, perturb=False)
+
+
+def test_layer_q1(ctx):
+    cfg = OY.LayerConfig(p=1, batch=1, seq=384, hidden=256, heads=4, ffn=768)
+    _check(ctx, cfg, 520, perturb=True)
+
+
+def test_layer_q4_head64(ctx):
+    cfg = OY.LayerConfig(p=4, batch=2, seq=1024, hidden=512, heads=8, ffn=2048)
+    _check(ctx, cfg, 530, perturb=True)
+
+
+def test_layer_gpt_b4_s1024_h2048_16heads(ctx):
+    cfg = OY.LayerConfig(p=2, batch=4, seq=1024, hidden=2048, heads=16, ffn=8192)
+    _check(ctx, cfg, S.SEED_BASE + 3, perturb=False)
+
+
+def test_layer_errors_before_launch(ctx):
+    x = torch.zeros(1 << 16, dtype=torch.bfloat16, device=device())
+    params = {k: x for k in t.PARAM_NAMES}
+    bad_seq = t.tp3d_layer_cfg(2, 2, 100, 256, 2, 1024, t.TP3D_BF16, 1e-5)
+    assert t.tp3d_layer_workspace_bytes(bad_seq) == 0
+    assert t.tp3d_layer_fwd(ctx, bad_seq, params, x, x, x) == 7       # seq % 128
+    bad_heads = t.tp3d_layer_cfg(2, 2, 256, 256, 3, 1024, t.TP3D_BF16, 1e-5)
+    assert t.tp3d_layer_fwd(ctx, bad_heads, params, x, x, x) == 2     # hidden % heads
+    bad_dt = t.tp3d_layer_cfg(2, 2, 256, 256, 2, 1024, t.TP3D_F32, 1e-5)
+    assert t.tp3d_layer_fwd(ctx, bad_dt, params, x, x, x) == 4
+    ok = t.tp3d_layer_cfg(2, 2, 256, 256, 2, 1024, t.TP3D_BF16, 1e-5)
+    p2 = dict(params)
+    p2["w_o"] = None
+    assert t.tp3d_layer_fwd(ctx, ok, p2, x, x, x) == 1
+    assert t.tp3d_sync_status(ctx) == 0
