@@ -40,17 +40,19 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "3D-partitioned layer TFLOP/s (% bf16 peak); resharding GB/s (% of HBM)"
-DEFAULT_WORKLOAD = "mlp_q2"
+DEFAULT_WORKLOAD = "layer_q2"
 
 WORKLOADS = {
+    "linear_f32_q2": dict(kind="linear_f32", q=2, M=64, N=64, K=64,
+                          name="3-D linear C=A.B on a q=2 cube (8 virtual devices), M=N=K=64, fp32"),
     "mlp_q2": dict(kind="mlp", q=2, M=2048, h=1024, f=4096,
                    name="Megatron MLP (column-split Linear+GELU, row-split Linear) on a q=2 cube: "
                         "tokens 2048, hidden 1024, ffn 4096, bf16"),
-    "mlp_q4": dict(kind="mlp", q=4, M=8192, h=4096, f=16384,
-                   name="MLP on a q=4 cube (64 virtual devices): tokens 8192, hidden 4096, ffn 16384, bf16"),
     "layer_q2": dict(kind="layer", q=2, batch=4, seq=1024, hidden=2048, heads=16, ffn=8192,
                      name="GPT decoder layer fwd+bwd on a q=2 cube: batch 4, seq 1024, hidden 2048, "
                           "16 heads, ffn 8192, bf16"),
+    "mlp_q4": dict(kind="mlp", q=4, M=8192, h=4096, f=16384,
+                   name="MLP on a q=4 cube (64 virtual devices): tokens 8192, hidden 4096, ffn 16384, bf16"),
     "reshard": dict(kind="reshard", R=8192, C=8192,
                     name="resharding sweep, 8192x8192 bf16, 20 ordered pairs of ROW4 COL4 BLK2x2 CUBE_A(q=2) REP4"),
 }
@@ -59,12 +61,14 @@ WORKLOADS = {
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU baseline sample budget")
-    ap.add_argument("--no-extras", action="store_true", help="skip the reshard sweep and the CPU baseline")
+    ap.add_argument("--no-extras", action="store_true", help="skip the other workloads and the CPU baseline")
+    ap.add_argument("--probe-only", action="store_true",
+                    help="only launch the dominant kernel three times (for profiler captures)")
     return ap.parse_args()
 
 
@@ -130,7 +134,13 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------- workloads
+def _randn(torch, n, dev, g, std=1.0):
+    return (torch.randn(n, device=dev, generator=g) * std).to(torch.bfloat16)
+
+
 class MlpBench:
+    """Config 2 / 4: tp3d_mlp (linear 1 with bias + GELU, linear 2 with bias)."""
+
     def __init__(self, t, ctx, dev, w, seed=20262):
         import torch
         self.t, self.ctx, self.w = t, ctx, w
@@ -138,16 +148,16 @@ class MlpBench:
         g = torch.Generator(device=dev)
         g.manual_seed(seed)
         bf = torch.bfloat16
-        self.X = torch.randn(M * h, device=dev, generator=g).to(bf)
-        self.W1 = (torch.randn(h * f, device=dev, generator=g) * 0.02).to(bf)
-        self.W2 = (torch.randn(f * h, device=dev, generator=g) * 0.02).to(bf)
+        self.X = _randn(torch, M * h, dev, g)
+        self.W1 = _randn(torch, h * f, dev, g, 0.02)
+        self.W2 = _randn(torch, f * h, dev, g, 0.02)
         self.b1 = torch.zeros(f, device=dev, dtype=bf)
         self.b2 = torch.zeros(h, device=dev, dtype=bf)
         self.Y1 = torch.empty(M * f, device=dev, dtype=bf)
         self.Y = torch.empty(M * h, device=dev, dtype=bf)
-        self.flops = 4.0 * M * h * f
+        self.units = 4.0 * M * h * f
         self.launches = 2
-        self.unit = "TFLOP/s"
+        self.unit, self.scale = "TFLOP/s", 1e12
         self.X_host = self.X.cpu().pin_memory()
         self.Y_host = torch.empty(M * h, dtype=bf).pin_memory()
 
@@ -162,17 +172,115 @@ class MlpBench:
         self.Y_host.copy_(self.Y, non_blocking=True)
 
     def e2e_bytes(self):
-        return self.X.numel() * 2, self.Y.numel() * 2
+        return self.X.numel() * 2, self.Y.numel() * 2, "X copied from pinned host memory, tp3d_mlp, Y copied back"
 
     def kernel_probe(self):
-        """(launch callable, algorithmic FLOPs per launch, name) of the dominant kernel."""
         w = self.w
+
         def launch():
             self.t.check(self.t.tp3d_linear(self.ctx, w["q"], 0, w["M"], w["h"], w["f"], self.t.TP3D_BF16, self.X,
                                             self.W1, self.b1, 1, self.Y1), "tp3d_linear")
-        return launch, 2.0 * w["M"] * w["h"] * w["f"], (
-            f"gemm_tc_kernel: 3-D linear 1 of the MLP (M={w['M']}, N={w['h']}, K={w['f']}, q={w['q']}, "
-            f"bias+GELU epilogue), {2.0 * w['M'] * w['h'] * w['f'] / 1e9:.2f} GFLOP per launch")
+        fl = 2.0 * w["M"] * w["h"] * w["f"]
+        return launch, fl, (f"gemm_tc_kernel: 3-D linear 1 of the MLP (M={w['M']}, N={w['h']}, K={w['f']}, "
+                            f"q={w['q']}, bias+GELU epilogue), {fl / 1e9:.2f} GFLOP per launch")
+
+
+class LayerBench:
+    """Config 3: tp3d_layer_fwd + tp3d_layer_bwd of the pre-LN GPT layer."""
+
+    def __init__(self, t, ctx, dev, w, seed=20263):
+        import torch
+        self.t, self.ctx, self.w = t, ctx, w
+        q, b, s, h, H, f = w["q"], w["batch"], w["seq"], w["hidden"], w["heads"], w["ffn"]
+        M = b * s
+        self.M, self.h, self.f, self.q = M, h, f, q
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+        bf = torch.bfloat16
+        shapes = {"w_qkv": h * 3 * h, "w_o": h * h, "w_1": h * f, "w_2": f * h}
+        self.params = {k: _randn(torch, n, dev, g, 0.02) for k, n in shapes.items()}
+        for k, n in (("b_qkv", 3 * h), ("b_o", h), ("b_1", f), ("b_2", h), ("ln1_b", h), ("ln2_b", h)):
+            self.params[k] = torch.zeros(n, device=dev, dtype=bf)
+        for k in ("ln1_g", "ln2_g"):
+            self.params[k] = torch.ones(h, device=dev, dtype=bf)
+        self.grads = {k: torch.empty_like(v) for k, v in self.params.items()}
+        self.X = _randn(torch, M * h, dev, g)
+        self.dY = _randn(torch, M * h, dev, g)
+        self.Y = torch.empty(M * h, device=dev, dtype=bf)
+        self.dX = torch.empty(M * h, device=dev, dtype=bf)
+        self.cfg = t.tp3d_layer_cfg(q, b, s, h, H, f, t.TP3D_BF16, 1e-5)
+        nb = t.tp3d_layer_workspace_bytes(self.cfg)
+        if nb == 0:
+            raise SystemExit("layer configuration rejected")
+        self.ws = torch.empty(nb, device=dev, dtype=torch.uint8)
+        d = h // H
+        lin = 2.0 * M * (3 * h * h + h * h + 2 * h * f)
+        att = 2.0 * (2.0 * s * s * d / 2) * b * H  # causal: the unmasked half of QK^T and PV
+        self.fwd_flops = lin + att
+        self.units = 3 * lin + 3 * att  # backward = twice the forward's products
+        # my kernels per step: forward 9 (2 LN, 6 GEMM, softmax); backward 27
+        # (12 GEMM, 2 LN, softmax, 4 column sums, 8 partial reductions)
+        self.launches = 9 + 27
+        self.unit, self.scale = "TFLOP/s", 1e12
+        self.X_host = self.X.cpu().pin_memory()
+        self.dY_host = self.dY.cpu().pin_memory()
+        self.dX_host = torch.empty(M * h, dtype=bf).pin_memory()
+
+    def fwd(self):
+        self.t.check(self.t.tp3d_layer_fwd(self.ctx, self.cfg, self.params, self.X, self.Y, self.ws), "tp3d_layer_fwd")
+
+    def bwd(self):
+        self.t.check(self.t.tp3d_layer_bwd(self.ctx, self.cfg, self.params, self.X, self.ws, self.dY, self.dX,
+                                           self.grads), "tp3d_layer_bwd")
+
+    def step(self):
+        self.fwd()
+        self.bwd()
+
+    def e2e_step(self):
+        self.X.copy_(self.X_host, non_blocking=True)
+        self.dY.copy_(self.dY_host, non_blocking=True)
+        self.step()
+        self.dX_host.copy_(self.dX, non_blocking=True)
+
+    def e2e_bytes(self):
+        return (2 * self.X.numel() * 2, self.dX.numel() * 2,
+                "X and dY copied from pinned host memory, tp3d_layer_fwd + tp3d_layer_bwd, dX copied back")
+
+    def kernel_probe(self):
+        """The layer's largest GEMM (MLP linear 1 with bias + GELU), same shape and epilogue."""
+        import torch
+        p = self.params
+        Y1 = torch.empty(self.M * self.f, device=self.X.device, dtype=torch.bfloat16)
+
+        def launch():
+            self.t.check(self.t.tp3d_linear(self.ctx, self.q, 0, self.M, self.h, self.f, self.t.TP3D_BF16, self.X,
+                                            p["w_1"], p["b_1"], 1, Y1), "tp3d_linear")
+        fl = 2.0 * self.M * self.h * self.f
+        return launch, fl, (f"gemm_tc_kernel: the layer's MLP linear 1 (M={self.M}, N={self.h}, K={self.f}, "
+                            f"q={self.q}, bias+GELU epilogue), {fl / 1e9:.2f} GFLOP per launch")
+
+
+class LinearF32Bench:
+    """Config 1: tp3d_linear in fp32 on the CUDA cores (latency-bound)."""
+
+    def __init__(self, t, ctx, dev, w, seed=20261):
+        import torch
+        self.t, self.ctx, self.w = t, ctx, w
+        M, N, K = w["M"], w["N"], w["K"]
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+        self.A = torch.randn(M * N, device=dev, generator=g)
+        self.B = torch.randn(N * K, device=dev, generator=g)
+        self.C = torch.empty(M * K, device=dev)
+        self.units = 2.0 * M * N * K
+        self.launches = 1
+        self.unit, self.scale = "GFLOP/s", 1e9
+
+    def step(self):
+        w = self.w
+        self.t.check(self.t.tp3d_linear(self.ctx, w["q"], 0, w["M"], w["N"], w["K"], self.t.TP3D_F32, self.A, self.B,
+                                        None, 0, self.C), "tp3d_linear f32")
 
 
 class ReshardBench:
@@ -196,9 +304,9 @@ class ReshardBench:
         self.pairs = [(a, b) for a in self.lays for b in self.lays if a[0] != b[0]]
         # bytes moved: one full read (a replicated source is read once) + every destination copy written
         self.pair_bytes = [R * C * 2 * (1 + b[2]) for a, b in self.pairs]
-        self.bytes = float(sum(self.pair_bytes))
+        self.units = float(sum(self.pair_bytes))
         self.launches = len(self.pairs)
-        self.unit = "GB/s"
+        self.unit, self.scale = "GB/s", 1e9
 
     def launch_pair(self, k):
         (an, al, _), (bn, bl, _) = self.pairs[k]
@@ -207,6 +315,9 @@ class ReshardBench:
     def step(self):
         for k in range(len(self.pairs)):
             self.launch_pair(k)
+
+
+BENCHES = {"mlp": MlpBench, "layer": LayerBench, "linear_f32": LinearF32Bench, "reshard": ReshardBench}
 
 
 def time_steps(torch, fn, steps, warmup, flush, stream):
@@ -249,7 +360,77 @@ def cpu_baseline_mlp(w, seconds):
     fl = 4.0 * rows * h * f * n
     return {"value": fl / el / 1e12, "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
             "sample": f"{n} x MLP forward on {rows} of {w['M']} token rows (row-separable), float64 numpy, "
-                      f"{el:.1f} s", "seconds": el}
+                      f"{el:.1f} s"}
+
+
+def _oracle_layer_sample(w):
+    import numpy as np
+    from oracle import layer as OY
+
+    cfg = OY.LayerConfig(p=w["q"], batch=1, seq=w["seq"], hidden=w["hidden"], heads=w["heads"], ffn=w["ffn"])
+    rng = np.random.default_rng(0)
+    h, f = cfg.hidden, cfg.ffn
+    P = {k: 0.02 * rng.standard_normal(sh) for k, sh in OY.weight_shapes(cfg).items()}
+    for k, n in (("b_qkv", 3 * h), ("b_o", h), ("b_1", f), ("b_2", h), ("ln1_b", h), ("ln2_b", h)):
+        P[k] = np.zeros(n)
+    P["ln1_g"], P["ln2_g"] = np.ones(h), np.ones(h)
+    X = rng.standard_normal((cfg.M, h))
+    dY = rng.standard_normal((cfg.M, h))
+
+    def run():
+        OY.layer_forward_dense(X, P, cfg)
+        OY.layer_backward_dense(dY, X, P, cfg)
+    return run, float(OY.layer_flops(cfg)["total"]), cfg
+
+
+def cpu_baseline_layer(w, seconds):
+    """The oracle's layer forward + backward on one of the batch's sequences
+    (a bounded sample of the same workload), repeated up to the budget."""
+    run, fl, cfg = _oracle_layer_sample(w)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        run()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or n >= 100:
+            break
+    return {"value": fl * n / el / 1e12, "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"{n} x layer forward + backward on 1 of {w['batch']} sequences (seq {cfg.seq}), float64 "
+                      f"numpy, {el:.1f} s (the oracle's backward recomputes its forward)"}
+
+
+def roofline_probe(torch, wb, steps, flush, stream, pk):
+    launch, fl, kname = wb.kernel_probe()
+    kd = time_steps(torch, launch, max(10, steps), 3, flush, stream)
+    ach = fl / (statistics.mean(kd) / 1e3) / 1e12
+    return {"bound": "tensor", "achieved": ach, "peak": pk["bf16"], "unit": "TFLOP/s", "frac": ach / pk["bf16"],
+            "traffic": None, "kernel": kname, "peak_source": f"bf16_tflops ({pk['source']}, burst)",
+            "launch_ms": statistics.mean(kd)}
+
+
+def reshard_summary(torch, rb, flush, stream, pk, reps=5):
+    per = []
+    for k in range(len(rb.pairs)):
+        d = time_steps(torch, lambda k=k: rb.launch_pair(k), reps, 2, flush, stream)
+        per.append(statistics.median(d))
+    gbs = [rb.pair_bytes[k] / (per[k] / 1e3) / 1e9 for k in range(len(per))]
+    tot = rb.units / (sum(per) / 1e3) / 1e9
+    k_best = max(range(len(per)), key=lambda k: gbs[k])
+    return {
+        "value": tot, "unit": "GB/s", "frac_of_measured_hbm": tot / pk["hbm"], "frac_of_8TBs": tot / 8000.0,
+        "min_pair_gbs": min(gbs), "max_pair_gbs": max(gbs), "ms_per_sweep": sum(per),
+        "pairs": {f"{rb.pairs[k][0][0]}->{rb.pairs[k][1][0]}": round(gbs[k], 1) for k in range(len(gbs))},
+        "roofline": {"bound": "hbm", "achieved": tot, "peak": pk["hbm"], "unit": "GB/s", "frac": tot / pk["hbm"],
+                     "traffic": None, "kernel": "reshard_vec_kernel (sweep average; bytes = read once + every "
+                                                "destination copy written)",
+                     "peak_source": f"hbm_gbs ({pk['source']})"},
+        "workload": WORKLOADS["reshard"]["name"]}
+
+
+def make_bench(t, ctx, dev, name):
+    w = WORKLOADS[name]
+    return BENCHES[w["kind"]](t, ctx, dev, w)
 
 
 def run_ours(args, rank, world, dist):
@@ -265,12 +446,15 @@ def run_ours(args, rank, world, dist):
     flush = torch.empty(256 * 1024 * 1024 // 4, device=dev, dtype=torch.float32)
     w = WORKLOADS[args.workload]
     pk = peaks()
-    if w["kind"] == "mlp":
-        wb = MlpBench(t, ctx, dev, w)
-    elif w["kind"] == "reshard":
-        wb = ReshardBench(t, ctx, dev, w)
-    else:
-        raise SystemExit(f"workload {args.workload} is not available yet")
+    wb = make_bench(t, ctx, dev, args.workload)
+    if args.probe_only:
+        launch, _, _ = wb.kernel_probe()
+        for _ in range(3):
+            launch()
+        torch.cuda.synchronize()
+        t.check(t.tp3d_sync_status(ctx), "probe")
+        t.tp3d_destroy(ctx)
+        return
 
     sampler = ClockSampler(local)
     if rank == 0:
@@ -294,102 +478,110 @@ def run_ours(args, rank, world, dist):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         total_ms = float(tt.item())
     ms = total_ms / args.steps
-    units = wb.flops if w["kind"] != "reshard" else wb.bytes
-    scale = 1e12 if w["kind"] != "reshard" else 1e9
-    value = world * units * args.steps / (total_ms / 1e3) / scale
-
-    # end to end through the public call with host buffers
-    e2e = None
-    if hasattr(wb, "e2e_step"):
-        edurs = time_steps(torch, wb.e2e_step, max(3, args.steps // 2), 2, flush, stream)
-        bi, bo = wb.e2e_bytes()
-        e2e = {"value": units / (statistics.mean(edurs) / 1e3) / scale * world, "unit": wb.unit,
-               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-               "ms_per_step": statistics.mean(edurs),
-               "what": "X copied from pinned host memory, tp3d_mlp, Y copied back, per step"}
-
-    # roofline of the dominant kernel, timed live
-    roof = None
-    if w["kind"] == "mlp":
-        launch, fl, kname = wb.kernel_probe()
-        kd = time_steps(torch, launch, max(10, args.steps), 3, flush, stream)
-        ach = fl / (statistics.mean(kd) / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": ach, "peak": pk["bf16"], "unit": "TFLOP/s", "frac": ach / pk["bf16"],
-                "traffic": None, "kernel": kname, "peak_source": f"bf16_tflops ({pk['source']}, burst)",
-                "launch_ms": statistics.mean(kd)}
-
-    extras = {}
-    if rank == 0 and not args.no_extras and w["kind"] != "reshard":
-        rb = ReshardBench(t, ctx, dev, WORKLOADS["reshard"])
-        per = []
-        for k in range(len(rb.pairs)):
-            d = time_steps(torch, lambda k=k: rb.launch_pair(k), 5, 2, flush, stream)
-            per.append(statistics.median(d))
-        gbs = [rb.pair_bytes[k] / (per[k] / 1e3) / 1e9 for k in range(len(per))]
-        tot = rb.bytes / (sum(per) / 1e3) / 1e9
-        extras["reshard"] = {
-            "value": tot, "unit": "GB/s", "frac_of_measured_hbm": tot / pk["hbm"], "frac_of_8TBs": tot / 8000.0,
-            "min_pair_gbs": min(gbs), "max_pair_gbs": max(gbs),
-            "pairs": {f"{rb.pairs[k][0][0]}->{rb.pairs[k][1][0]}": round(gbs[k], 1) for k in range(len(gbs))},
-            "workload": WORKLOADS["reshard"]["name"], "kernel": "reshard_vec_kernel",
-            "bytes_convention": "read once + every destination copy written"}
-        del rb
+    value = world * wb.units * args.steps / (total_ms / 1e3) / wb.scale
 
     line = {
         "metric": METRIC, "value": value, "unit": wb.unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded device RNG; N(0,1) inputs, N(0,0.02) weights)",
+        "vs_baseline": None, "dtype": "bf16" if w["kind"] != "linear_f32" else "f32",
+        "data": "synthetic (seeded device RNG; N(0,1) inputs, N(0,0.02) weights)",
         "config": {"workload": w["name"], "l2": "flushed between timed steps (256 MiB write outside the events)",
-                   "parallelism": "replicas" if world > 1 else "single GPU, q^3 virtual devices in HBM"},
+                   "parallelism": "replicas (no data-path collective)" if world > 1
+                   else "single GPU, q^3 virtual devices in HBM"},
         "gpu_launches": wb.launches * args.steps,
     }
-    if e2e:
-        line["e2e"] = e2e
-    if roof:
-        line["roofline"] = roof
-    line.update(extras)
+    if w["kind"] == "layer":
+        fd = time_steps(torch, wb.fwd, max(5, args.steps // 2), 2, flush, stream)
+        bd = time_steps(torch, wb.bwd, max(5, args.steps // 2), 2, flush, stream)
+        fwd_ms, bwd_ms = statistics.mean(fd), statistics.mean(bd)
+        line["layer"] = {"fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+                         "avg_step_time_ms_per_sequence": (fwd_ms + bwd_ms) / w["batch"],
+                         "fwd_tflops": wb.fwd_flops / (fwd_ms / 1e3) / 1e12,
+                         "bwd_tflops": (wb.units - wb.fwd_flops) / (bwd_ms / 1e3) / 1e12,
+                         "flops_per_step": wb.units}
+    if hasattr(wb, "e2e_step"):
+        edurs = time_steps(torch, wb.e2e_step, max(3, args.steps // 2), 2, flush, stream)
+        bi, bo, what = wb.e2e_bytes()
+        line["e2e"] = {"value": world * wb.units / (statistics.mean(edurs) / 1e3) / wb.scale, "unit": wb.unit,
+                       "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+                       "ms_per_step": statistics.mean(edurs), "what": what + ", per step"}
+    if hasattr(wb, "kernel_probe"):
+        line["roofline"] = roofline_probe(torch, wb, args.steps, flush, stream, pk)
+    elif w["kind"] == "reshard":
+        line["roofline"] = reshard_summary(torch, wb, flush, stream, pk)["roofline"]
+
+    if rank == 0 and not args.no_extras:
+        extras = {}
+        for name in WORKLOADS:
+            if name == args.workload:
+                continue
+            eb = make_bench(t, ctx, dev, name)
+            if WORKLOADS[name]["kind"] == "reshard":
+                extras[name] = reshard_summary(torch, eb, flush, stream, pk)
+            else:
+                d = time_steps(torch, eb.step, 10, 3, flush, stream)
+                e = {"value": eb.units / (statistics.mean(d) / 1e3) / eb.scale, "unit": eb.unit,
+                     "ms_per_step": statistics.mean(d), "workload": WORKLOADS[name]["name"]}
+                if hasattr(eb, "kernel_probe"):
+                    e["roofline"] = roofline_probe(torch, eb, 10, flush, stream, pk)
+                    e["frac_of_bf16_peak"] = e["value"] / pk["bf16"]
+                extras[name] = e
+            del eb
+            torch.cuda.empty_cache()
+        line["configs"] = extras
+        st = t.tp3d_sync_status(ctx)
+        if st != 0:
+            raise SystemExit(f"device error in the extra workloads: {t.STATUS[st]}")
     if rank == 0:
         line["clocks"] = ClockSampler.summarize(rows, t0, t1) if isinstance(rows, list) else rows
-        if not args.no_extras and w["kind"] == "mlp":
-            line["cpu_baseline"] = cpu_baseline_mlp(w, args.cpu_seconds)
+        if not args.no_extras and w["kind"] in ("mlp", "layer"):
+            line["cpu_baseline"] = (cpu_baseline_layer if w["kind"] == "layer" else cpu_baseline_mlp)(
+                w, args.cpu_seconds)
         print(json.dumps(line), flush=True)
     t.tp3d_destroy(ctx)
 
 
 def run_reference(args, rank):
+    """The reference arm: the fp64 oracle on the host cores, one bounded
+    sample of the workload per step."""
     if rank != 0:
         return
     import numpy as np
-    from oracle import mlp as OM
 
     w = WORKLOADS[args.workload]
-    if w["kind"] != "mlp":
-        print(json.dumps({"impl": "reference", "unavailable": f"oracle arm for {args.workload} not built yet"}))
+    cores = len(os.sched_getaffinity(0))
+    if w["kind"] == "layer":
+        run, fl, cfg = _oracle_layer_sample(w)
+        sample = f"each step: layer forward + backward on 1 of {w['batch']} sequences (seq {cfg.seq}), float64 numpy"
+    elif w["kind"] == "mlp":
+        from oracle import mlp as OM
+        rng = np.random.default_rng(0)
+        h, f, rows = w["h"], w["f"], 256
+        X = rng.standard_normal((rows, h))
+        W1 = 0.02 * rng.standard_normal((h, f))
+        W2 = 0.02 * rng.standard_normal((f, h))
+        b1, b2 = np.zeros(f), np.zeros(h)
+
+        def run():
+            OM.mlp_rows_dense(X, W1, b1, W2, b2)
+        fl = 4.0 * rows * h * f
+        sample = f"each step: MLP forward on {rows} of {w['M']} token rows (row-separable), float64 numpy"
+    else:
+        print(json.dumps({"impl": "reference", "unavailable": f"no oracle arm for {args.workload}"}))
         return
-    rng = np.random.default_rng(0)
-    h, f = w["h"], w["f"]
-    rows = 256
-    X = rng.standard_normal((rows, h))
-    W1 = 0.02 * rng.standard_normal((h, f))
-    W2 = 0.02 * rng.standard_normal((f, h))
-    b1, b2 = np.zeros(f), np.zeros(h)
     for _ in range(args.warmup):
-        OM.mlp_rows_dense(X, W1, b1, W2, b2)
+        run()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        OM.mlp_rows_dense(X, W1, b1, W2, b2)
+        run()
     el = time.perf_counter() - t0
-    fl = 4.0 * rows * h * f * args.steps
-    v = fl / el / 1e12
-    cores = len(os.sched_getaffinity(0))
+    v = fl * args.steps / el / 1e12
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w["name"]},
-        "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": f"each step: MLP forward on {rows} of {w['M']} token rows (row-separable), "
-                                   f"float64 numpy on the host cores"},
+        "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}), flush=True)
 
 
