@@ -39,8 +39,9 @@ struct TcCfg {
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int STAGE_OUT = 4096;  // per epilogue warp: 32 rows x 128 bytes of output staging
   static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + kEpiWarps * STAGE_OUT + BAR_BYTES + 1024;
 };
 
 struct TileInfo {
@@ -135,6 +136,7 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                   const __grid_constant__ CUtensorMap mapC, const __grid_constant__ CUtensorMap mapZ,
                    const GemmProblem P) {
   using Cfg = TcCfg<BN>;
   constexpr int S = Cfg::STAGES;
@@ -142,7 +144,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base_ptr + S * Cfg::STAGE_BYTES);
+  uint8_t* stage_out = base_ptr + S * Cfg::STAGE_BYTES;  // kEpiWarps x 4 KiB, 1024-aligned
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stage_out + kEpiWarps * Cfg::STAGE_OUT);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
@@ -353,14 +356,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // -------------------------------------------------------------- epilogue
     // warp w may read TMEM lanes 32*(w%4) .. +31 only: two warps share each
-    // lane quarter (= 32 rows of the tile) and split its columns in halves
+    // lane quarter (= 32 rows of the tile) and split its columns in halves.
+    // A 32-row x 32-column chunk that lies inside the tile's segment goes out
+    // through this warp's shared-memory staging buffer and one TMA store per
+    // output (64-byte swizzle for bf16 rows of 64 bytes, 128-byte swizzle
+    // for fp32 rows of 128 bytes); a chunk that crosses the segment's edge
+    // is written element-wise under a mask.
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int ew = warp - 2;
+    const int half = ew >> 2;
     const int row = quarter * 32 + lane;
     constexpr int CH = BN / 64;  // 32-column chunks per warp
     uint32_t tc = 0;
     const Grid& cg = P.c.g;
-    const int esz = P.epi.out_f32 ? 4 : 2;
+    const bool f32 = P.epi.out_f32 != 0;
+    uint8_t* stg = stage_out + ew * Cfg::STAGE_OUT;
+    const uint32_t stg_y = smem_u32(stg), stg_z = stg_y + 2048u;
+    bool pending = false;  // a TMA store still reads this warp's staging buffer
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
       TileInfo T;
       decode_tile<BN>(P, t, T);
@@ -379,12 +391,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       const int64_t m = T.m0 + row;
       const bool row_ok = m < T.m_end;
+      const bool rows_full = T.m0 + quarter * 32 + 31 < T.m_end;
       const int64_t gm = m + op_off(P.c.hi1, P.c.lo1, P.c.base1, T.z, P.Hz);
       const int64_t gn0 = T.n0 + op_off(P.c.hi2, P.c.lo2, P.c.base2, T.z, P.Hz);
+      const int64_t cbr = (gm - lane) / cg.bh, cbc = gn0 / cg.bw;  // C block of the warp's rows
       int64_t row_base = 0;
       if (row_ok) {
-        const int64_t br = gm / cg.bh, bc = gn0 / cg.bw;
-        row_base = cg.block_base((int32_t)br, (int32_t)bc) + (gm - br * cg.bh) * cg.bw + (gn0 - bc * cg.bw);
+        const int64_t br = gm / cg.bh;
+        row_base = cg.block_base((int32_t)br, (int32_t)cbc) + (gm - br * cg.bh) * cg.bw + (gn0 - cbc * cg.bw);
       }
 #pragma unroll 1
       for (int cc = 0; cc < CH; ++cc) {
@@ -398,11 +412,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(tempty_bar(buf));
         }
         const int64_t n = T.n0 + ch * 32;
-        if (!row_ok || n >= T.n_end) continue;
+        if (n >= T.n_end) continue;
+        const bool via_tma = rows_full && n + 32 <= T.n_end;
+        if (via_tma && pending) {
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+          pending = false;
+        }
+        if (!via_tma && !row_ok) continue;
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
           const int64_t nv = n + v * 8;
-          if (nv >= T.n_end) break;
+          if (!via_tma && nv >= T.n_end) break;
           const int64_t off = row_base + (nv - T.n0);
           float x[8];
 #pragma unroll
@@ -413,7 +434,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 8; ++e) x[e] += bb[e];
           }
-          if (P.epi.zsave) *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(P.epi.zsave) + off) = pack8(x);
+          if (P.epi.zsave) {
+            const uint4 zv = pack8(x);
+            if (via_tma)
+              *reinterpret_cast<uint4*>(stg + 2048 + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4)) = zv;
+            else
+              *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(P.epi.zsave) + off) = zv;
+          }
           if (P.epi.act == EPI_GELU) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) x[e] = gelu_f(x[e]);
@@ -429,17 +456,42 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 8; ++e) x[e] += rr[e];
           }
-          if (esz == 2) {
-            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(const_cast<void*>(P.c.ptr)) + off) = pack8(x);
+          if (!f32) {
+            const uint4 yv = pack8(x);
+            if (via_tma)
+              *reinterpret_cast<uint4*>(stg + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4)) = yv;
+            else
+              *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(const_cast<void*>(P.c.ptr)) + off) = yv;
           } else {
-            float4* o = reinterpret_cast<float4*>(static_cast<float*>(const_cast<void*>(P.c.ptr)) + off);
-            o[0] = make_float4(x[0], x[1], x[2], x[3]);
-            o[1] = make_float4(x[4], x[5], x[6], x[7]);
+            const float4 lo = make_float4(x[0], x[1], x[2], x[3]), hi = make_float4(x[4], x[5], x[6], x[7]);
+            if (via_tma) {
+              *reinterpret_cast<float4*>(stg + lane * 128 + (((2 * v) ^ (lane & 7)) << 4)) = lo;
+              *reinterpret_cast<float4*>(stg + lane * 128 + (((2 * v + 1) ^ (lane & 7)) << 4)) = hi;
+            } else {
+              float4* o = reinterpret_cast<float4*>(static_cast<float*>(const_cast<void*>(P.c.ptr)) + off);
+              o[0] = lo;
+              o[1] = hi;
+            }
           }
+        }
+        if (via_tma) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const int c0 = (int)(gn0 + (n - T.n0) - cbc * cg.bw);
+            const int c1 = (int)(gm - lane - cbr * cg.bh);
+            const int c2 = cg.shard((int32_t)cbr, (int32_t)cbc);
+            tma_store_3d(&mapC, stg_y, c0, c1, c2);
+            if (P.epi.zsave) tma_store_3d(&mapZ, stg_z, c0, c1, c2);
+            bulk_commit();
+          }
+          pending = true;
         }
       }
       ++tc;
     }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -463,32 +515,42 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 3-D map over a stored bf16 matrix: (column in shard, row in shard, shard).
-tp3d_status make_map(CUtensorMap* m, const Grid& g, const void* ptr, uint32_t box_inner, uint32_t box_rows) {
+// 3-D map over a stored matrix: (column in shard, row in shard, shard).
+tp3d_status make_map(CUtensorMap* m, const Grid& g, const void* ptr, uint32_t box_inner, uint32_t box_rows,
+                     CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, int esz = 2,
+                     CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = encode_fn();
   if (!fn) return TP3D_ECUDA;
   cuuint64_t dims[3] = {(cuuint64_t)g.bw, (cuuint64_t)g.bh, (cuuint64_t)g.nshards()};
-  cuuint64_t strides[2] = {(cuuint64_t)g.bw * 2, (cuuint64_t)(g.bh * g.bw * 2)};
+  cuuint64_t strides[2] = {(cuuint64_t)g.bw * esz, (cuuint64_t)(g.bh * g.bw * esz)};
   cuuint32_t box[3] = {box_inner, box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = fn(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? TP3D_OK : TP3D_ECUDA;
 }
 
 template <int BN>
 tp3d_status launch(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t s) {
   using Cfg = TcCfg<BN>;
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, mc, mz;
   TP3D_TRY(make_map(&ma, P.a.g, P.a.ptr, 64, P.a.mn_major ? 64 : BM));
   TP3D_TRY(make_map(&mb, P.b.g, P.b.ptr, 64, P.b.mn_major ? 64 : BN));
+  // output boxes: 32 rows x 32 columns (64-byte bf16 rows or 128-byte fp32 rows)
+  if (P.epi.out_f32)
+    TP3D_TRY(make_map(&mc, P.c.g, P.c.ptr, 32, 32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, CU_TENSOR_MAP_SWIZZLE_128B));
+  else
+    TP3D_TRY(make_map(&mc, P.c.g, P.c.ptr, 32, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, CU_TENSOR_MAP_SWIZZLE_64B));
+  if (P.epi.zsave)
+    TP3D_TRY(make_map(&mz, P.c.g, P.epi.zsave, 32, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, CU_TENSOR_MAP_SWIZZLE_64B));
+  else
+    mz = mc;
   TP3D_CUDA_TRY(cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM));
   const int64_t tpsM = (P.segM + BM - 1) / BM, tpsN = (P.segN + BN - 1) / BN;
   const int64_t ntiles = (int64_t)P.Z * (P.M / P.segM) * tpsM * (P.N / P.segN) * tpsN;
   if (ntiles <= 0) return TP3D_OK;
   const int grid = (int)(ntiles < ctx->num_sms ? ntiles : ctx->num_sms);
-  gemm_tc_kernel<BN><<<grid, kThreads, Cfg::SMEM, s>>>(ma, mb, P);
+  gemm_tc_kernel<BN><<<grid, kThreads, Cfg::SMEM, s>>>(ma, mb, mc, mz, P);
   return cudaGetLastError() == cudaSuccess ? TP3D_OK : TP3D_ECUDA;
 }
 

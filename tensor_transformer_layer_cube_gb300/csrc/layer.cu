@@ -68,7 +68,6 @@ tp3d_status make_plan(const tp3d_layer_cfg* c, Plan* p) {
   const int64_t m = x.M / q2;
   if ((x.h / q2) % 8 || (x.f / q2) % 8) return TP3D_ESHAPE;
   if (x.d % 64 || x.s % 128 || gcd64(m, x.s) % 128 || ((3 * (int64_t)x.h / x.q) % x.d)) return TP3D_EUNSUPPORTED;
-  if ((int64_t)x.h * 8 > 200 * 1024) return TP3D_EUNSUPPORTED;  // LayerNorm backward's shared-memory partials
   const int64_t M = x.M, h = x.h, f = x.f, Z = x.Z, s = x.s;
   size_t o = 0;
   auto take = [&](size_t bytes) {
@@ -99,7 +98,7 @@ tp3d_status make_plan(const tp3d_layer_cfg* c, Plan* p) {
   Grid gc;
   TP3D_TRY(make_grid(cube(TP3D_CUBE_C, x.q), M, f, &gc));
   const int64_t pc = colsum_parts(gc) * (f > 3 * h ? f : 3 * h);
-  const int64_t pl = (int64_t)ln_bwd_parts(M) * 2 * h;
+  const int64_t pl = colsum_parts(gc) * 2 * h;
   x.part_floats = (size_t)(pc > pl ? pc : pl);
   x.part = take(x.part_floats * 4);
   x.total = o;
@@ -307,11 +306,13 @@ tp3d_status tp3d_layer_bwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_
   TP3D_TRY(run(ctx, G, st));
   TP3D_TRY(plan_dgrad(ctx, q, 0, M, h, f, W(p.dz1), w->w_1, W(p.dxn), &G));                // dLN2 = dZ1 W1^T
   TP3D_TRY(run(ctx, G, st));
-  int np = 0;
+  const int64_t np = colsum_parts(gA);
   TP3D_TRY(launch_ln_bwd(ctx, gA, W(p.dxn), W(p.Hres), (const float*)W(p.mean2), (const float*)W(p.rstd2),
-                         w->ln2_g, dY, W(p.dH), part, part + (int64_t)ln_bwd_parts(M) * h, &np, st));  // dH
+                         w->ln2_g, dY, W(p.dH), st));                                                  // dH
+  TP3D_TRY(launch_ln_param_grads(ctx, gA, W(p.dxn), W(p.Hres), (const float*)W(p.mean2), (const float*)W(p.rstd2),
+                                 part, part + np * h, st));
   TP3D_TRY(launch_reduce_parts(part, np, h, g->ln2_g, st));
-  TP3D_TRY(launch_reduce_parts(part + (int64_t)np * h, np, h, g->ln2_b, st));
+  TP3D_TRY(launch_reduce_parts(part + np * h, np, h, g->ln2_b, st));
 
   // ---- attention block
   TP3D_TRY(colsum(ctx, TP3D_CUBE_A, q, M, h, W(p.dH), part, g->b_o, st));                 // dbo
@@ -369,9 +370,11 @@ tp3d_status tp3d_layer_bwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_
   TP3D_TRY(plan_dgrad(ctx, q, 0, M, h, 3 * h, W(p.dqkv), w->w_qkv, W(p.dxn), &G));         // dLN1 = dQKV Wqkv^T
   TP3D_TRY(run(ctx, G, st));
   TP3D_TRY(launch_ln_bwd(ctx, gA, W(p.dxn), X, (const float*)W(p.mean1), (const float*)W(p.rstd1), w->ln1_g,
-                         W(p.dH), dX, part, part + (int64_t)ln_bwd_parts(M) * h, &np, st));   // dX
+                         W(p.dH), dX, st));                                                            // dX
+  TP3D_TRY(launch_ln_param_grads(ctx, gA, W(p.dxn), X, (const float*)W(p.mean1), (const float*)W(p.rstd1), part,
+                                 part + np * h, st));
   TP3D_TRY(launch_reduce_parts(part, np, h, g->ln1_g, st));
-  return launch_reduce_parts(part + (int64_t)np * h, np, h, g->ln1_b, st);
+  return launch_reduce_parts(part + np * h, np, h, g->ln1_b, st);
 }
 
 }  // extern "C"

@@ -110,13 +110,7 @@ __global__ void __launch_bounds__(kThreads) ln_bwd_kernel(const Grid g, const bf
                                                           const bf16* __restrict__ x, const float* __restrict__ mean,
                                                           const float* __restrict__ rstd,
                                                           const bf16* __restrict__ gamma,
-                                                          const bf16* __restrict__ dres, bf16* __restrict__ dx,
-                                                          float* __restrict__ part_g, float* __restrict__ part_b) {
-  extern __shared__ float sm[];
-  float* sg = sm;
-  float* sb = sm + g.C;
-  for (int64_t c = threadIdx.x; c < 2 * g.C; c += kThreads) sm[c] = 0.0f;
-  __syncthreads();
+                                                          const bf16* __restrict__ dres, bf16* __restrict__ dx) {
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = (int64_t)gridDim.x * kWarps;
   const int64_t vpb = g.bw / 8;
@@ -135,15 +129,11 @@ __global__ void __launch_bounds__(kThreads) ln_bwd_kernel(const Grid g, const bf
         unpack8(dp[v], d);
         unpack8(xp[v], xv);
         unpack8(gp[v], gg);
-        const int64_t c0 = (int64_t)bc * g.bw + v * 8;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const float xh = (xv[e] - mu) * rs;
           const float dxh = d[e] * gg[e];
           a += dxh;
-          b += dxh * xh;
-          atomicAdd(&sg[c0 + e], d[e] * xh);
-          atomicAdd(&sb[c0 + e], d[e]);
+          b += dxh * (xv[e] - mu) * rs;
         }
       }
     }
@@ -163,18 +153,10 @@ __global__ void __launch_bounds__(kThreads) ln_bwd_kernel(const Grid g, const bf
         unpack8(gp[v], gg);
         unpack8(rp[v], rv);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float xh = (xv[e] - mu) * rs;
-          o[e] = rv[e] + rs * (d[e] * gg[e] - a - xh * b);
-        }
+        for (int e = 0; e < 8; ++e) o[e] = rv[e] + rs * (d[e] * gg[e] - a - (xv[e] - mu) * rs * b);
         op[v] = pack8(o);
       }
     }
-  }
-  __syncthreads();
-  for (int64_t c = threadIdx.x; c < g.C; c += kThreads) {
-    part_g[(int64_t)blockIdx.x * g.C + c] = sg[c];
-    part_b[(int64_t)blockIdx.x * g.C + c] = sb[c];
   }
 }
 
@@ -265,39 +247,75 @@ __global__ void __launch_bounds__(kThreads) softmax_bwd_kernel(const bf16* __res
 // CTA (x, y): columns [256 x, +256) over the rows of part y (rows_per_part
 // rows inside one row block); lane l of every warp holds columns 8l..8l+7,
 // warps stride over rows; the 8 warps are summed in shared memory.
+// With mean != nullptr it sums dy * (x - mean) * rstd into part and dy into
+// part2 (the LayerNorm gamma and beta gradients); else it sums x into part.
 __global__ void __launch_bounds__(kThreads) colsum_kernel(const Grid g, const bf16* __restrict__ x,
-                                                          float* __restrict__ part, int64_t rows_per_part) {
+                                                          const bf16* __restrict__ dy,
+                                                          const float* __restrict__ mean,
+                                                          const float* __restrict__ rstd, float* __restrict__ part,
+                                                          float* __restrict__ part2, int64_t rows_per_part) {
   __shared__ float red[kWarps][257];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int64_t c = (int64_t)blockIdx.x * 256 + lane * 8;
   const int64_t r0 = (int64_t)blockIdx.y * rows_per_part;
-  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0}, acc2[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  const bool ln = mean != nullptr;
   if (c < g.C) {
     const int64_t br = r0 / g.bh, bc = c / g.bw;
-    const bf16* base = x + g.block_base((int32_t)br, (int32_t)bc) + (r0 - br * g.bh) * g.bw + (c - bc * g.bw);
+    const int64_t base = g.block_base((int32_t)br, (int32_t)bc) + (r0 - br * g.bh) * g.bw + (c - bc * g.bw);
     for (int64_t rr = w; rr < rows_per_part; rr += kWarps) {
       float f[8];
-      unpack8(*reinterpret_cast<const uint4*>(base + rr * g.bw), f);
+      unpack8(*reinterpret_cast<const uint4*>(x + base + rr * g.bw), f);
+      if (!ln) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] += f[e];
+        for (int e = 0; e < 8; ++e) acc[e] += f[e];
+      } else {
+        float d[8];
+        unpack8(*reinterpret_cast<const uint4*>(dy + base + rr * g.bw), d);
+        const float mu = mean[r0 + rr], rs = rstd[r0 + rr];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          acc[e] += d[e] * (f[e] - mu) * rs;
+          acc2[e] += d[e];
+        }
+      }
     }
   }
+  const int64_t cc = (int64_t)blockIdx.x * 256 + threadIdx.x;
 #pragma unroll
   for (int e = 0; e < 8; ++e) red[w][lane * 8 + e] = acc[e];
   __syncthreads();
   float s = 0.0f;
 #pragma unroll
   for (int k = 0; k < kWarps; ++k) s += red[k][threadIdx.x];
-  const int64_t cc = (int64_t)blockIdx.x * 256 + threadIdx.x;
   if (cc < g.C) part[(int64_t)blockIdx.y * g.C + cc] = s;
+  if (!ln) return;
+  __syncthreads();
+#pragma unroll
+  for (int e = 0; e < 8; ++e) red[w][lane * 8 + e] = acc2[e];
+  __syncthreads();
+  s = 0.0f;
+#pragma unroll
+  for (int k = 0; k < kWarps; ++k) s += red[k][threadIdx.x];
+  if (cc < g.C) part2[(int64_t)blockIdx.y * g.C + cc] = s;
 }
 
+// out[c] = sum over p of part[p][c]: CTA = 32 columns x 8 groups of parts.
 __global__ void __launch_bounds__(kThreads) reduce_parts_kernel(const float* __restrict__ part, int64_t nparts,
                                                                 int64_t C, bf16* __restrict__ out) {
-  for (int64_t c = (int64_t)blockIdx.x * kThreads + threadIdx.x; c < C; c += (int64_t)gridDim.x * kThreads) {
-    float s = 0.0f;
-    for (int64_t p = 0; p < nparts; ++p) s += part[p * C + c];
-    out[c] = __float2bfloat16_rn(s);
+  __shared__ float red[kWarps][33];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int64_t c = (int64_t)blockIdx.x * 32 + tx;
+  float s = 0.0f;
+  if (c < C)
+    for (int64_t p = ty; p < nparts; p += kWarps) s += part[p * C + c];
+  red[ty][tx] = s;
+  __syncthreads();
+  if (ty == 0 && c < C) {
+    float t = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kWarps; ++k) t += red[k][tx];
+    out[c] = __float2bfloat16_rn(t);
   }
 }
 
@@ -319,23 +337,11 @@ tp3d_status launch_ln_fwd(const tp3d_ctx* ctx, const Grid& g, const void* x, con
   return last_error();
 }
 
-int ln_bwd_parts(int64_t R) {
-  const int64_t g = (R + kWarps - 1) / kWarps;
-  return (int)(g < 512 ? g : 512);
-}
-
-tp3d_status launch_ln_bwd(const tp3d_ctx*, const Grid& g, const void* dy, const void* x, const float* mean,
-                          const float* rstd, const void* gamma, const void* dres, void* dx, float* part_g,
-                          float* part_b, int* nparts, cudaStream_t s) {
-  const unsigned grid = (unsigned)ln_bwd_parts(g.R);
-  const size_t smem = (size_t)g.C * 2 * sizeof(float);
-  if (smem > 200 * 1024) return TP3D_EUNSUPPORTED;
-  if (smem > 48 * 1024)
-    TP3D_CUDA_TRY(cudaFuncSetAttribute(ln_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-  ln_bwd_kernel<<<grid, kThreads, smem, s>>>(g, static_cast<const bf16*>(dy), static_cast<const bf16*>(x), mean,
-                                              rstd, static_cast<const bf16*>(gamma), static_cast<const bf16*>(dres),
-                                              static_cast<bf16*>(dx), part_g, part_b);
-  *nparts = (int)grid;
+tp3d_status launch_ln_bwd(const tp3d_ctx* ctx, const Grid& g, const void* dy, const void* x, const float* mean,
+                          const float* rstd, const void* gamma, const void* dres, void* dx, cudaStream_t s) {
+  ln_bwd_kernel<<<grid_for_rows(ctx, g.R, 16), kThreads, 0, s>>>(
+      g, static_cast<const bf16*>(dy), static_cast<const bf16*>(x), mean, rstd, static_cast<const bf16*>(gamma),
+      static_cast<const bf16*>(dres), static_cast<bf16*>(dx));
   return last_error();
 }
 
@@ -351,18 +357,29 @@ tp3d_status launch_softmax_bwd(const tp3d_ctx* ctx, const void* P, const float* 
   return last_error();
 }
 
-int64_t colsum_parts(const Grid& g) { return g.R / gcd64(g.bh, 256); }
+int64_t colsum_parts(const Grid& g) { return g.R / gcd64(g.bh, 64); }
 
-tp3d_status launch_colsum(const tp3d_ctx*, const Grid& g, const void* x, float* part, cudaStream_t s) {
-  const int64_t rpp = gcd64(g.bh, 256);
+static tp3d_status colsum_launch(const Grid& g, const void* x, const void* dy, const float* mean, const float* rstd,
+                                 float* part, float* part2, cudaStream_t s) {
+  const int64_t rpp = gcd64(g.bh, 64);
   const dim3 grid((unsigned)((g.C + 255) / 256), (unsigned)(g.R / rpp));
   if (grid.y > 65535u) return TP3D_EUNSUPPORTED;
-  colsum_kernel<<<grid, kThreads, 0, s>>>(g, static_cast<const bf16*>(x), part, rpp);
+  colsum_kernel<<<grid, kThreads, 0, s>>>(g, static_cast<const bf16*>(x), static_cast<const bf16*>(dy), mean, rstd,
+                                         part, part2, rpp);
   return last_error();
 }
 
+tp3d_status launch_colsum(const tp3d_ctx*, const Grid& g, const void* x, float* part, cudaStream_t s) {
+  return colsum_launch(g, x, nullptr, nullptr, nullptr, part, nullptr, s);
+}
+
+tp3d_status launch_ln_param_grads(const tp3d_ctx*, const Grid& g, const void* dy, const void* x, const float* mean,
+                                  const float* rstd, float* part_g, float* part_b, cudaStream_t s) {
+  return colsum_launch(g, x, dy, mean, rstd, part_g, part_b, s);
+}
+
 tp3d_status launch_reduce_parts(const float* part, int64_t nparts, int64_t C, void* out, cudaStream_t s) {
-  const unsigned grid = (unsigned)((C + kThreads - 1) / kThreads);
+  const unsigned grid = (unsigned)((C + 31) / 32);
   reduce_parts_kernel<<<grid, kThreads, 0, s>>>(part, nparts, C, static_cast<bf16*>(out));
   return last_error();
 }

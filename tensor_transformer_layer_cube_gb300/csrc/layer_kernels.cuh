@@ -15,12 +15,14 @@ tp3d_status launch_ln_fwd(const tp3d_ctx* ctx, const Grid& g, const void* x, con
                           void* y, float* mean, float* rstd, float eps, cudaStream_t s);
 
 // dx = dres + rstd * (dxh - mean(dxh) - xh * mean(dxh * xh)), dxh = dy * gamma,
-// xh = (x - mean) * rstd.  Per-CTA column partial sums of dy * xh (gamma) and
-// dy (beta) go to part_g / part_b, ln_bwd_parts(R) rows of C floats each.
+// xh = (x - mean) * rstd, per row (dy, x, dres, dx in layout g).
 tp3d_status launch_ln_bwd(const tp3d_ctx* ctx, const Grid& g, const void* dy, const void* x, const float* mean,
-                          const float* rstd, const void* gamma, const void* dres, void* dx, float* part_g,
-                          float* part_b, int* nparts, cudaStream_t s);
-int ln_bwd_parts(int64_t R);
+                          const float* rstd, const void* gamma, const void* dres, void* dx, cudaStream_t s);
+
+// LayerNorm parameter gradients as column partial sums: part_g gets
+// sum dy * (x - mean) * rstd, part_b sum dy (colsum_parts(g) rows of C floats).
+tp3d_status launch_ln_param_grads(const tp3d_ctx* ctx, const Grid& g, const void* dy, const void* x,
+                                  const float* mean, const float* rstd, float* part_g, float* part_b, cudaStream_t s);
 
 // Causal softmax over rows of the dense fp32 scores S (Z blocks of s x s):
 // P[i][c] = exp(S[i][c] - max) / sum for c <= i, 0 for i < c < (i/128+1)*128.
