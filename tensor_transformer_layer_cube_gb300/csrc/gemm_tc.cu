@@ -133,6 +133,135 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
   return v;
 }
 
+
+// One tile's epilogue for the calling epilogue warp (32 rows x BN/2 columns
+// of the tile's TMEM accumulator `buf`).  Warp w may read TMEM lanes
+// 32*(w%4) .. +31 only: two warps share each lane quarter (= 32 rows of the
+// tile) and split its columns in halves.  A 32-row x 32-column chunk that
+// lies inside the tile's segment goes out through this warp's shared-memory
+// staging buffer and one TMA store per output (64-byte swizzle for bf16 rows
+// of 64 bytes, 128-byte swizzle for fp32 rows of 128 bytes); a chunk that
+// crosses the segment's edge is written element-wise under a mask.  After
+// its last TMEM load the warp arrives on `tempty` (in the peer CTA when
+// `tempty_remote`, a shared::cluster address).
+template <int BN>
+__device__ __forceinline__ void epilogue_tile(const GemmProblem& P, const TileInfo& T, bool any_k, int buf,
+                                              uint32_t tmem_base, int warp, int lane, uint8_t* stg,
+                                              const CUtensorMap* mapC, const CUtensorMap* mapZ, uint32_t tempty,
+                                              bool tempty_remote, bool& pending) {
+  const int quarter = warp & 3;
+  const int half = (warp - 2) >> 2;
+  const int row = quarter * 32 + lane;
+  constexpr int CH = BN / 64;  // 32-column chunks per warp
+  const Grid& cg = P.c.g;
+  const bool f32 = P.epi.out_f32 != 0;
+  const uint32_t stg_y = smem_u32(stg), stg_z = stg_y + 2048u;
+  const int64_t m = T.m0 + row;
+  const bool row_ok = m < T.m_end;
+  const bool rows_full = T.m0 + quarter * 32 + 31 < T.m_end;
+  const int64_t gm = m + op_off(P.c.hi1, P.c.lo1, P.c.base1, T.z, P.Hz);
+  const int64_t gn0 = T.n0 + op_off(P.c.hi2, P.c.lo2, P.c.base2, T.z, P.Hz);
+  const int64_t cbr = (gm - lane) / cg.bh, cbc = gn0 / cg.bw;  // C block of the warp's rows
+  int64_t row_base = 0;
+  if (row_ok) {
+    const int64_t br = gm / cg.bh;
+    row_base = cg.block_base((int32_t)br, (int32_t)cbc) + (gm - br * cg.bh) * cg.bw + (gn0 - cbc * cg.bw);
+  }
+#pragma unroll 1
+  for (int cc = 0; cc < CH; ++cc) {
+    const int ch = half * CH + cc;
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * BN + ch * 32), r);
+    tmem_ld_wait();
+    if (cc == CH - 1) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (tempty_remote)
+          mbar_arrive_remote(tempty);
+        else
+          mbar_arrive(tempty);
+      }
+    }
+    const int64_t n = T.n0 + ch * 32;
+    if (n >= T.n_end) continue;
+    const bool via_tma = rows_full && n + 32 <= T.n_end;
+    if (via_tma && pending) {
+      if (lane == 0) bulk_wait_read_all();
+      __syncwarp();
+      pending = false;
+    }
+    if (!via_tma && !row_ok) continue;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const int64_t nv = n + v * 8;
+      if (!via_tma && nv >= T.n_end) break;
+      const int64_t off = row_base + (nv - T.n0);
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = any_k ? __uint_as_float(r[v * 8 + e]) * P.epi.alpha : 0.0f;
+      if (P.epi.bias) {
+        float bb[8];
+        unpack8(*reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(P.epi.bias) + (gn0 + (nv - T.n0))), bb);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] += bb[e];
+      }
+      if (P.epi.zsave) {
+        const uint4 zv = pack8(x);
+        if (via_tma)
+          *reinterpret_cast<uint4*>(stg + 2048 + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4)) = zv;
+        else
+          *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(P.epi.zsave) + off) = zv;
+      }
+      if (P.epi.act == EPI_GELU) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = gelu_f(x[e]);
+      } else if (P.epi.act == EPI_GELU_BWD) {
+        float zz[8];
+        unpack8(*reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(P.epi.gin) + off), zz);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] *= gelu_grad_f(zz[e]);
+      }
+      if (P.epi.resid) {
+        float rr[8];
+        unpack8(*reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(P.epi.resid) + off), rr);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] += rr[e];
+      }
+      if (!f32) {
+        const uint4 yv = pack8(x);
+        if (via_tma)
+          *reinterpret_cast<uint4*>(stg + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4)) = yv;
+        else
+          *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(const_cast<void*>(P.c.ptr)) + off) = yv;
+      } else {
+        const float4 lo = make_float4(x[0], x[1], x[2], x[3]), hi = make_float4(x[4], x[5], x[6], x[7]);
+        if (via_tma) {
+          *reinterpret_cast<float4*>(stg + lane * 128 + (((2 * v) ^ (lane & 7)) << 4)) = lo;
+          *reinterpret_cast<float4*>(stg + lane * 128 + (((2 * v + 1) ^ (lane & 7)) << 4)) = hi;
+        } else {
+          float4* o = reinterpret_cast<float4*>(static_cast<float*>(const_cast<void*>(P.c.ptr)) + off);
+          o[0] = lo;
+          o[1] = hi;
+        }
+      }
+    }
+    if (via_tma) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const int c0 = (int)(gn0 + (n - T.n0) - cbc * cg.bw);
+        const int c1 = (int)(gm - lane - cbr * cg.bh);
+        const int c2 = cg.shard((int32_t)cbr, (int32_t)cbc);
+        tma_store_3d(mapC, stg_y, c0, c1, c2);
+        if (P.epi.zsave) tma_store_3d(mapZ, stg_z, c0, c1, c2);
+        bulk_commit();
+      }
+      pending = true;
+    }
+  }
+}
+
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
@@ -355,24 +484,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // -------------------------------------------------------------- epilogue
-    // warp w may read TMEM lanes 32*(w%4) .. +31 only: two warps share each
-    // lane quarter (= 32 rows of the tile) and split its columns in halves.
-    // A 32-row x 32-column chunk that lies inside the tile's segment goes out
-    // through this warp's shared-memory staging buffer and one TMA store per
-    // output (64-byte swizzle for bf16 rows of 64 bytes, 128-byte swizzle
-    // for fp32 rows of 128 bytes); a chunk that crosses the segment's edge
-    // is written element-wise under a mask.
-    const int quarter = warp & 3;
-    const int ew = warp - 2;
-    const int half = ew >> 2;
-    const int row = quarter * 32 + lane;
-    constexpr int CH = BN / 64;  // 32-column chunks per warp
     uint32_t tc = 0;
-    const Grid& cg = P.c.g;
-    const bool f32 = P.epi.out_f32 != 0;
-    uint8_t* stg = stage_out + ew * Cfg::STAGE_OUT;
-    const uint32_t stg_y = smem_u32(stg), stg_z = stg_y + 2048u;
     bool pending = false;  // a TMA store still reads this warp's staging buffer
+    uint8_t* stg = stage_out + (warp - 2) * Cfg::STAGE_OUT;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
       TileInfo T;
       decode_tile<BN>(P, t, T);
@@ -383,111 +497,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int buf = (int)(tc & 1u);
       const uint32_t tph = (tc >> 1) & 1u;
       // one lane waits and the warp follows it, so the warp stays converged
-      // for the .sync.aligned tensor-memory loads below
+      // for the .sync.aligned tensor-memory loads
       bool ok = lane == 0 ? mbar_wait(tfull_bar(buf), tph, abort_flag, P.err) : false;
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       tc_fence_after();
-
-      const int64_t m = T.m0 + row;
-      const bool row_ok = m < T.m_end;
-      const bool rows_full = T.m0 + quarter * 32 + 31 < T.m_end;
-      const int64_t gm = m + op_off(P.c.hi1, P.c.lo1, P.c.base1, T.z, P.Hz);
-      const int64_t gn0 = T.n0 + op_off(P.c.hi2, P.c.lo2, P.c.base2, T.z, P.Hz);
-      const int64_t cbr = (gm - lane) / cg.bh, cbc = gn0 / cg.bw;  // C block of the warp's rows
-      int64_t row_base = 0;
-      if (row_ok) {
-        const int64_t br = gm / cg.bh;
-        row_base = cg.block_base((int32_t)br, (int32_t)cbc) + (gm - br * cg.bh) * cg.bw + (gn0 - cbc * cg.bw);
-      }
-#pragma unroll 1
-      for (int cc = 0; cc < CH; ++cc) {
-        const int ch = half * CH + cc;
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * BN + ch * 32), r);
-        tmem_ld_wait();
-        if (cc == CH - 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(tempty_bar(buf));
-        }
-        const int64_t n = T.n0 + ch * 32;
-        if (n >= T.n_end) continue;
-        const bool via_tma = rows_full && n + 32 <= T.n_end;
-        if (via_tma && pending) {
-          if (lane == 0) bulk_wait_read_all();
-          __syncwarp();
-          pending = false;
-        }
-        if (!via_tma && !row_ok) continue;
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const int64_t nv = n + v * 8;
-          if (!via_tma && nv >= T.n_end) break;
-          const int64_t off = row_base + (nv - T.n0);
-          float x[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = any_k ? __uint_as_float(r[v * 8 + e]) * P.epi.alpha : 0.0f;
-          if (P.epi.bias) {
-            float bb[8];
-            unpack8(*reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(P.epi.bias) + (gn0 + (nv - T.n0))), bb);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] += bb[e];
-          }
-          if (P.epi.zsave) {
-            const uint4 zv = pack8(x);
-            if (via_tma)
-              *reinterpret_cast<uint4*>(stg + 2048 + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4)) = zv;
-            else
-              *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(P.epi.zsave) + off) = zv;
-          }
-          if (P.epi.act == EPI_GELU) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = gelu_f(x[e]);
-          } else if (P.epi.act == EPI_GELU_BWD) {
-            float zz[8];
-            unpack8(*reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(P.epi.gin) + off), zz);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] *= gelu_grad_f(zz[e]);
-          }
-          if (P.epi.resid) {
-            float rr[8];
-            unpack8(*reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(P.epi.resid) + off), rr);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] += rr[e];
-          }
-          if (!f32) {
-            const uint4 yv = pack8(x);
-            if (via_tma)
-              *reinterpret_cast<uint4*>(stg + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4)) = yv;
-            else
-              *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(const_cast<void*>(P.c.ptr)) + off) = yv;
-          } else {
-            const float4 lo = make_float4(x[0], x[1], x[2], x[3]), hi = make_float4(x[4], x[5], x[6], x[7]);
-            if (via_tma) {
-              *reinterpret_cast<float4*>(stg + lane * 128 + (((2 * v) ^ (lane & 7)) << 4)) = lo;
-              *reinterpret_cast<float4*>(stg + lane * 128 + (((2 * v + 1) ^ (lane & 7)) << 4)) = hi;
-            } else {
-              float4* o = reinterpret_cast<float4*>(static_cast<float*>(const_cast<void*>(P.c.ptr)) + off);
-              o[0] = lo;
-              o[1] = hi;
-            }
-          }
-        }
-        if (via_tma) {
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            const int c0 = (int)(gn0 + (n - T.n0) - cbc * cg.bw);
-            const int c1 = (int)(gm - lane - cbr * cg.bh);
-            const int c2 = cg.shard((int32_t)cbr, (int32_t)cbc);
-            tma_store_3d(&mapC, stg_y, c0, c1, c2);
-            if (P.epi.zsave) tma_store_3d(&mapZ, stg_z, c0, c1, c2);
-            bulk_commit();
-          }
-          pending = true;
-        }
-      }
+      epilogue_tile<BN>(P, T, any_k, buf, tmem_base, warp, lane, stg, &mapC, &mapZ, tempty_bar(buf), false, pending);
       ++tc;
     }
     if (lane == 0) bulk_wait_all();
@@ -499,6 +514,287 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ CTA pairs
+// The same GEMM on a cluster of two CTAs (tcgen05 cta_group::2): the pair
+// computes a 256 x 256 tile; CTA r of the pair loads rows [128 r, +128) of
+// A and columns [128 r, +128) of B, the even CTA issues M = 256, N = 256
+// products that read A from each CTA's own shared memory and B from both,
+// and each CTA's tensor memory receives its 128 rows.  Per SM this moves
+// 32 KiB per contraction step instead of 48 KiB (B is loaded once per pair)
+// and leaves room for a 6-deep ring.  Only for problems without a causal
+// mask (both CTAs of a pair run the same contraction range).
+//
+// Barriers: full[s] lives in the even CTA and takes the even producer's
+// expect-tx arrival for both CTAs' bytes plus both CTAs' TMA completions; empty[s] and tfull[b]
+// live in each CTA and are arrived on by the even CTA's commits (multicast
+// to both); tempty[b] lives in the even CTA and takes the arrivals of both
+// CTAs' epilogue warps.
+struct Tc2Cfg {
+  static constexpr int BN = 256;
+  static constexpr int STAGES = 6;
+  static constexpr int A_BYTES = 128 * BK * 2;
+  static constexpr int B_BYTES = 128 * BK * 2;  // this CTA's half of B
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int STAGE_OUT = 4096;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + kEpiWarps * STAGE_OUT + BAR_BYTES + 1024;
+};
+
+__device__ __forceinline__ void decode_pair_tile(const GemmProblem& P, int64_t t, uint32_t rank, TileInfo& T) {
+  const int64_t tpsM = ceil_div(P.segM, 256), tpsN = ceil_div(P.segN, 256);
+  const int64_t tiles_m = (P.M / P.segM) * tpsM;
+  const int64_t per_z = tiles_m * (P.N / P.segN) * tpsN;
+  T.z = (int32_t)(t / per_z);
+  const int64_t r = t - (int64_t)T.z * per_z;
+  const int64_t tn = r / tiles_m, tm = r - tn * tiles_m;
+  const int64_t sm = tm / tpsM, sn = tn / tpsN;
+  T.m0 = sm * P.segM + (tm - sm * tpsM) * 256 + 128 * (int64_t)rank;
+  T.n0 = sn * P.segN + (tn - sn * tpsN) * 256;
+  T.m_end = sm * P.segM + P.segM;
+  T.n_end = sn * P.segN + P.segN;
+}
+
+__device__ __forceinline__ int64_t total_pair_tiles(const GemmProblem& P) {
+  return (int64_t)P.Z * (P.M / P.segM) * ceil_div(P.segM, 256) * (P.N / P.segN) * ceil_div(P.segN, 256);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc2_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                    const __grid_constant__ CUtensorMap mapC, const __grid_constant__ CUtensorMap mapZ,
+                    const GemmProblem P) {
+  using Cfg = Tc2Cfg;
+  constexpr int S = Cfg::STAGES;
+  constexpr int BN = Cfg::BN;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  uint8_t* stage_out = base_ptr + S * Cfg::STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stage_out + kEpiWarps * Cfg::STAGE_OUT);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * S + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * S + 2 + b); };
+  const uint32_t final_bar = bar0 + 8u * (2 * S + 4);
+  auto a_stage = [&](int s) { return base + (uint32_t)(s * Cfg::A_BYTES); };
+  auto b_stage = [&](int s) { return base + (uint32_t)(S * Cfg::A_BYTES + s * Cfg::B_BYTES); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 2 * kEpiWarps);
+    }
+    mbar_init(final_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_holder), Cfg::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&mapA);
+    tma_prefetch_map(&mapB);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any cross-CTA arrival
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  const int64_t ntiles = total_pair_tiles(P);
+  const int64_t nclusters = gridDim.x >> 1, cid = blockIdx.x >> 1;
+  const int32_t segK = (int32_t)P.segK;
+  const int32_t tpsK = (segK + BK - 1) / BK;
+  const int32_t nsegK = (int32_t)(P.K / P.segK);
+  const bool a_mn = P.a.mn_major != 0, b_mn = P.b.mn_major != 0;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- producer
+      uint32_t it = 0;
+      bool ok = true;
+      for (int64_t t = cid; t < ntiles && ok; t += nclusters) {
+        TileInfo T;
+        decode_pair_tile(P, t, rank, T);
+        const int64_t am = T.m0 + op_off(P.a.hi1, P.a.lo1, P.a.base1, T.z, P.Hz);
+        const int64_t ak = op_off(P.a.hi2, P.a.lo2, P.a.base2, T.z, P.Hz);
+        const int64_t bk = op_off(P.b.hi1, P.b.lo1, P.b.base1, T.z, P.Hz);
+        const int64_t bn = T.n0 + 128 * (int64_t)rank + op_off(P.b.hi2, P.b.lo2, P.b.base2, T.z, P.Hz);
+        int64_t a_br = 0, b_br = 0;
+        int a_c1 = 0, b_c1 = 0;
+        int64_t a_bc[2], b_bc[2];
+        int a_c0[2], b_c0[2];
+        if (!a_mn) {
+          a_br = am / P.a.g.bh;
+          a_c1 = (int)(am - a_br * P.a.g.bh);
+        } else {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            a_bc[h] = (am + 64 * h) / P.a.g.bw;
+            a_c0[h] = (int)(am + 64 * h - a_bc[h] * P.a.g.bw);
+          }
+        }
+        if (!b_mn) {
+          b_br = bn / P.b.g.bh;
+          b_c1 = (int)(bn - b_br * P.b.g.bh);
+        } else {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            b_bc[h] = (bn + 64 * h) / P.b.g.bw;
+            b_c0[h] = (int)(bn + 64 * h - b_bc[h] * P.b.g.bw);
+          }
+        }
+        for (int32_t sg = 0; sg < nsegK && ok; ++sg) {
+          const int64_t ks = (int64_t)sg * segK;
+          int a_k = 0, b_k = 0, a_sh = 0, b_sh = 0;
+          int a_shh[2], b_shh[2];
+          if (!a_mn) {
+            const int64_t bc = (ak + ks) / P.a.g.bw;
+            a_k = (int)(ak + ks - bc * P.a.g.bw);
+            a_sh = shard_or_oob(P.a.g, a_br, bc);
+          } else {
+            const int64_t br = (ak + ks) / P.a.g.bh;
+            a_k = (int)(ak + ks - br * P.a.g.bh);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) a_shh[h] = shard_or_oob(P.a.g, br, a_bc[h]);
+          }
+          if (!b_mn) {
+            const int64_t bc = (bk + ks) / P.b.g.bw;
+            b_k = (int)(bk + ks - bc * P.b.g.bw);
+            b_sh = shard_or_oob(P.b.g, b_br, bc);
+          } else {
+            const int64_t br = (bk + ks) / P.b.g.bh;
+            b_k = (int)(bk + ks - br * P.b.g.bh);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) b_shh[h] = shard_or_oob(P.b.g, br, b_bc[h]);
+          }
+          for (int32_t kt = 0; kt < tpsK; ++kt) {
+            const int s = (int)(it % S);
+            const uint32_t ph = (it / S) & 1u;
+            if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, P.err)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = map_to_cta(full_bar(s), 0);
+            // the even CTA expects both CTAs' bytes; the odd CTA's loads may land first
+            // (the transaction count goes negative, the phase cannot end before this arrival)
+            if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * Cfg::STAGE_BYTES);
+            const int kofs = kt * BK;
+            if (!a_mn) {
+              tma_load_3d_pair(a_stage(s), &mapA, fb, a_k + kofs, a_c1, a_sh);
+            } else {
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                tma_load_3d_pair(a_stage(s) + h * 8192u, &mapA, fb, a_c0[h], a_k + kofs, a_shh[h]);
+            }
+            if (!b_mn) {
+              tma_load_3d_pair(b_stage(s), &mapB, fb, b_k + kofs, b_c1, b_sh);
+            } else {
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                tma_load_3d_pair(b_stage(s) + h * 8192u, &mapB, fb, b_c0[h], b_k + kofs, b_shh[h]);
+            }
+            ++it;
+          }
+        }
+      }
+      if (!ok && leader) {
+        // drain: every load of both CTAs completes on the even CTA's full barriers
+        const uint32_t first = it > (uint32_t)S ? it - S : 0u;
+        for (uint32_t j = first; j < it; ++j) mbar_wait_drain(full_bar((int)(j % S)), (j / S) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ---------------------------------------------------------- MMA issuer (even CTA)
+      const uint32_t idesc = idesc_bf16_f32(256, BN, a_mn ? 1 : 0, b_mn ? 1 : 0);
+      uint32_t it = 0, tc = 0;
+      bool ok = true;
+      for (int64_t t = cid; t < ntiles && ok; t += nclusters) {
+        const int buf = (int)(tc & 1u);
+        const uint32_t tph = (tc >> 1) & 1u;
+        if (!mbar_wait(tempty_bar(buf), tph ^ 1u, abort_flag, P.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+        bool first = true;
+        for (int32_t sg = 0; sg < nsegK && ok; ++sg) {
+          for (int32_t kt = 0; kt < tpsK; ++kt) {
+            const int s = (int)(it % S);
+            const uint32_t ph = (it / S) & 1u;
+            if (!mbar_wait(full_bar(s), ph, abort_flag, P.err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int k16 = 0; k16 < BK / 16; ++k16) {
+              const uint64_t ad = a_mn ? smem_desc_sw128(a_stage(s) + k16 * 2048u, 8192u, 1024u)
+                                       : smem_desc_sw128(a_stage(s) + k16 * 32u, 16u, 1024u);
+              const uint64_t bd = b_mn ? smem_desc_sw128(b_stage(s) + k16 * 2048u, 8192u, 1024u)
+                                       : smem_desc_sw128(b_stage(s) + k16 * 32u, 16u, 1024u);
+              umma_bf16_pair(d_tmem, ad, bd, idesc, (first && k16 == 0) ? 0u : 1u);
+            }
+            first = false;
+            umma_commit_pair_mc(empty_bar(s), 3);
+            ++it;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair_mc(tfull_bar(buf), 3);
+        ++tc;
+      }
+      // every product issued must finish before the pair frees its TMEM
+      umma_commit_pair_mc(final_bar, 1);
+      mbar_wait_drain(final_bar, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    uint32_t tc = 0;
+    bool pending = false;
+    uint8_t* stg = stage_out + (warp - 2) * Cfg::STAGE_OUT;
+    for (int64_t t = cid; t < ntiles; t += nclusters) {
+      TileInfo T;
+      decode_pair_tile(P, t, rank, T);
+      const int buf = (int)(tc & 1u);
+      const uint32_t tph = (tc >> 1) & 1u;
+      bool ok = lane == 0 ? mbar_wait(tfull_bar(buf), tph, abort_flag, P.err) : false;
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      tc_fence_after();
+      epilogue_tile<BN>(P, T, true, buf, tmem_base, warp, lane, stg, &mapC, &mapZ, map_to_cta(tempty_bar(buf), 0),
+                        true, pending);
+      ++tc;
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // neither CTA frees the pair's TMEM or barriers while the other still uses them
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
   }
 }
 
@@ -554,6 +850,44 @@ tp3d_status launch(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t s) {
   return cudaGetLastError() == cudaSuccess ? TP3D_OK : TP3D_ECUDA;
 }
 
+tp3d_status launch_pair(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t s) {
+  using Cfg = Tc2Cfg;
+  CUtensorMap ma, mb, mc, mz;
+  TP3D_TRY(make_map(&ma, P.a.g, P.a.ptr, 64, P.a.mn_major ? 64 : 128));
+  TP3D_TRY(make_map(&mb, P.b.g, P.b.ptr, 64, P.b.mn_major ? 64 : 128));
+  if (P.epi.out_f32)
+    TP3D_TRY(make_map(&mc, P.c.g, P.c.ptr, 32, 32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, CU_TENSOR_MAP_SWIZZLE_128B));
+  else
+    TP3D_TRY(make_map(&mc, P.c.g, P.c.ptr, 32, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, CU_TENSOR_MAP_SWIZZLE_64B));
+  if (P.epi.zsave)
+    TP3D_TRY(make_map(&mz, P.c.g, P.epi.zsave, 32, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, CU_TENSOR_MAP_SWIZZLE_64B));
+  else
+    mz = mc;
+  TP3D_CUDA_TRY(cudaFuncSetAttribute(gemm_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM));
+  const int64_t ntiles = (int64_t)P.Z * (P.M / P.segM) * ((P.segM + 255) / 256) * (P.N / P.segN) *
+                         ((P.segN + 255) / 256);
+  if (ntiles <= 0) return TP3D_OK;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg::SMEM;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int max_clusters = 0;
+  cfg.gridDim = dim3(2 * (unsigned)(ctx->num_sms / 2));
+  if (cudaOccupancyMaxActiveClusters(&max_clusters, gemm_tc2_kernel, &cfg) != cudaSuccess || max_clusters < 1)
+    max_clusters = ctx->num_sms / 2;
+  const int64_t nc = ntiles < max_clusters ? ntiles : max_clusters;
+  cfg.gridDim = dim3(2 * (unsigned)nc);
+  TP3D_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_tc2_kernel, ma, mb, mc, mz, P));
+  return TP3D_OK;
+}
+
 }  // namespace
 
 tp3d_status gemm_bf16_tc(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t s) {
@@ -571,6 +905,14 @@ tp3d_status gemm_bf16_tc(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t
     const int64_t kb = P.b.mn_major ? P.b.g.bh : P.b.g.bw;
     if (ka != P.segK && kb != P.segK) return TP3D_EUNSUPPORTED;
   }
+  // CTA pairs (256 x 256 tiles) when there is no causal mask, the segments
+  // hold whole 256-row / 256-column pair tiles, and the pair tiles fill the
+  // GPU; else one CTA per tile, 128 x 256 or, for narrow or small problems,
+  // 128 x 128.
+  const int64_t pair_tiles = (int64_t)P.Z * (P.M / P.segM) * ((P.segM + 255) / 256) * (P.N / P.segN) *
+                             ((P.segN + 255) / 256);
+  if (P.causal == CAUSAL_NONE && P.segM >= 256 && P.segN >= 256 && pair_tiles >= ctx->num_sms / 2)
+    return launch_pair(ctx, P, s);
   const int64_t tiles256 = (int64_t)P.Z * (P.M / P.segM) * ((P.segM + BM - 1) / BM) * (P.N / P.segN) * ((P.segN + 255) / 256);
   const bool narrow = P.segN <= 128 || tiles256 < ctx->num_sms;
   return narrow ? launch<128>(ctx, P, s) : launch<256>(ctx, P, s);

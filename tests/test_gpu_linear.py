@@ -60,6 +60,7 @@ def test_linear_bf16_parity(ctx, q, M, N, K, y):
 
 
 @pytest.mark.parametrize("q,M,N,K", [
+    (2, 4000, 1040, 4192),   # large enough for CTA pairs: 1000-row shards, 520 / 1048-wide blocks
     (2, 800, 192, 416),      # m = 200 rows, contraction block 96, weight block 104: ragged everywhere
     (2, 4 * 136, 2 * 72, 4 * 264),
     (3, 9 * 72, 3 * 80, 9 * 40),
