@@ -218,10 +218,10 @@ class LayerBench:
         att = 2.0 * (2.0 * s * s * d / 2) * b * H  # causal: the unmasked half of QK^T and PV
         self.fwd_flops = lin + att
         self.units = 3 * lin + 3 * att  # backward = twice the forward's products
-        # my kernels per step: forward 9 (2 LN, 6 GEMM, softmax); backward 29
-        # (12 GEMM, 2 LN rows, 2 LN column sums, softmax, 4 bias column sums,
-        # 8 partial reductions)
-        self.launches = 9 + 29
+        # my kernels per step: forward 7 (2 LN, 4 GEMM, attention); backward 28
+        # (8 GEMM, 3 attention, 2 LN rows, 2 LN column sums, 4 bias column
+        # sums, 8 partial reductions)
+        self.launches = 7 + 28
         self.unit, self.scale = "TFLOP/s", 1e12
         self.X_host = self.X.cpu().pin_memory()
         self.dY_host = self.dY.cpu().pin_memory()

@@ -1,0 +1,740 @@
+// attention.cu - fused causal attention of the GPT layer on the cube.
+//
+// "Maximizing Parallelism in Distributed Training for Huge Neural Networks"
+// §3.2 puts a Self-Attention block between the two 3-D linears of the first
+// block; its core is not partitioned by the page.  Here the heads are read in
+// place from the CUBE_C shards of the QKV matrix (the output layout of the
+// first linear): head t of sequence b is the window rows [b*s, +s) x columns
+// [t*d, +d) (Q), [h + t*d, +d) (K), [2h + t*d, +d) (V).
+//
+// Three tcgen05 kernels, 128-row tiles, one CTA per work item, warp 0 = TMA
+// producer, warp 1 = MMA issuer (and TMEM owner), warps 2-5 = one thread per
+// tile row (TMEM lane) for the softmax arithmetic:
+//  * forward: per query tile, pass 1 runs S = Q K^T over the key tiles at or
+//    below the diagonal and keeps the row maximum and sum (online, in
+//    registers); pass 2 recomputes S, writes P = exp(S - m) / l (bf16) to
+//    shared memory and accumulates O += P V in tensor memory; the row's
+//    log-sum-exp is saved for the backward.  No rescaling of O is needed.
+//  * backward dK/dV: per key tile, over the query tiles at or above the
+//    diagonal: S^T = K Q^T, dP^T = V dO^T, P^T = exp(S^T - lse), then
+//    dV += P^T dO and dK += dS^T Q with dS = P (dP - rowsum(dO O)) / sqrt(d).
+//  * backward dQ: per query tile, over the key tiles at or below the
+//    diagonal: S, dP, dS as above, dQ += dS K.
+// The score and probability matrices never leave the SM.  Every mbarrier
+// wait is bounded; a wait that runs out sets the error word and the CTA
+// returns.
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include "attention.cuh"
+
+namespace tp3d {
+
+namespace {
+
+constexpr int TR = 128;              // rows of a tile (queries or keys)
+constexpr int kThreads = 192;        // 6 warps
+constexpr int kComputeWarps = 4;     // warps 2..5
+constexpr uint32_t kChunk = 16384;   // 128 rows x 64 bf16 columns (one 128-byte swizzle span)
+constexpr uint32_t kTile = 2 * kChunk;  // a 128 x 128 bf16 tile
+constexpr int kSmem = 7 * kTile + 512 + 1024;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+using bf16 = __nv_bfloat16;
+
+struct Ctx {
+  uint32_t base;       // 1024-aligned shared address of the tile area
+  uint8_t* base_ptr;
+  uint32_t bar0;       // first mbarrier
+  volatile int* abort_flag;
+  uint32_t* tmem_holder;
+};
+
+__device__ __forceinline__ Ctx setup_smem(uint8_t* smem_raw) {
+  Ctx c;
+  const uint32_t raw = smem_u32(smem_raw);
+  c.base = (raw + 1023u) & ~1023u;
+  c.base_ptr = smem_raw + (c.base - raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(c.base_ptr + 7 * kTile);
+  c.bar0 = smem_u32(bars);
+  c.tmem_holder = reinterpret_cast<uint32_t*>(bars + 40);
+  c.abort_flag = reinterpret_cast<volatile int*>(c.tmem_holder + 1);
+  return c;
+}
+
+// TMA of a 128-row x d-column window at global (row0, col0) of a matrix with
+// grid g (the window lies inside one shard): d / 64 boxes of 64 columns.
+__device__ __forceinline__ void load_tile(const CUtensorMap* m, const Grid& g, int64_t row0, int64_t col0, int nch,
+                                          uint32_t dst, uint32_t bar) {
+  const int64_t br = row0 / g.bh, bc = col0 / g.bw;
+  const int sh = g.shard((int32_t)br, (int32_t)bc);
+  const int c1 = (int)(row0 - br * g.bh), c0 = (int)(col0 - bc * g.bw);
+  for (int c = 0; c < nch; ++c) tma_load_3d(dst + c * kChunk, m, bar, c0 + 64 * c, c1, sh);
+}
+
+// descriptors of a 128-row tile stored as 64-column swizzled chunks
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int k16) {  // contraction along the columns
+  return smem_desc_sw128(tile + (uint32_t)(k16 >> 2) * kChunk + (uint32_t)(k16 & 3) * 32u, 16u, 1024u);
+}
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int k16) {  // contraction along the rows
+  return smem_desc_sw128(tile + (uint32_t)k16 * 2048u, kChunk, 1024u);
+}
+
+// 8 bf16 values for columns [8 g, +8) of row r of a K-major 128 x 128 tile
+__device__ __forceinline__ void st_tile8(uint8_t* tile, int r, int g, uint4 v) {
+  *reinterpret_cast<uint4*>(tile + (g >> 3) * kChunk + r * 128 + (((g & 7) ^ (r & 7)) << 4)) = v;
+}
+
+__device__ __forceinline__ uint4 pack8f(const float* f) {
+  uint4 v;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+  return v;
+}
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Ctx& c, int* err, int lane) {
+  bool ok = lane == 0 ? mbar_wait(bar, parity, c.abort_flag, err) : false;
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+__device__ __forceinline__ void warp_arrive(uint32_t bar, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+}
+
+__device__ __forceinline__ uint32_t tmem_row(uint32_t tmem, int quarter, uint32_t col) {
+  return tmem + ((uint32_t)(quarter * 32) << 16) + col;
+}
+
+// store 32 fp32 values as bf16 to global row pointer + column offset (16-byte aligned)
+__device__ __forceinline__ void store_row32(bf16* dst, const uint32_t (&r)[32]) {
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    float f[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(r[v * 8 + e]);
+    *reinterpret_cast<uint4*>(dst + v * 8) = pack8f(f);
+  }
+}
+
+__device__ __forceinline__ void mma_tile(uint32_t d_tmem, uint32_t a_tile, bool a_mn, uint32_t b_tile, bool b_mn,
+                                         int ksteps, uint32_t idesc, bool accumulate) {
+  for (int k = 0; k < ksteps; ++k) {
+    const uint64_t ad = a_mn ? desc_mnmajor(a_tile, k) : desc_kmajor(a_tile, k);
+    const uint64_t bd = b_mn ? desc_mnmajor(b_tile, k) : desc_kmajor(b_tile, k);
+    umma_bf16(d_tmem, ad, bd, idesc, (accumulate || k > 0) ? 1u : 0u);
+  }
+}
+
+__device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) {
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return;
+}
+
+// ------------------------------------------------------------------ forward
+// smem: Q | K0 V0 | K1 V1 | P0 | P1 (32 KiB each)
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap mqkv, const AttnProblem A, bf16* __restrict__ O,
+                    float* __restrict__ lse) {
+  extern __shared__ uint8_t smem_raw[];
+  const Ctx c = setup_smem(smem_raw);
+  const uint32_t sQ = c.base, sK[2] = {c.base + kTile, c.base + 3 * kTile}, sV[2] = {c.base + 2 * kTile, c.base + 4 * kTile};
+  const uint32_t sP[2] = {c.base + 5 * kTile, c.base + 6 * kTile};
+  uint8_t* pP[2] = {c.base_ptr + 5 * kTile, c.base_ptr + 6 * kTile};
+  auto bar = [&](int k) { return c.bar0 + 8u * k; };
+  const uint32_t q_full = bar(0), o_full = bar(1);
+  auto kv_full = [&](int s) { return bar(2 + s); };
+  auto kv_empty = [&](int s) { return bar(4 + s); };
+  auto s_full = [&](int b) { return bar(6 + b); };
+  auto s_empty = [&](int b) { return bar(8 + b); };
+  auto p_full = [&](int b) { return bar(10 + b); };
+  auto p_empty = [&](int b) { return bar(12 + b); };
+  const uint32_t final_bar = bar(14);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t nq = A.s / TR;
+  const int64_t z = blockIdx.x / nq, it_q = nq - 1 - (blockIdx.x % nq);  // longest rows first
+  const int64_t b = z / A.H, t = z % A.H;
+  const int nkv = (int)it_q + 1;
+  const int nch = (int)(A.d / 64);
+  const uint32_t dbytes = (uint32_t)(A.d * TR * 2);
+
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < 15; ++k)
+      mbar_init(bar(k), (k == 8 || k == 9 || k == 10 || k == 11) ? kComputeWarps : 1);
+    *c.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(c.tmem_holder), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *c.tmem_holder;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const int64_t row_q = b * A.s + it_q * TR;
+      mbar_arrive_expect_tx(q_full, dbytes);
+      load_tile(&mqkv, A.qkv, row_q, t * A.d, nch, sQ, q_full);
+      bool ok = true;
+      for (int n = 0; n < 2 * nkv && ok; ++n) {
+        const int j = n < nkv ? n : n - nkv;
+        const bool with_v = n >= nkv;
+        const int s = n & 1;
+        if (!mbar_wait(kv_empty(s), ((n >> 1) & 1) ^ 1, c.abort_flag, A.err)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(kv_full(s), with_v ? 2 * dbytes : dbytes);
+        const int64_t row_k = b * A.s + (int64_t)j * TR;
+        load_tile(&mqkv, A.qkv, row_k, A.h + t * A.d, nch, sK[s], kv_full(s));
+        if (with_v) load_tile(&mqkv, A.qkv, row_k, 2 * A.h + t * A.d, nch, sV[s], kv_full(s));
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16_f32(TR, TR, 0, 0);
+      const uint32_t id_o = idesc_bf16_f32(TR, (int)A.d, 0, 1);
+      const int ks_d = (int)(A.d / 16);
+      bool ok = mbar_wait(q_full, 0, c.abort_flag, A.err);
+      int n = 0, sc = 0, pc = 0;
+      // S_n = Q K^T for ring entry n into S buffer sc % 2
+      auto issue_s = [&](int nn) -> bool {
+        const int s = nn & 1;
+        if (!mbar_wait(kv_full(s), (nn >> 1) & 1, c.abort_flag, A.err)) return false;
+        const int sb = sc & 1;
+        if (!mbar_wait(s_empty(sb), ((sc >> 1) & 1) ^ 1, c.abort_flag, A.err)) return false;
+        tc_fence_after();
+        mma_tile(tmem + (uint32_t)(sb * TR), sQ, false, sK[s], false, ks_d, id_s, false);
+        umma_commit(s_full(sb));
+        ++sc;
+        return true;
+      };
+      for (; n < nkv && ok; ++n) {  // pass 1: scores only
+        ok = issue_s(n);
+        if (ok) umma_commit(kv_empty(n & 1));
+      }
+      if (ok) ok = issue_s(nkv);
+      for (int j = 0; j < nkv && ok; ++j) {  // pass 2
+        if (j + 1 < nkv) ok = issue_s(nkv + j + 1);
+        if (!ok) break;
+        const int pb = pc & 1;
+        if (!mbar_wait(p_full(pb), (pc >> 1) & 1, c.abort_flag, A.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        mma_tile(tmem + 256u, sP[pb], false, sV[(nkv + j) & 1], true, TR / 16, id_o, j > 0);
+        umma_commit(p_empty(pb));
+        umma_commit(kv_empty((nkv + j) & 1));
+        ++pc;
+      }
+      if (ok) umma_commit(o_full);
+      umma_commit(final_bar);
+      drain(final_bar, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax rows
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const float sl2 = A.scale * kLog2e;
+    float m = -INFINITY, l = 0.0f;
+    int sc = 0, pc = 0;
+    bool ok = true;
+    for (int j = 0; j < nkv && ok; ++j) {  // pass 1: row max and sum
+      const int sb = sc & 1;
+      if (!(ok = warp_wait(s_full(sb), (sc >> 1) & 1, c, A.err, lane))) break;
+      tc_fence_after();
+      const bool diag = j == nkv - 1;
+#pragma unroll 1
+      for (int cc = 0; cc < TR / 32; ++cc) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(sb * TR + cc * 32)), v);
+        tmem_ld_wait();
+        float mx = m;
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (!diag || cc * 32 + e <= r) mx = fmaxf(mx, __uint_as_float(v[e]) * sl2);
+        float sum = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (!diag || cc * 32 + e <= r) sum += exp2f(__uint_as_float(v[e]) * sl2 - mx);
+        l = l * exp2f(m - mx) + sum;
+        m = mx;
+      }
+      tc_fence_before();
+      warp_arrive(s_empty(sb), lane);
+      ++sc;
+    }
+    const float inv_l = 1.0f / l;
+    for (int j = 0; j < nkv && ok; ++j) {  // pass 2: P = exp(S - m) / l into shared memory
+      const int sb = sc & 1, pb = pc & 1;
+      if (!(ok = warp_wait(s_full(sb), (sc >> 1) & 1, c, A.err, lane))) break;
+      if (!(ok = warp_wait(p_empty(pb), ((pc >> 1) & 1) ^ 1, c, A.err, lane))) break;
+      tc_fence_after();
+      const bool diag = j == nkv - 1;
+#pragma unroll 1
+      for (int cc = 0; cc < TR / 32; ++cc) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(sb * TR + cc * 32)), v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int col = cc * 32 + g * 8 + e;
+            f[e] = (!diag || col <= r) ? exp2f(__uint_as_float(v[g * 8 + e]) * sl2 - m) * inv_l : 0.0f;
+          }
+          st_tile8(pP[pb], r, cc * 4 + g, pack8f(f));
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      warp_arrive(p_full(pb), lane);
+      warp_arrive(s_empty(sb), lane);
+      ++sc;
+      ++pc;
+    }
+    if (ok) ok = warp_wait(o_full, 0, c, A.err, lane);
+    if (ok) {
+      tc_fence_after();
+      const int64_t grow = b * A.s + it_q * TR + r;
+      const int64_t gcol = t * A.d;
+      const int64_t br = grow / A.o.bh, bc = gcol / A.o.bw;
+      bf16* dst = O + A.o.block_base((int32_t)br, (int32_t)bc) + (grow - br * A.o.bh) * A.o.bw + (gcol - bc * A.o.bw);
+      for (int cc = 0; cc < (int)(A.d / 32); ++cc) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem_row(tmem, quarter, 256u + cc * 32), v);
+        tmem_ld_wait();
+        store_row32(dst + cc * 32, v);
+      }
+      lse[z * A.s + it_q * TR + r] = (m + log2f(l)) * kLn2;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------------ backward: dK, dV
+// smem: K | V | Q0 dO0 | Q1 dO1 | PdS (32 KiB each); PdS holds P^T, then dS^T
+// TMEM: S^T [0,128) dP^T [128,256) dV [256,256+d) dK [256+d, 256+2d)
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mqkv, const __grid_constant__ CUtensorMap mo,
+                         const AttnProblem A, const float* __restrict__ lse, const float* __restrict__ delta,
+                         bf16* __restrict__ dqkv) {
+  extern __shared__ uint8_t smem_raw[];
+  const Ctx c = setup_smem(smem_raw);
+  const uint32_t sK = c.base, sV = c.base + kTile;
+  const uint32_t sQ[2] = {c.base + 2 * kTile, c.base + 4 * kTile}, sdO[2] = {c.base + 3 * kTile, c.base + 5 * kTile};
+  const uint32_t sPdS = c.base + 6 * kTile;
+  uint8_t* pPdS = c.base_ptr + 6 * kTile;
+  auto bar = [&](int k) { return c.bar0 + 8u * k; };
+  const uint32_t kv_full = bar(0), st_full = bar(1), st_empty = bar(2), pds_full = bar(3), pds_empty = bar(4),
+                 acc_full = bar(5), final_bar = bar(6);
+  auto r_full = [&](int s) { return bar(7 + s); };
+  auto r_empty = [&](int s) { return bar(9 + s); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t nq = A.s / TR;
+  const int64_t z = blockIdx.x / nq, jk = blockIdx.x % nq;  // key tile; the most query tiles first
+  const int64_t b = z / A.H, t = z % A.H;
+  const int niter = (int)(nq - jk);
+  const int nch = (int)(A.d / 64);
+  const uint32_t dbytes = (uint32_t)(A.d * TR * 2);
+
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < 11; ++k) mbar_init(bar(k), (k == 2 || k == 3) ? kComputeWarps : 1);
+    *c.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(c.tmem_holder), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *c.tmem_holder;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const int64_t row_k = b * A.s + jk * TR;
+      mbar_arrive_expect_tx(kv_full, 2 * dbytes);
+      load_tile(&mqkv, A.qkv, row_k, A.h + t * A.d, nch, sK, kv_full);
+      load_tile(&mqkv, A.qkv, row_k, 2 * A.h + t * A.d, nch, sV, kv_full);
+      for (int it = 0; it < niter; ++it) {
+        const int s = it & 1;
+        if (!mbar_wait(r_empty(s), ((it >> 1) & 1) ^ 1, c.abort_flag, A.err)) break;
+        mbar_arrive_expect_tx(r_full(s), 2 * dbytes);
+        const int64_t row_q = b * A.s + (jk + it) * TR;
+        load_tile(&mqkv, A.qkv, row_q, t * A.d, nch, sQ[s], r_full(s));
+        load_tile(&mo, A.o, row_q, t * A.d, nch, sdO[s], r_full(s));
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16_f32(TR, TR, 0, 0);
+      const uint32_t id_acc = idesc_bf16_f32(TR, (int)A.d, 0, 1);
+      const int ks_d = (int)(A.d / 16);
+      bool ok = mbar_wait(kv_full, 0, c.abort_flag, A.err);
+      for (int it = 0; it < niter && ok; ++it) {
+        const int s = it & 1;
+        if (!(ok = mbar_wait(r_full(s), (it >> 1) & 1, c.abort_flag, A.err))) break;
+        if (!(ok = mbar_wait(st_empty, (it & 1) ^ 1, c.abort_flag, A.err))) break;
+        tc_fence_after();
+        mma_tile(tmem, sK, false, sQ[s], false, ks_d, id_s, false);          // S^T = K Q^T
+        mma_tile(tmem + 128u, sV, false, sdO[s], false, ks_d, id_s, false);  // dP^T = V dO^T
+        umma_commit(st_full);
+        if (!(ok = mbar_wait(pds_full, 0, c.abort_flag, A.err))) break;
+        tc_fence_after();
+        mma_tile(tmem + 256u, sPdS, false, sdO[s], true, TR / 16, id_acc, it > 0);  // dV += P^T dO
+        umma_commit(pds_empty);
+        if (!(ok = mbar_wait(pds_full, 1, c.abort_flag, A.err))) break;
+        tc_fence_after();
+        mma_tile(tmem + 256u + (uint32_t)A.d, sPdS, false, sQ[s], true, TR / 16, id_acc, it > 0);  // dK += dS^T Q
+        umma_commit(pds_empty);
+        umma_commit(r_empty(s));
+      }
+      if (ok) umma_commit(acc_full);
+      umma_commit(final_bar);
+      drain(final_bar, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ key rows
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const float sl2 = A.scale * kLog2e;
+    bool ok = true;
+    for (int it = 0; it < niter && ok; ++it) {
+      if (!(ok = warp_wait(st_full, it & 1, c, A.err, lane))) break;
+      if (!(ok = warp_wait(pds_empty, 1, c, A.err, lane))) break;  // previous dK product done
+      tc_fence_after();
+      const bool diag = it == 0;
+      const int64_t q0 = z * A.s + (jk + it) * TR;  // first query row of this tile in lse / delta
+      // P^T = exp(S^T - lse), zero where the query precedes the key
+#pragma unroll 1
+      for (int cc = 0; cc < TR / 32; ++cc) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(cc * 32)), v);
+        tmem_ld_wait();
+        const float4* lp = reinterpret_cast<const float4*>(lse + q0 + cc * 32);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const float4 l0 = lp[2 * g], l1 = lp[2 * g + 1];
+          const float ls[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int q = cc * 32 + g * 8 + e;
+            f[e] = (!diag || q >= r) ? exp2f(__uint_as_float(v[g * 8 + e]) * sl2 - ls[e] * kLog2e) : 0.0f;
+          }
+          st_tile8(pPdS, r, cc * 4 + g, pack8f(f));
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      warp_arrive(pds_full, lane);
+      if (!(ok = warp_wait(pds_empty, 0, c, A.err, lane))) break;  // dV product has read P^T
+      tc_fence_after();
+      // dS^T = P^T (dP^T - delta) * scale
+#pragma unroll 1
+      for (int cc = 0; cc < TR / 32; ++cc) {
+        uint32_t v[32], w[32];
+        tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(cc * 32)), v);
+        tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(128 + cc * 32)), w);
+        tmem_ld_wait();
+        const float4* lp = reinterpret_cast<const float4*>(lse + q0 + cc * 32);
+        const float4* dp = reinterpret_cast<const float4*>(delta + q0 + cc * 32);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const float4 l0 = lp[2 * g], l1 = lp[2 * g + 1], d0 = dp[2 * g], d1 = dp[2 * g + 1];
+          const float ls[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+          const float ds[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int q = cc * 32 + g * 8 + e;
+            const float p = (!diag || q >= r) ? exp2f(__uint_as_float(v[g * 8 + e]) * sl2 - ls[e] * kLog2e) : 0.0f;
+            f[e] = p * (__uint_as_float(w[g * 8 + e]) - ds[e]) * A.scale;
+          }
+          st_tile8(pPdS, r, cc * 4 + g, pack8f(f));
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      warp_arrive(pds_full, lane);
+      warp_arrive(st_empty, lane);
+    }
+    if (ok) ok = warp_wait(acc_full, 0, c, A.err, lane);
+    if (ok) {
+      tc_fence_after();
+      const int64_t grow = b * A.s + jk * TR + r;
+      for (int which = 0; which < 2; ++which) {  // 0: dV at 2h + t d, 1: dK at h + t d
+        const int64_t gcol = (which == 0 ? 2 * A.h : A.h) + t * A.d;
+        const int64_t br = grow / A.qkv.bh, bc = gcol / A.qkv.bw;
+        bf16* dst = dqkv + A.qkv.block_base((int32_t)br, (int32_t)bc) + (grow - br * A.qkv.bh) * A.qkv.bw +
+                    (gcol - bc * A.qkv.bw);
+        for (int cc = 0; cc < (int)(A.d / 32); ++cc) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem_row(tmem, quarter, 256u + (uint32_t)(which * A.d) + cc * 32), v);
+          tmem_ld_wait();
+          store_row32(dst + cc * 32, v);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------------ backward: dQ
+// smem: Q | dO | K0 V0 | K1 V1 | dS (32 KiB each)
+// TMEM: S [0,128) dP [128,256) dQ [256,256+d)
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap mqkv, const __grid_constant__ CUtensorMap mo,
+                       const AttnProblem A, const float* __restrict__ lse, const float* __restrict__ delta,
+                       bf16* __restrict__ dqkv) {
+  extern __shared__ uint8_t smem_raw[];
+  const Ctx c = setup_smem(smem_raw);
+  const uint32_t sQ = c.base, sdO = c.base + kTile;
+  const uint32_t sK[2] = {c.base + 2 * kTile, c.base + 4 * kTile}, sV[2] = {c.base + 3 * kTile, c.base + 5 * kTile};
+  const uint32_t sdS = c.base + 6 * kTile;
+  uint8_t* pdS = c.base_ptr + 6 * kTile;
+  auto bar = [&](int k) { return c.bar0 + 8u * k; };
+  const uint32_t qo_full = bar(0), s_full = bar(1), s_empty = bar(2), ds_full = bar(3), ds_empty = bar(4),
+                 acc_full = bar(5), final_bar = bar(6);
+  auto r_full = [&](int s) { return bar(7 + s); };
+  auto r_empty = [&](int s) { return bar(9 + s); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t nq = A.s / TR;
+  const int64_t z = blockIdx.x / nq, iq = nq - 1 - (blockIdx.x % nq);  // longest rows first
+  const int64_t b = z / A.H, t = z % A.H;
+  const int niter = (int)iq + 1;
+  const int nch = (int)(A.d / 64);
+  const uint32_t dbytes = (uint32_t)(A.d * TR * 2);
+
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < 11; ++k) mbar_init(bar(k), (k == 2 || k == 3) ? kComputeWarps : 1);
+    *c.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(c.tmem_holder), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *c.tmem_holder;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const int64_t row_q = b * A.s + iq * TR;
+      mbar_arrive_expect_tx(qo_full, 2 * dbytes);
+      load_tile(&mqkv, A.qkv, row_q, t * A.d, nch, sQ, qo_full);
+      load_tile(&mo, A.o, row_q, t * A.d, nch, sdO, qo_full);
+      for (int it = 0; it < niter; ++it) {
+        const int s = it & 1;
+        if (!mbar_wait(r_empty(s), ((it >> 1) & 1) ^ 1, c.abort_flag, A.err)) break;
+        mbar_arrive_expect_tx(r_full(s), 2 * dbytes);
+        const int64_t row_k = b * A.s + (int64_t)it * TR;
+        load_tile(&mqkv, A.qkv, row_k, A.h + t * A.d, nch, sK[s], r_full(s));
+        load_tile(&mqkv, A.qkv, row_k, 2 * A.h + t * A.d, nch, sV[s], r_full(s));
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16_f32(TR, TR, 0, 0);
+      const uint32_t id_acc = idesc_bf16_f32(TR, (int)A.d, 0, 1);
+      const int ks_d = (int)(A.d / 16);
+      bool ok = mbar_wait(qo_full, 0, c.abort_flag, A.err);
+      for (int it = 0; it < niter && ok; ++it) {
+        const int s = it & 1;
+        if (!(ok = mbar_wait(r_full(s), (it >> 1) & 1, c.abort_flag, A.err))) break;
+        if (!(ok = mbar_wait(s_empty, (it & 1) ^ 1, c.abort_flag, A.err))) break;
+        tc_fence_after();
+        mma_tile(tmem, sQ, false, sK[s], false, ks_d, id_s, false);          // S = Q K^T
+        mma_tile(tmem + 128u, sdO, false, sV[s], false, ks_d, id_s, false);  // dP = dO V^T
+        umma_commit(s_full);
+        if (!(ok = mbar_wait(ds_full, it & 1, c.abort_flag, A.err))) break;
+        tc_fence_after();
+        mma_tile(tmem + 256u, sdS, false, sK[s], true, TR / 16, id_acc, it > 0);  // dQ += dS K
+        umma_commit(ds_empty);
+        umma_commit(r_empty(s));
+      }
+      if (ok) umma_commit(acc_full);
+      umma_commit(final_bar);
+      drain(final_bar, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ query rows
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const float sl2 = A.scale * kLog2e;
+    const int64_t qrow = z * A.s + iq * TR + r;
+    const float l2 = lse[qrow] * kLog2e, dr = delta[qrow];
+    bool ok = true;
+    for (int it = 0; it < niter && ok; ++it) {
+      if (!(ok = warp_wait(s_full, it & 1, c, A.err, lane))) break;
+      if (!(ok = warp_wait(ds_empty, (it & 1) ^ 1, c, A.err, lane))) break;
+      tc_fence_after();
+      const bool diag = it == niter - 1;
+#pragma unroll 1
+      for (int cc = 0; cc < TR / 32; ++cc) {
+        uint32_t v[32], w[32];
+        tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(cc * 32)), v);
+        tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(128 + cc * 32)), w);
+        tmem_ld_wait();
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int k = cc * 32 + g * 8 + e;
+            const float p = (!diag || k <= r) ? exp2f(__uint_as_float(v[g * 8 + e]) * sl2 - l2) : 0.0f;
+            f[e] = p * (__uint_as_float(w[g * 8 + e]) - dr) * A.scale;
+          }
+          st_tile8(pdS, r, cc * 4 + g, pack8f(f));
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      warp_arrive(ds_full, lane);
+      warp_arrive(s_empty, lane);
+    }
+    if (ok) ok = warp_wait(acc_full, 0, c, A.err, lane);
+    if (ok) {
+      tc_fence_after();
+      const int64_t grow = b * A.s + iq * TR + r;
+      const int64_t gcol = t * A.d;
+      const int64_t br = grow / A.qkv.bh, bc = gcol / A.qkv.bw;
+      bf16* dst = dqkv + A.qkv.block_base((int32_t)br, (int32_t)bc) + (grow - br * A.qkv.bh) * A.qkv.bw +
+                  (gcol - bc * A.qkv.bw);
+      for (int cc = 0; cc < (int)(A.d / 32); ++cc) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem_row(tmem, quarter, 256u + cc * 32), v);
+        tmem_ld_wait();
+        store_row32(dst + cc * 32, v);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// delta[z*s + r] = sum over the head's d columns of dO * O (one warp per row)
+__global__ void __launch_bounds__(256) attn_delta_kernel(const AttnProblem A, const bf16* __restrict__ O,
+                                                         const bf16* __restrict__ dO, float* __restrict__ delta) {
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = A.Z * A.s;
+  for (int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); row < rows; row += (int64_t)gridDim.x * 8) {
+    const int64_t z = row / A.s, rr = row - z * A.s;
+    const int64_t b = z / A.H, t = z % A.H;
+    const int64_t grow = b * A.s + rr, gcol = t * A.d;
+    const int64_t br = grow / A.o.bh, bc = gcol / A.o.bw;
+    const int64_t off = A.o.block_base((int32_t)br, (int32_t)bc) + (grow - br * A.o.bh) * A.o.bw + (gcol - bc * A.o.bw);
+    float acc = 0.0f;
+    for (int64_t cidx = lane * 4; cidx < A.d; cidx += 128) {
+      const uint2 a = *reinterpret_cast<const uint2*>(O + off + cidx);
+      const uint2 g = *reinterpret_cast<const uint2*>(dO + off + cidx);
+      const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a.x));
+      const float2 a1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a.y));
+      const float2 g0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g.x));
+      const float2 g1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g.y));
+      acc += a0.x * g0.x + a0.y * g0.y + a1.x * g1.x + a1.y * g1.y;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) delta[row] = acc;
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// box of 64 columns x 128 rows over a bf16 matrix grid
+tp3d_status tile_map(CUtensorMap* m, const Grid& g, const void* ptr) {
+  auto fn = encode();
+  if (!fn) return TP3D_ECUDA;
+  cuuint64_t dims[3] = {(cuuint64_t)g.bw, (cuuint64_t)g.bh, (cuuint64_t)g.nshards()};
+  cuuint64_t strides[2] = {(cuuint64_t)g.bw * 2, (cuuint64_t)(g.bh * g.bw * 2)};
+  cuuint32_t box[3] = {64, TR, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? TP3D_OK : TP3D_ECUDA;
+}
+
+tp3d_status check(const AttnProblem& A) {
+  if (A.d != 64 && A.d != 128) return TP3D_EUNSUPPORTED;
+  if (A.s % TR || A.qkv.bh % TR || A.o.bh % TR || A.qkv.bw % A.d || A.o.bw % A.d) return TP3D_EUNSUPPORTED;
+  if (A.Z * (A.s / TR) > 0x7fffffff) return TP3D_EUNSUPPORTED;
+  return TP3D_OK;
+}
+
+}  // namespace
+
+tp3d_status launch_attn_fwd(const tp3d_ctx* ctx, const AttnProblem& A, const void* qkv, void* o, float* lse,
+                            cudaStream_t s) {
+  (void)ctx;
+  TP3D_TRY(check(A));
+  CUtensorMap mq;
+  TP3D_TRY(tile_map(&mq, A.qkv, qkv));
+  TP3D_CUDA_TRY(cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem));
+  const unsigned grid = (unsigned)(A.Z * (A.s / TR));
+  attn_fwd_kernel<<<grid, kThreads, kSmem, s>>>(mq, A, static_cast<bf16*>(o), lse);
+  return cudaGetLastError() == cudaSuccess ? TP3D_OK : TP3D_ECUDA;
+}
+
+tp3d_status launch_attn_bwd(const tp3d_ctx* ctx, const AttnProblem& A, const void* qkv, const void* o,
+                            const void* dO, const float* lse, float* delta, void* dqkv, cudaStream_t s) {
+  TP3D_TRY(check(A));
+  CUtensorMap mq, mo;
+  TP3D_TRY(tile_map(&mq, A.qkv, qkv));
+  TP3D_TRY(tile_map(&mo, A.o, dO));
+  const int64_t rows = A.Z * A.s;
+  int64_t dgrid = (rows + 7) / 8;
+  if (dgrid > (int64_t)ctx->num_sms * 16) dgrid = (int64_t)ctx->num_sms * 16;
+  attn_delta_kernel<<<(unsigned)dgrid, 256, 0, s>>>(A, static_cast<const bf16*>(o), static_cast<const bf16*>(dO),
+                                                    delta);
+  TP3D_CUDA_TRY(cudaGetLastError());
+  TP3D_CUDA_TRY(cudaFuncSetAttribute(attn_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem));
+  TP3D_CUDA_TRY(cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem));
+  const unsigned grid = (unsigned)(A.Z * (A.s / TR));
+  attn_bwd_dkdv_kernel<<<grid, kThreads, kSmem, s>>>(mq, mo, A, lse, delta, static_cast<bf16*>(dqkv));
+  TP3D_CUDA_TRY(cudaGetLastError());
+  attn_bwd_dq_kernel<<<grid, kThreads, kSmem, s>>>(mq, mo, A, lse, delta, static_cast<bf16*>(dqkv));
+  return cudaGetLastError() == cudaSuccess ? TP3D_OK : TP3D_ECUDA;
+}
+
+}  // namespace tp3d

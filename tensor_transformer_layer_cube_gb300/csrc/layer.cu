@@ -10,15 +10,15 @@
 // read by its definition (bias gradient = column sums over every row) and
 // §3.1.3's gamma gradient sum(dC * A-hat).
 //
-// Everything runs on the caller's stream: LayerNorm, the six forward GEMMs
-// (QKV, Q K^T, P V, output projection + residual, W1 + GELU, W2 + residual)
-// and the causal softmax; the backward's twelve GEMMs, softmax backward,
-// LayerNorm backward and the column sums of the bias / gamma / beta
-// gradients.  Attention runs per (batch, head) as batched GEMMs whose
-// windows sit at (batch * seq, head * d) of the QKV and O matrices, so the
-// heads are read in place from their CUBE_C shards.
+// Everything runs on the caller's stream: LayerNorm, the four linear GEMMs
+// (QKV, output projection + residual, W1 + GELU, W2 + residual) and the fused
+// causal attention forward; the backward's eight linear GEMMs, the fused
+// attention backward, LayerNorm backward and the column sums of the bias /
+// gamma / beta gradients.  Attention reads each (batch, head) window in
+// place from the CUBE_C shards of the QKV matrix (attention.cu).
 #include <math.h>
 
+#include "attention.cuh"
 #include "gemm.cuh"
 #include "layer_kernels.cuh"
 
@@ -36,8 +36,8 @@ struct Plan {
   int64_t M, Z;
   float eps;
   // workspace offsets (bytes)
-  size_t xn1, mean1, rstd1, qkv, P, O, Hres, xn2, mean2, rstd2, z1, y1;  // saved by the forward
-  size_t S, dS, dz1, dxn, dH, dO, dqkv, part;                           // scratch
+  size_t xn1, mean1, rstd1, qkv, lse, O, Hres, xn2, mean2, rstd2, z1, y1;  // saved by the forward
+  size_t delta, dz1, dxn, dH, dO, dqkv, part;                              // scratch
   size_t part_floats, total;
 };
 
@@ -67,7 +67,7 @@ tp3d_status make_plan(const tp3d_layer_cfg* c, Plan* p) {
   // inside shards (the causal tiles of the attention products are 128 rows)
   const int64_t m = x.M / q2;
   if ((x.h / q2) % 8 || (x.f / q2) % 8) return TP3D_ESHAPE;
-  if (x.d % 64 || x.s % 128 || gcd64(m, x.s) % 128 || ((3 * (int64_t)x.h / x.q) % x.d)) return TP3D_EUNSUPPORTED;
+  if ((x.d != 64 && x.d != 128) || x.s % 128 || m % 128 || ((x.h / x.q) % x.d)) return TP3D_EUNSUPPORTED;
   const int64_t M = x.M, h = x.h, f = x.f, Z = x.Z, s = x.s;
   size_t o = 0;
   auto take = [&](size_t bytes) {
@@ -79,7 +79,7 @@ tp3d_status make_plan(const tp3d_layer_cfg* c, Plan* p) {
   x.mean1 = take(M * 4);
   x.rstd1 = take(M * 4);
   x.qkv = take(M * 3 * h * 2);
-  x.P = take(Z * s * s * 2);
+  x.lse = take(Z * s * 4);
   x.O = take(M * h * 2);
   x.Hres = take(M * h * 2);
   x.xn2 = take(M * h * 2);
@@ -87,8 +87,7 @@ tp3d_status make_plan(const tp3d_layer_cfg* c, Plan* p) {
   x.rstd2 = take(M * 4);
   x.z1 = take(M * f * 2);
   x.y1 = take(M * f * 2);
-  x.S = take(Z * s * s * 4);
-  x.dS = take(Z * s * s * 2);
+  x.delta = take(Z * s * 4);
   x.dz1 = take(M * f * 2);
   x.dxn = take(M * h * 2);
   x.dH = take(M * h * 2);
@@ -106,20 +105,20 @@ tp3d_status make_plan(const tp3d_layer_cfg* c, Plan* p) {
   return TP3D_OK;
 }
 
-// The attention products per (batch, head) z = b * heads + t.
-// Windows: Q_z rows [b*s, +s) cols [t*d, +d) of QKV, K_z at cols h + t*d,
-// V_z at 2h + t*d; O_z and dO_z at cols t*d of O / dO; S_z, P_z, dS_z are the
-// z-th s x s block of a dense buffer (layout ROW with Z blocks).
-GemmProblem att_base(const Plan& p, int64_t M, int64_t N, int64_t K, int* err) {
-  GemmProblem P{};
-  P.Z = (int32_t)p.Z;
-  P.Hz = p.H;
-  P.M = M;
-  P.N = N;
-  P.K = K;
-  P.epi.alpha = 1.0f;
-  P.err = err;
-  return P;
+// The attention windows: head t of sequence b reads rows [b*s, +s) of QKV at
+// columns t*d (Q), h + t*d (K), 2h + t*d (V) and writes O at columns t*d.
+AttnProblem attn_problem(const Plan& p, int* err) {
+  AttnProblem A{};
+  make_grid(cube(TP3D_CUBE_C, p.q), p.M, 3 * (int64_t)p.h, &A.qkv);
+  make_grid(cube(TP3D_CUBE_C, p.q), p.M, p.h, &A.o);
+  A.s = p.s;
+  A.h = p.h;
+  A.d = p.d;
+  A.H = p.H;
+  A.Z = p.Z;
+  A.scale = 1.0f / sqrtf((float)p.d);
+  A.err = err;
+  return A;
 }
 
 tp3d_status run(const tp3d_ctx* ctx, GemmProblem& P, cudaStream_t s) {
@@ -207,7 +206,7 @@ tp3d_status tp3d_layer_fwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_
   for (const void* ptr : need)
     if (!aligned16(ptr)) return TP3D_EALIGN;
   if (!aligned16(X) || !aligned16(Y) || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return TP3D_EALIGN;
-  const int64_t M = p.M, h = p.h, f = p.f, s = p.s;
+  const int64_t M = p.M, h = p.h, f = p.f;
   if (overlaps(Y, M * h * 2, X, M * h * 2) || overlaps(workspace, p.total, X, M * h * 2) ||
       overlaps(workspace, p.total, Y, M * h * 2))
     return TP3D_EOVERLAP;
@@ -224,32 +223,8 @@ tp3d_status tp3d_layer_fwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_
   GemmProblem G;
   TP3D_TRY(plan_linear(ctx, q, 0, M, h, 3 * h, W(p.xn1), w->w_qkv, w->b_qkv, 0, W(p.qkv), &G));
   TP3D_TRY(gemm_bf16_tc(ctx, G, st));
-  // S_z = Q_z K_z^T / sqrt(d)  (MP3D's C = A B^T form), causal tiles only
-  Grid gQKV, gO, gD;
-  TP3D_TRY(make_grid(cube(TP3D_CUBE_C, q), M, 3 * h, &gQKV));
-  TP3D_TRY(make_grid(cube(TP3D_CUBE_C, q), M, h, &gO));
-  tp3d_layout rowZ{TP3D_ROW, 0, (int32_t)p.Z, 0};
-  TP3D_TRY(make_grid(rowZ, p.Z * s, s, &gD));
-  {
-    GemmProblem P = att_base(p, s, s, p.d, ctx->d_err);
-    P.a = Operand{gQKV, W(p.qkv), 0, s, 0, 0, 0, p.d, 0};          // Q_z: m = b*s, k = t*d
-    P.b = Operand{gQKV, W(p.qkv), 0, 0, p.d, h, s, 0, 0};          // K_z (stored keys x d): k = h + t*d, n = b*s
-    P.c = Operand{gD, W(p.S), 0, (int64_t)p.H * s, s, 0, 0, 0, 0};  // S block z
-    P.causal = CAUSAL_SKIP_UPPER;
-    P.epi.alpha = 1.0f / sqrtf((float)p.d);
-    P.epi.out_f32 = 1;
-    TP3D_TRY(run(ctx, P, st));
-  }
-  TP3D_TRY(launch_softmax_fwd(ctx, (const float*)W(p.S), W(p.P), p.Z, s, st));
-  {
-    // O_z = P_z V_z, keys <= query only
-    GemmProblem P = att_base(p, s, p.d, s, ctx->d_err);
-    P.a = Operand{gD, W(p.P), 0, (int64_t)p.H * s, s, 0, 0, 0, 0};
-    P.b = Operand{gQKV, W(p.qkv), 1, s, 0, 0, 0, p.d, 2 * h};  // V_z stored keys x d: k = b*s, n = 2h + t*d
-    P.c = Operand{gO, W(p.O), 0, s, 0, 0, 0, p.d, 0};
-    P.causal = CAUSAL_K_LE_M;
-    TP3D_TRY(run(ctx, P, st));
-  }
+  // causal attention per (batch, head), fused: O = softmax(Q K^T / sqrt(d)) V
+  TP3D_TRY(launch_attn_fwd(ctx, attn_problem(p, ctx->d_err), W(p.qkv), W(p.O), (float*)W(p.lse), st));
   // H = X + O W_o + b_o   (y = 1: CUBE_C -> CUBE_A)
   TP3D_TRY(plan_linear(ctx, q, 1, M, h, h, W(p.O), w->w_o, w->b_o, 0, W(p.Hres), &G));
   G.epi.resid = X;
@@ -280,7 +255,7 @@ tp3d_status tp3d_layer_bwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_
     if (!aligned16(ptr)) return TP3D_EALIGN;
   if (!aligned16(X) || !aligned16(dY) || !aligned16(dX) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return TP3D_EALIGN;
-  const int64_t M = p.M, h = p.h, f = p.f, s = p.s;
+  const int64_t M = p.M, h = p.h, f = p.f;
   if (overlaps(dX, M * h * 2, dY, M * h * 2) || overlaps(dX, M * h * 2, X, M * h * 2) ||
       overlaps(workspace, p.total, dX, M * h * 2) || overlaps(workspace, p.total, dY, M * h * 2))
     return TP3D_EOVERLAP;
@@ -320,50 +295,9 @@ tp3d_status tp3d_layer_bwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_
   TP3D_TRY(run(ctx, G, st));
   TP3D_TRY(plan_dgrad(ctx, q, 1, M, h, h, W(p.dH), w->w_o, W(p.dO), &G));                  // dO = dH Wo^T
   TP3D_TRY(run(ctx, G, st));
-  Grid gQKV, gO, gD;
-  TP3D_TRY(make_grid(cube(TP3D_CUBE_C, q), M, 3 * h, &gQKV));
-  TP3D_TRY(make_grid(cube(TP3D_CUBE_C, q), M, h, &gO));
-  tp3d_layout rowZ{TP3D_ROW, 0, (int32_t)p.Z, 0};
-  TP3D_TRY(make_grid(rowZ, p.Z * s, s, &gD));
-  const int64_t Hs = (int64_t)p.H * s;
-  {
-    // dP_z = dO_z V_z^T (fp32, causal tiles)
-    GemmProblem P = att_base(p, s, s, p.d, ctx->d_err);
-    P.a = Operand{gO, W(p.dO), 0, s, 0, 0, 0, p.d, 0};
-    P.b = Operand{gQKV, W(p.qkv), 0, 0, p.d, 2 * h, s, 0, 0};
-    P.c = Operand{gD, W(p.S), 0, Hs, s, 0, 0, 0, 0};
-    P.causal = CAUSAL_SKIP_UPPER;
-    P.epi.out_f32 = 1;
-    TP3D_TRY(run(ctx, P, st));
-  }
-  TP3D_TRY(launch_softmax_bwd(ctx, W(p.P), (const float*)W(p.S), W(p.dS), p.Z, s, 1.0f / sqrtf((float)p.d), st));
-  {
-    // dV_z = P_z^T dO_z (contraction over queries >= key)
-    GemmProblem P = att_base(p, s, p.d, s, ctx->d_err);
-    P.a = Operand{gD, W(p.P), 1, 0, 0, 0, Hs, s, 0};
-    P.b = Operand{gO, W(p.dO), 1, s, 0, 0, 0, p.d, 0};
-    P.c = Operand{gQKV, W(p.dqkv), 0, s, 0, 0, 0, p.d, 2 * h};
-    P.causal = CAUSAL_K_GE_M;
-    TP3D_TRY(run(ctx, P, st));
-  }
-  {
-    // dQ_z = dS_z K_z (keys <= query)
-    GemmProblem P = att_base(p, s, p.d, s, ctx->d_err);
-    P.a = Operand{gD, W(p.dS), 0, Hs, s, 0, 0, 0, 0};
-    P.b = Operand{gQKV, W(p.qkv), 1, s, 0, 0, 0, p.d, h};
-    P.c = Operand{gQKV, W(p.dqkv), 0, s, 0, 0, 0, p.d, 0};
-    P.causal = CAUSAL_K_LE_M;
-    TP3D_TRY(run(ctx, P, st));
-  }
-  {
-    // dK_z = dS_z^T Q_z (queries >= key)
-    GemmProblem P = att_base(p, s, p.d, s, ctx->d_err);
-    P.a = Operand{gD, W(p.dS), 1, 0, 0, 0, Hs, s, 0};
-    P.b = Operand{gQKV, W(p.qkv), 1, s, 0, 0, 0, p.d, 0};
-    P.c = Operand{gQKV, W(p.dqkv), 0, s, 0, 0, 0, p.d, h};
-    P.causal = CAUSAL_K_GE_M;
-    TP3D_TRY(run(ctx, P, st));
-  }
+  // attention backward, fused: dQ, dK, dV into dQKV (MP3D's C = A B^T and C = A^T B forms)
+  TP3D_TRY(launch_attn_bwd(ctx, attn_problem(p, ctx->d_err), W(p.qkv), W(p.O), W(p.dO), (const float*)W(p.lse),
+                           (float*)W(p.delta), W(p.dqkv), st));
   TP3D_TRY(colsum(ctx, TP3D_CUBE_C, q, M, 3 * h, W(p.dqkv), part, g->b_qkv, st));          // dbqkv
   TP3D_TRY(plan_wgrad(ctx, q, 0, M, h, 3 * h, W(p.xn1), W(p.dqkv), g->w_qkv, &G));         // dWqkv = LN1(X)^T dQKV
   TP3D_TRY(run(ctx, G, st));

@@ -17,16 +17,10 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
 
@@ -160,89 +154,6 @@ __global__ void __launch_bounds__(kThreads) ln_bwd_kernel(const Grid g, const bf
   }
 }
 
-// ------------------------------------------------------------------ softmax
-// One warp per row i of one (batch, head) block; lanes take 4 consecutive
-// columns per step.  Columns past the row's last key but inside its
-// 128-column tile are written as 0 (the P.V and P^T.dO products read them).
-__global__ void __launch_bounds__(kThreads) softmax_fwd_kernel(const float* __restrict__ S, bf16* __restrict__ P,
-                                                               int64_t rows, int64_t s) {
-  const int lane = threadIdx.x & 31;
-  const int64_t nwarps = (int64_t)gridDim.x * kWarps;
-  for (int64_t row = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); row < rows; row += nwarps) {
-    const int64_t i = row % s;
-    const int64_t n = i + 1;
-    const int64_t nw = ((i >> 7) + 1) << 7;
-    const float* sr = S + row * s;
-    bf16* pr = P + row * s;
-    float mx = -INFINITY;
-    for (int64_t c = lane * 4; c < n; c += 128) {
-      const float4 v = *reinterpret_cast<const float4*>(sr + c);
-      const float e[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        if (c + k < n) mx = fmaxf(mx, e[k]);
-    }
-    mx = warp_max(mx);
-    float sum = 0.0f;
-    for (int64_t c = lane * 4; c < n; c += 128) {
-      const float4 v = *reinterpret_cast<const float4*>(sr + c);
-      const float e[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        if (c + k < n) sum += exp2f((e[k] - mx) * kLog2e);
-    }
-    const float inv = 1.0f / warp_sum(sum);
-    for (int64_t c = lane * 4; c < nw; c += 128) {
-      const float4 v = *reinterpret_cast<const float4*>(sr + c);
-      const float e[4] = {v.x, v.y, v.z, v.w};
-      float p[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) p[k] = (c + k < n) ? exp2f((e[k] - mx) * kLog2e) * inv : 0.0f;
-      __nv_bfloat162 h[2] = {__floats2bfloat162_rn(p[0], p[1]), __floats2bfloat162_rn(p[2], p[3])};
-      *reinterpret_cast<uint2*>(pr + c) = *reinterpret_cast<const uint2*>(h);
-    }
-  }
-}
-
-__global__ void __launch_bounds__(kThreads) softmax_bwd_kernel(const bf16* __restrict__ P,
-                                                               const float* __restrict__ dP, bf16* __restrict__ dS,
-                                                               int64_t rows, int64_t s, float scale) {
-  const int lane = threadIdx.x & 31;
-  const int64_t nwarps = (int64_t)gridDim.x * kWarps;
-  for (int64_t row = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); row < rows; row += nwarps) {
-    const int64_t i = row % s;
-    const int64_t n = i + 1;
-    const int64_t nw = ((i >> 7) + 1) << 7;
-    const bf16* pr = P + row * s;
-    const float* gr = dP + row * s;
-    bf16* orow = dS + row * s;
-    float dsum = 0.0f;
-    for (int64_t c = lane * 4; c < n; c += 128) {
-      const uint2 pv = *reinterpret_cast<const uint2*>(pr + c);
-      const float2 p01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pv.x));
-      const float2 p23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pv.y));
-      const float4 g = *reinterpret_cast<const float4*>(gr + c);
-      const float pp[4] = {p01.x, p01.y, p23.x, p23.y}, gg[4] = {g.x, g.y, g.z, g.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        if (c + k < n) dsum += pp[k] * gg[k];
-    }
-    const float D = warp_sum(dsum);
-    for (int64_t c = lane * 4; c < nw; c += 128) {
-      const uint2 pv = *reinterpret_cast<const uint2*>(pr + c);
-      const float2 p01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pv.x));
-      const float2 p23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pv.y));
-      const float4 g = *reinterpret_cast<const float4*>(gr + c);
-      const float pp[4] = {p01.x, p01.y, p23.x, p23.y}, gg[4] = {g.x, g.y, g.z, g.w};
-      float o[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) o[k] = (c + k < n) ? scale * pp[k] * (gg[k] - D) : 0.0f;
-      __nv_bfloat162 h[2] = {__floats2bfloat162_rn(o[0], o[1]), __floats2bfloat162_rn(o[2], o[3])};
-      *reinterpret_cast<uint2*>(orow + c) = *reinterpret_cast<const uint2*>(h);
-    }
-  }
-}
-
 // ------------------------------------------------------------------ column sums
 // CTA (x, y): columns [256 x, +256) over the rows of part y (rows_per_part
 // rows inside one row block); lane l of every warp holds columns 8l..8l+7,
@@ -342,18 +253,6 @@ tp3d_status launch_ln_bwd(const tp3d_ctx* ctx, const Grid& g, const void* dy, co
   ln_bwd_kernel<<<grid_for_rows(ctx, g.R, 16), kThreads, 0, s>>>(
       g, static_cast<const bf16*>(dy), static_cast<const bf16*>(x), mean, rstd, static_cast<const bf16*>(gamma),
       static_cast<const bf16*>(dres), static_cast<bf16*>(dx));
-  return last_error();
-}
-
-tp3d_status launch_softmax_fwd(const tp3d_ctx* ctx, const float* S, void* P, int64_t Z, int64_t s, cudaStream_t st) {
-  softmax_fwd_kernel<<<grid_for_rows(ctx, Z * s, 16), kThreads, 0, st>>>(S, static_cast<bf16*>(P), Z * s, s);
-  return last_error();
-}
-
-tp3d_status launch_softmax_bwd(const tp3d_ctx* ctx, const void* P, const float* dP, void* dS, int64_t Z, int64_t s,
-                               float scale, cudaStream_t st) {
-  softmax_bwd_kernel<<<grid_for_rows(ctx, Z * s, 16), kThreads, 0, st>>>(
-      static_cast<const bf16*>(P), dP, static_cast<bf16*>(dS), Z * s, s, scale);
   return last_error();
 }
 

@@ -1,6 +1,5 @@
 // layer_kernels.cuh - host launchers of the layer's bandwidth-bound kernels
-// (layer_kernels.cu): LayerNorm forward/backward, causal softmax
-// forward/backward and column sums.  All read and write matrices through
+// (layer_kernels.cu): LayerNorm forward/backward and column sums.  All read and write matrices through
 // their layout grid, so a row that the cube splits over q shards is read from
 // those q shards.
 #pragma once
@@ -23,14 +22,6 @@ tp3d_status launch_ln_bwd(const tp3d_ctx* ctx, const Grid& g, const void* dy, co
 // sum dy * (x - mean) * rstd, part_b sum dy (colsum_parts(g) rows of C floats).
 tp3d_status launch_ln_param_grads(const tp3d_ctx* ctx, const Grid& g, const void* dy, const void* x,
                                   const float* mean, const float* rstd, float* part_g, float* part_b, cudaStream_t s);
-
-// Causal softmax over rows of the dense fp32 scores S (Z blocks of s x s):
-// P[i][c] = exp(S[i][c] - max) / sum for c <= i, 0 for i < c < (i/128+1)*128.
-tp3d_status launch_softmax_fwd(const tp3d_ctx* ctx, const float* S, void* P, int64_t Z, int64_t s, cudaStream_t st);
-
-// dS = scale * P * (dP - sum_c P dP) on the same causal support as P.
-tp3d_status launch_softmax_bwd(const tp3d_ctx* ctx, const void* P, const float* dP, void* dS, int64_t Z, int64_t s,
-                               float scale, cudaStream_t st);
 
 // Column sums of the R x C bf16 matrix x (layout g): partials in `part`
 // (colsum_parts(g) rows of C floats), then reduce_parts writes the bf16 vector.
