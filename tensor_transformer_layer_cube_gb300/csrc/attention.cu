@@ -7,7 +7,7 @@
 // first linear): head t of sequence b is the window rows [b*s, +s) x columns
 // [t*d, +d) (Q), [h + t*d, +d) (K), [2h + t*d, +d) (V).
 //
-// Three tcgen05 kernels, 128-row tiles, one CTA per work item, warp 0 = TMA
+// Three persistent tcgen05 kernels, 128-row tiles, warp 0 = TMA
 // producer, warp 1 = MMA issuer (and TMEM owner), warps 2-5 = one thread per
 // tile row (TMEM lane) for the softmax arithmetic:
 //  * forward: per query tile, pass 1 runs S = Q K^T over the key tiles at or
@@ -134,8 +134,14 @@ __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) {
     if (globaltimer_ns() - t0 > kWaitLimitNs) return;
 }
 
+// All three kernels are persistent: CTA c takes work items c, c + grid, ...
+// in longest-first order, and the producer loads the next item's tiles while
+// the current one finishes (phase counters run across items).
+
 // ------------------------------------------------------------------ forward
+// item w: query tile nq-1-(w / Z) of (batch, head) w % Z
 // smem: Q | K0 V0 | K1 V1 | P0 | P1 (32 KiB each)
+// TMEM: S0 [0,128) S1 [128,256) O [256,256+d)
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap mqkv, const AttnProblem A, bf16* __restrict__ O,
                     float* __restrict__ lse) {
@@ -145,26 +151,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sP[2] = {c.base + 5 * kTile, c.base + 6 * kTile};
   uint8_t* pP[2] = {c.base_ptr + 5 * kTile, c.base_ptr + 6 * kTile};
   auto bar = [&](int k) { return c.bar0 + 8u * k; };
-  const uint32_t q_full = bar(0), o_full = bar(1);
-  auto kv_full = [&](int s) { return bar(2 + s); };
-  auto kv_empty = [&](int s) { return bar(4 + s); };
-  auto s_full = [&](int b) { return bar(6 + b); };
-  auto s_empty = [&](int b) { return bar(8 + b); };
-  auto p_full = [&](int b) { return bar(10 + b); };
-  auto p_empty = [&](int b) { return bar(12 + b); };
-  const uint32_t final_bar = bar(14);
+  const uint32_t q_full = bar(0), q_empty = bar(1), o_full = bar(2), o_empty = bar(3);
+  auto kv_full = [&](int s) { return bar(4 + s); };
+  auto kv_empty = [&](int s) { return bar(6 + s); };
+  auto s_full = [&](int b) { return bar(8 + b); };
+  auto s_empty = [&](int b) { return bar(10 + b); };
+  auto p_full = [&](int b) { return bar(12 + b); };
+  auto p_empty = [&](int b) { return bar(14 + b); };
+  const uint32_t final_bar = bar(16);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t nq = A.s / TR;
-  const int64_t z = blockIdx.x / nq, it_q = nq - 1 - (blockIdx.x % nq);  // longest rows first
-  const int64_t b = z / A.H, t = z % A.H;
-  const int nkv = (int)it_q + 1;
+  const int64_t nq = A.s / TR, items = A.Z * nq;
   const int nch = (int)(A.d / 64);
   const uint32_t dbytes = (uint32_t)(A.d * TR * 2);
 
   if (threadIdx.x == 0) {
-    for (int k = 0; k < 15; ++k)
-      mbar_init(bar(k), (k == 8 || k == 9 || k == 10 || k == 11) ? kComputeWarps : 1);
+    for (int k = 0; k < 17; ++k)
+      mbar_init(bar(k), (k == 3 || k == 10 || k == 11 || k == 12 || k == 13) ? kComputeWarps : 1);
     *c.abort_flag = 0;
     fence_barrier_init();
   }
@@ -179,22 +182,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      const int64_t row_q = b * A.s + it_q * TR;
-      mbar_arrive_expect_tx(q_full, dbytes);
-      load_tile(&mqkv, A.qkv, row_q, t * A.d, nch, sQ, q_full);
+      uint32_t n = 0, ic = 0;
       bool ok = true;
-      for (int n = 0; n < 2 * nkv && ok; ++n) {
-        const int j = n < nkv ? n : n - nkv;
-        const bool with_v = n >= nkv;
-        const int s = n & 1;
-        if (!mbar_wait(kv_empty(s), ((n >> 1) & 1) ^ 1, c.abort_flag, A.err)) {
-          ok = false;
-          break;
+      for (int64_t w = blockIdx.x; w < items && ok; w += gridDim.x, ++ic) {
+        const int64_t iq = nq - 1 - w / A.Z, z = w % A.Z, b = z / A.H, t = z % A.H;
+        const int nkv = (int)iq + 1;
+        if (!(ok = mbar_wait(q_empty, (ic & 1) ^ 1, c.abort_flag, A.err))) break;
+        mbar_arrive_expect_tx(q_full, dbytes);
+        load_tile(&mqkv, A.qkv, b * A.s + iq * TR, t * A.d, nch, sQ, q_full);
+        for (int e = 0; e < 2 * nkv; ++e, ++n) {
+          const int j = e < nkv ? e : e - nkv;
+          const bool with_v = e >= nkv;
+          const int s = n & 1;
+          if (!(ok = mbar_wait(kv_empty(s), ((n >> 1) & 1) ^ 1, c.abort_flag, A.err))) break;
+          mbar_arrive_expect_tx(kv_full(s), with_v ? 2 * dbytes : dbytes);
+          const int64_t row_k = b * A.s + (int64_t)j * TR;
+          load_tile(&mqkv, A.qkv, row_k, A.h + t * A.d, nch, sK[s], kv_full(s));
+          if (with_v) load_tile(&mqkv, A.qkv, row_k, 2 * A.h + t * A.d, nch, sV[s], kv_full(s));
         }
-        mbar_arrive_expect_tx(kv_full(s), with_v ? 2 * dbytes : dbytes);
-        const int64_t row_k = b * A.s + (int64_t)j * TR;
-        load_tile(&mqkv, A.qkv, row_k, A.h + t * A.d, nch, sK[s], kv_full(s));
-        if (with_v) load_tile(&mqkv, A.qkv, row_k, 2 * A.h + t * A.d, nch, sV[s], kv_full(s));
       }
     }
   } else if (warp == 1) {
@@ -202,40 +207,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t id_s = idesc_bf16_f32(TR, TR, 0, 0);
       const uint32_t id_o = idesc_bf16_f32(TR, (int)A.d, 0, 1);
       const int ks_d = (int)(A.d / 16);
-      bool ok = mbar_wait(q_full, 0, c.abort_flag, A.err);
-      int n = 0, sc = 0, pc = 0;
-      // S_n = Q K^T for ring entry n into S buffer sc % 2
-      auto issue_s = [&](int nn) -> bool {
-        const int s = nn & 1;
-        if (!mbar_wait(kv_full(s), (nn >> 1) & 1, c.abort_flag, A.err)) return false;
+      uint32_t n = 0, sc = 0, pc = 0, ic = 0;
+      bool ok = true;
+      // S = Q K^T for the next ring entry into S buffer sc % 2; returns the ring stage
+      auto issue_s = [&](int& stage) -> bool {
+        const int s = n & 1;
+        if (!mbar_wait(kv_full(s), (n >> 1) & 1, c.abort_flag, A.err)) return false;
         const int sb = sc & 1;
         if (!mbar_wait(s_empty(sb), ((sc >> 1) & 1) ^ 1, c.abort_flag, A.err)) return false;
         tc_fence_after();
         mma_tile(tmem + (uint32_t)(sb * TR), sQ, false, sK[s], false, ks_d, id_s, false);
         umma_commit(s_full(sb));
         ++sc;
+        ++n;
+        stage = s;
         return true;
       };
-      for (; n < nkv && ok; ++n) {  // pass 1: scores only
-        ok = issue_s(n);
-        if (ok) umma_commit(kv_empty(n & 1));
-      }
-      if (ok) ok = issue_s(nkv);
-      for (int j = 0; j < nkv && ok; ++j) {  // pass 2
-        if (j + 1 < nkv) ok = issue_s(nkv + j + 1);
-        if (!ok) break;
-        const int pb = pc & 1;
-        if (!mbar_wait(p_full(pb), (pc >> 1) & 1, c.abort_flag, A.err)) {
-          ok = false;
-          break;
+      for (int64_t w = blockIdx.x; w < items && ok; w += gridDim.x, ++ic) {
+        const int nkv = (int)(nq - 1 - w / A.Z) + 1;
+        if (!(ok = mbar_wait(q_full, ic & 1, c.abort_flag, A.err))) break;
+        int st = 0;
+        for (int e = 0; e < nkv && ok; ++e) {  // pass 1: scores only
+          if ((ok = issue_s(st))) umma_commit(kv_empty(st));
         }
-        tc_fence_after();
-        mma_tile(tmem + 256u, sP[pb], false, sV[(nkv + j) & 1], true, TR / 16, id_o, j > 0);
-        umma_commit(p_empty(pb));
-        umma_commit(kv_empty((nkv + j) & 1));
-        ++pc;
+        if (!ok) break;
+        int st_cur = 0, issued = 1;
+        if (!(ok = issue_s(st_cur))) break;
+        if (issued == nkv) umma_commit(q_empty);
+        for (int j = 0; j < nkv && ok; ++j) {  // pass 2
+          int st_next = 0;
+          if (j + 1 < nkv) {
+            if (!(ok = issue_s(st_next))) break;
+            if (++issued == nkv) umma_commit(q_empty);
+          }
+          const int pb = pc & 1;
+          if (!(ok = mbar_wait(p_full(pb), (pc >> 1) & 1, c.abort_flag, A.err))) break;
+          if (j == 0 && !(ok = mbar_wait(o_empty, (ic & 1) ^ 1, c.abort_flag, A.err))) break;
+          tc_fence_after();
+          mma_tile(tmem + 256u, sP[pb], false, sV[st_cur], true, TR / 16, id_o, j > 0);
+          umma_commit(p_empty(pb));
+          umma_commit(kv_empty(st_cur));
+          ++pc;
+          st_cur = st_next;
+        }
+        if (ok) umma_commit(o_full);
       }
-      if (ok) umma_commit(o_full);
       umma_commit(final_bar);
       drain(final_bar, 0);
     }
@@ -244,68 +260,70 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const float sl2 = A.scale * kLog2e;
-    float m = -INFINITY, l = 0.0f;
-    int sc = 0, pc = 0;
+    uint32_t sc = 0, pc = 0, ic = 0;
     bool ok = true;
-    for (int j = 0; j < nkv && ok; ++j) {  // pass 1: row max and sum
-      const int sb = sc & 1;
-      if (!(ok = warp_wait(s_full(sb), (sc >> 1) & 1, c, A.err, lane))) break;
-      tc_fence_after();
-      const bool diag = j == nkv - 1;
+    for (int64_t w = blockIdx.x; w < items && ok; w += gridDim.x, ++ic) {
+      const int64_t iq = nq - 1 - w / A.Z, z = w % A.Z, b = z / A.H, t = z % A.H;
+      const int nkv = (int)iq + 1;
+      float m = -INFINITY, l = 0.0f;
+      for (int j = 0; j < nkv && ok; ++j) {  // pass 1: row max and sum
+        const int sb = sc & 1;
+        if (!(ok = warp_wait(s_full(sb), (sc >> 1) & 1, c, A.err, lane))) break;
+        tc_fence_after();
+        const bool diag = j == nkv - 1;
 #pragma unroll 1
-      for (int cc = 0; cc < TR / 32; ++cc) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(sb * TR + cc * 32)), v);
-        tmem_ld_wait();
-        float mx = m;
+        for (int cc = 0; cc < TR / 32; ++cc) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(sb * TR + cc * 32)), v);
+          tmem_ld_wait();
+          float mx = m;
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (!diag || cc * 32 + e <= r) mx = fmaxf(mx, __uint_as_float(v[e]) * sl2);
-        float sum = 0.0f;
+          for (int e = 0; e < 32; ++e)
+            if (!diag || cc * 32 + e <= r) mx = fmaxf(mx, __uint_as_float(v[e]) * sl2);
+          float sum = 0.0f;
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (!diag || cc * 32 + e <= r) sum += exp2f(__uint_as_float(v[e]) * sl2 - mx);
-        l = l * exp2f(m - mx) + sum;
-        m = mx;
-      }
-      tc_fence_before();
-      warp_arrive(s_empty(sb), lane);
-      ++sc;
-    }
-    const float inv_l = 1.0f / l;
-    for (int j = 0; j < nkv && ok; ++j) {  // pass 2: P = exp(S - m) / l into shared memory
-      const int sb = sc & 1, pb = pc & 1;
-      if (!(ok = warp_wait(s_full(sb), (sc >> 1) & 1, c, A.err, lane))) break;
-      if (!(ok = warp_wait(p_empty(pb), ((pc >> 1) & 1) ^ 1, c, A.err, lane))) break;
-      tc_fence_after();
-      const bool diag = j == nkv - 1;
-#pragma unroll 1
-      for (int cc = 0; cc < TR / 32; ++cc) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(sb * TR + cc * 32)), v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          float f[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int col = cc * 32 + g * 8 + e;
-            f[e] = (!diag || col <= r) ? exp2f(__uint_as_float(v[g * 8 + e]) * sl2 - m) * inv_l : 0.0f;
-          }
-          st_tile8(pP[pb], r, cc * 4 + g, pack8f(f));
+          for (int e = 0; e < 32; ++e)
+            if (!diag || cc * 32 + e <= r) sum += exp2f(__uint_as_float(v[e]) * sl2 - mx);
+          l = l * exp2f(m - mx) + sum;
+          m = mx;
         }
+        tc_fence_before();
+        warp_arrive(s_empty(sb), lane);
+        ++sc;
       }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      warp_arrive(p_full(pb), lane);
-      warp_arrive(s_empty(sb), lane);
-      ++sc;
-      ++pc;
-    }
-    if (ok) ok = warp_wait(o_full, 0, c, A.err, lane);
-    if (ok) {
+      const float inv_l = 1.0f / l;
+      for (int j = 0; j < nkv && ok; ++j) {  // pass 2: P = exp(S - m) / l into shared memory
+        const int sb = sc & 1, pb = pc & 1;
+        if (!(ok = warp_wait(s_full(sb), (sc >> 1) & 1, c, A.err, lane))) break;
+        if (!(ok = warp_wait(p_empty(pb), ((pc >> 1) & 1) ^ 1, c, A.err, lane))) break;
+        tc_fence_after();
+        const bool diag = j == nkv - 1;
+#pragma unroll 1
+        for (int cc = 0; cc < TR / 32; ++cc) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(sb * TR + cc * 32)), v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int col = cc * 32 + g * 8 + e;
+              f[e] = (!diag || col <= r) ? exp2f(__uint_as_float(v[g * 8 + e]) * sl2 - m) * inv_l : 0.0f;
+            }
+            st_tile8(pP[pb], r, cc * 4 + g, pack8f(f));
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        warp_arrive(p_full(pb), lane);
+        warp_arrive(s_empty(sb), lane);
+        ++sc;
+        ++pc;
+      }
+      if (!ok || !(ok = warp_wait(o_full, ic & 1, c, A.err, lane))) break;
       tc_fence_after();
-      const int64_t grow = b * A.s + it_q * TR + r;
+      const int64_t grow = b * A.s + iq * TR + r;
       const int64_t gcol = t * A.d;
       const int64_t br = grow / A.o.bh, bc = gcol / A.o.bw;
       bf16* dst = O + A.o.block_base((int32_t)br, (int32_t)bc) + (grow - br * A.o.bh) * A.o.bw + (gcol - bc * A.o.bw);
@@ -315,7 +333,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
         store_row32(dst + cc * 32, v);
       }
-      lse[z * A.s + it_q * TR + r] = (m + log2f(l)) * kLn2;
+      tc_fence_before();
+      warp_arrive(o_empty, lane);
+      lse[z * A.s + iq * TR + r] = (m + log2f(l)) * kLn2;
     }
   }
   tc_fence_before();
@@ -327,6 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ backward: dK, dV
+// item w: key tile w / Z of (batch, head) w % Z (the most query tiles first)
 // smem: K | V | Q0 dO0 | Q1 dO1 | PdS (32 KiB each); PdS holds P^T, then dS^T
 // TMEM: S^T [0,128) dP^T [128,256) dV [256,256+d) dK [256+d, 256+2d)
 __global__ void __launch_bounds__(kThreads, 1)
@@ -340,21 +361,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sPdS = c.base + 6 * kTile;
   uint8_t* pPdS = c.base_ptr + 6 * kTile;
   auto bar = [&](int k) { return c.bar0 + 8u * k; };
-  const uint32_t kv_full = bar(0), st_full = bar(1), st_empty = bar(2), pds_full = bar(3), pds_empty = bar(4),
-                 acc_full = bar(5), final_bar = bar(6);
-  auto r_full = [&](int s) { return bar(7 + s); };
-  auto r_empty = [&](int s) { return bar(9 + s); };
+  const uint32_t kv_full = bar(0), kv_empty = bar(1), st_full = bar(2), st_empty = bar(3), pds_full = bar(4),
+                 pds_empty = bar(5), acc_full = bar(6), acc_empty = bar(7), final_bar = bar(8);
+  auto r_full = [&](int s) { return bar(9 + s); };
+  auto r_empty = [&](int s) { return bar(11 + s); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t nq = A.s / TR;
-  const int64_t z = blockIdx.x / nq, jk = blockIdx.x % nq;  // key tile; the most query tiles first
-  const int64_t b = z / A.H, t = z % A.H;
-  const int niter = (int)(nq - jk);
+  const int64_t nq = A.s / TR, items = A.Z * nq;
   const int nch = (int)(A.d / 64);
   const uint32_t dbytes = (uint32_t)(A.d * TR * 2);
 
   if (threadIdx.x == 0) {
-    for (int k = 0; k < 11; ++k) mbar_init(bar(k), (k == 2 || k == 3) ? kComputeWarps : 1);
+    for (int k = 0; k < 13; ++k) mbar_init(bar(k), (k == 3 || k == 4 || k == 7) ? kComputeWarps : 1);
     *c.abort_flag = 0;
     fence_barrier_init();
   }
@@ -369,17 +387,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      const int64_t row_k = b * A.s + jk * TR;
-      mbar_arrive_expect_tx(kv_full, 2 * dbytes);
-      load_tile(&mqkv, A.qkv, row_k, A.h + t * A.d, nch, sK, kv_full);
-      load_tile(&mqkv, A.qkv, row_k, 2 * A.h + t * A.d, nch, sV, kv_full);
-      for (int it = 0; it < niter; ++it) {
-        const int s = it & 1;
-        if (!mbar_wait(r_empty(s), ((it >> 1) & 1) ^ 1, c.abort_flag, A.err)) break;
-        mbar_arrive_expect_tx(r_full(s), 2 * dbytes);
-        const int64_t row_q = b * A.s + (jk + it) * TR;
-        load_tile(&mqkv, A.qkv, row_q, t * A.d, nch, sQ[s], r_full(s));
-        load_tile(&mo, A.o, row_q, t * A.d, nch, sdO[s], r_full(s));
+      uint32_t n = 0, ic = 0;
+      bool ok = true;
+      for (int64_t w = blockIdx.x; w < items && ok; w += gridDim.x, ++ic) {
+        const int64_t jk = w / A.Z, z = w % A.Z, b = z / A.H, t = z % A.H;
+        const int niter = (int)(nq - jk);
+        if (!(ok = mbar_wait(kv_empty, (ic & 1) ^ 1, c.abort_flag, A.err))) break;
+        const int64_t row_k = b * A.s + jk * TR;
+        mbar_arrive_expect_tx(kv_full, 2 * dbytes);
+        load_tile(&mqkv, A.qkv, row_k, A.h + t * A.d, nch, sK, kv_full);
+        load_tile(&mqkv, A.qkv, row_k, 2 * A.h + t * A.d, nch, sV, kv_full);
+        for (int it = 0; it < niter; ++it, ++n) {
+          const int s = n & 1;
+          if (!(ok = mbar_wait(r_empty(s), ((n >> 1) & 1) ^ 1, c.abort_flag, A.err))) break;
+          mbar_arrive_expect_tx(r_full(s), 2 * dbytes);
+          const int64_t row_q = b * A.s + (jk + it) * TR;
+          load_tile(&mqkv, A.qkv, row_q, t * A.d, nch, sQ[s], r_full(s));
+          load_tile(&mo, A.o, row_q, t * A.d, nch, sdO[s], r_full(s));
+        }
       }
     }
   } else if (warp == 1) {
@@ -387,26 +412,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t id_s = idesc_bf16_f32(TR, TR, 0, 0);
       const uint32_t id_acc = idesc_bf16_f32(TR, (int)A.d, 0, 1);
       const int ks_d = (int)(A.d / 16);
-      bool ok = mbar_wait(kv_full, 0, c.abort_flag, A.err);
-      for (int it = 0; it < niter && ok; ++it) {
-        const int s = it & 1;
-        if (!(ok = mbar_wait(r_full(s), (it >> 1) & 1, c.abort_flag, A.err))) break;
-        if (!(ok = mbar_wait(st_empty, (it & 1) ^ 1, c.abort_flag, A.err))) break;
-        tc_fence_after();
-        mma_tile(tmem, sK, false, sQ[s], false, ks_d, id_s, false);          // S^T = K Q^T
-        mma_tile(tmem + 128u, sV, false, sdO[s], false, ks_d, id_s, false);  // dP^T = V dO^T
-        umma_commit(st_full);
-        if (!(ok = mbar_wait(pds_full, 0, c.abort_flag, A.err))) break;
-        tc_fence_after();
-        mma_tile(tmem + 256u, sPdS, false, sdO[s], true, TR / 16, id_acc, it > 0);  // dV += P^T dO
-        umma_commit(pds_empty);
-        if (!(ok = mbar_wait(pds_full, 1, c.abort_flag, A.err))) break;
-        tc_fence_after();
-        mma_tile(tmem + 256u + (uint32_t)A.d, sPdS, false, sQ[s], true, TR / 16, id_acc, it > 0);  // dK += dS^T Q
-        umma_commit(pds_empty);
-        umma_commit(r_empty(s));
+      uint32_t n = 0, ic = 0;
+      bool ok = true;
+      for (int64_t w = blockIdx.x; w < items && ok; w += gridDim.x, ++ic) {
+        const int niter = (int)(nq - w / A.Z);
+        if (!(ok = mbar_wait(kv_full, ic & 1, c.abort_flag, A.err))) break;
+        for (int it = 0; it < niter && ok; ++it, ++n) {
+          const int s = n & 1;
+          if (!(ok = mbar_wait(r_full(s), (n >> 1) & 1, c.abort_flag, A.err))) break;
+          if (!(ok = mbar_wait(st_empty, (n & 1) ^ 1, c.abort_flag, A.err))) break;
+          tc_fence_after();
+          mma_tile(tmem, sK, false, sQ[s], false, ks_d, id_s, false);          // S^T = K Q^T
+          mma_tile(tmem + 128u, sV, false, sdO[s], false, ks_d, id_s, false);  // dP^T = V dO^T
+          if (it == niter - 1) umma_commit(kv_empty);
+          umma_commit(st_full);
+          if (!(ok = mbar_wait(pds_full, 0, c.abort_flag, A.err))) break;
+          if (it == 0 && !(ok = mbar_wait(acc_empty, (ic & 1) ^ 1, c.abort_flag, A.err))) break;
+          tc_fence_after();
+          mma_tile(tmem + 256u, sPdS, false, sdO[s], true, TR / 16, id_acc, it > 0);  // dV += P^T dO
+          umma_commit(pds_empty);
+          if (!(ok = mbar_wait(pds_full, 1, c.abort_flag, A.err))) break;
+          tc_fence_after();
+          mma_tile(tmem + 256u + (uint32_t)A.d, sPdS, false, sQ[s], true, TR / 16, id_acc, it > 0);  // dK += dS^T Q
+          umma_commit(pds_empty);
+          umma_commit(r_empty(s));
+        }
+        if (ok) umma_commit(acc_full);
       }
-      if (ok) umma_commit(acc_full);
       umma_commit(final_bar);
       drain(final_bar, 0);
     }
@@ -415,69 +447,79 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const float sl2 = A.scale * kLog2e;
+    uint32_t n = 0, ic = 0;
     bool ok = true;
-    for (int it = 0; it < niter && ok; ++it) {
-      if (!(ok = warp_wait(st_full, it & 1, c, A.err, lane))) break;
-      if (!(ok = warp_wait(pds_empty, 1, c, A.err, lane))) break;  // previous dK product done
-      tc_fence_after();
-      const bool diag = it == 0;
-      const int64_t q0 = z * A.s + (jk + it) * TR;  // first query row of this tile in lse / delta
-      // P^T = exp(S^T - lse), zero where the query precedes the key
-#pragma unroll 1
-      for (int cc = 0; cc < TR / 32; ++cc) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(cc * 32)), v);
-        tmem_ld_wait();
-        const float4* lp = reinterpret_cast<const float4*>(lse + q0 + cc * 32);
+    for (int64_t w = blockIdx.x; w < items && ok; w += gridDim.x, ++ic) {
+      const int64_t jk = w / A.Z, z = w % A.Z, b = z / A.H, t = z % A.H;
+      const int niter = (int)(nq - jk);
+      for (int it = 0; it < niter && ok; ++it, ++n) {
+        if (!(ok = warp_wait(st_full, n & 1, c, A.err, lane))) break;
+        if (!(ok = warp_wait(pds_empty, 1, c, A.err, lane))) break;  // previous dK product done
+        tc_fence_after();
+        const bool diag = it == 0;
+        const int64_t q0 = z * A.s + (jk + it) * TR;  // first query row of this tile in lse / delta
+        // lane l holds lse (pre-scaled by log2 e) and delta of queries
+        // 32 cc + l of the tile; query 32 cc + j is read with a shuffle from lane j
+        float lq[TR / 32], dq[TR / 32];
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const float4 l0 = lp[2 * g], l1 = lp[2 * g + 1];
-          const float ls[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
-          float f[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int q = cc * 32 + g * 8 + e;
-            f[e] = (!diag || q >= r) ? exp2f(__uint_as_float(v[g * 8 + e]) * sl2 - ls[e] * kLog2e) : 0.0f;
-          }
-          st_tile8(pPdS, r, cc * 4 + g, pack8f(f));
+        for (int cc = 0; cc < TR / 32; ++cc) {
+          lq[cc] = lse[q0 + cc * 32 + lane] * kLog2e;
+          dq[cc] = delta[q0 + cc * 32 + lane];
         }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      warp_arrive(pds_full, lane);
-      if (!(ok = warp_wait(pds_empty, 0, c, A.err, lane))) break;  // dV product has read P^T
-      tc_fence_after();
-      // dS^T = P^T (dP^T - delta) * scale
-#pragma unroll 1
-      for (int cc = 0; cc < TR / 32; ++cc) {
-        uint32_t v[32], w[32];
-        tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(cc * 32)), v);
-        tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(128 + cc * 32)), w);
-        tmem_ld_wait();
-        const float4* lp = reinterpret_cast<const float4*>(lse + q0 + cc * 32);
-        const float4* dp = reinterpret_cast<const float4*>(delta + q0 + cc * 32);
+        // P^T = exp(S^T - lse), zero where the query precedes the key
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const float4 l0 = lp[2 * g], l1 = lp[2 * g + 1], d0 = dp[2 * g], d1 = dp[2 * g + 1];
-          const float ls[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
-          const float ds[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
-          float f[8];
+        for (int cc = 0; cc < TR / 32; ++cc) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(cc * 32)), v);
+          tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int q = cc * 32 + g * 8 + e;
-            const float p = (!diag || q >= r) ? exp2f(__uint_as_float(v[g * 8 + e]) * sl2 - ls[e] * kLog2e) : 0.0f;
-            f[e] = p * (__uint_as_float(w[g * 8 + e]) - ds[e]) * A.scale;
+          for (int g = 0; g < 4; ++g) {
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int q = cc * 32 + g * 8 + e;
+              const float ls = __shfl_sync(0xffffffffu, lq[cc], g * 8 + e);
+              f[e] = (!diag || q >= r) ? exp2f(__uint_as_float(v[g * 8 + e]) * sl2 - ls) : 0.0f;
+            }
+            st_tile8(pPdS, r, cc * 4 + g, pack8f(f));
           }
-          st_tile8(pPdS, r, cc * 4 + g, pack8f(f));
         }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        warp_arrive(pds_full, lane);
+        if (!(ok = warp_wait(pds_empty, 0, c, A.err, lane))) break;  // dV product has read P^T
+        tc_fence_after();
+        // dS^T = P^T (dP^T - delta) * scale, P^T read back (bf16) from this
+        // thread's own row of the buffer and overwritten in place
+#pragma unroll
+        for (int cc = 0; cc < TR / 32; ++cc) {
+          uint32_t wv[32];
+          tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(128 + cc * 32)), wv);
+          tmem_ld_wait();
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            uint4* slot = reinterpret_cast<uint4*>(pPdS + ((cc * 4 + g) >> 3) * kChunk + r * 128 +
+                                                   ((((cc * 4 + g) & 7) ^ (r & 7)) << 4));
+            const uint4 pv = *slot;
+            const __nv_bfloat162* ph = reinterpret_cast<const __nv_bfloat162*>(&pv);
+            float f[8];
+#pragma unroll
+            for (int e2 = 0; e2 < 4; ++e2) {
+              const float2 p2 = __bfloat1622float2(ph[e2]);
+              const float ds0 = __shfl_sync(0xffffffffu, dq[cc], g * 8 + 2 * e2);
+              const float ds1 = __shfl_sync(0xffffffffu, dq[cc], g * 8 + 2 * e2 + 1);
+              f[2 * e2] = p2.x * (__uint_as_float(wv[g * 8 + 2 * e2]) - ds0) * A.scale;
+              f[2 * e2 + 1] = p2.y * (__uint_as_float(wv[g * 8 + 2 * e2 + 1]) - ds1) * A.scale;
+            }
+            *slot = pack8f(f);
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        warp_arrive(pds_full, lane);
+        warp_arrive(st_empty, lane);
       }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      warp_arrive(pds_full, lane);
-      warp_arrive(st_empty, lane);
-    }
-    if (ok) ok = warp_wait(acc_full, 0, c, A.err, lane);
-    if (ok) {
+      if (!ok || !(ok = warp_wait(acc_full, ic & 1, c, A.err, lane))) break;
       tc_fence_after();
       const int64_t grow = b * A.s + jk * TR + r;
       for (int which = 0; which < 2; ++which) {  // 0: dV at 2h + t d, 1: dK at h + t d
@@ -492,6 +534,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           store_row32(dst + cc * 32, v);
         }
       }
+      tc_fence_before();
+      warp_arrive(acc_empty, lane);
     }
   }
   tc_fence_before();
@@ -503,6 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ backward: dQ
+// item w: query tile nq-1-(w / Z) of (batch, head) w % Z
 // smem: Q | dO | K0 V0 | K1 V1 | dS (32 KiB each)
 // TMEM: S [0,128) dP [128,256) dQ [256,256+d)
 __global__ void __launch_bounds__(kThreads, 1)
@@ -516,21 +561,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sdS = c.base + 6 * kTile;
   uint8_t* pdS = c.base_ptr + 6 * kTile;
   auto bar = [&](int k) { return c.bar0 + 8u * k; };
-  const uint32_t qo_full = bar(0), s_full = bar(1), s_empty = bar(2), ds_full = bar(3), ds_empty = bar(4),
-                 acc_full = bar(5), final_bar = bar(6);
-  auto r_full = [&](int s) { return bar(7 + s); };
-  auto r_empty = [&](int s) { return bar(9 + s); };
+  const uint32_t qo_full = bar(0), qo_empty = bar(1), s_full = bar(2), s_empty = bar(3), ds_full = bar(4),
+                 ds_empty = bar(5), acc_full = bar(6), acc_empty = bar(7), final_bar = bar(8);
+  auto r_full = [&](int s) { return bar(9 + s); };
+  auto r_empty = [&](int s) { return bar(11 + s); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t nq = A.s / TR;
-  const int64_t z = blockIdx.x / nq, iq = nq - 1 - (blockIdx.x % nq);  // longest rows first
-  const int64_t b = z / A.H, t = z % A.H;
-  const int niter = (int)iq + 1;
+  const int64_t nq = A.s / TR, items = A.Z * nq;
   const int nch = (int)(A.d / 64);
   const uint32_t dbytes = (uint32_t)(A.d * TR * 2);
 
   if (threadIdx.x == 0) {
-    for (int k = 0; k < 11; ++k) mbar_init(bar(k), (k == 2 || k == 3) ? kComputeWarps : 1);
+    for (int k = 0; k < 13; ++k) mbar_init(bar(k), (k == 3 || k == 4 || k == 7) ? kComputeWarps : 1);
     *c.abort_flag = 0;
     fence_barrier_init();
   }
@@ -545,17 +587,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      const int64_t row_q = b * A.s + iq * TR;
-      mbar_arrive_expect_tx(qo_full, 2 * dbytes);
-      load_tile(&mqkv, A.qkv, row_q, t * A.d, nch, sQ, qo_full);
-      load_tile(&mo, A.o, row_q, t * A.d, nch, sdO, qo_full);
-      for (int it = 0; it < niter; ++it) {
-        const int s = it & 1;
-        if (!mbar_wait(r_empty(s), ((it >> 1) & 1) ^ 1, c.abort_flag, A.err)) break;
-        mbar_arrive_expect_tx(r_full(s), 2 * dbytes);
-        const int64_t row_k = b * A.s + (int64_t)it * TR;
-        load_tile(&mqkv, A.qkv, row_k, A.h + t * A.d, nch, sK[s], r_full(s));
-        load_tile(&mqkv, A.qkv, row_k, 2 * A.h + t * A.d, nch, sV[s], r_full(s));
+      uint32_t n = 0, ic = 0;
+      bool ok = true;
+      for (int64_t w = blockIdx.x; w < items && ok; w += gridDim.x, ++ic) {
+        const int64_t iq = nq - 1 - w / A.Z, z = w % A.Z, b = z / A.H, t = z % A.H;
+        const int niter = (int)iq + 1;
+        if (!(ok = mbar_wait(qo_empty, (ic & 1) ^ 1, c.abort_flag, A.err))) break;
+        const int64_t row_q = b * A.s + iq * TR;
+        mbar_arrive_expect_tx(qo_full, 2 * dbytes);
+        load_tile(&mqkv, A.qkv, row_q, t * A.d, nch, sQ, qo_full);
+        load_tile(&mo, A.o, row_q, t * A.d, nch, sdO, qo_full);
+        for (int it = 0; it < niter; ++it, ++n) {
+          const int s = n & 1;
+          if (!(ok = mbar_wait(r_empty(s), ((n >> 1) & 1) ^ 1, c.abort_flag, A.err))) break;
+          mbar_arrive_expect_tx(r_full(s), 2 * dbytes);
+          const int64_t row_k = b * A.s + (int64_t)it * TR;
+          load_tile(&mqkv, A.qkv, row_k, A.h + t * A.d, nch, sK[s], r_full(s));
+          load_tile(&mqkv, A.qkv, row_k, 2 * A.h + t * A.d, nch, sV[s], r_full(s));
+        }
       }
     }
   } else if (warp == 1) {
@@ -563,22 +612,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t id_s = idesc_bf16_f32(TR, TR, 0, 0);
       const uint32_t id_acc = idesc_bf16_f32(TR, (int)A.d, 0, 1);
       const int ks_d = (int)(A.d / 16);
-      bool ok = mbar_wait(qo_full, 0, c.abort_flag, A.err);
-      for (int it = 0; it < niter && ok; ++it) {
-        const int s = it & 1;
-        if (!(ok = mbar_wait(r_full(s), (it >> 1) & 1, c.abort_flag, A.err))) break;
-        if (!(ok = mbar_wait(s_empty, (it & 1) ^ 1, c.abort_flag, A.err))) break;
-        tc_fence_after();
-        mma_tile(tmem, sQ, false, sK[s], false, ks_d, id_s, false);          // S = Q K^T
-        mma_tile(tmem + 128u, sdO, false, sV[s], false, ks_d, id_s, false);  // dP = dO V^T
-        umma_commit(s_full);
-        if (!(ok = mbar_wait(ds_full, it & 1, c.abort_flag, A.err))) break;
-        tc_fence_after();
-        mma_tile(tmem + 256u, sdS, false, sK[s], true, TR / 16, id_acc, it > 0);  // dQ += dS K
-        umma_commit(ds_empty);
-        umma_commit(r_empty(s));
+      uint32_t n = 0, ic = 0;
+      bool ok = true;
+      for (int64_t w = blockIdx.x; w < items && ok; w += gridDim.x, ++ic) {
+        const int niter = (int)(nq - 1 - w / A.Z) + 1;
+        if (!(ok = mbar_wait(qo_full, ic & 1, c.abort_flag, A.err))) break;
+        for (int it = 0; it < niter && ok; ++it, ++n) {
+          const int s = n & 1;
+          if (!(ok = mbar_wait(r_full(s), (n >> 1) & 1, c.abort_flag, A.err))) break;
+          if (!(ok = mbar_wait(s_empty, (n & 1) ^ 1, c.abort_flag, A.err))) break;
+          tc_fence_after();
+          mma_tile(tmem, sQ, false, sK[s], false, ks_d, id_s, false);          // S = Q K^T
+          mma_tile(tmem + 128u, sdO, false, sV[s], false, ks_d, id_s, false);  // dP = dO V^T
+          if (it == niter - 1) umma_commit(qo_empty);
+          umma_commit(s_full);
+          if (!(ok = mbar_wait(ds_full, n & 1, c.abort_flag, A.err))) break;
+          if (it == 0 && !(ok = mbar_wait(acc_empty, (ic & 1) ^ 1, c.abort_flag, A.err))) break;
+          tc_fence_after();
+          mma_tile(tmem + 256u, sdS, false, sK[s], true, TR / 16, id_acc, it > 0);  // dQ += dS K
+          umma_commit(ds_empty);
+          umma_commit(r_empty(s));
+        }
+        if (ok) umma_commit(acc_full);
       }
-      if (ok) umma_commit(acc_full);
       umma_commit(final_bar);
       drain(final_bar, 0);
     }
@@ -587,39 +643,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const float sl2 = A.scale * kLog2e;
-    const int64_t qrow = z * A.s + iq * TR + r;
-    const float l2 = lse[qrow] * kLog2e, dr = delta[qrow];
+    uint32_t n = 0, ic = 0;
     bool ok = true;
-    for (int it = 0; it < niter && ok; ++it) {
-      if (!(ok = warp_wait(s_full, it & 1, c, A.err, lane))) break;
-      if (!(ok = warp_wait(ds_empty, (it & 1) ^ 1, c, A.err, lane))) break;
-      tc_fence_after();
-      const bool diag = it == niter - 1;
+    for (int64_t w = blockIdx.x; w < items && ok; w += gridDim.x, ++ic) {
+      const int64_t iq = nq - 1 - w / A.Z, z = w % A.Z, b = z / A.H, t = z % A.H;
+      const int niter = (int)iq + 1;
+      const int64_t qrow = z * A.s + iq * TR + r;
+      const float l2 = lse[qrow] * kLog2e, dr = delta[qrow];
+      for (int it = 0; it < niter && ok; ++it, ++n) {
+        if (!(ok = warp_wait(s_full, n & 1, c, A.err, lane))) break;
+        if (!(ok = warp_wait(ds_empty, (n & 1) ^ 1, c, A.err, lane))) break;
+        tc_fence_after();
+        const bool diag = it == niter - 1;
 #pragma unroll 1
-      for (int cc = 0; cc < TR / 32; ++cc) {
-        uint32_t v[32], w[32];
-        tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(cc * 32)), v);
-        tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(128 + cc * 32)), w);
-        tmem_ld_wait();
+        for (int cc = 0; cc < TR / 32; ++cc) {
+          uint32_t v[32], wv[32];
+          tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(cc * 32)), v);
+          tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(128 + cc * 32)), wv);
+          tmem_ld_wait();
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          float f[8];
+          for (int g = 0; g < 4; ++g) {
+            float f[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int k = cc * 32 + g * 8 + e;
-            const float p = (!diag || k <= r) ? exp2f(__uint_as_float(v[g * 8 + e]) * sl2 - l2) : 0.0f;
-            f[e] = p * (__uint_as_float(w[g * 8 + e]) - dr) * A.scale;
+            for (int e = 0; e < 8; ++e) {
+              const int k = cc * 32 + g * 8 + e;
+              const float p = (!diag || k <= r) ? exp2f(__uint_as_float(v[g * 8 + e]) * sl2 - l2) : 0.0f;
+              f[e] = p * (__uint_as_float(wv[g * 8 + e]) - dr) * A.scale;
+            }
+            st_tile8(pdS, r, cc * 4 + g, pack8f(f));
           }
-          st_tile8(pdS, r, cc * 4 + g, pack8f(f));
         }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        warp_arrive(ds_full, lane);
+        warp_arrive(s_empty, lane);
       }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      warp_arrive(ds_full, lane);
-      warp_arrive(s_empty, lane);
-    }
-    if (ok) ok = warp_wait(acc_full, 0, c, A.err, lane);
-    if (ok) {
+      if (!ok || !(ok = warp_wait(acc_full, ic & 1, c, A.err, lane))) break;
       tc_fence_after();
       const int64_t grow = b * A.s + iq * TR + r;
       const int64_t gcol = t * A.d;
@@ -632,6 +691,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
         store_row32(dst + cc * 32, v);
       }
+      tc_fence_before();
+      warp_arrive(acc_empty, lane);
     }
   }
   tc_fence_before();
@@ -706,12 +767,12 @@ tp3d_status check(const AttnProblem& A) {
 
 tp3d_status launch_attn_fwd(const tp3d_ctx* ctx, const AttnProblem& A, const void* qkv, void* o, float* lse,
                             cudaStream_t s) {
-  (void)ctx;
   TP3D_TRY(check(A));
   CUtensorMap mq;
   TP3D_TRY(tile_map(&mq, A.qkv, qkv));
   TP3D_CUDA_TRY(cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem));
-  const unsigned grid = (unsigned)(A.Z * (A.s / TR));
+  const int64_t items = A.Z * (A.s / TR);
+  const unsigned grid = (unsigned)(items < ctx->num_sms ? items : ctx->num_sms);
   attn_fwd_kernel<<<grid, kThreads, kSmem, s>>>(mq, A, static_cast<bf16*>(o), lse);
   return cudaGetLastError() == cudaSuccess ? TP3D_OK : TP3D_ECUDA;
 }
@@ -730,7 +791,8 @@ tp3d_status launch_attn_bwd(const tp3d_ctx* ctx, const AttnProblem& A, const voi
   TP3D_CUDA_TRY(cudaGetLastError());
   TP3D_CUDA_TRY(cudaFuncSetAttribute(attn_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem));
   TP3D_CUDA_TRY(cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem));
-  const unsigned grid = (unsigned)(A.Z * (A.s / TR));
+  const int64_t items = A.Z * (A.s / TR);
+  const unsigned grid = (unsigned)(items < ctx->num_sms ? items : ctx->num_sms);
   attn_bwd_dkdv_kernel<<<grid, kThreads, kSmem, s>>>(mq, mo, A, lse, delta, static_cast<bf16*>(dqkv));
   TP3D_CUDA_TRY(cudaGetLastError());
   attn_bwd_dq_kernel<<<grid, kThreads, kSmem, s>>>(mq, mo, A, lse, delta, static_cast<bf16*>(dqkv));

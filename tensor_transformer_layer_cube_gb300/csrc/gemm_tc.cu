@@ -147,8 +147,14 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
 template <int BN>
 __device__ __forceinline__ void epilogue_tile(const GemmProblem& P, const TileInfo& T, bool any_k, int buf,
                                               uint32_t tmem_base, int warp, int lane, uint8_t* stg,
-                                              const CUtensorMap* mapC, const CUtensorMap* mapZ, uint32_t tempty,
-                                              bool tempty_remote, bool& pending) {
+                                              const CUtensorMap* mapC, const CUtensorMap* mapZ,
+                                              const CUtensorMap* mapX, uint32_t aux_bar, uint32_t& aux_phase,
+                                              volatile int* abort_flag, uint32_t tempty, bool tempty_remote,
+                                              bool& pending) {
+  // the residual or GELU input is fetched per chunk by TMA into the second
+  // half of the staging buffer (free when no pre-activation is saved)
+  const void* aux = P.epi.resid ? P.epi.resid : P.epi.gin;
+  const bool aux_ok = aux != nullptr && P.epi.zsave == nullptr && !P.epi.out_f32;
   const int quarter = warp & 3;
   const int half = (warp - 2) >> 2;
   const int row = quarter * 32 + lane;
@@ -170,9 +176,22 @@ __device__ __forceinline__ void epilogue_tile(const GemmProblem& P, const TileIn
 #pragma unroll 1
   for (int cc = 0; cc < CH; ++cc) {
     const int ch = half * CH + cc;
+    const int64_t n_ch = T.n0 + ch * 32;
+    const bool aux_tma = aux_ok && rows_full && n_ch + 32 <= T.n_end;
+    if (aux_tma && lane == 0) {
+      mbar_arrive_expect_tx(aux_bar, 2048u);
+      tma_load_3d(stg_z, mapX, aux_bar, (int)(gn0 + (n_ch - T.n0) - cbc * cg.bw), (int)(gm - lane - cbr * cg.bh),
+                  cg.shard((int32_t)cbr, (int32_t)cbc));
+    }
     uint32_t r[32];
     tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * BN + ch * 32), r);
     tmem_ld_wait();
+    if (aux_tma) {
+      bool ok = lane == 0 ? mbar_wait(aux_bar, aux_phase & 1u, abort_flag, P.err) : false;
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      ++aux_phase;
+      if (!ok) return;
+    }
     if (cc == CH - 1) {
       tc_fence_before();
       __syncwarp();
@@ -218,13 +237,17 @@ __device__ __forceinline__ void epilogue_tile(const GemmProblem& P, const TileIn
         for (int e = 0; e < 8; ++e) x[e] = gelu_f(x[e]);
       } else if (P.epi.act == EPI_GELU_BWD) {
         float zz[8];
-        unpack8(*reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(P.epi.gin) + off), zz);
+        unpack8(aux_tma ? *reinterpret_cast<const uint4*>(stg + 2048 + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4))
+                        : *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(P.epi.gin) + off),
+                zz);
 #pragma unroll
         for (int e = 0; e < 8; ++e) x[e] *= gelu_grad_f(zz[e]);
       }
       if (P.epi.resid) {
         float rr[8];
-        unpack8(*reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(P.epi.resid) + off), rr);
+        unpack8(aux_tma ? *reinterpret_cast<const uint4*>(stg + 2048 + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4))
+                        : *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(P.epi.resid) + off),
+                rr);
 #pragma unroll
         for (int e = 0; e < 8; ++e) x[e] += rr[e];
       }
@@ -266,7 +289,7 @@ template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                    const __grid_constant__ CUtensorMap mapC, const __grid_constant__ CUtensorMap mapZ,
-                   const GemmProblem P) {
+                   const __grid_constant__ CUtensorMap mapX, const GemmProblem P) {
   using Cfg = TcCfg<BN>;
   constexpr int S = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -275,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* base_ptr = smem_raw + (base - raw);
   uint8_t* stage_out = base_ptr + S * Cfg::STAGE_BYTES;  // kEpiWarps x 4 KiB, 1024-aligned
   uint64_t* bars = reinterpret_cast<uint64_t*>(stage_out + kEpiWarps * Cfg::STAGE_OUT);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 5 + kEpiWarps);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const uint32_t bar0 = smem_u32(bars);
@@ -284,6 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * S + b); };
   auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * S + 2 + b); };
   const uint32_t final_bar = bar0 + 8u * (2 * S + 4);
+  auto aux_bar = [&](int ew) { return bar0 + 8u * (2 * S + 5 + ew); };  // one per epilogue warp
   auto a_stage = [&](int s) { return base + (uint32_t)(s * Cfg::A_BYTES); };
   auto b_stage = [&](int s) { return base + (uint32_t)(S * Cfg::A_BYTES + s * Cfg::B_BYTES); };
 
@@ -299,6 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(tempty_bar(b), kEpiWarps);
     }
     mbar_init(final_bar, 1);
+    for (int e = 0; e < kEpiWarps; ++e) mbar_init(aux_bar(e), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -486,6 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // -------------------------------------------------------------- epilogue
     uint32_t tc = 0;
     bool pending = false;  // a TMA store still reads this warp's staging buffer
+    uint32_t aux_phase = 0;
     uint8_t* stg = stage_out + (warp - 2) * Cfg::STAGE_OUT;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
       TileInfo T;
@@ -502,7 +528,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       tc_fence_after();
-      epilogue_tile<BN>(P, T, any_k, buf, tmem_base, warp, lane, stg, &mapC, &mapZ, tempty_bar(buf), false, pending);
+      epilogue_tile<BN>(P, T, any_k, buf, tmem_base, warp, lane, stg, &mapC, &mapZ, &mapX, aux_bar(warp - 2),
+                        aux_phase, abort_flag, tempty_bar(buf), false, pending);
       ++tc;
     }
     if (lane == 0) bulk_wait_all();
@@ -565,7 +592,7 @@ __device__ __forceinline__ int64_t total_pair_tiles(const GemmProblem& P) {
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                     const __grid_constant__ CUtensorMap mapC, const __grid_constant__ CUtensorMap mapZ,
-                    const GemmProblem P) {
+                    const __grid_constant__ CUtensorMap mapX, const GemmProblem P) {
   using Cfg = Tc2Cfg;
   constexpr int S = Cfg::STAGES;
   constexpr int BN = Cfg::BN;
@@ -575,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* base_ptr = smem_raw + (base - raw);
   uint8_t* stage_out = base_ptr + S * Cfg::STAGE_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(stage_out + kEpiWarps * Cfg::STAGE_OUT);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 5 + kEpiWarps);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const uint32_t bar0 = smem_u32(bars);
@@ -584,6 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * S + b); };
   auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * S + 2 + b); };
   const uint32_t final_bar = bar0 + 8u * (2 * S + 4);
+  auto aux_bar = [&](int ew) { return bar0 + 8u * (2 * S + 5 + ew); };  // one per epilogue warp
   auto a_stage = [&](int s) { return base + (uint32_t)(s * Cfg::A_BYTES); };
   auto b_stage = [&](int s) { return base + (uint32_t)(S * Cfg::A_BYTES + s * Cfg::B_BYTES); };
 
@@ -601,6 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(tempty_bar(b), 2 * kEpiWarps);
     }
     mbar_init(final_bar, 1);
+    for (int e = 0; e < kEpiWarps; ++e) mbar_init(aux_bar(e), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -771,6 +800,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue (both CTAs)
     uint32_t tc = 0;
     bool pending = false;
+    uint32_t aux_phase = 0;
     uint8_t* stg = stage_out + (warp - 2) * Cfg::STAGE_OUT;
     for (int64_t t = cid; t < ntiles; t += nclusters) {
       TileInfo T;
@@ -781,8 +811,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       tc_fence_after();
-      epilogue_tile<BN>(P, T, true, buf, tmem_base, warp, lane, stg, &mapC, &mapZ, map_to_cta(tempty_bar(buf), 0),
-                        true, pending);
+      epilogue_tile<BN>(P, T, true, buf, tmem_base, warp, lane, stg, &mapC, &mapZ, &mapX, aux_bar(warp - 2),
+                        aux_phase, abort_flag, map_to_cta(tempty_bar(buf), 0), true, pending);
       ++tc;
     }
     if (lane == 0) bulk_wait_all();
@@ -829,7 +859,7 @@ tp3d_status make_map(CUtensorMap* m, const Grid& g, const void* ptr, uint32_t bo
 template <int BN>
 tp3d_status launch(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t s) {
   using Cfg = TcCfg<BN>;
-  CUtensorMap ma, mb, mc, mz;
+  CUtensorMap ma, mb, mc, mz, mx;
   TP3D_TRY(make_map(&ma, P.a.g, P.a.ptr, 64, P.a.mn_major ? 64 : BM));
   TP3D_TRY(make_map(&mb, P.b.g, P.b.ptr, 64, P.b.mn_major ? 64 : BN));
   // output boxes: 32 rows x 32 columns (64-byte bf16 rows or 128-byte fp32 rows)
@@ -841,18 +871,23 @@ tp3d_status launch(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t s) {
     TP3D_TRY(make_map(&mz, P.c.g, P.epi.zsave, 32, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, CU_TENSOR_MAP_SWIZZLE_64B));
   else
     mz = mc;
+  const void* aux = P.epi.resid ? P.epi.resid : P.epi.gin;
+  if (aux)
+    TP3D_TRY(make_map(&mx, P.c.g, aux, 32, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, CU_TENSOR_MAP_SWIZZLE_64B));
+  else
+    mx = mc;
   TP3D_CUDA_TRY(cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM));
   const int64_t tpsM = (P.segM + BM - 1) / BM, tpsN = (P.segN + BN - 1) / BN;
   const int64_t ntiles = (int64_t)P.Z * (P.M / P.segM) * tpsM * (P.N / P.segN) * tpsN;
   if (ntiles <= 0) return TP3D_OK;
   const int grid = (int)(ntiles < ctx->num_sms ? ntiles : ctx->num_sms);
-  gemm_tc_kernel<BN><<<grid, kThreads, Cfg::SMEM, s>>>(ma, mb, mc, mz, P);
+  gemm_tc_kernel<BN><<<grid, kThreads, Cfg::SMEM, s>>>(ma, mb, mc, mz, mx, P);
   return cudaGetLastError() == cudaSuccess ? TP3D_OK : TP3D_ECUDA;
 }
 
 tp3d_status launch_pair(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t s) {
   using Cfg = Tc2Cfg;
-  CUtensorMap ma, mb, mc, mz;
+  CUtensorMap ma, mb, mc, mz, mx;
   TP3D_TRY(make_map(&ma, P.a.g, P.a.ptr, 64, P.a.mn_major ? 64 : 128));
   TP3D_TRY(make_map(&mb, P.b.g, P.b.ptr, 64, P.b.mn_major ? 64 : 128));
   if (P.epi.out_f32)
@@ -863,6 +898,11 @@ tp3d_status launch_pair(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t 
     TP3D_TRY(make_map(&mz, P.c.g, P.epi.zsave, 32, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, CU_TENSOR_MAP_SWIZZLE_64B));
   else
     mz = mc;
+  const void* aux = P.epi.resid ? P.epi.resid : P.epi.gin;
+  if (aux)
+    TP3D_TRY(make_map(&mx, P.c.g, aux, 32, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, CU_TENSOR_MAP_SWIZZLE_64B));
+  else
+    mx = mc;
   TP3D_CUDA_TRY(cudaFuncSetAttribute(gemm_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM));
   const int64_t ntiles = (int64_t)P.Z * (P.M / P.segM) * ((P.segM + 255) / 256) * (P.N / P.segN) *
                          ((P.segN + 255) / 256);
@@ -884,7 +924,7 @@ tp3d_status launch_pair(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t 
     max_clusters = ctx->num_sms / 2;
   const int64_t nc = ntiles < max_clusters ? ntiles : max_clusters;
   cfg.gridDim = dim3(2 * (unsigned)nc);
-  TP3D_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_tc2_kernel, ma, mb, mc, mz, P));
+  TP3D_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_tc2_kernel, ma, mb, mc, mz, mx, P));
   return TP3D_OK;
 }
 
@@ -905,17 +945,21 @@ tp3d_status gemm_bf16_tc(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t
     const int64_t kb = P.b.mn_major ? P.b.g.bh : P.b.g.bw;
     if (ka != P.segK && kb != P.segK) return TP3D_EUNSUPPORTED;
   }
-  // CTA pairs (256 x 256 tiles) when there is no causal mask, the segments
-  // hold whole 256-row / 256-column pair tiles, and the pair tiles fill the
-  // GPU; else one CTA per tile, 128 x 256 or, for narrow or small problems,
-  // 128 x 128.
-  const int64_t pair_tiles = (int64_t)P.Z * (P.M / P.segM) * ((P.segM + 255) / 256) * (P.N / P.segN) *
-                             ((P.segN + 255) / 256);
-  if (P.causal == CAUSAL_NONE && P.segM >= 256 && P.segN >= 256 && pair_tiles >= ctx->num_sms / 2)
-    return launch_pair(ctx, P, s);
-  const int64_t tiles256 = (int64_t)P.Z * (P.M / P.segM) * ((P.segM + BM - 1) / BM) * (P.N / P.segN) * ((P.segN + 255) / 256);
-  const bool narrow = P.segN <= 128 || tiles256 < ctx->num_sms;
-  return narrow ? launch<128>(ctx, P, s) : launch<256>(ctx, P, s);
+  // Pick the tile shape by a wave-count cost model: the time of one SM on a
+  // 128 x 256 x K slice is one unit at the shape's measured efficiency
+  // (CTA pairs move the least data per product and reach the highest).
+  // Pairs need no causal mask and segments that hold whole 256 x 256 tiles.
+  auto tiles = [&](int64_t tm, int64_t tn) {
+    return (int64_t)P.Z * (P.M / P.segM) * ((P.segM + tm - 1) / tm) * (P.N / P.segN) * ((P.segN + tn - 1) / tn);
+  };
+  auto waves = [&](int64_t n, int64_t slots) { return (double)((n + slots - 1) / slots); };
+  const int64_t sms = ctx->num_sms;
+  const double c256 = P.segN > 128 ? waves(tiles(BM, 256), sms) / 0.60 : 1e30;
+  const double c128 = waves(tiles(BM, 128), sms) * 0.5 / 0.45;
+  const double cpair = (P.causal == CAUSAL_NONE && P.segM >= 256 && P.segN >= 256)
+                           ? waves(tiles(256, 256), sms / 2) / 0.80 : 1e30;
+  if (cpair <= c256 && cpair <= c128) return launch_pair(ctx, P, s);
+  return c256 <= c128 ? launch<256>(ctx, P, s) : launch<128>(ctx, P, s);
 }
 
 tp3d_status plan_segments(GemmProblem& P) {
