@@ -137,12 +137,17 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
 // One tile's epilogue for the calling epilogue warp (32 rows x BN/2 columns
 // of the tile's TMEM accumulator `buf`).  Warp w may read TMEM lanes
 // 32*(w%4) .. +31 only: two warps share each lane quarter (= 32 rows of the
-// tile) and split its columns in halves.  A 32-row x 32-column chunk that
-// lies inside the tile's segment goes out through this warp's shared-memory
-// staging buffer and one TMA store per output (64-byte swizzle for bf16 rows
-// of 64 bytes, 128-byte swizzle for fp32 rows of 128 bytes); a chunk that
-// crosses the segment's edge is written element-wise under a mask.  After
-// its last TMEM load the warp arrives on `tempty` (in the peer CTA when
+// tile) and split its columns in halves, 32 columns per chunk.
+// A chunk inside the tile's segment (the common case) takes the fast path:
+//  - the residual or GELU input comes by TMA into the second half of the
+//    warp's staging buffer; the next chunk's load is issued as soon as this
+//    one has been read, so its latency hides behind the arithmetic;
+//  - the results are computed into registers first, then (once the previous
+//    TMA store has finished reading the staging buffer) written there with
+//    the 64-byte (bf16) or 128-byte (fp32) swizzle and sent out by one TMA
+//    store per output.
+// A chunk crossing the segment's edge is written element-wise under a mask.
+// After its last TMEM load the warp arrives on `tempty` (in the peer CTA when
 // `tempty_remote`, a shared::cluster address).
 template <int BN>
 __device__ __forceinline__ void epilogue_tile(const GemmProblem& P, const TileInfo& T, bool any_k, int buf,
@@ -151,8 +156,6 @@ __device__ __forceinline__ void epilogue_tile(const GemmProblem& P, const TileIn
                                               const CUtensorMap* mapX, uint32_t aux_bar, uint32_t& aux_phase,
                                               volatile int* abort_flag, uint32_t tempty, bool tempty_remote,
                                               bool& pending) {
-  // the residual or GELU input is fetched per chunk by TMA into the second
-  // half of the staging buffer (free when no pre-activation is saved)
   const void* aux = P.epi.resid ? P.epi.resid : P.epi.gin;
   const bool aux_ok = aux != nullptr && P.epi.zsave == nullptr && !P.epi.out_f32;
   const int quarter = warp & 3;
@@ -168,30 +171,30 @@ __device__ __forceinline__ void epilogue_tile(const GemmProblem& P, const TileIn
   const int64_t gm = m + op_off(P.c.hi1, P.c.lo1, P.c.base1, T.z, P.Hz);
   const int64_t gn0 = T.n0 + op_off(P.c.hi2, P.c.lo2, P.c.base2, T.z, P.Hz);
   const int64_t cbr = (gm - lane) / cg.bh, cbc = gn0 / cg.bw;  // C block of the warp's rows
+  const int c1 = (int)(gm - lane - cbr * cg.bh);
+  const int c2 = cg.shard((int32_t)cbr, (int32_t)cbc);
   int64_t row_base = 0;
   if (row_ok) {
     const int64_t br = gm / cg.bh;
     row_base = cg.block_base((int32_t)br, (int32_t)cbc) + (gm - br * cg.bh) * cg.bw + (gn0 - cbc * cg.bw);
   }
+  auto chunk_n = [&](int cc) { return T.n0 + (half * CH + cc) * 32; };
+  auto fast = [&](int cc) { return rows_full && chunk_n(cc) + 32 <= T.n_end; };
+  auto chunk_c0 = [&](int cc) { return (int)(gn0 + (chunk_n(cc) - T.n0) - cbc * cg.bw); };
+  auto aux_issue = [&](int cc) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(aux_bar, 2048u);
+      tma_load_3d(stg_z, mapX, aux_bar, chunk_c0(cc), c1, c2);
+    }
+  };
+  if (aux_ok && fast(0)) aux_issue(0);
+  const __nv_bfloat16* bias = static_cast<const __nv_bfloat16*>(P.epi.bias);
 #pragma unroll 1
   for (int cc = 0; cc < CH; ++cc) {
     const int ch = half * CH + cc;
-    const int64_t n_ch = T.n0 + ch * 32;
-    const bool aux_tma = aux_ok && rows_full && n_ch + 32 <= T.n_end;
-    if (aux_tma && lane == 0) {
-      mbar_arrive_expect_tx(aux_bar, 2048u);
-      tma_load_3d(stg_z, mapX, aux_bar, (int)(gn0 + (n_ch - T.n0) - cbc * cg.bw), (int)(gm - lane - cbr * cg.bh),
-                  cg.shard((int32_t)cbr, (int32_t)cbc));
-    }
     uint32_t r[32];
     tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * BN + ch * 32), r);
     tmem_ld_wait();
-    if (aux_tma) {
-      bool ok = lane == 0 ? mbar_wait(aux_bar, aux_phase & 1u, abort_flag, P.err) : false;
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      ++aux_phase;
-      if (!ok) return;
-    }
     if (cc == CH - 1) {
       tc_fence_before();
       __syncwarp();
@@ -202,85 +205,126 @@ __device__ __forceinline__ void epilogue_tile(const GemmProblem& P, const TileIn
           mbar_arrive(tempty);
       }
     }
-    const int64_t n = T.n0 + ch * 32;
+    const int64_t n = chunk_n(cc);
     if (n >= T.n_end) continue;
-    const bool via_tma = rows_full && n + 32 <= T.n_end;
-    if (via_tma && pending) {
-      if (lane == 0) bulk_wait_read_all();
-      __syncwarp();
-      pending = false;
-    }
-    if (!via_tma && !row_ok) continue;
+    if (fast(cc)) {
+      // ---------------------------------------------------------- fast path
+      // sv: the auxiliary input read from staging, or the pre-activation to
+      // save (a problem never has both)
+      uint4 sv[4];
+      if (aux_ok) {
+        bool ok = lane == 0 ? mbar_wait(aux_bar, aux_phase & 1u, abort_flag, P.err) : false;
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        ++aux_phase;
+        if (!ok) return;
 #pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      const int64_t nv = n + v * 8;
-      if (!via_tma && nv >= T.n_end) break;
-      const int64_t off = row_base + (nv - T.n0);
-      float x[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = any_k ? __uint_as_float(r[v * 8 + e]) * P.epi.alpha : 0.0f;
-      if (P.epi.bias) {
-        float bb[8];
-        unpack8(*reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(P.epi.bias) + (gn0 + (nv - T.n0))), bb);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] += bb[e];
+        for (int v = 0; v < 4; ++v)
+          sv[v] = *reinterpret_cast<const uint4*>(stg + 2048 + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4));
+        __syncwarp();
+        if (cc + 1 < CH && fast(cc + 1)) aux_issue(cc + 1);
       }
-      if (P.epi.zsave) {
-        const uint4 zv = pack8(x);
-        if (via_tma)
-          *reinterpret_cast<uint4*>(stg + 2048 + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4)) = zv;
-        else
-          *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(P.epi.zsave) + off) = zv;
+      if (f32 && pending) {  // fp32 rows fill the whole staging buffer: wait before writing
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+        pending = false;
       }
-      if (P.epi.act == EPI_GELU) {
+      uint4 yv[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = gelu_f(x[e]);
-      } else if (P.epi.act == EPI_GELU_BWD) {
-        float zz[8];
-        unpack8(aux_tma ? *reinterpret_cast<const uint4*>(stg + 2048 + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4))
-                        : *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(P.epi.gin) + off),
-                zz);
+      for (int v = 0; v < 4; ++v) {
+        float x[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] *= gelu_grad_f(zz[e]);
-      }
-      if (P.epi.resid) {
-        float rr[8];
-        unpack8(aux_tma ? *reinterpret_cast<const uint4*>(stg + 2048 + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4))
-                        : *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(P.epi.resid) + off),
-                rr);
+        for (int e = 0; e < 8; ++e) x[e] = any_k ? __uint_as_float(r[v * 8 + e]) * P.epi.alpha : 0.0f;
+        if (bias) {
+          float bb[8];
+          unpack8(*reinterpret_cast<const uint4*>(bias + (gn0 + (n - T.n0) + v * 8)), bb);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] += rr[e];
-      }
-      if (!f32) {
-        const uint4 yv = pack8(x);
-        if (via_tma)
-          *reinterpret_cast<uint4*>(stg + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4)) = yv;
-        else
-          *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(const_cast<void*>(P.c.ptr)) + off) = yv;
-      } else {
-        const float4 lo = make_float4(x[0], x[1], x[2], x[3]), hi = make_float4(x[4], x[5], x[6], x[7]);
-        if (via_tma) {
-          *reinterpret_cast<float4*>(stg + lane * 128 + (((2 * v) ^ (lane & 7)) << 4)) = lo;
-          *reinterpret_cast<float4*>(stg + lane * 128 + (((2 * v + 1) ^ (lane & 7)) << 4)) = hi;
+          for (int e = 0; e < 8; ++e) x[e] += bb[e];
+        }
+        if (P.epi.zsave) sv[v] = pack8(x);
+        if (P.epi.act == EPI_GELU) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = gelu_f(x[e]);
+        } else if (P.epi.act == EPI_GELU_BWD) {
+          float zz[8];
+          unpack8(sv[v], zz);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] *= gelu_grad_f(zz[e]);
+        }
+        if (P.epi.resid) {
+          float rr[8];
+          unpack8(sv[v], rr);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] += rr[e];
+        }
+        if (!f32) {
+          yv[v] = pack8(x);
         } else {
-          float4* o = reinterpret_cast<float4*>(static_cast<float*>(const_cast<void*>(P.c.ptr)) + off);
-          o[0] = lo;
-          o[1] = hi;
+          *reinterpret_cast<float4*>(stg + lane * 128 + (((2 * v) ^ (lane & 7)) << 4)) = make_float4(x[0], x[1], x[2], x[3]);
+          *reinterpret_cast<float4*>(stg + lane * 128 + (((2 * v + 1) ^ (lane & 7)) << 4)) = make_float4(x[4], x[5], x[6], x[7]);
         }
       }
-    }
-    if (via_tma) {
+      if (!f32) {
+        if (pending) {
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+          pending = false;
+        }
+#pragma unroll
+        for (int v = 0; v < 4; ++v) *reinterpret_cast<uint4*>(stg + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4)) = yv[v];
+        if (P.epi.zsave) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            *reinterpret_cast<uint4*>(stg + 2048 + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4)) = sv[v];
+        }
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        const int c0 = (int)(gn0 + (n - T.n0) - cbc * cg.bw);
-        const int c1 = (int)(gm - lane - cbr * cg.bh);
-        const int c2 = cg.shard((int32_t)cbr, (int32_t)cbc);
-        tma_store_3d(mapC, stg_y, c0, c1, c2);
-        if (P.epi.zsave) tma_store_3d(mapZ, stg_z, c0, c1, c2);
+        tma_store_3d(mapC, stg_y, chunk_c0(cc), c1, c2);
+        if (P.epi.zsave) tma_store_3d(mapZ, stg_z, chunk_c0(cc), c1, c2);
         bulk_commit();
       }
       pending = true;
+    } else if (row_ok) {
+      // ---------------------------------------------------------- masked path
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const int64_t nv = n + v * 8;
+        if (nv >= T.n_end) break;
+        const int64_t off = row_base + (nv - T.n0);
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = any_k ? __uint_as_float(r[v * 8 + e]) * P.epi.alpha : 0.0f;
+        if (bias) {
+          float bb[8];
+          unpack8(*reinterpret_cast<const uint4*>(bias + (gn0 + (nv - T.n0))), bb);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] += bb[e];
+        }
+        if (P.epi.zsave) *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(P.epi.zsave) + off) = pack8(x);
+        if (P.epi.act == EPI_GELU) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = gelu_f(x[e]);
+        } else if (P.epi.act == EPI_GELU_BWD) {
+          float zz[8];
+          unpack8(*reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(P.epi.gin) + off), zz);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] *= gelu_grad_f(zz[e]);
+        }
+        if (P.epi.resid) {
+          float rr[8];
+          unpack8(*reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(P.epi.resid) + off), rr);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] += rr[e];
+        }
+        if (!f32) {
+          *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(const_cast<void*>(P.c.ptr)) + off) = pack8(x);
+        } else {
+          float4* o = reinterpret_cast<float4*>(static_cast<float*>(const_cast<void*>(P.c.ptr)) + off);
+          o[0] = make_float4(x[0], x[1], x[2], x[3]);
+          o[1] = make_float4(x[4], x[5], x[6], x[7]);
+        }
+      }
     }
   }
 }
