@@ -181,8 +181,8 @@ class MlpBench:
             self.t.check(self.t.tp3d_linear(self.ctx, w["q"], 0, w["M"], w["h"], w["f"], self.t.TP3D_BF16, self.X,
                                             self.W1, self.b1, 1, self.Y1), "tp3d_linear")
         fl = 2.0 * w["M"] * w["h"] * w["f"]
-        return launch, fl, (f"gemm_tc_kernel: 3-D linear 1 of the MLP (M={w['M']}, N={w['h']}, K={w['f']}, "
-                            f"q={w['q']}, bias+GELU epilogue), {fl / 1e9:.2f} GFLOP per launch")
+        return launch, fl, (f"gemm_tc2_kernel (CTA-pair tcgen05 GEMM): 3-D linear 1 of the MLP (M={w['M']}, "
+                            f"N={w['h']}, K={w['f']}, q={w['q']}, bias+GELU epilogue), {fl / 1e9:.2f} GFLOP per launch")
 
 
 class LayerBench:
@@ -258,8 +258,9 @@ class LayerBench:
             self.t.check(self.t.tp3d_linear(self.ctx, self.q, 0, self.M, self.h, self.f, self.t.TP3D_BF16, self.X,
                                             p["w_1"], p["b_1"], 1, Y1), "tp3d_linear")
         fl = 2.0 * self.M * self.h * self.f
-        return launch, fl, (f"gemm_tc_kernel: the layer's MLP linear 1 (M={self.M}, N={self.h}, K={self.f}, "
-                            f"q={self.q}, bias+GELU epilogue), {fl / 1e9:.2f} GFLOP per launch")
+        return launch, fl, (f"gemm_tc2_kernel (CTA-pair tcgen05 GEMM): the layer's MLP linear 1 (M={self.M}, "
+                            f"N={self.h}, K={self.f}, q={self.q}, bias+GELU epilogue, pre-activation saved by the "
+                            f"layer), {fl / 1e9:.2f} GFLOP per launch")
 
 
 class LinearF32Bench:
