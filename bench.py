@@ -450,6 +450,58 @@ def reshard_summary(torch, rb, flush, stream, pk, reps=5):
         "workload": WORKLOADS["reshard"]["name"]}
 
 
+def host_planner_summary(t):
+    """The library's host-side planners, timed on the CPU: the cross-mesh
+    resharding planner on a 8192 x 8192 bf16 activation handed from a
+    (8, 16) mesh S1 R (16 row slices, each held on all 8 source hosts) to a
+    (8, 16) mesh S01 R (16 devices per host), and the pipeline simulator on
+    the printed bubble-table configurations.  The oracle's planner is timed
+    beside it as the CPU baseline."""
+    from oracle import cmr as OC
+    from oracle import layouts as OL
+
+    R = C = 8192
+    _, src = t.tp3d_mesh_rects(R, C, t.tp3d_mesh_spec(8, 16, t.TP3D_SPEC_S1, t.TP3D_SPEC_R))
+    _, dst = t.tp3d_mesh_rects(R, C, t.tp3d_mesh_spec(8, 16, t.TP3D_SPEC_S01, t.TP3D_SPEC_R))
+    st, plan = t.tp3d_cmr_plan_create(R, C, 2, src, 0, dst, 128, 16)
+    t.check(st, "tp3d_cmr_plan_create")
+    out = {"instance": "8192 x 8192 bf16, (8, 16) S1 R on devices 0-127 -> (8, 16) S01 R on devices 128-255, "
+                       "16 devices per host; durations in bytes at unit bandwidth",
+           "tasks": t.tp3d_cmr_plan_num_tasks(plan), "lower_bound": t.tp3d_cmr_plan_lower_bound(plan)}
+    algos = {"naive": (t.TP3D_CMR_NAIVE, {}), "load_balance": (t.TP3D_CMR_LOAD_BALANCE, {}),
+             "random_greedy": (t.TP3D_CMR_RANDOM_GREEDY, {"trials": 16, "seed": 20260}),
+             "dfs": (t.TP3D_CMR_DFS, {"node_limit": 200000})}
+    for name, (algo, kw) in algos.items():
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            st, _, _, _, res = t.tp3d_cmr_schedule(plan, algo, **kw)
+            t.check(st, "tp3d_cmr_schedule")
+            reps += 1
+            if time.perf_counter() - t0 > 0.2:
+                break
+        out[name] = {"makespan_over_lower_bound": res.makespan / out["lower_bound"],
+                     "us_per_plan": (time.perf_counter() - t0) / reps * 1e6}
+        if name == "dfs":
+            out[name].update({"nodes": res.nodes, "complete": bool(res.complete)})
+    t.tp3d_cmr_plan_destroy(plan)
+    t0 = time.perf_counter()
+    tasks = OC.make_tasks(OL.MeshSpec(8, 16, ("S1", "R")), OL.MeshSpec(8, 16, ("S01", "R")), R, C, 2, 0, 128, 16)
+    OC.random_greedy(tasks, 16, 20260)
+    out["cpu_baseline"] = {"kind": "oracle", "cores": 1, "what": "oracle unit tasks + randomised greedy, same "
+                           "instance", "us_per_plan": (time.perf_counter() - t0) * 1e6}
+    rows = []
+    for sch, p, m, v in (("gpipe", 4, 8, 1), ("1f1b", 4, 8, 1), ("interleaved", 4, 8, 2), ("interleaved", 4, 8, 4),
+                         ("1f1b", 8, 32, 1), ("interleaved", 8, 32, 4), ("gpipe", 16, 32, 1), ("1f1b", 16, 64, 1)):
+        code = {"gpipe": t.TP3D_PIPE_GPIPE, "1f1b": t.TP3D_PIPE_1F1B, "interleaved": t.TP3D_PIPE_INTERLEAVED}[sch]
+        t0 = time.perf_counter()
+        st, res, _ = t.tp3d_pipeline_simulate(t.tp3d_pipe_cfg(code, p, m, v, 4, 8))
+        t.check(st, "tp3d_pipeline_simulate")
+        rows.append({"schedule": sch, "p": p, "m": m, "v": v, "bubble": res.bubble,
+                     "closed_form": (p - 1) / (v * m), "us": (time.perf_counter() - t0) * 1e6})
+    out["pipeline"] = rows
+    return out
+
+
 def make_bench(t, ctx, dev, name):
     w = WORKLOADS[name]
     return BENCHES[w["kind"]](t, ctx, dev, w)
@@ -551,6 +603,7 @@ def run_ours(args, rank, world, dist):
             del eb
             torch.cuda.empty_cache()
         line["configs"] = extras
+        line["host_planners"] = host_planner_summary(t)
         st = t.tp3d_sync_status(ctx)
         if st != 0:
             raise SystemExit(f"device error in the extra workloads: {t.STATUS[st]}")

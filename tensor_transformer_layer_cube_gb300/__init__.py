@@ -5,7 +5,9 @@ block and GPT decoder layer of "Maximizing Parallelism in Distributed
 Training for Huge Neural Networks" over a virtual q x q x q device cube held
 in one GB300's memory, plus bit-exact resharding between row, column, 2-D
 block, cube and replicated layouts ("On Optimizing the Communication of Model
-Parallelism", §2), in hand-written sm_103a kernels.
+Parallelism", §2), in hand-written sm_103a kernels; and (``include/tp3d_plan.h``)
+the host-side planners: the cross-mesh resharding planner of that page's
+§3.2 and a pipeline-bubble simulator.
 
 This module only marshals arguments: every function has the name of the C
 entry point it calls and returns its status code (0 = TP3D_OK).  Tensor
@@ -28,12 +30,21 @@ __all__ = [
     "tp3d_linear", "tp3d_mlp", "tp3d_mlp_noalloc", "tp3d_layer_workspace_bytes", "tp3d_layer_fwd", "tp3d_layer_bwd",
     "tp3d_layout", "tp3d_layer_cfg", "tp3d_layer_params", "tp3d_layer_grads",
     "TP3D_F32", "TP3D_BF16", "CUBE_A", "CUBE_B", "CUBE_C", "CUBE_B_SWAP", "ROW", "COL", "BLOCK2D", "REPLICATED",
+    "tp3d_rect", "tp3d_mesh_spec", "tp3d_cmr_options", "tp3d_cmr_result", "tp3d_pipe_cfg", "tp3d_pipe_op",
+    "tp3d_pipe_result", "tp3d_layout_rects", "tp3d_mesh_rects", "tp3d_cmr_plan_create", "tp3d_cmr_plan_destroy",
+    "tp3d_cmr_plan_num_tasks", "tp3d_cmr_plan_task", "tp3d_cmr_plan_lower_bound", "tp3d_cmr_schedule",
+    "tp3d_pipeline_simulate", "TP3D_SPEC_R", "TP3D_SPEC_S0", "TP3D_SPEC_S1", "TP3D_SPEC_S01", "TP3D_CMR_NAIVE",
+    "TP3D_CMR_LOAD_BALANCE", "TP3D_CMR_DFS", "TP3D_CMR_RANDOM_GREEDY", "TP3D_PIPE_GPIPE", "TP3D_PIPE_1F1B",
+    "TP3D_PIPE_INTERLEAVED",
 ]
 
 STATUS = {0: "TP3D_OK", 1: "TP3D_EINVAL", 2: "TP3D_ESHAPE", 3: "TP3D_EALIGN", 4: "TP3D_EDTYPE",
           5: "TP3D_ECUDA", 6: "TP3D_ETIMEOUT", 7: "TP3D_EUNSUPPORTED", 8: "TP3D_EOVERLAP"}
 TP3D_F32, TP3D_BF16 = 0, 1
 CUBE_A, CUBE_B, CUBE_C, CUBE_B_SWAP, ROW, COL, BLOCK2D, REPLICATED = range(8)
+TP3D_SPEC_R, TP3D_SPEC_S0, TP3D_SPEC_S1, TP3D_SPEC_S01 = range(4)
+TP3D_CMR_NAIVE, TP3D_CMR_LOAD_BALANCE, TP3D_CMR_DFS, TP3D_CMR_RANDOM_GREEDY = range(4)
+TP3D_PIPE_GPIPE, TP3D_PIPE_1F1B, TP3D_PIPE_INTERLEAVED = range(3)
 
 
 class tp3d_layout(ctypes.Structure):
@@ -55,6 +66,41 @@ class tp3d_layer_params(ctypes.Structure):
 
 class tp3d_layer_grads(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in PARAM_NAMES]
+
+
+class tp3d_rect(ctypes.Structure):
+    _fields_ = [("row0", ctypes.c_int64), ("rows", ctypes.c_int64), ("col0", ctypes.c_int64),
+                ("cols", ctypes.c_int64)]
+
+
+class tp3d_mesh_spec(ctypes.Structure):
+    _fields_ = [("m1", ctypes.c_int32), ("m2", ctypes.c_int32), ("row_spec", ctypes.c_int32),
+                ("col_spec", ctypes.c_int32)]
+
+
+class tp3d_cmr_options(ctypes.Structure):
+    _fields_ = [("algo", ctypes.c_int32), ("trials", ctypes.c_int32), ("seed", ctypes.c_uint64),
+                ("node_limit", ctypes.c_int64)]
+
+
+class tp3d_cmr_result(ctypes.Structure):
+    _fields_ = [("makespan", ctypes.c_int64), ("nodes", ctypes.c_int64), ("complete", ctypes.c_int32),
+                ("rounds", ctypes.c_int32)]
+
+
+class tp3d_pipe_cfg(ctypes.Structure):
+    _fields_ = [("schedule", ctypes.c_int32), ("p", ctypes.c_int32), ("m", ctypes.c_int32), ("v", ctypes.c_int32),
+                ("t_f", ctypes.c_int64), ("t_b", ctypes.c_int64)]
+
+
+class tp3d_pipe_op(ctypes.Structure):
+    _fields_ = [("device", ctypes.c_int32), ("microbatch", ctypes.c_int32), ("chunk", ctypes.c_int32),
+                ("backward", ctypes.c_int32), ("start", ctypes.c_int64), ("end", ctypes.c_int64)]
+
+
+class tp3d_pipe_result(ctypes.Structure):
+    _fields_ = [("makespan", ctypes.c_int64), ("busy", ctypes.c_int64), ("idle", ctypes.c_int64),
+                ("bubble", ctypes.c_double), ("max_in_flight", ctypes.c_int32)]
 
 
 class Tp3dError(RuntimeError):
@@ -99,6 +145,26 @@ _SIGS = {
                                       ctypes.POINTER(tp3d_layer_params), ctypes.c_void_p, ctypes.c_void_p,
                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(tp3d_layer_grads),
                                       ctypes.c_void_p]),
+    "tp3d_layout_rects": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, tp3d_layout, ctypes.POINTER(tp3d_rect),
+                                         ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]),
+    "tp3d_mesh_rects": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, tp3d_mesh_spec, ctypes.POINTER(tp3d_rect),
+                                       ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]),
+    "tp3d_cmr_plan_create": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                            ctypes.POINTER(tp3d_rect), ctypes.c_int32, ctypes.c_int32,
+                                            ctypes.POINTER(tp3d_rect), ctypes.c_int32, ctypes.c_int32,
+                                            ctypes.c_int32, ctypes.POINTER(ctypes.c_void_p)]),
+    "tp3d_cmr_plan_destroy": (None, [ctypes.c_void_p]),
+    "tp3d_cmr_plan_num_tasks": (ctypes.c_int32, [ctypes.c_void_p]),
+    "tp3d_cmr_plan_task": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(tp3d_rect),
+                                          ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32),
+                                          ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
+                                          ctypes.POINTER(ctypes.c_int32)]),
+    "tp3d_cmr_plan_lower_bound": (ctypes.c_int64, [ctypes.c_void_p]),
+    "tp3d_cmr_schedule": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(tp3d_cmr_options),
+                                         ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
+                                         ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(tp3d_cmr_result)]),
+    "tp3d_pipeline_simulate": (ctypes.c_int, [ctypes.POINTER(tp3d_pipe_cfg), ctypes.POINTER(tp3d_pipe_op),
+                                              ctypes.c_int64, ctypes.POINTER(tp3d_pipe_result)]),
 }
 
 
@@ -191,3 +257,92 @@ def tp3d_layer_bwd(ctx, cfg: tp3d_layer_cfg, params: dict, X, workspace, dY, dX,
     g = _params(tp3d_layer_grads, grads)
     return lib().tp3d_layer_bwd(ctx, ctypes.byref(cfg), ctypes.byref(p), _p(X), _p(workspace), _p(dY), _p(dX),
                                 ctypes.byref(g), _s(stream))
+
+
+# ---------------------------------------------------------------------------
+# Host-side planners (include/tp3d_plan.h): no GPU involved.  Rectangles are
+# (row0, rows, col0, cols) tuples.
+# ---------------------------------------------------------------------------
+
+def _rects_out(fn, R, C, spec):
+    n = ctypes.c_int32(0)
+    st = fn(R, C, spec, None, 0, ctypes.byref(n))
+    if n.value <= 0:
+        return st, []
+    arr = (tp3d_rect * n.value)()
+    st = fn(R, C, spec, arr, n.value, ctypes.byref(n))
+    return st, [(r.row0, r.rows, r.col0, r.cols) for r in arr] if st == 0 else []
+
+
+def tp3d_layout_rects(R, C, l: tp3d_layout):
+    """(status, rectangles of the layout's shards in shard order)."""
+    return _rects_out(lib().tp3d_layout_rects, R, C, l)
+
+
+def tp3d_mesh_rects(R, C, s: tp3d_mesh_spec):
+    """(status, rectangles of the mesh devices in mesh order)."""
+    return _rects_out(lib().tp3d_mesh_rects, R, C, s)
+
+
+def _rect_array(rects):
+    arr = (tp3d_rect * len(rects))()
+    for k, r in enumerate(rects):
+        arr[k] = tp3d_rect(*r)
+    return arr
+
+
+def tp3d_cmr_plan_create(R, C, elem_bytes, src_rects, src_first, dst_rects, dst_first, devices_per_host):
+    """(status, plan handle or None)."""
+    h = ctypes.c_void_p()
+    st = lib().tp3d_cmr_plan_create(R, C, elem_bytes, _rect_array(src_rects), len(src_rects), src_first,
+                                    _rect_array(dst_rects), len(dst_rects), dst_first, devices_per_host,
+                                    ctypes.byref(h))
+    return st, h.value
+
+
+def tp3d_cmr_plan_destroy(plan) -> None:
+    lib().tp3d_cmr_plan_destroy(plan)
+
+
+def tp3d_cmr_plan_num_tasks(plan) -> int:
+    return lib().tp3d_cmr_plan_num_tasks(plan)
+
+
+def tp3d_cmr_plan_task(plan, i, max_senders, max_receivers):
+    """(status, slice, duration, sender devices, receiver devices) of task i;
+    max_senders / max_receivers: the create call's source / destination
+    device counts."""
+    r, d = tp3d_rect(), ctypes.c_int64()
+    ns, nr = ctypes.c_int32(), ctypes.c_int32()
+    sa, ra = (ctypes.c_int32 * max_senders)(), (ctypes.c_int32 * max_receivers)()
+    st = lib().tp3d_cmr_plan_task(plan, i, ctypes.byref(r), ctypes.byref(d), sa, ctypes.byref(ns), ra,
+                                  ctypes.byref(nr))
+    if st != 0:
+        return st, None, None, [], []
+    return st, (r.row0, r.rows, r.col0, r.cols), d.value, list(sa[:ns.value]), list(ra[:nr.value])
+
+
+def tp3d_cmr_plan_lower_bound(plan) -> int:
+    return lib().tp3d_cmr_plan_lower_bound(plan)
+
+
+def tp3d_cmr_schedule(plan, algo, trials=1, seed=0, node_limit=1):
+    """(status, sender host per task, global order, start time per task,
+    tp3d_cmr_result)."""
+    n = max(lib().tp3d_cmr_plan_num_tasks(plan), 0)
+    snd, order, start = (ctypes.c_int32 * n)(), (ctypes.c_int32 * n)(), (ctypes.c_int64 * n)()
+    res = tp3d_cmr_result()
+    opt = tp3d_cmr_options(algo, trials, seed, node_limit)
+    st = lib().tp3d_cmr_schedule(plan, ctypes.byref(opt), snd, order, start, ctypes.byref(res))
+    return st, list(snd), list(order), list(start), res
+
+
+def tp3d_pipeline_simulate(cfg: tp3d_pipe_cfg, want_ops: bool = False):
+    """(status, tp3d_pipe_result, list of tp3d_pipe_op or None)."""
+    res = tp3d_pipe_result()
+    if not want_ops:
+        return lib().tp3d_pipeline_simulate(ctypes.byref(cfg), None, 0, ctypes.byref(res)), res, None
+    n = 2 * max(cfg.p, 0) * max(cfg.m, 0) * max(cfg.v, 0)
+    ops = (tp3d_pipe_op * max(n, 1))()
+    st = lib().tp3d_pipeline_simulate(ctypes.byref(cfg), ops, n, ctypes.byref(res))
+    return st, res, list(ops[:n]) if st == 0 else None

@@ -1,8 +1,9 @@
 """Builds ``libtp3d.so`` in-tree with nvcc for sm_103a.
 
-Each ``csrc/*.cu`` is compiled in parallel into ``_build/`` at the repository
-root, then linked into ``tensor_transformer_layer_cube_gb300/libtp3d.so``
-(static CUDA runtime, so the library loads on a machine without a GPU).
+Each ``csrc/*.cu`` (kernels) and ``csrc/*.cpp`` (host-only planners) is
+compiled in parallel into ``_build/`` at the repository root, then linked
+into ``tensor_transformer_layer_cube_gb300/libtp3d.so`` (static CUDA runtime,
+so the library loads on a machine without a GPU).
 ``python -m tensor_transformer_layer_cube_gb300.build`` runs it.
 """
 from __future__ import annotations
@@ -33,7 +34,7 @@ def _nvcc() -> str:
 
 
 def _sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _headers():
@@ -54,7 +55,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     jobs = []
     objs = []
     for src in _sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(BUILD, os.path.splitext(os.path.basename(src))[0] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src] + headers):
             jobs.append([nvcc, *ARCH, *NVFLAGS, "-c", src, "-o", obj])

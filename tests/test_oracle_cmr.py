@@ -172,3 +172,31 @@ def test_check_schedule_rejects_overlap_and_wrong_sender():
     with pytest.raises(AssertionError):
         O.check_schedule(tasks, [1, 1], [0, 4])     # host 1 does not hold slice 0
     assert O.check_schedule(tasks, [0, 1], [0, 4]) == 8
+
+
+def test_replicated_source_spreads_the_senders():
+    # 8 row slices (S1 over the second axis of a (4, 8) mesh, replicated over
+    # its first), 8 devices per host: every slice has one holder on each of
+    # hosts 0-3.  The destination (4, 8) S01 R puts the receivers of slices
+    # 2k and 2k+1 on host 4+k.  By hand:
+    # - naive: host 0 sends all 8, one after the other: 8 T;
+    # - load balance only: slice k from host k % 4 (2 T of sending each), but
+    #   in plan order slices 4 and 5 wait for hosts 0 and 1 and slice 5 also
+    #   for receiver host 6: it runs in [2T, 3T): 3 T;
+    # - randomised greedy: rounds of 4 host-disjoint tasks, 2 rounds: 2 T,
+    #   the receive-load bound.
+    src = L.MeshSpec(4, 8, ("S1", "R"))
+    dst = L.MeshSpec(4, 8, ("S01", "R"))
+    tasks = O.make_tasks(src, dst, 64, 32, 2, 0, 32, 8)
+    T = 8 * 32 * 2
+    assert len(tasks) == 8 and all(t["dur"] == T and t["src_hosts"] == [0, 1, 2, 3] for t in tasks)
+    assert [t["dst_hosts"] for t in tasks] == [[4 + k // 2] for k in range(8)]
+    assert O.lower_bound(tasks) == 2 * T
+    s, o = O.naive(tasks)
+    assert O.list_schedule(tasks, o, s)[1] == 8 * T
+    s, o = O.load_balance(tasks)
+    assert s == [k % 4 for k in range(8)]
+    assert O.list_schedule(tasks, o, s)[1] == 3 * T
+    s, o, rounds = O.random_greedy(tasks, 4, 11)
+    start, mk = O.list_schedule(tasks, o, s)
+    assert O.check_schedule(tasks, s, start) == mk == 2 * T and len(rounds) == 2
