@@ -109,11 +109,39 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
   return true;
 }
 
-__device__ __forceinline__ float gelu_f(float x) { return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f)); }
+// GELU(x) = x Phi(x), Phi(x) = (1 + erf(x / sqrt 2)) / 2, with erf from
+// Abramowitz and Stegun, "Handbook of Mathematical Functions", formula
+// 7.1.26 (Hastings' rational approximation, |error| <= 1.5e-7 for z >= 0):
+//   erf(z) = 1 - t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-z^2),
+//   t = 1 / (1 + p z),
+// extended to z < 0 by odd symmetry.  Branch-free: one reciprocal and one
+// exponential per element; exp(-z^2) = exp(-x^2 / 2) is also the Gaussian
+// density the backward needs.  The lower tail Phi(x) = erfc(|x| / sqrt 2) / 2
+// (x < 0) is taken directly, without the cancellation of 1 - erf.
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ float gauss_cdf(float x, float& e) {
+  const float z = fabsf(x) * 0.70710678118654752f;
+  const float t = rcp_approx(fmaf(0.3275911f, z, 1.0f));
+  float p = fmaf(t, 1.061405429f, -1.453152027f);
+  p = fmaf(t, p, 1.421413741f);
+  p = fmaf(t, p, -0.284496736f);
+  p = fmaf(t, p, 0.254829592f);
+  e = __expf(-z * z);
+  const float tail = 0.5f * (p * t) * e;  // erfc(|x| / sqrt 2) / 2
+  return x < 0.0f ? tail : 1.0f - tail;
+}
+__device__ __forceinline__ float gelu_f(float x) {
+  float e;
+  return x * gauss_cdf(x, e);
+}
 __device__ __forceinline__ float gelu_grad_f(float x) {
-  const float cdf = 0.5f * (1.0f + erff(x * 0.70710678118654752f));
-  const float pdf = 0.39894228040143268f * expf(-0.5f * x * x);
-  return cdf + x * pdf;
+  float e;
+  const float cdf = gauss_cdf(x, e);
+  return fmaf(x * 0.39894228040143268f, e, cdf);  // Phi(x) + x phi(x)
 }
 
 __device__ __forceinline__ void unpack8(const uint4& v, float* f) {
@@ -155,7 +183,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmProblem& P, const TileIn
                                               const CUtensorMap* mapC, const CUtensorMap* mapZ,
                                               const CUtensorMap* mapX, uint32_t aux_bar, uint32_t& aux_phase,
                                               volatile int* abort_flag, uint32_t tempty, bool tempty_remote,
-                                              bool& pending) {
+                                              uint32_t& stores) {
   const void* aux = P.epi.resid ? P.epi.resid : P.epi.gin;
   const bool aux_ok = aux != nullptr && P.epi.zsave == nullptr && !P.epi.out_f32;
   const int quarter = warp & 3;
@@ -189,11 +217,18 @@ __device__ __forceinline__ void epilogue_tile(const GemmProblem& P, const TileIn
   };
   if (aux_ok && fast(0)) aux_issue(0);
   const __nv_bfloat16* bias = static_cast<const __nv_bfloat16*>(P.epi.bias);
+  const bool scaled = P.epi.alpha != 1.0f;
 #pragma unroll 1
   for (int cc = 0; cc < CH; ++cc) {
     const int ch = half * CH + cc;
     uint32_t r[32];
     tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * BN + ch * 32), r);
+    // the chunk's 32 bias values (the same for every lane) load under the TMEM read
+    uint4 bv[4];
+    if (bias && chunk_n(cc) + 32 <= T.n_end) {
+#pragma unroll
+      for (int v = 0; v < 4; ++v) bv[v] = *reinterpret_cast<const uint4*>(bias + (gn0 + (chunk_n(cc) - T.n0) + v * 8));
+    }
     tmem_ld_wait();
     if (cc == CH - 1) {
       tc_fence_before();
@@ -223,20 +258,27 @@ __device__ __forceinline__ void epilogue_tile(const GemmProblem& P, const TileIn
         __syncwarp();
         if (cc + 1 < CH && fast(cc + 1)) aux_issue(cc + 1);
       }
-      if (f32 && pending) {  // fp32 rows fill the whole staging buffer: wait before writing
+      if (f32 && stores) {  // fp32 rows fill the whole staging buffer: wait before writing
         if (lane == 0) bulk_wait_read_all();
         __syncwarp();
-        pending = false;
       }
+      // bf16 output without an auxiliary input or saved pre-activation uses
+      // both 2 KiB halves of the staging buffer in turn
+      const bool dbl = !aux_ok && P.epi.zsave == nullptr && !f32;
+      uint8_t* ybuf = stg + (dbl ? (stores & 1u) * 2048u : 0u);
       uint4 yv[4];
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
         float x[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = any_k ? __uint_as_float(r[v * 8 + e]) * P.epi.alpha : 0.0f;
+        for (int e = 0; e < 8; ++e) x[e] = any_k ? __uint_as_float(r[v * 8 + e]) : 0.0f;
+        if (scaled) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] *= P.epi.alpha;
+        }
         if (bias) {
           float bb[8];
-          unpack8(*reinterpret_cast<const uint4*>(bias + (gn0 + (n - T.n0) + v * 8)), bb);
+          unpack8(bv[v], bb);
 #pragma unroll
           for (int e = 0; e < 8; ++e) x[e] += bb[e];
         }
@@ -264,13 +306,18 @@ __device__ __forceinline__ void epilogue_tile(const GemmProblem& P, const TileIn
         }
       }
       if (!f32) {
-        if (pending) {
-          if (lane == 0) bulk_wait_read_all();
+        if (stores) {
+          // double-buffered: the store that last used this half was issued two chunks ago
+          if (lane == 0) {
+            if (dbl)
+              bulk_wait_read_1();
+            else
+              bulk_wait_read_all();
+          }
           __syncwarp();
-          pending = false;
         }
 #pragma unroll
-        for (int v = 0; v < 4; ++v) *reinterpret_cast<uint4*>(stg + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4)) = yv[v];
+        for (int v = 0; v < 4; ++v) *reinterpret_cast<uint4*>(ybuf + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4)) = yv[v];
         if (P.epi.zsave) {
 #pragma unroll
           for (int v = 0; v < 4; ++v)
@@ -280,11 +327,11 @@ __device__ __forceinline__ void epilogue_tile(const GemmProblem& P, const TileIn
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        tma_store_3d(mapC, stg_y, chunk_c0(cc), c1, c2);
+        tma_store_3d(mapC, smem_u32(ybuf), chunk_c0(cc), c1, c2);
         if (P.epi.zsave) tma_store_3d(mapZ, stg_z, chunk_c0(cc), c1, c2);
         bulk_commit();
       }
-      pending = true;
+      ++stores;
     } else if (row_ok) {
       // ---------------------------------------------------------- masked path
 #pragma unroll
@@ -554,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // -------------------------------------------------------------- epilogue
     uint32_t tc = 0;
-    bool pending = false;  // a TMA store still reads this warp's staging buffer
+    uint32_t stores = 0;  // TMA stores this warp has issued from its staging buffer
     uint32_t aux_phase = 0;
     uint8_t* stg = stage_out + (warp - 2) * Cfg::STAGE_OUT;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
@@ -573,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       epilogue_tile<BN>(P, T, any_k, buf, tmem_base, warp, lane, stg, &mapC, &mapZ, &mapX, aux_bar(warp - 2),
-                        aux_phase, abort_flag, tempty_bar(buf), false, pending);
+                        aux_phase, abort_flag, tempty_bar(buf), false, stores);
       ++tc;
     }
     if (lane == 0) bulk_wait_all();
@@ -589,20 +636,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ CTA pairs
-// The same GEMM on a cluster of two CTAs (tcgen05 cta_group::2): the pair
-// computes a 256 x 256 tile; CTA r of the pair loads rows [128 r, +128) of
-// A and columns [128 r, +128) of B, the even CTA issues M = 256, N = 256
-// products that read A from each CTA's own shared memory and B from both,
-// and each CTA's tensor memory receives its 128 rows.  Per SM this moves
-// 32 KiB per contraction step instead of 48 KiB (B is loaded once per pair)
-// and leaves room for a 6-deep ring.  Only for problems without a causal
-// mask (both CTAs of a pair run the same contraction range).
+// The same GEMM on clusters of two CTAs (tcgen05 cta_group::2): a pair
+// computes a 256 x 256 tile; CTA r of the pair holds rows [128 r, +128) of
+// the A tile and columns [128 r, +128) of the B tile, the even CTA issues
+// M = 256, N = 256 products that read A from each CTA's own shared memory and
+// B from both, and each CTA's tensor memory receives its 128 rows.  Per SM
+// this moves 32 KiB per contraction step instead of 48 KiB (B is loaded once
+// per pair) and leaves room for a 6-deep ring.  Only for problems without a
+// causal mask (both CTAs of a pair run the same contraction range).
 //
 // Barriers: full[s] lives in the even CTA and takes the even producer's
-// expect-tx arrival for both CTAs' bytes plus both CTAs' TMA completions; empty[s] and tfull[b]
-// live in each CTA and are arrived on by the even CTA's commits (multicast
-// to both); tempty[b] lives in the even CTA and takes the arrivals of both
-// CTAs' epilogue warps.
+// expect-tx arrival for both CTAs' bytes plus both CTAs' TMA completions;
+// empty[s] and tfull[b] live in each CTA and are arrived on by the even CTA's
+// commits (multicast to both); tempty[b] lives in the even CTA and takes the
+// arrivals of both CTAs' epilogue warps.
 struct Tc2Cfg {
   static constexpr int BN = 256;
   static constexpr int STAGES = 6;
@@ -615,15 +662,16 @@ struct Tc2Cfg {
   static constexpr int SMEM = STAGES * STAGE_BYTES + kEpiWarps * STAGE_OUT + BAR_BYTES + 1024;
 };
 
-__device__ __forceinline__ void decode_pair_tile(const GemmProblem& P, int64_t t, uint32_t rank, TileInfo& T) {
+// Tile t for CTA r of the pair.
+__device__ __forceinline__ void decode_pair_tile(const GemmProblem& P, int64_t t, uint32_t r, TileInfo& T) {
   const int64_t tpsM = ceil_div(P.segM, 256), tpsN = ceil_div(P.segN, 256);
   const int64_t tiles_m = (P.M / P.segM) * tpsM;
   const int64_t per_z = tiles_m * (P.N / P.segN) * tpsN;
   T.z = (int32_t)(t / per_z);
-  const int64_t r = t - (int64_t)T.z * per_z;
-  const int64_t tn = r / tiles_m, tm = r - tn * tiles_m;
+  const int64_t rem = t - (int64_t)T.z * per_z;
+  const int64_t tn = rem / tiles_m, tm = rem - tn * tiles_m;
   const int64_t sm = tm / tpsM, sn = tn / tpsN;
-  T.m0 = sm * P.segM + (tm - sm * tpsM) * 256 + 128 * (int64_t)rank;
+  T.m0 = sm * P.segM + (tm - sm * tpsM) * 256 + 128 * (int64_t)r;
   T.n0 = sn * P.segN + (tn - sn * tpsN) * 256;
   T.m_end = sm * P.segM + P.segM;
   T.n_end = sn * P.segN + P.segN;
@@ -843,7 +891,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
     uint32_t tc = 0;
-    bool pending = false;
+    uint32_t stores = 0;
     uint32_t aux_phase = 0;
     uint8_t* stg = stage_out + (warp - 2) * Cfg::STAGE_OUT;
     for (int64_t t = cid; t < ntiles; t += nclusters) {
@@ -856,7 +904,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       epilogue_tile<BN>(P, T, true, buf, tmem_base, warp, lane, stg, &mapC, &mapZ, &mapX, aux_bar(warp - 2),
-                        aux_phase, abort_flag, map_to_cta(tempty_bar(buf), 0), true, pending);
+                        aux_phase, abort_flag, map_to_cta(tempty_bar(buf), 0), true, stores);
       ++tc;
     }
     if (lane == 0) bulk_wait_all();
@@ -929,6 +977,34 @@ tp3d_status launch(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t s) {
   return cudaGetLastError() == cudaSuccess ? TP3D_OK : TP3D_ECUDA;
 }
 
+// CTA pairs that fit on the device at once (0 if the query fails).
+int pair_clusters(const tp3d_ctx* ctx) {
+  static int cached[64] = {};
+  const int dev = ctx->device & 63;
+  if (cached[dev] != 0) return cached[dev] > 0 ? cached[dev] : 0;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Tc2Cfg::SMEM;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(2 * (unsigned)(ctx->num_sms / 2));
+  int n = 0;
+  if (cudaFuncSetAttribute(gemm_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Tc2Cfg::SMEM) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveClusters(&n, gemm_tc2_kernel, &cfg) != cudaSuccess || n < 1) {
+    (void)cudaGetLastError();
+    cached[dev] = -1;
+    return 0;
+  }
+  cached[dev] = n;
+  return n;
+}
+
 tp3d_status launch_pair(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t s) {
   using Cfg = Tc2Cfg;
   CUtensorMap ma, mb, mc, mz, mx;
@@ -947,10 +1023,11 @@ tp3d_status launch_pair(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t 
     TP3D_TRY(make_map(&mx, P.c.g, aux, 32, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, CU_TENSOR_MAP_SWIZZLE_64B));
   else
     mx = mc;
-  TP3D_CUDA_TRY(cudaFuncSetAttribute(gemm_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM));
   const int64_t ntiles = (int64_t)P.Z * (P.M / P.segM) * ((P.segM + 255) / 256) * (P.N / P.segN) *
                          ((P.segN + 255) / 256);
   if (ntiles <= 0) return TP3D_OK;
+  const int max_clusters = pair_clusters(ctx);
+  if (max_clusters < 1) return TP3D_ECUDA;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -962,10 +1039,6 @@ tp3d_status launch_pair(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t 
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  int max_clusters = 0;
-  cfg.gridDim = dim3(2 * (unsigned)(ctx->num_sms / 2));
-  if (cudaOccupancyMaxActiveClusters(&max_clusters, gemm_tc2_kernel, &cfg) != cudaSuccess || max_clusters < 1)
-    max_clusters = ctx->num_sms / 2;
   const int64_t nc = ntiles < max_clusters ? ntiles : max_clusters;
   cfg.gridDim = dim3(2 * (unsigned)nc);
   TP3D_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_tc2_kernel, ma, mb, mc, mz, mx, P));
@@ -1000,8 +1073,8 @@ tp3d_status gemm_bf16_tc(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t
   const int64_t sms = ctx->num_sms;
   const double c256 = P.segN > 128 ? waves(tiles(BM, 256), sms) / 0.60 : 1e30;
   const double c128 = waves(tiles(BM, 128), sms) * 0.5 / 0.45;
-  const double cpair = (P.causal == CAUSAL_NONE && P.segM >= 256 && P.segN >= 256)
-                           ? waves(tiles(256, 256), sms / 2) / 0.80 : 1e30;
+  const bool pairs_ok = P.causal == CAUSAL_NONE && P.segM >= 256 && P.segN >= 256;
+  const double cpair = pairs_ok ? waves(tiles(256, 256), sms / 2) / 0.80 : 1e30;
   if (cpair <= c256 && cpair <= c128) return launch_pair(ctx, P, s);
   return c256 <= c128 ? launch<256>(ctx, P, s) : launch<128>(ctx, P, s);
 }

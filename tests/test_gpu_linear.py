@@ -64,6 +64,8 @@ def test_linear_bf16_parity(ctx, q, M, N, K, y):
     (2, 800, 192, 416),      # m = 200 rows, contraction block 96, weight block 104: ragged everywhere
     (2, 4 * 136, 2 * 72, 4 * 264),
     (3, 9 * 72, 3 * 80, 9 * 40),
+    (1, 2048, 1024, 1280),   # an odd number of 256-column tiles: clusters of two CTA pairs end half-used
+    (1, 2304, 512, 768),
 ])
 def test_linear_bf16_ragged_tiles(ctx, q, M, N, K):
     for y in (0, 1):
@@ -132,6 +134,25 @@ def test_mlp_q4_tokens8192_hidden4096_ffn16384_sampled_rows(ctx):
     rows = np.concatenate([blk * m + rng.choice(m, 16, replace=False) for blk in range(q * q)])
     e, _ = _mlp_case(ctx, q, M, 4096, 16384, S.SEED_BASE + 4, 0.0, sample_rows=np.sort(rows))
     assert e <= BF16_TOL
+
+
+def test_linear_gelu_activation_values(ctx):
+    # A = 0: every output is GELU(bias) of its column, for bf16 biases densely
+    # covering [-8, 8] (the epilogue's erf is a rational approximation,
+    # |error| <= 1.5e-7): within one bf16 unit of the exact value, plus 1e-6
+    # absolute where GELU's lower tail is far below fp32's resolution of 1 + erf
+    q, M, N, K = 1, 256, 64, 4096
+    b = torch.linspace(-8.0, 8.0, K, dtype=torch.float64).to(torch.bfloat16)
+    A = torch.zeros(M * N, dtype=torch.bfloat16, device=device())
+    B = torch.zeros(N * K, dtype=torch.bfloat16, device=device())
+    C = torch.full((M * K,), float("nan"), dtype=torch.bfloat16, device=device())
+    assert t.tp3d_linear(ctx, q, 0, M, N, K, t.TP3D_BF16, A, B, b.to(device()), 1, C) == 0
+    assert t.tp3d_sync_status(ctx) == 0
+    x = b.double()
+    want = (x * 0.5 * (1.0 + torch.erf(x / np.sqrt(2.0)))).numpy()
+    got = C.view(M, K).double().cpu().numpy()
+    ulp = np.maximum(np.abs(want), 2.0 ** -126) * 2.0 ** -7
+    assert np.all(np.abs(got - want[None, :]) <= ulp[None, :] + 1e-6)
 
 
 def test_linear_errors_before_launch(ctx):
