@@ -8,13 +8,12 @@
 // [t*d, +d) (Q), [h + t*d, +d) (K), [2h + t*d, +d) (V).
 //
 // Three persistent tcgen05 kernels, 128-row tiles, warp 0 = TMA
-// producer, warp 1 = MMA issuer (and TMEM owner), warps 2-5 = one thread per
-// tile row (TMEM lane) for the softmax arithmetic:
-//  * forward: per query tile, pass 1 runs S = Q K^T over the key tiles at or
-//    below the diagonal and keeps the row maximum and sum (online, in
-//    registers); pass 2 recomputes S, writes P = exp(S - m) / l (bf16) to
-//    shared memory and accumulates O += P V in tensor memory; the row's
-//    log-sum-exp is saved for the backward.  No rescaling of O is needed.
+// producer, warp 1 = MMA issuer (and TMEM owner), then one thread per tile
+// row (TMEM lane) for the softmax arithmetic:
+//  * forward: two query tiles per CTA, one pass over the key tiles at or
+//    below the diagonal with an online softmax (S = Q K^T in TMEM, P to
+//    shared memory, O += P V in TMEM, O rescaled only when the row maximum
+//    grows by more than 2^8); the row's log-sum-exp is saved for the backward.
 //  * backward dK/dV: per key tile, over the query tiles at or above the
 //    diagonal: S^T = K Q^T, dP^T = V dO^T, P^T = exp(S^T - lse), then
 //    dV += P^T dO and dK += dS^T Q with dS = P (dP - rowsum(dO O)) / sqrt(d).
@@ -139,35 +138,61 @@ __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) {
 // the current one finishes (phase counters run across items).
 
 // ------------------------------------------------------------------ forward
-// item w: query tile nq-1-(w / Z) of (batch, head) w % Z
-// smem: Q | K0 V0 | K1 V1 | P0 | P1 (32 KiB each)
-// TMEM: S0 [0,128) S1 [128,256) O [256,256+d)
-__global__ void __launch_bounds__(kThreads, 1)
+// One pass with an online softmax over two query tiles at once (slots 0 and
+// 1: query tiles 2k and 2k+1 of one (batch, head); item w = (k, z) with the
+// longest k first).  Both slots share every K and V tile.  The MMA issuer
+// interleaves the slots so that one slot's softmax overlaps the other's
+// products: S0(0) S1(0) | PV0(j) S0(j+1) PV1(j) S1(j+1) | ...
+//
+// Softmax rows (one thread per query row, four warps per slot): each key
+// tile's scores are read from TMEM, the row maximum updated, and
+// P = 2^(S log2e / sqrt d - m) written to shared memory (bf16, unnormalised)
+// together with the running row sum l.  The exponent base m only moves when
+// the row maximum exceeds it by more than 8 (2^8: P and l stay far from
+// overflow); then l and the row of O already accumulated in TMEM are scaled
+// by 2^(m_old - m_new) before the next product adds to it.  At the end
+// O / l is stored and the row's log-sum-exp (m + log2 l) ln 2 saved.
+//
+// warps: 0 TMA producer, 1 MMA issuer + TMEM owner, 2-3 idle (warpgroup 0);
+// 4-7 slot 0 rows (warpgroup 1); 8-11 slot 1 rows (warpgroup 2).  Warpgroup 0
+// gives registers to the two row warpgroups (setmaxnreg) so that each row
+// thread holds its whole 128-score row in registers.
+// smem: Q0 | Q1 | P0 | P1 | R0 R1 R2 (a ring of K_0 V_0 K_1 V_1 ...), 32 KiB each
+// TMEM: S0 [0,128) S1 [128,256) O0 [256, 256+d) O1 [256+d, 256+2d)
+constexpr int kFwdThreads = 384;
+constexpr int kFwdRegsLow = 64, kFwdRegsHigh = 216;  // 128 x 64 + 256 x 216 <= 384 x 168
+constexpr float kRescaleLog2 = 8.0f;
+
+__global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap mqkv, const AttnProblem A, bf16* __restrict__ O,
                     float* __restrict__ lse) {
   extern __shared__ uint8_t smem_raw[];
   const Ctx c = setup_smem(smem_raw);
-  const uint32_t sQ = c.base, sK[2] = {c.base + kTile, c.base + 3 * kTile}, sV[2] = {c.base + 2 * kTile, c.base + 4 * kTile};
-  const uint32_t sP[2] = {c.base + 5 * kTile, c.base + 6 * kTile};
-  uint8_t* pP[2] = {c.base_ptr + 5 * kTile, c.base_ptr + 6 * kTile};
+  auto sQ = [&](int sl) { return c.base + (uint32_t)sl * kTile; };
+  auto sP = [&](int sl) { return c.base + (uint32_t)(2 + sl) * kTile; };
+  auto sR = [&](uint32_t i) { return c.base + (4u + i) * kTile; };
   auto bar = [&](int k) { return c.bar0 + 8u * k; };
-  const uint32_t q_full = bar(0), q_empty = bar(1), o_full = bar(2), o_empty = bar(3);
-  auto kv_full = [&](int s) { return bar(4 + s); };
-  auto kv_empty = [&](int s) { return bar(6 + s); };
-  auto s_full = [&](int b) { return bar(8 + b); };
-  auto s_empty = [&](int b) { return bar(10 + b); };
-  auto p_full = [&](int b) { return bar(12 + b); };
-  auto p_empty = [&](int b) { return bar(14 + b); };
-  const uint32_t final_bar = bar(16);
+  const uint32_t q_full = bar(0), q_empty = bar(1);
+  auto r_full = [&](uint32_t i) { return bar(2 + (int)i); };
+  auto r_empty = [&](uint32_t i) { return bar(5 + (int)i); };
+  auto s_full = [&](int sl) { return bar(8 + sl); };
+  auto s_empty = [&](int sl) { return bar(10 + sl); };
+  auto p_full = [&](int sl) { return bar(12 + sl); };
+  auto p_empty = [&](int sl) { return bar(14 + sl); };
+  auto o_full = [&](int sl) { return bar(16 + sl); };
+  auto o_empty = [&](int sl) { return bar(18 + sl); };
+  const uint32_t final_bar = bar(20);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t nq = A.s / TR, items = A.Z * nq;
+  const int64_t nq = A.s / TR, npair = (nq + 1) / 2, items = A.Z * npair;
   const int nch = (int)(A.d / 64);
   const uint32_t dbytes = (uint32_t)(A.d * TR * 2);
 
   if (threadIdx.x == 0) {
-    for (int k = 0; k < 17; ++k)
-      mbar_init(bar(k), (k == 3 || k == 10 || k == 11 || k == 12 || k == 13) ? kComputeWarps : 1);
+    for (int k = 0; k < 21; ++k) {
+      const bool four = (k >= 10 && k <= 13) || k == 18 || k == 19;  // s_empty, p_full, o_empty
+      mbar_init(bar(k), four ? kComputeWarps : 1);
+    }
     *c.abort_flag = 0;
     fence_barrier_init();
   }
@@ -179,162 +204,195 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *c.tmem_holder;
-
-  if (warp == 0) {
-    if (lane == 0) {
+  if (warp < 4) {
+    // ---------------------------------------------------------- warpgroup 0
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kFwdRegsLow));
+    if (warp == 0 && lane == 0) {
+      // ------------------------------------------------------------ producer
       uint32_t n = 0, ic = 0;
       bool ok = true;
       for (int64_t w = blockIdx.x; w < items && ok; w += gridDim.x, ++ic) {
-        const int64_t iq = nq - 1 - w / A.Z, z = w % A.Z, b = z / A.H, t = z % A.H;
-        const int nkv = (int)iq + 1;
+        const int64_t k = npair - 1 - w / A.Z, z = w % A.Z, b = z / A.H, t = z % A.H;
+        const int64_t iq0 = 2 * k;
+        const bool two = iq0 + 1 < nq;
+        const int nmax = (int)iq0 + (two ? 2 : 1);
         if (!(ok = mbar_wait(q_empty, (ic & 1) ^ 1, c.abort_flag, A.err))) break;
-        mbar_arrive_expect_tx(q_full, dbytes);
-        load_tile(&mqkv, A.qkv, b * A.s + iq * TR, t * A.d, nch, sQ, q_full);
-        for (int e = 0; e < 2 * nkv; ++e, ++n) {
-          const int j = e < nkv ? e : e - nkv;
-          const bool with_v = e >= nkv;
-          const int s = n & 1;
-          if (!(ok = mbar_wait(kv_empty(s), ((n >> 1) & 1) ^ 1, c.abort_flag, A.err))) break;
-          mbar_arrive_expect_tx(kv_full(s), with_v ? 2 * dbytes : dbytes);
-          const int64_t row_k = b * A.s + (int64_t)j * TR;
-          load_tile(&mqkv, A.qkv, row_k, A.h + t * A.d, nch, sK[s], kv_full(s));
-          if (with_v) load_tile(&mqkv, A.qkv, row_k, 2 * A.h + t * A.d, nch, sV[s], kv_full(s));
+        mbar_arrive_expect_tx(q_full, dbytes * (two ? 2u : 1u));
+        load_tile(&mqkv, A.qkv, b * A.s + iq0 * TR, t * A.d, nch, sQ(0), q_full);
+        if (two) load_tile(&mqkv, A.qkv, b * A.s + (iq0 + 1) * TR, t * A.d, nch, sQ(1), q_full);
+        for (int j = 0; j < nmax && ok; ++j) {
+          for (int kv = 0; kv < 2; ++kv, ++n) {
+            const uint32_t slot = n % 3;
+            if (!(ok = mbar_wait(r_empty(slot), ((n / 3) & 1) ^ 1, c.abort_flag, A.err))) break;
+            mbar_arrive_expect_tx(r_full(slot), dbytes);
+            load_tile(&mqkv, A.qkv, b * A.s + (int64_t)j * TR, (kv == 0 ? A.h : 2 * A.h) + t * A.d, nch, sR(slot),
+                      r_full(slot));
+          }
         }
       }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
+    } else if (warp == 1 && lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
       const uint32_t id_s = idesc_bf16_f32(TR, TR, 0, 0);
       const uint32_t id_o = idesc_bf16_f32(TR, (int)A.d, 0, 1);
       const int ks_d = (int)(A.d / 16);
-      uint32_t n = 0, sc = 0, pc = 0, ic = 0;
+      uint32_t n = 0, ic = 0;
+      uint32_t sc[2] = {0, 0}, pc[2] = {0, 0}, oc[2] = {0, 0};
       bool ok = true;
-      // S = Q K^T for the next ring entry into S buffer sc % 2; returns the ring stage
-      auto issue_s = [&](int& stage) -> bool {
-        const int s = n & 1;
-        if (!mbar_wait(kv_full(s), (n >> 1) & 1, c.abort_flag, A.err)) return false;
-        const int sb = sc & 1;
-        if (!mbar_wait(s_empty(sb), ((sc >> 1) & 1) ^ 1, c.abort_flag, A.err)) return false;
+      auto ring = [&](uint32_t idx, uint32_t& slot) -> bool {
+        slot = idx % 3;
+        return mbar_wait(r_full(slot), (idx / 3) & 1, c.abort_flag, A.err);
+      };
+      auto issue_s = [&](int sl, uint32_t kslot) -> bool {  // S_sl = Q_sl K^T
+        if (!mbar_wait(s_empty(sl), (sc[sl] & 1) ^ 1, c.abort_flag, A.err)) return false;
         tc_fence_after();
-        mma_tile(tmem + (uint32_t)(sb * TR), sQ, false, sK[s], false, ks_d, id_s, false);
-        umma_commit(s_full(sb));
-        ++sc;
-        ++n;
-        stage = s;
+        mma_tile(tmem + (uint32_t)(sl * TR), sQ(sl), false, sR(kslot), false, ks_d, id_s, false);
+        umma_commit(s_full(sl));
+        ++sc[sl];
+        return true;
+      };
+      auto issue_pv = [&](int sl, uint32_t vslot, bool first) -> bool {  // O_sl += P_sl V
+        if (!mbar_wait(p_full(sl), pc[sl] & 1, c.abort_flag, A.err)) return false;
+        if (first && !mbar_wait(o_empty(sl), (oc[sl] & 1) ^ 1, c.abort_flag, A.err)) return false;
+        tc_fence_after();
+        mma_tile(tmem + 256u + (uint32_t)(sl * A.d), sP(sl), false, sR(vslot), true, TR / 16, id_o, !first);
+        umma_commit(p_empty(sl));
+        ++pc[sl];
         return true;
       };
       for (int64_t w = blockIdx.x; w < items && ok; w += gridDim.x, ++ic) {
-        const int nkv = (int)(nq - 1 - w / A.Z) + 1;
+        const int64_t iq0 = 2 * (npair - 1 - w / A.Z);
+        const bool two = iq0 + 1 < nq;
+        const int nkv0 = (int)iq0 + 1, nkv1 = two ? nkv0 + 1 : 0, nmax = two ? nkv1 : nkv0;
         if (!(ok = mbar_wait(q_full, ic & 1, c.abort_flag, A.err))) break;
-        int st = 0;
-        for (int e = 0; e < nkv && ok; ++e) {  // pass 1: scores only
-          if ((ok = issue_s(st))) umma_commit(kv_empty(st));
+        const uint32_t n0 = n;  // ring index of K_0; K_j = n0 + 2j, V_j = n0 + 2j + 1
+        uint32_t ks = 0;
+        if (!(ok = ring(n0, ks) && issue_s(0, ks) && (!two || issue_s(1, ks)))) break;
+        if (nmax == 1) umma_commit(q_empty);
+        umma_commit(r_empty(ks));
+        for (int j = 0; j < nmax && ok; ++j) {
+          uint32_t vs = 0, kn = 0;
+          if (!(ok = ring(n0 + 2 * j + 1, vs))) break;
+          if (j < nkv0 && !(ok = issue_pv(0, vs, j == 0))) break;
+          const bool more = j + 1 < nmax;
+          if (more) {
+            if (!(ok = ring(n0 + 2 * j + 2, kn))) break;
+            if (j + 1 < nkv0 && !(ok = issue_s(0, kn))) break;
+          }
+          if (j < nkv1 && !(ok = issue_pv(1, vs, j == 0))) break;
+          if (more) {
+            if (j + 1 < nkv1 && !(ok = issue_s(1, kn))) break;
+            if (j + 2 == nmax) umma_commit(q_empty);  // the item's last product with Q issued
+            umma_commit(r_empty(kn));
+          }
+          umma_commit(r_empty(vs));
         }
         if (!ok) break;
-        int st_cur = 0, issued = 1;
-        if (!(ok = issue_s(st_cur))) break;
-        if (issued == nkv) umma_commit(q_empty);
-        for (int j = 0; j < nkv && ok; ++j) {  // pass 2
-          int st_next = 0;
-          if (j + 1 < nkv) {
-            if (!(ok = issue_s(st_next))) break;
-            if (++issued == nkv) umma_commit(q_empty);
-          }
-          const int pb = pc & 1;
-          if (!(ok = mbar_wait(p_full(pb), (pc >> 1) & 1, c.abort_flag, A.err))) break;
-          if (j == 0 && !(ok = mbar_wait(o_empty, (ic & 1) ^ 1, c.abort_flag, A.err))) break;
-          tc_fence_after();
-          mma_tile(tmem + 256u, sP[pb], false, sV[st_cur], true, TR / 16, id_o, j > 0);
-          umma_commit(p_empty(pb));
-          umma_commit(kv_empty(st_cur));
-          ++pc;
-          st_cur = st_next;
+        umma_commit(o_full(0));
+        ++oc[0];
+        if (two) {
+          umma_commit(o_full(1));
+          ++oc[1];
         }
-        if (ok) umma_commit(o_full);
+        n = n0 + 2 * (uint32_t)nmax;
       }
       umma_commit(final_bar);
       drain(final_bar, 0);
     }
   } else {
-    // ------------------------------------------------------------ softmax rows
+    // ------------------------------------------------------------ softmax rows (warpgroups 1, 2)
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kFwdRegsHigh));
+    const int sl = (warp - 4) >> 2;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const float sl2 = A.scale * kLog2e;
-    uint32_t sc = 0, pc = 0, ic = 0;
+    const uint32_t s_col = (uint32_t)(sl * TR), o_col = 256u + (uint32_t)(sl * A.d);
+    uint32_t sc = 0, pc = 0, oc = 0;
     bool ok = true;
-    for (int64_t w = blockIdx.x; w < items && ok; w += gridDim.x, ++ic) {
-      const int64_t iq = nq - 1 - w / A.Z, z = w % A.Z, b = z / A.H, t = z % A.H;
+    for (int64_t w = blockIdx.x; w < items && ok; w += gridDim.x) {
+      const int64_t k = npair - 1 - w / A.Z, z = w % A.Z, b = z / A.H, t = z % A.H;
+      const int64_t iq = 2 * k + sl;
+      if (iq >= nq) continue;  // an odd tile count leaves the last item's slot 1 empty
       const int nkv = (int)iq + 1;
       float m = -INFINITY, l = 0.0f;
-      for (int j = 0; j < nkv && ok; ++j) {  // pass 1: row max and sum
-        const int sb = sc & 1;
-        if (!(ok = warp_wait(s_full(sb), (sc >> 1) & 1, c, A.err, lane))) break;
+      for (int j = 0; j < nkv && ok; ++j) {
+        if (!(ok = warp_wait(s_full(sl), sc & 1, c, A.err, lane))) break;
         tc_fence_after();
+        // the whole row of scores into registers (four loads, one wait)
         const bool diag = j == nkv - 1;
-#pragma unroll 1
-        for (int cc = 0; cc < TR / 32; ++cc) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(sb * TR + cc * 32)), v);
-          tmem_ld_wait();
-          float mx = m;
+        uint32_t v[TR / 32][32];
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (!diag || cc * 32 + e <= r) mx = fmaxf(mx, __uint_as_float(v[e]) * sl2);
-          float sum = 0.0f;
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (!diag || cc * 32 + e <= r) sum += exp2f(__uint_as_float(v[e]) * sl2 - mx);
-          l = l * exp2f(m - mx) + sum;
-          m = mx;
-        }
+        for (int cc = 0; cc < TR / 32; ++cc) tmem_ld_32x32b_x32(tmem_row(tmem, quarter, s_col + (uint32_t)(cc * 32)), v[cc]);
+        tmem_ld_wait();
         tc_fence_before();
-        warp_arrive(s_empty(sb), lane);
+        warp_arrive(s_empty(sl), lane);
         ++sc;
-      }
-      const float inv_l = 1.0f / l;
-      for (int j = 0; j < nkv && ok; ++j) {  // pass 2: P = exp(S - m) / l into shared memory
-        const int sb = sc & 1, pb = pc & 1;
-        if (!(ok = warp_wait(s_full(sb), (sc >> 1) & 1, c, A.err, lane))) break;
-        if (!(ok = warp_wait(p_empty(pb), ((pc >> 1) & 1) ^ 1, c, A.err, lane))) break;
+        // eight independent partial maxima (short dependency chains)
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < TR; ++e)
+          if (!diag || e <= r) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(v[e >> 5][e & 31]));
+        float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        mt *= sl2;
+        // the product of the previous tile has finished: P is free and O current
+        if (!(ok = warp_wait(p_empty(sl), (pc & 1) ^ 1, c, A.err, lane))) break;
         tc_fence_after();
-        const bool diag = j == nkv - 1;
-#pragma unroll 1
-        for (int cc = 0; cc < TR / 32; ++cc) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(sb * TR + cc * 32)), v);
-          tmem_ld_wait();
+        // the TMEM accesses are warp-collective (.sync.aligned): the warp
+        // rescales when any of its rows needs it, each row by its own factor
+        const bool move = mt > m + kRescaleLog2;
+        if (j > 0 && __any_sync(0xffffffffu, move)) {
+          const float f = move ? ex2_approx(m - mt) : 1.0f;
+          l *= f;
+          for (int cc = 0; cc < (int)(A.d / 32); ++cc) {
+            uint32_t ov[32];
+            tmem_ld_32x32b_x32(tmem_row(tmem, quarter, o_col + (uint32_t)(cc * 32)), ov);
+            tmem_ld_wait();
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            float f[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int col = cc * 32 + g * 8 + e;
-              f[e] = (!diag || col <= r) ? exp2f(__uint_as_float(v[g * 8 + e]) * sl2 - m) * inv_l : 0.0f;
-            }
-            st_tile8(pP[pb], r, cc * 4 + g, pack8f(f));
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
+            tmem_st_32x32b_x32(tmem_row(tmem, quarter, o_col + (uint32_t)(cc * 32)), ov);
           }
+          tmem_st_wait();
         }
+        if (move) m = mt;
+        float ps[8];  // eight partial row sums
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ps[i] = 0.0f;
+#pragma unroll
+        for (int g = 0; g < TR / 8; ++g) {
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int col = g * 8 + e;
+            f[e] = (!diag || col <= r) ? ex2_approx(fmaf(__uint_as_float(v[col >> 5][col & 31]), sl2, -m)) : 0.0f;
+            ps[e] += f[e];
+          }
+          st_tile8(c.base_ptr + (2 + sl) * kTile, r, g, pack8f(f));
+        }
+        l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
         fence_proxy_async_smem();
         tc_fence_before();
-        warp_arrive(p_full(pb), lane);
-        warp_arrive(s_empty(sb), lane);
-        ++sc;
+        warp_arrive(p_full(sl), lane);
         ++pc;
       }
-      if (!ok || !(ok = warp_wait(o_full, ic & 1, c, A.err, lane))) break;
+      if (!ok || !(ok = warp_wait(o_full(sl), oc & 1, c, A.err, lane))) break;
       tc_fence_after();
+      const float inv_l = 1.0f / l;
       const int64_t grow = b * A.s + iq * TR + r;
       const int64_t gcol = t * A.d;
       const int64_t br = grow / A.o.bh, bc = gcol / A.o.bw;
       bf16* dst = O + A.o.block_base((int32_t)br, (int32_t)bc) + (grow - br * A.o.bh) * A.o.bw + (gcol - bc * A.o.bw);
       for (int cc = 0; cc < (int)(A.d / 32); ++cc) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem_row(tmem, quarter, 256u + cc * 32), v);
+        uint32_t ov[32];
+        tmem_ld_32x32b_x32(tmem_row(tmem, quarter, o_col + (uint32_t)(cc * 32)), ov);
         tmem_ld_wait();
-        store_row32(dst + cc * 32, v);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * inv_l);
+        store_row32(dst + cc * 32, ov);
       }
       tc_fence_before();
-      warp_arrive(o_empty, lane);
+      warp_arrive(o_empty(sl), lane);
+      ++oc;
       lse[z * A.s + iq * TR + r] = (m + log2f(l)) * kLn2;
     }
   }
@@ -771,9 +829,13 @@ tp3d_status launch_attn_fwd(const tp3d_ctx* ctx, const AttnProblem& A, const voi
   CUtensorMap mq;
   TP3D_TRY(tile_map(&mq, A.qkv, qkv));
   TP3D_CUDA_TRY(cudaFuncSetAttribute(attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem));
-  const int64_t items = A.Z * (A.s / TR);
+  // setmaxnreg.inc waits until the block's launch registers cover the split
+  cudaFuncAttributes fa;
+  TP3D_CUDA_TRY(cudaFuncGetAttributes(&fa, attn_fwd_kernel));
+  if (fa.numRegs * kFwdThreads < 128 * kFwdRegsLow + 256 * kFwdRegsHigh) return TP3D_EUNSUPPORTED;
+  const int64_t items = A.Z * ((A.s / TR + 1) / 2);  // pairs of query tiles
   const unsigned grid = (unsigned)(items < ctx->num_sms ? items : ctx->num_sms);
-  attn_fwd_kernel<<<grid, kThreads, kSmem, s>>>(mq, A, static_cast<bf16*>(o), lse);
+  attn_fwd_kernel<<<grid, kFwdThreads, kSmem, s>>>(mq, A, static_cast<bf16*>(o), lse);
   return cudaGetLastError() == cudaSuccess ? TP3D_OK : TP3D_ECUDA;
 }
 
