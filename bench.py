@@ -219,9 +219,9 @@ class LayerBench:
         self.fwd_flops = lin + att
         self.units = 3 * lin + 3 * att  # backward = twice the forward's products
         # library kernels per step: forward 7 (2 LN, 4 GEMM, attention);
-        # backward 27 (8 GEMM, 3 attention, 2 LN rows, 2 LN column sums, 4
-        # bias column sums, 8 partial reductions)
-        self.launches = 7 + 27
+        # backward 19 (8 GEMM, 3 attention, 2 LN rows, 2 LN column sums, 4
+        # bias column sums; each column sum finishes its own reduction)
+        self.launches = 7 + 19
         self.unit, self.scale = "TFLOP/s", 1e12
         self.X_host = self.X.cpu().pin_memory()
         self.dY_host = self.dY.cpu().pin_memory()

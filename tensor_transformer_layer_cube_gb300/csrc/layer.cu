@@ -37,11 +37,13 @@ struct Plan {
   float eps;
   // workspace offsets (bytes)
   size_t xn1, mean1, rstd1, qkv, lse, O, Hres, xn2, mean2, rstd2, z1, y1;  // saved by the forward
-  size_t delta, dz1, dxn, dH, dO, dqkv, part;                              // scratch
+  size_t delta, dz1, dxn, dH, dO, dqkv, part, counters;                    // scratch
   size_t part_floats, total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+constexpr int64_t kCounters = 1024;  // column-sum arrival counters in the workspace
 
 tp3d_status make_plan(const tp3d_layer_cfg* c, Plan* p) {
   if (!c) return TP3D_EINVAL;
@@ -100,6 +102,9 @@ tp3d_status make_plan(const tp3d_layer_cfg* c, Plan* p) {
   const int64_t pl = colsum_parts(gc) * 2 * h;
   x.part_floats = (size_t)(pc > pl ? pc : pl);
   x.part = take(x.part_floats * 4);
+  // one arrival counter per 256-column strip of the widest column sum
+  if ((f > 3 * h ? f : 3 * h) / 256 + 1 > kCounters) return TP3D_EUNSUPPORTED;
+  x.counters = take(kCounters * 4);
   x.total = o;
   *p = x;
   return TP3D_OK;
@@ -172,12 +177,11 @@ tp3d_status plan_wgrad(const tp3d_ctx* ctx, int q, int y, int64_t M, int64_t Nin
   return TP3D_OK;
 }
 
-tp3d_status colsum(const tp3d_ctx* ctx, int kind, int q, int64_t R, int64_t C, const void* x, float* part, void* out,
-                   cudaStream_t s) {
+tp3d_status colsum(const tp3d_ctx* ctx, int kind, int q, int64_t R, int64_t C, const void* x, float* part,
+                   int* counters, void* out, cudaStream_t s) {
   Grid g;
   TP3D_TRY(make_grid(cube(kind, q), R, C, &g));
-  TP3D_TRY(launch_colsum(ctx, g, x, part, s));
-  return launch_reduce_parts(part, colsum_parts(g), C, out, s);
+  return launch_colsum(ctx, g, x, part, counters, out, s);
 }
 
 }  // namespace
@@ -262,35 +266,35 @@ tp3d_status tp3d_layer_bwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   auto W = [&](size_t off) { return static_cast<void*>(ws + off); };
   float* part = (float*)W(p.part);
+  int* counters = (int*)W(p.counters);
   const cudaStream_t st = as_stream(stream);
+  // the column sums' arrival counters start at zero (each sum leaves them so)
+  TP3D_CUDA_TRY(cudaMemsetAsync(counters, 0, kCounters * 4, st));
   const int q = p.q;
   GemmProblem G;
   Grid gA;
   TP3D_TRY(make_grid(cube(TP3D_CUBE_A, q), M, h, &gA));
 
   // ---- MLP block
-  TP3D_TRY(colsum(ctx, TP3D_CUBE_A, q, M, h, dY, part, g->b_2, st));                      // db2
+  TP3D_TRY(colsum(ctx, TP3D_CUBE_A, q, M, h, dY, part, counters, g->b_2, st));            // db2
   TP3D_TRY(plan_wgrad(ctx, q, 1, M, f, h, W(p.y1), dY, g->w_2, &G));                       // dW2 = Y1^T dY
   TP3D_TRY(run(ctx, G, st));
   TP3D_TRY(plan_dgrad(ctx, q, 1, M, f, h, dY, w->w_2, W(p.dz1), &G));                      // dZ1 = (dY W2^T) GELU'(Z1)
   G.epi.act = EPI_GELU_BWD;
   G.epi.gin = W(p.z1);
   TP3D_TRY(run(ctx, G, st));
-  TP3D_TRY(colsum(ctx, TP3D_CUBE_C, q, M, f, W(p.dz1), part, g->b_1, st));                // db1
+  TP3D_TRY(colsum(ctx, TP3D_CUBE_C, q, M, f, W(p.dz1), part, counters, g->b_1, st));      // db1
   TP3D_TRY(plan_wgrad(ctx, q, 0, M, h, f, W(p.xn2), W(p.dz1), g->w_1, &G));                // dW1 = LN2(H)^T dZ1
   TP3D_TRY(run(ctx, G, st));
   TP3D_TRY(plan_dgrad(ctx, q, 0, M, h, f, W(p.dz1), w->w_1, W(p.dxn), &G));                // dLN2 = dZ1 W1^T
   TP3D_TRY(run(ctx, G, st));
-  const int64_t np = colsum_parts(gA);
   TP3D_TRY(launch_ln_bwd(ctx, gA, W(p.dxn), W(p.Hres), (const float*)W(p.mean2), (const float*)W(p.rstd2),
                          w->ln2_g, dY, W(p.dH), st));                                                  // dH
   TP3D_TRY(launch_ln_param_grads(ctx, gA, W(p.dxn), W(p.Hres), (const float*)W(p.mean2), (const float*)W(p.rstd2),
-                                 part, part + np * h, st));
-  TP3D_TRY(launch_reduce_parts(part, np, h, g->ln2_g, st));
-  TP3D_TRY(launch_reduce_parts(part + np * h, np, h, g->ln2_b, st));
+                                 part, counters, g->ln2_g, g->ln2_b, st));
 
   // ---- attention block
-  TP3D_TRY(colsum(ctx, TP3D_CUBE_A, q, M, h, W(p.dH), part, g->b_o, st));                 // dbo
+  TP3D_TRY(colsum(ctx, TP3D_CUBE_A, q, M, h, W(p.dH), part, counters, g->b_o, st));       // dbo
   TP3D_TRY(plan_wgrad(ctx, q, 1, M, h, h, W(p.O), W(p.dH), g->w_o, &G));                   // dWo = O^T dH
   TP3D_TRY(run(ctx, G, st));
   TP3D_TRY(plan_dgrad(ctx, q, 1, M, h, h, W(p.dH), w->w_o, W(p.dO), &G));                  // dO = dH Wo^T
@@ -298,17 +302,15 @@ tp3d_status tp3d_layer_bwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_
   // attention backward, fused: dQ, dK, dV into dQKV (MP3D's C = A B^T and C = A^T B forms)
   TP3D_TRY(launch_attn_bwd(ctx, attn_problem(p, ctx->d_err), W(p.qkv), W(p.O), W(p.dO), (const float*)W(p.lse),
                            (float*)W(p.delta), W(p.dqkv), st));
-  TP3D_TRY(colsum(ctx, TP3D_CUBE_C, q, M, 3 * h, W(p.dqkv), part, g->b_qkv, st));          // dbqkv
+  TP3D_TRY(colsum(ctx, TP3D_CUBE_C, q, M, 3 * h, W(p.dqkv), part, counters, g->b_qkv, st));  // dbqkv
   TP3D_TRY(plan_wgrad(ctx, q, 0, M, h, 3 * h, W(p.xn1), W(p.dqkv), g->w_qkv, &G));         // dWqkv = LN1(X)^T dQKV
   TP3D_TRY(run(ctx, G, st));
   TP3D_TRY(plan_dgrad(ctx, q, 0, M, h, 3 * h, W(p.dqkv), w->w_qkv, W(p.dxn), &G));         // dLN1 = dQKV Wqkv^T
   TP3D_TRY(run(ctx, G, st));
   TP3D_TRY(launch_ln_bwd(ctx, gA, W(p.dxn), X, (const float*)W(p.mean1), (const float*)W(p.rstd1), w->ln1_g,
                          W(p.dH), dX, st));                                                            // dX
-  TP3D_TRY(launch_ln_param_grads(ctx, gA, W(p.dxn), X, (const float*)W(p.mean1), (const float*)W(p.rstd1), part,
-                                 part + np * h, st));
-  TP3D_TRY(launch_reduce_parts(part, np, h, g->ln1_g, st));
-  return launch_reduce_parts(part + np * h, np, h, g->ln1_b, st);
+  return launch_ln_param_grads(ctx, gA, W(p.dxn), X, (const float*)W(p.mean1), (const float*)W(p.rstd1), part,
+                               counters, g->ln1_g, g->ln1_b, st);
 }
 
 }  // extern "C"

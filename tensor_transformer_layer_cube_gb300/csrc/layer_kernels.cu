@@ -157,37 +157,61 @@ __global__ void __launch_bounds__(kThreads) ln_bwd_kernel(const Grid g, const bf
 // ------------------------------------------------------------------ column sums
 // CTA (x, y): columns [256 x, +256) over the rows of part y (rows_per_part
 // rows inside one row block); lane l of every warp holds columns 8l..8l+7,
-// warps stride over rows; the 8 warps are summed in shared memory.
-// With mean != nullptr it sums dy * (x - mean) * rstd into part and dy into
-// part2 (the LayerNorm gamma and beta gradients); else it sums x into part.
+// warps stride over rows with eight rows' loads in flight; the 8 warps are
+// summed in shared memory into the part's partial row.  The last CTA of a
+// column strip to finish (an atomic count per strip, reset to zero after)
+// adds the partial rows of all parts and writes the bf16 sums.
+// LN: sums dy * (x - mean) * rstd into out and dy into out2 (the LayerNorm
+// gamma and beta gradients); else sums x into out.
+template <bool LN>
 __global__ void __launch_bounds__(kThreads) colsum_kernel(const Grid g, const bf16* __restrict__ x,
                                                           const bf16* __restrict__ dy,
                                                           const float* __restrict__ mean,
                                                           const float* __restrict__ rstd, float* __restrict__ part,
-                                                          float* __restrict__ part2, int64_t rows_per_part) {
+                                                          float* __restrict__ part2, int64_t rows_per_part,
+                                                          int* __restrict__ counters, bf16* __restrict__ out,
+                                                          bf16* __restrict__ out2) {
+  constexpr int U = 8;  // rows in flight per warp
   __shared__ float red[kWarps][257];
+  __shared__ int is_last;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int64_t c = (int64_t)blockIdx.x * 256 + lane * 8;
   const int64_t r0 = (int64_t)blockIdx.y * rows_per_part;
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0}, acc2[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  const bool ln = mean != nullptr;
   if (c < g.C) {
     const int64_t br = r0 / g.bh, bc = c / g.bw;
     const int64_t base = g.block_base((int32_t)br, (int32_t)bc) + (r0 - br * g.bh) * g.bw + (c - bc * g.bw);
-    for (int64_t rr = w; rr < rows_per_part; rr += kWarps) {
-      float f[8];
-      unpack8(*reinterpret_cast<const uint4*>(x + base + rr * g.bw), f);
-      if (!ln) {
+    for (int64_t rr0 = w; rr0 < rows_per_part; rr0 += (int64_t)kWarps * U) {
+      uint4 xv[U], dv[U];
+      float mu[U], rs[U];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] += f[e];
-      } else {
-        float d[8];
-        unpack8(*reinterpret_cast<const uint4*>(dy + base + rr * g.bw), d);
-        const float mu = mean[r0 + rr], rs = rstd[r0 + rr];
+      for (int u = 0; u < U; ++u) {
+        const int64_t rr = rr0 + (int64_t)u * kWarps;
+        if (rr < rows_per_part) {
+          xv[u] = *reinterpret_cast<const uint4*>(x + base + rr * g.bw);
+          if (LN) {
+            dv[u] = *reinterpret_cast<const uint4*>(dy + base + rr * g.bw);
+            mu[u] = mean[r0 + rr];
+            rs[u] = rstd[r0 + rr];
+          }
+        }
+      }
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          acc[e] += d[e] * (f[e] - mu) * rs;
-          acc2[e] += d[e];
+      for (int u = 0; u < U; ++u) {
+        if (rr0 + (int64_t)u * kWarps >= rows_per_part) break;
+        float f[8];
+        unpack8(xv[u], f);
+        if (!LN) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[e] += f[e];
+        } else {
+          float d[8];
+          unpack8(dv[u], d);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            acc[e] += d[e] * (f[e] - mu[u]) * rs[u];
+            acc2[e] += d[e];
+          }
         }
       }
     }
@@ -200,34 +224,68 @@ __global__ void __launch_bounds__(kThreads) colsum_kernel(const Grid g, const bf
 #pragma unroll
   for (int k = 0; k < kWarps; ++k) s += red[k][threadIdx.x];
   if (cc < g.C) part[(int64_t)blockIdx.y * g.C + cc] = s;
-  if (!ln) return;
-  __syncthreads();
+  if (LN) {
+    __syncthreads();
 #pragma unroll
-  for (int e = 0; e < 8; ++e) red[w][lane * 8 + e] = acc2[e];
-  __syncthreads();
-  s = 0.0f;
+    for (int e = 0; e < 8; ++e) red[w][lane * 8 + e] = acc2[e];
+    __syncthreads();
+    s = 0.0f;
 #pragma unroll
-  for (int k = 0; k < kWarps; ++k) s += red[k][threadIdx.x];
-  if (cc < g.C) part2[(int64_t)blockIdx.y * g.C + cc] = s;
-}
-
-// out[c] = sum over p of part[p][c]: CTA = 32 columns x 8 groups of parts.
-__global__ void __launch_bounds__(kThreads) reduce_parts_kernel(const float* __restrict__ part, int64_t nparts,
-                                                                int64_t C, bf16* __restrict__ out) {
-  __shared__ float red[kWarps][33];
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  const int64_t c = (int64_t)blockIdx.x * 32 + tx;
-  float s = 0.0f;
-  if (c < C)
-    for (int64_t p = ty; p < nparts; p += kWarps) s += part[p * C + c];
-  red[ty][tx] = s;
-  __syncthreads();
-  if (ty == 0 && c < C) {
-    float t = 0.0f;
-#pragma unroll
-    for (int k = 0; k < kWarps; ++k) t += red[k][tx];
-    out[c] = __float2bfloat16_rn(t);
+    for (int k = 0; k < kWarps; ++k) s += red[k][threadIdx.x];
+    if (cc < g.C) part2[(int64_t)blockIdx.y * g.C + cc] = s;
   }
+  // the last part of this strip to finish reduces all of them: the block's
+  // writes are ordered before its arrival by the barrier and thread 0's
+  // (cumulative) device-scope fence
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    is_last = atomicAdd(&counters[blockIdx.x], 1) == (int)gridDim.y - 1;
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  // warp w adds parts w, w + 8, ...; lane l columns 8l..8l+7 of the strip
+  for (int which = 0; which < (LN ? 2 : 1); ++which) {
+    const float* src = which == 0 ? part : part2;
+    float t[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (c < g.C) {
+      const int64_t np = gridDim.y;
+      for (int64_t p0 = w; p0 < np; p0 += (int64_t)kWarps * 4) {
+        float4 v[4][2];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int64_t p = p0 + (int64_t)u * kWarps;
+          if (p < np) {
+            v[u][0] = __ldcg(reinterpret_cast<const float4*>(src + p * g.C + c));
+            v[u][1] = __ldcg(reinterpret_cast<const float4*>(src + p * g.C + c + 4));
+          } else {
+            v[u][0] = v[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          t[0] += v[u][0].x;
+          t[1] += v[u][0].y;
+          t[2] += v[u][0].z;
+          t[3] += v[u][0].w;
+          t[4] += v[u][1].x;
+          t[5] += v[u][1].y;
+          t[6] += v[u][1].z;
+          t[7] += v[u][1].w;
+        }
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < 8; ++e) red[w][lane * 8 + e] = t[e];
+    __syncthreads();
+    float u = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kWarps; ++k) u += red[k][threadIdx.x];
+    if (cc < g.C) (which == 0 ? out : out2)[cc] = __float2bfloat16_rn(u);
+  }
+  if (threadIdx.x == 0) counters[blockIdx.x] = 0;
 }
 
 unsigned grid_for_rows(const tp3d_ctx* ctx, int64_t rows, int per_sm) {
@@ -242,44 +300,55 @@ tp3d_status last_error() { return cudaGetLastError() == cudaSuccess ? TP3D_OK : 
 
 tp3d_status launch_ln_fwd(const tp3d_ctx* ctx, const Grid& g, const void* x, const void* gamma, const void* beta,
                           void* y, float* mean, float* rstd, float eps, cudaStream_t s) {
-  ln_fwd_kernel<<<grid_for_rows(ctx, g.R, 16), kThreads, 0, s>>>(
-      g, static_cast<const bf16*>(x), static_cast<const bf16*>(gamma), static_cast<const bf16*>(beta),
-      static_cast<bf16*>(y), mean, rstd, eps);
+  const unsigned grid = grid_for_rows(ctx, g.R, 16);
+  const bf16 *xb = static_cast<const bf16*>(x), *gb = static_cast<const bf16*>(gamma),
+             *bb = static_cast<const bf16*>(beta);
+  bf16* yb = static_cast<bf16*>(y);
+  ln_fwd_kernel<<<grid, kThreads, 0, s>>>(g, xb, gb, bb, yb, mean, rstd, eps);
   return last_error();
 }
 
 tp3d_status launch_ln_bwd(const tp3d_ctx* ctx, const Grid& g, const void* dy, const void* x, const float* mean,
                           const float* rstd, const void* gamma, const void* dres, void* dx, cudaStream_t s) {
-  ln_bwd_kernel<<<grid_for_rows(ctx, g.R, 16), kThreads, 0, s>>>(
-      g, static_cast<const bf16*>(dy), static_cast<const bf16*>(x), mean, rstd, static_cast<const bf16*>(gamma),
-      static_cast<const bf16*>(dres), static_cast<bf16*>(dx));
+  const unsigned grid = grid_for_rows(ctx, g.R, 16);
+  const bf16 *db = static_cast<const bf16*>(dy), *xb = static_cast<const bf16*>(x),
+             *gb = static_cast<const bf16*>(gamma), *rb = static_cast<const bf16*>(dres);
+  bf16* ob = static_cast<bf16*>(dx);
+  ln_bwd_kernel<<<grid, kThreads, 0, s>>>(g, db, xb, mean, rstd, gb, rb, ob);
   return last_error();
 }
 
+int64_t colsum_strips(const Grid& g) { return (g.C + 255) / 256; }
+// the most parts any launch uses (64-row parts), for sizing the scratch
 int64_t colsum_parts(const Grid& g) { return g.R / gcd64(g.bh, 64); }
+// rows per part: a power of two (64..1024, dividing the row block) that
+// gives about three CTAs per SM
+int64_t colsum_rows(const tp3d_ctx* ctx, const Grid& g) {
+  const int64_t want = colsum_strips(g) * g.R / (3 * (int64_t)ctx->num_sms);
+  int64_t p = 64;
+  while (p < 1024 && p * 2 <= want) p *= 2;
+  return gcd64(g.bh, p);
+}
 
-static tp3d_status colsum_launch(const Grid& g, const void* x, const void* dy, const float* mean, const float* rstd,
-                                 float* part, float* part2, cudaStream_t s) {
-  const int64_t rpp = gcd64(g.bh, 64);
-  const dim3 grid((unsigned)((g.C + 255) / 256), (unsigned)(g.R / rpp));
+tp3d_status launch_colsum(const tp3d_ctx* ctx, const Grid& g, const void* x, float* part, int* counters, void* out,
+                          cudaStream_t s) {
+  const int64_t rpp = colsum_rows(ctx, g);
+  const dim3 grid((unsigned)colsum_strips(g), (unsigned)(g.R / rpp));
   if (grid.y > 65535u) return TP3D_EUNSUPPORTED;
-  colsum_kernel<<<grid, kThreads, 0, s>>>(g, static_cast<const bf16*>(x), static_cast<const bf16*>(dy), mean, rstd,
-                                         part, part2, rpp);
+  colsum_kernel<false><<<grid, kThreads, 0, s>>>(g, static_cast<const bf16*>(x), nullptr, nullptr, nullptr, part,
+                                                 nullptr, rpp, counters, static_cast<bf16*>(out), nullptr);
   return last_error();
 }
 
-tp3d_status launch_colsum(const tp3d_ctx*, const Grid& g, const void* x, float* part, cudaStream_t s) {
-  return colsum_launch(g, x, nullptr, nullptr, nullptr, part, nullptr, s);
-}
-
-tp3d_status launch_ln_param_grads(const tp3d_ctx*, const Grid& g, const void* dy, const void* x, const float* mean,
-                                  const float* rstd, float* part_g, float* part_b, cudaStream_t s) {
-  return colsum_launch(g, x, dy, mean, rstd, part_g, part_b, s);
-}
-
-tp3d_status launch_reduce_parts(const float* part, int64_t nparts, int64_t C, void* out, cudaStream_t s) {
-  const unsigned grid = (unsigned)((C + 31) / 32);
-  reduce_parts_kernel<<<grid, kThreads, 0, s>>>(part, nparts, C, static_cast<bf16*>(out));
+tp3d_status launch_ln_param_grads(const tp3d_ctx* ctx, const Grid& g, const void* dy, const void* x,
+                                  const float* mean, const float* rstd, float* part, int* counters, void* out_g,
+                                  void* out_b, cudaStream_t s) {
+  const int64_t rpp = colsum_rows(ctx, g);
+  const dim3 grid((unsigned)colsum_strips(g), (unsigned)(g.R / rpp));
+  if (grid.y > 65535u) return TP3D_EUNSUPPORTED;
+  colsum_kernel<true><<<grid, kThreads, 0, s>>>(g, static_cast<const bf16*>(x), static_cast<const bf16*>(dy), mean,
+                                                rstd, part, part + (int64_t)grid.y * g.C, rpp, counters,
+                                                static_cast<bf16*>(out_g), static_cast<bf16*>(out_b));
   return last_error();
 }
 

@@ -18,15 +18,21 @@ tp3d_status launch_ln_fwd(const tp3d_ctx* ctx, const Grid& g, const void* x, con
 tp3d_status launch_ln_bwd(const tp3d_ctx* ctx, const Grid& g, const void* dy, const void* x, const float* mean,
                           const float* rstd, const void* gamma, const void* dres, void* dx, cudaStream_t s);
 
-// LayerNorm parameter gradients as column partial sums: part_g gets
-// sum dy * (x - mean) * rstd, part_b sum dy (colsum_parts(g) rows of C floats).
+// LayerNorm parameter gradients: out_g = column sums of dy * (x - mean) *
+// rstd, out_b = column sums of dy (bf16, C each).  Scratch: `part` holds
+// 2 * colsum_parts(g) rows of C floats; `counters` (colsum_strips(g) ints,
+// zero on entry) is zero again on exit.
 tp3d_status launch_ln_param_grads(const tp3d_ctx* ctx, const Grid& g, const void* dy, const void* x,
-                                  const float* mean, const float* rstd, float* part_g, float* part_b, cudaStream_t s);
+                                  const float* mean, const float* rstd, float* part, int* counters, void* out_g,
+                                  void* out_b, cudaStream_t s);
 
-// Column sums of the R x C bf16 matrix x (layout g): partials in `part`
-// (colsum_parts(g) rows of C floats), then reduce_parts writes the bf16 vector.
+// Column sums of the R x C bf16 matrix x (layout g) into the bf16 vector
+// `out`, in one launch: partial rows in `part` (colsum_parts(g) rows of C
+// floats), reduced by the last CTA of each 256-column strip; `counters`
+// (colsum_strips(g) ints, zero on entry) is zero again on exit.
 int64_t colsum_parts(const Grid& g);
-tp3d_status launch_colsum(const tp3d_ctx* ctx, const Grid& g, const void* x, float* part, cudaStream_t s);
-tp3d_status launch_reduce_parts(const float* part, int64_t nparts, int64_t C, void* out, cudaStream_t s);
+int64_t colsum_strips(const Grid& g);
+tp3d_status launch_colsum(const tp3d_ctx* ctx, const Grid& g, const void* x, float* part, int* counters, void* out,
+                          cudaStream_t s);
 
 }  // namespace tp3d
