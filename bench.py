@@ -502,6 +502,62 @@ def host_planner_summary(t):
     return out
 
 
+def layout_comparison(torch, t, ctx, dev, flush, stream):
+    """The MLP block of the q = 4 workload (tokens 8192, hidden 4096, ffn
+    16384; 64 virtual devices) in the three layouts that "Maximizing
+    Parallelism in Distributed Training for Huge Neural Networks" compares:
+    1-D Megatron (t = 64), 2-D SUMMA (8 x 8) and the 3-D cube (q = 4).  Time
+    on this GPU, per-device memory and per-device communication (elements
+    received or sent per forward, from each scheme's collectives), and the
+    resharding of X between the schemes' input layouts."""
+    M, h, f = 8192, 4096, 16384
+    bf = torch.bfloat16
+    g = torch.Generator(device=dev)
+    g.manual_seed(20264)
+    X = torch.randn(M * h, device=dev, generator=g).to(bf)
+    W1 = (torch.randn(h * f, device=dev, generator=g) * 0.02).to(bf)
+    W2 = (torch.randn(f * h, device=dev, generator=g) * 0.02).to(bf)
+    b1 = torch.zeros(f, device=dev, dtype=bf)
+    b2 = torch.zeros(h, device=dev, dtype=bf)
+    Y1 = torch.empty(M * f, device=dev, dtype=bf)
+    Y = torch.empty(M * h, device=dev, dtype=bf)
+    fl = 4.0 * M * h * f
+    out = {"workload": "MLP, tokens 8192, hidden 4096, ffn 16384, bf16, 64 virtual devices (values are layout "
+                       "independent for timing: one buffer serves every layout)"}
+    for name, scheme, p in (("1d_megatron_t64", t.TP3D_SCHEME_1D, 64), ("2d_summa_8x8", t.TP3D_SCHEME_2D, 8),
+                            ("3d_cube_q4", t.TP3D_SCHEME_3D, 4)):
+        def step(scheme=scheme, p=p):
+            t.check(t.tp3d_mlp_layout(ctx, scheme, p, M, h, f, t.TP3D_BF16, X, W1, b1, W2, b2, Y1, Y),
+                    "tp3d_mlp_layout")
+        d = time_steps(torch, step, 10, 3, flush, stream)
+        ms = statistics.mean(d)
+        if scheme == t.TP3D_SCHEME_1D:
+            mem = M * h + h * f // p + M * f // p + f * h // p + M * h
+            comm = 2 * (p - 1) * M * h // p  # ring all-reduce of Y
+        elif scheme == t.TP3D_SCHEME_2D:
+            mem = (2 * M * h + 2 * h * f + M * f) // (p * p)
+            # SUMMA: q steps, each receiving an A panel along the row and a B panel along the column
+            comm = (p - 1) * ((M * h + h * f) + (M * f + f * h)) // (p * p)
+        else:
+            def lin(Mm, N, K):
+                return (Mm // (p * p)) * (N // p) + (N // p) * (K // (p * p)) + (Mm // (p * p)) * (K // p)
+            mem = lin(M, h, f) + lin(M, f, h) - (M // (p * p)) * (f // p)  # Y1 counted once
+            # per linear: all-gather of A over y, of B over x, reduce-scatter of C over z,
+            # each over q - 1 peers' shards
+            comm = (p - 1) * (lin(M, h, f) + lin(M, f, h))
+        out[name] = {"ms": ms, "tflops": fl / (ms / 1e3) / 1e12, "devices": p if scheme == 1 else p * p if scheme == 2
+                     else p ** 3, "mem_elems_per_device": int(mem), "comm_elems_per_device": int(comm)}
+    # resharding X (8192 x 4096 bf16) from the cube's layout to the other two
+    for name, dst in (("x_cube_to_1d", t.layout(t.REPLICATED, 0, 1)), ("x_cube_to_2d", t.layout(t.BLOCK2D, 0, 8, 8))):
+        Xd = torch.empty_like(X)
+
+        def rs(dst=dst, Xd=Xd):
+            t.check(t.tp3d_reshard(ctx, M, h, 2, t.layout(t.CUBE_A, 4), X, dst, Xd), "tp3d_reshard")
+        d = time_steps(torch, rs, 10, 3, flush, stream)
+        out[name] = {"ms": statistics.mean(d), "gbs": 2 * M * h * 2 / (statistics.mean(d) / 1e3) / 1e9}
+    return out
+
+
 def make_bench(t, ctx, dev, name):
     w = WORKLOADS[name]
     return BENCHES[w["kind"]](t, ctx, dev, w)
@@ -604,6 +660,8 @@ def run_ours(args, rank, world, dist):
             torch.cuda.empty_cache()
         line["configs"] = extras
         line["host_planners"] = host_planner_summary(t)
+        line["layout_comparison"] = layout_comparison(torch, t, ctx, dev, flush, stream)
+        torch.cuda.empty_cache()
         st = t.tp3d_sync_status(ctx)
         if st != 0:
             raise SystemExit(f"device error in the extra workloads: {t.STATUS[st]}")

@@ -141,6 +141,26 @@ tp3d_status tp3d_mlp(tp3d_ctx* ctx, int q, int64_t M, int64_t h, int64_t f, tp3d
                      const void* X, const void* W1, const void* b1, const void* W2,
                      const void* b2, void* Y1, void* Y, void* stream);
 
+/* The same MLP block in the layouts the pages compare the cube with
+ * ("Maximizing Parallelism in Distributed Training for Huge Neural
+ * Networks" §2 and §4: Megatron's 1-D and Optimus' 2-D SUMMA partitioning),
+ * computed on this GPU by the same tensor-core GEMM.
+ *   TP3D_SCHEME_1D, p = t devices (Megatron): X (M x h) replicated; W1
+ *     COL(t) (each device f/t columns), b1 split the same way, Y1 COL(t);
+ *     W2 ROW(t); Y replicated.  The all-reduce of the row-split GEMM is its
+ *     contraction across the t shards.  A replicated matrix is stored once
+ *     (every virtual device reads that copy).
+ *   TP3D_SCHEME_2D, p = q, a q x q mesh (SUMMA): X, W1, Y1, W2, Y in
+ *     BLOCK2D(q, q) (block (r, c) = device r*q + c); C_rc = sum_k A_rk B_kc.
+ *   TP3D_SCHEME_3D, p = q: the cube, exactly tp3d_mlp.
+ * Biases are plain vectors (either may be NULL).  bf16 only.  TP3D_ESHAPE
+ * when a dimension is not divisible by the scheme's block counts or a block's
+ * row is not a multiple of 8 elements; other errors as tp3d_mlp.             */
+typedef enum { TP3D_SCHEME_1D = 1, TP3D_SCHEME_2D = 2, TP3D_SCHEME_3D = 3 } tp3d_scheme;
+tp3d_status tp3d_mlp_layout(tp3d_ctx* ctx, int scheme, int p, int64_t M, int64_t h, int64_t f, tp3d_dtype dtype,
+                            const void* X, const void* W1, const void* b1, const void* W2, const void* b2, void* Y1,
+                            void* Y, void* stream);
+
 /* tp3d_mlp without the hidden-activation argument, for callers that cannot
  * allocate device memory: code that must not call cudaMalloc (it would
  * synchronise the device, or the process's memory is all handed to another

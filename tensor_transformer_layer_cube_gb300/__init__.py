@@ -33,7 +33,7 @@ __all__ = [
     "tp3d_rect", "tp3d_mesh_spec", "tp3d_cmr_options", "tp3d_cmr_result", "tp3d_pipe_cfg", "tp3d_pipe_op",
     "tp3d_pipe_result", "tp3d_layout_rects", "tp3d_mesh_rects", "tp3d_cmr_plan_create", "tp3d_cmr_plan_destroy",
     "tp3d_cmr_plan_num_tasks", "tp3d_cmr_plan_task", "tp3d_cmr_plan_lower_bound", "tp3d_cmr_schedule",
-    "tp3d_pipeline_simulate", "TP3D_SPEC_R", "TP3D_SPEC_S0", "TP3D_SPEC_S1", "TP3D_SPEC_S01", "TP3D_CMR_NAIVE",
+    "tp3d_pipeline_simulate", "tp3d_mlp_layout", "TP3D_SCHEME_1D", "TP3D_SCHEME_2D", "TP3D_SCHEME_3D", "TP3D_SPEC_R", "TP3D_SPEC_S0", "TP3D_SPEC_S1", "TP3D_SPEC_S01", "TP3D_CMR_NAIVE",
     "TP3D_CMR_LOAD_BALANCE", "TP3D_CMR_DFS", "TP3D_CMR_RANDOM_GREEDY", "TP3D_PIPE_GPIPE", "TP3D_PIPE_1F1B",
     "TP3D_PIPE_INTERLEAVED",
 ]
@@ -45,6 +45,7 @@ CUBE_A, CUBE_B, CUBE_C, CUBE_B_SWAP, ROW, COL, BLOCK2D, REPLICATED = range(8)
 TP3D_SPEC_R, TP3D_SPEC_S0, TP3D_SPEC_S1, TP3D_SPEC_S01 = range(4)
 TP3D_CMR_NAIVE, TP3D_CMR_LOAD_BALANCE, TP3D_CMR_DFS, TP3D_CMR_RANDOM_GREEDY = range(4)
 TP3D_PIPE_GPIPE, TP3D_PIPE_1F1B, TP3D_PIPE_INTERLEAVED = range(3)
+TP3D_SCHEME_1D, TP3D_SCHEME_2D, TP3D_SCHEME_3D = 1, 2, 3
 
 
 class tp3d_layout(ctypes.Structure):
@@ -137,6 +138,10 @@ _SIGS = {
                                         ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                         ctypes.c_void_p]),
+    "tp3d_mlp_layout": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                       ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                       ctypes.c_void_p, ctypes.c_void_p]),
     "tp3d_layer_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(tp3d_layer_cfg)]),
     "tp3d_layer_fwd": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(tp3d_layer_cfg),
                                       ctypes.POINTER(tp3d_layer_params), ctypes.c_void_p, ctypes.c_void_p,
@@ -237,6 +242,12 @@ def tp3d_mlp_noalloc(ctx, q, M, h, f, dtype, X, W1, b1, W2, b2, Y, stream=None) 
     """tp3d_mlp for callers that cannot allocate: the hidden activation lives
     in the library's own fixed 16 MiB device array (M * f <= 8388608)."""
     return lib().tp3d_mlp_noalloc(ctx, q, M, h, f, dtype, _p(X), _p(W1), _p(b1), _p(W2), _p(b2), _p(Y), _s(stream))
+
+
+def tp3d_mlp_layout(ctx, scheme, p, M, h, f, dtype, X, W1, b1, W2, b2, Y1, Y, stream=None) -> int:
+    """The MLP block in the 1-D (Megatron), 2-D (SUMMA) or 3-D (cube) layout."""
+    return lib().tp3d_mlp_layout(ctx, scheme, p, M, h, f, dtype, _p(X), _p(W1), _p(b1), _p(W2), _p(b2), _p(Y1),
+                                 _p(Y), _s(stream))
 
 
 def tp3d_layer_workspace_bytes(cfg: tp3d_layer_cfg) -> int:

@@ -39,11 +39,49 @@ tp3d_status plan_linear(const tp3d_ctx* ctx, int q, int y, int64_t M, int64_t N,
   return TP3D_OK;
 }
 
+// C (M x K) = act(A (M x N) B (N x K) + bias) with each operand in its own
+// layout: one GEMM over the layouts' blocks (the contraction runs across the
+// shards of A's columns / B's rows).
+tp3d_status plan_layouts(const tp3d_ctx* ctx, tp3d_layout la, tp3d_layout lb, tp3d_layout lc, int64_t M, int64_t N,
+                         int64_t K, const void* A, const void* B, const void* bias, int act, void* C,
+                         GemmProblem* out) {
+  GemmProblem P{};
+  TP3D_TRY(make_grid(la, M, N, &P.a.g));
+  TP3D_TRY(make_grid(lb, N, K, &P.b.g));
+  TP3D_TRY(make_grid(lc, M, K, &P.c.g));
+  P.Z = 1;
+  P.Hz = 1;
+  P.M = M;
+  P.N = K;
+  P.K = N;
+  P.a.ptr = A;
+  P.a.mn_major = 0;
+  P.b.ptr = B;
+  P.b.mn_major = 1;
+  P.c.ptr = C;
+  P.epi.act = act ? EPI_GELU : EPI_NONE;
+  P.epi.alpha = 1.0f;
+  P.epi.bias = bias;
+  P.err = ctx->d_err;
+  TP3D_TRY(plan_segments(P));
+  *out = P;
+  return TP3D_OK;
+}
+
 tp3d_status run_gemm(const tp3d_ctx* ctx, tp3d_dtype dt, const GemmProblem& P, cudaStream_t s) {
   return dt == TP3D_BF16 ? gemm_bf16_tc(ctx, P, s) : gemm_f32_simt(ctx, P, s);
 }
 
 static size_t esize(tp3d_dtype dt) { return dt == TP3D_BF16 ? 2 : 4; }
+
+static tp3d_layout layout_of(int kind, int a, int b) {
+  tp3d_layout l;
+  l.kind = kind;
+  l.q = 0;
+  l.a = a;
+  l.b = b;
+  return l;
+}
 
 }  // namespace tp3d
 
@@ -134,6 +172,44 @@ tp3d_status tp3d_mlp(tp3d_ctx* ctx, int q, int64_t M, int64_t h, int64_t f, tp3d
   GemmProblem P1, P2;
   TP3D_TRY(plan_linear(ctx, q, 0, M, h, f, X, W1, b1, 1, Y1, &P1));
   TP3D_TRY(plan_linear(ctx, q, 1, M, f, h, Y1, W2, b2, 0, Y, &P2));
+  for (const GemmProblem* P : {&P1, &P2})
+    if (P->a.g.bw % 8 || P->b.g.bw % 8 || P->c.g.bw % 8) return TP3D_ESHAPE;
+  const size_t y1b = (size_t)(M * f) * 2, yb = (size_t)(M * h) * 2;
+  const struct { const void* p; size_t n; } ins[] = {{X, (size_t)(M * h) * 2}, {W1, (size_t)(h * f) * 2},
+                                                     {b1, (size_t)f * 2}, {W2, (size_t)(f * h) * 2},
+                                                     {b2, (size_t)h * 2}};
+  for (const auto& in : ins)
+    if (overlaps(Y1, y1b, in.p, in.n) || overlaps(Y, yb, in.p, in.n)) return TP3D_EOVERLAP;
+  if (overlaps(Y, yb, Y1, y1b)) return TP3D_EOVERLAP;
+  const cudaStream_t s = as_stream(stream);
+  TP3D_TRY(gemm_bf16_tc(ctx, P1, s));
+  return gemm_bf16_tc(ctx, P2, s);
+}
+
+tp3d_status tp3d_mlp_layout(tp3d_ctx* ctx, int scheme, int p, int64_t M, int64_t h, int64_t f, tp3d_dtype dtype,
+                            const void* X, const void* W1, const void* b1, const void* W2, const void* b2, void* Y1,
+                            void* Y, void* stream) {
+  if (scheme == TP3D_SCHEME_3D) return tp3d_mlp(ctx, p, M, h, f, dtype, X, W1, b1, W2, b2, Y1, Y, stream);
+  if (!ctx || !X || !W1 || !W2 || !Y1 || !Y) return TP3D_EINVAL;
+  if ((scheme != TP3D_SCHEME_1D && scheme != TP3D_SCHEME_2D) || p < 1 || p > 1024 || M <= 0 || h <= 0 || f <= 0)
+    return TP3D_EINVAL;
+  if (dtype != TP3D_BF16) return TP3D_EDTYPE;
+  const void* ptrs[] = {X, W1, b1, W2, b2, Y1, Y};
+  for (const void* ptr : ptrs)
+    if (ptr && !aligned16(ptr)) return TP3D_EALIGN;
+  tp3d_layout lx, lw1, ly1, lw2, ly;
+  if (scheme == TP3D_SCHEME_1D) {
+    lx = layout_of(TP3D_REPLICATED, 1, 1);
+    lw1 = layout_of(TP3D_COL, p, 1);
+    ly1 = layout_of(TP3D_COL, p, 1);
+    lw2 = layout_of(TP3D_ROW, p, 1);
+    ly = layout_of(TP3D_REPLICATED, 1, 1);
+  } else {
+    lx = lw1 = ly1 = lw2 = ly = layout_of(TP3D_BLOCK2D, p, p);
+  }
+  GemmProblem P1, P2;
+  TP3D_TRY(plan_layouts(ctx, lx, lw1, ly1, M, h, f, X, W1, b1, 1, Y1, &P1));
+  TP3D_TRY(plan_layouts(ctx, ly1, lw2, ly, M, f, h, Y1, W2, b2, 0, Y, &P2));
   for (const GemmProblem* P : {&P1, &P2})
     if (P->a.g.bw % 8 || P->b.g.bw % 8 || P->c.g.bw % 8) return TP3D_ESHAPE;
   const size_t y1b = (size_t)(M * f) * 2, yb = (size_t)(M * h) * 2;
