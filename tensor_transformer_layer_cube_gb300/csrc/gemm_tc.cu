@@ -650,11 +650,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 // empty[s] and tfull[b] live in each CTA and are arrived on by the even CTA's
 // commits (multicast to both); tempty[b] lives in the even CTA and takes the
 // arrivals of both CTAs' epilogue warps.
+// KD: contraction depth of a stage, 64 (six stages) or 128 (three stages of
+// 16 KiB boxes: fewer, larger TMA transfers for the same bytes in flight).
+template <int KD>
 struct Tc2Cfg {
   static constexpr int BN = 256;
-  static constexpr int STAGES = 6;
-  static constexpr int A_BYTES = 128 * BK * 2;
-  static constexpr int B_BYTES = 128 * BK * 2;  // this CTA's half of B
+  static constexpr int BKP = KD;
+  static constexpr int STAGES = KD == 64 ? 6 : 3;
+  static constexpr int A_BYTES = 128 * KD * 2;
+  static constexpr int B_BYTES = 128 * KD * 2;  // this CTA's half of B
+  static constexpr uint32_t KCHUNK = 128 * 128;  // one 64-column K-major chunk of 128 rows
+  static constexpr uint32_t MNBOX = KD * 128;    // one 64-column MN-major box of KD rows
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TMEM_COLS = 512;
   static constexpr int STAGE_OUT = 4096;
@@ -681,12 +687,14 @@ __device__ __forceinline__ int64_t total_pair_tiles(const GemmProblem& P) {
   return (int64_t)P.Z * (P.M / P.segM) * ceil_div(P.segM, 256) * (P.N / P.segN) * ceil_div(P.segN, 256);
 }
 
+template <int KD>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                     const __grid_constant__ CUtensorMap mapC, const __grid_constant__ CUtensorMap mapZ,
                     const __grid_constant__ CUtensorMap mapX, const GemmProblem P) {
-  using Cfg = Tc2Cfg;
+  using Cfg = Tc2Cfg<KD>;
   constexpr int S = Cfg::STAGES;
+  constexpr int BKP = Cfg::BKP;
   constexpr int BN = Cfg::BN;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -742,7 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t ntiles = total_pair_tiles(P);
   const int64_t nclusters = gridDim.x >> 1, cid = blockIdx.x >> 1;
   const int32_t segK = (int32_t)P.segK;
-  const int32_t tpsK = (segK + BK - 1) / BK;
+  const int32_t tpsK = (segK + BKP - 1) / BKP;
   const int32_t nsegK = (int32_t)(P.K / P.segK);
   const bool a_mn = P.a.mn_major != 0, b_mn = P.b.mn_major != 0;
 
@@ -817,20 +825,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the even CTA expects both CTAs' bytes; the odd CTA's loads may land first
             // (the transaction count goes negative, the phase cannot end before this arrival)
             if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * Cfg::STAGE_BYTES);
-            const int kofs = kt * BK;
+            const int kofs = kt * BKP;
             if (!a_mn) {
-              tma_load_3d_pair(a_stage(s), &mapA, fb, a_k + kofs, a_c1, a_sh);
+#pragma unroll
+              for (int c = 0; c < BKP / 64; ++c)
+                tma_load_3d_pair(a_stage(s) + c * Cfg::KCHUNK, &mapA, fb, a_k + kofs + 64 * c, a_c1, a_sh);
             } else {
 #pragma unroll
               for (int h = 0; h < 2; ++h)
-                tma_load_3d_pair(a_stage(s) + h * 8192u, &mapA, fb, a_c0[h], a_k + kofs, a_shh[h]);
+                tma_load_3d_pair(a_stage(s) + h * Cfg::MNBOX, &mapA, fb, a_c0[h], a_k + kofs, a_shh[h]);
             }
             if (!b_mn) {
-              tma_load_3d_pair(b_stage(s), &mapB, fb, b_k + kofs, b_c1, b_sh);
+#pragma unroll
+              for (int c = 0; c < BKP / 64; ++c)
+                tma_load_3d_pair(b_stage(s) + c * Cfg::KCHUNK, &mapB, fb, b_k + kofs + 64 * c, b_c1, b_sh);
             } else {
 #pragma unroll
               for (int h = 0; h < 2; ++h)
-                tma_load_3d_pair(b_stage(s) + h * 8192u, &mapB, fb, b_c0[h], b_k + kofs, b_shh[h]);
+                tma_load_3d_pair(b_stage(s) + h * Cfg::MNBOX, &mapB, fb, b_c0[h], b_k + kofs, b_shh[h]);
             }
             ++it;
           }
@@ -868,11 +880,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
 #pragma unroll
-            for (int k16 = 0; k16 < BK / 16; ++k16) {
-              const uint64_t ad = a_mn ? smem_desc_sw128(a_stage(s) + k16 * 2048u, 8192u, 1024u)
-                                       : smem_desc_sw128(a_stage(s) + k16 * 32u, 16u, 1024u);
-              const uint64_t bd = b_mn ? smem_desc_sw128(b_stage(s) + k16 * 2048u, 8192u, 1024u)
-                                       : smem_desc_sw128(b_stage(s) + k16 * 32u, 16u, 1024u);
+            for (int k16 = 0; k16 < BKP / 16; ++k16) {
+              // K-major: 64-column chunks of 128 rows, +32 B per 16 columns;
+              // MN-major: 64-wide boxes of BKP rows, +16 rows per step
+              const uint32_t kk = (uint32_t)(k16 >> 2) * Cfg::KCHUNK + (uint32_t)(k16 & 3) * 32u;
+              const uint64_t ad = a_mn ? smem_desc_sw128(a_stage(s) + k16 * 2048u, Cfg::MNBOX, 1024u)
+                                       : smem_desc_sw128(a_stage(s) + kk, 16u, 1024u);
+              const uint64_t bd = b_mn ? smem_desc_sw128(b_stage(s) + k16 * 2048u, Cfg::MNBOX, 1024u)
+                                       : smem_desc_sw128(b_stage(s) + kk, 16u, 1024u);
               umma_bf16_pair(d_tmem, ad, bd, idesc, (first && k16 == 0) ? 0u : 1u);
             }
             first = false;
@@ -978,6 +993,7 @@ tp3d_status launch(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t s) {
 }
 
 // CTA pairs that fit on the device at once (0 if the query fails).
+template <int KD>
 int pair_clusters(const tp3d_ctx* ctx) {
   static int cached[64] = {};
   const int dev = ctx->device & 63;
@@ -989,14 +1005,14 @@ int pair_clusters(const tp3d_ctx* ctx) {
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Tc2Cfg::SMEM;
+  cfg.dynamicSmemBytes = Tc2Cfg<KD>::SMEM;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cfg.gridDim = dim3(2 * (unsigned)(ctx->num_sms / 2));
   int n = 0;
-  if (cudaFuncSetAttribute(gemm_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Tc2Cfg::SMEM) !=
+  if (cudaFuncSetAttribute(gemm_tc2_kernel<KD>, cudaFuncAttributeMaxDynamicSharedMemorySize, Tc2Cfg<KD>::SMEM) !=
           cudaSuccess ||
-      cudaOccupancyMaxActiveClusters(&n, gemm_tc2_kernel, &cfg) != cudaSuccess || n < 1) {
+      cudaOccupancyMaxActiveClusters(&n, gemm_tc2_kernel<KD>, &cfg) != cudaSuccess || n < 1) {
     (void)cudaGetLastError();
     cached[dev] = -1;
     return 0;
@@ -1005,11 +1021,12 @@ int pair_clusters(const tp3d_ctx* ctx) {
   return n;
 }
 
+template <int KD>
 tp3d_status launch_pair(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t s) {
-  using Cfg = Tc2Cfg;
+  using Cfg = Tc2Cfg<KD>;
   CUtensorMap ma, mb, mc, mz, mx;
-  TP3D_TRY(make_map(&ma, P.a.g, P.a.ptr, 64, P.a.mn_major ? 64 : 128));
-  TP3D_TRY(make_map(&mb, P.b.g, P.b.ptr, 64, P.b.mn_major ? 64 : 128));
+  TP3D_TRY(make_map(&ma, P.a.g, P.a.ptr, 64, P.a.mn_major ? KD : 128));
+  TP3D_TRY(make_map(&mb, P.b.g, P.b.ptr, 64, P.b.mn_major ? KD : 128));
   if (P.epi.out_f32)
     TP3D_TRY(make_map(&mc, P.c.g, P.c.ptr, 32, 32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, CU_TENSOR_MAP_SWIZZLE_128B));
   else
@@ -1026,7 +1043,7 @@ tp3d_status launch_pair(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t 
   const int64_t ntiles = (int64_t)P.Z * (P.M / P.segM) * ((P.segM + 255) / 256) * (P.N / P.segN) *
                          ((P.segN + 255) / 256);
   if (ntiles <= 0) return TP3D_OK;
-  const int max_clusters = pair_clusters(ctx);
+  const int max_clusters = pair_clusters<KD>(ctx);
   if (max_clusters < 1) return TP3D_ECUDA;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -1041,7 +1058,7 @@ tp3d_status launch_pair(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t 
   cfg.numAttrs = 1;
   const int64_t nc = ntiles < max_clusters ? ntiles : max_clusters;
   cfg.gridDim = dim3(2 * (unsigned)nc);
-  TP3D_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_tc2_kernel, ma, mb, mc, mz, mx, P));
+  TP3D_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<KD>, ma, mb, mc, mz, mx, P));
   return TP3D_OK;
 }
 
@@ -1075,7 +1092,8 @@ tp3d_status gemm_bf16_tc(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t
   const double c128 = waves(tiles(BM, 128), sms) * 0.5 / 0.45;
   const bool pairs_ok = P.causal == CAUSAL_NONE && P.segM >= 256 && P.segN >= 256;
   const double cpair = pairs_ok ? waves(tiles(256, 256), sms / 2) / 0.80 : 1e30;
-  if (cpair <= c256 && cpair <= c128) return launch_pair(ctx, P, s);
+  if (cpair <= c256 && cpair <= c128)
+    return P.segK % 128 == 0 ? launch_pair<128>(ctx, P, s) : launch_pair<64>(ctx, P, s);
   return c256 <= c128 ? launch<256>(ctx, P, s) : launch<128>(ctx, P, s);
 }
 
