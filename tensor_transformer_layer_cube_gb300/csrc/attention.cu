@@ -32,8 +32,11 @@ namespace tp3d {
 namespace {
 
 constexpr int TR = 128;              // rows of a tile (queries or keys)
-constexpr int kThreads = 192;        // 6 warps
-constexpr int kComputeWarps = 4;     // warps 2..5
+constexpr int kComputeWarps = 4;     // forward: row warps per query tile (one per TMEM lane quarter)
+// backward: warp 0 producer, warp 1 MMA issuer, warps 2-9 element-wise work,
+// two per TMEM lane quarter, each on half of a tile row's 128 columns
+constexpr int kBwdComputeWarps = 8;
+constexpr int kBwdThreads = 32 * (2 + kBwdComputeWarps);
 constexpr uint32_t kChunk = 16384;   // 128 rows x 64 bf16 columns (one 128-byte swizzle span)
 constexpr uint32_t kTile = 2 * kChunk;  // a 128 x 128 bf16 tile
 constexpr int kSmem = 7 * kTile + 512 + 1024;
@@ -408,7 +411,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 // item w: key tile w / Z of (batch, head) w % Z (the most query tiles first)
 // smem: K | V | Q0 dO0 | Q1 dO1 | PdS (32 KiB each); PdS holds P^T, then dS^T
 // TMEM: S^T [0,128) dP^T [128,256) dV [256,256+d) dK [256+d, 256+2d)
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mqkv, const __grid_constant__ CUtensorMap mo,
                          const AttnProblem A, const float* __restrict__ lse, const float* __restrict__ delta,
                          bf16* __restrict__ dqkv) {
@@ -430,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t dbytes = (uint32_t)(A.d * TR * 2);
 
   if (threadIdx.x == 0) {
-    for (int k = 0; k < 13; ++k) mbar_init(bar(k), (k == 3 || k == 4 || k == 7) ? kComputeWarps : 1);
+    for (int k = 0; k < 13; ++k) mbar_init(bar(k), (k == 3 || k == 4 || k == 7) ? kBwdComputeWarps : 1);
     *c.abort_flag = 0;
     fence_barrier_init();
   }
@@ -503,6 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ key rows
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;  // query columns [64 half, +64) of the tile
     const int r = quarter * 32 + lane;
     const float sl2 = A.scale * kLog2e;
     uint32_t n = 0, ic = 0;
@@ -518,15 +522,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t q0 = z * A.s + (jk + it) * TR;  // first query row of this tile in lse / delta
         // lane l holds lse (pre-scaled by log2 e) and delta of queries
         // 32 cc + l of the tile; query 32 cc + j is read with a shuffle from lane j
-        float lq[TR / 32], dq[TR / 32];
+        float lq[2], dq[2];
 #pragma unroll
-        for (int cc = 0; cc < TR / 32; ++cc) {
-          lq[cc] = lse[q0 + cc * 32 + lane] * kLog2e;
-          dq[cc] = delta[q0 + cc * 32 + lane];
+        for (int i = 0; i < 2; ++i) {
+          const int cc = 2 * half + i;
+          lq[i] = lse[q0 + cc * 32 + lane] * kLog2e;
+          dq[i] = delta[q0 + cc * 32 + lane];
         }
         // P^T = exp(S^T - lse), zero where the query precedes the key
 #pragma unroll
-        for (int cc = 0; cc < TR / 32; ++cc) {
+        for (int i = 0; i < 2; ++i) {
+          const int cc = 2 * half + i;
           uint32_t v[32];
           tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(cc * 32)), v);
           tmem_ld_wait();
@@ -536,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               const int q = cc * 32 + g * 8 + e;
-              const float ls = __shfl_sync(0xffffffffu, lq[cc], g * 8 + e);
+              const float ls = __shfl_sync(0xffffffffu, lq[i], g * 8 + e);
               f[e] = (!diag || q >= r) ? exp2f(__uint_as_float(v[g * 8 + e]) * sl2 - ls) : 0.0f;
             }
             st_tile8(pPdS, r, cc * 4 + g, pack8f(f));
@@ -550,7 +556,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dS^T = P^T (dP^T - delta) * scale, P^T read back (bf16) from this
         // thread's own row of the buffer and overwritten in place
 #pragma unroll
-        for (int cc = 0; cc < TR / 32; ++cc) {
+        for (int i = 0; i < 2; ++i) {
+          const int cc = 2 * half + i;
           uint32_t wv[32];
           tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(128 + cc * 32)), wv);
           tmem_ld_wait();
@@ -564,8 +571,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e2 = 0; e2 < 4; ++e2) {
               const float2 p2 = __bfloat1622float2(ph[e2]);
-              const float ds0 = __shfl_sync(0xffffffffu, dq[cc], g * 8 + 2 * e2);
-              const float ds1 = __shfl_sync(0xffffffffu, dq[cc], g * 8 + 2 * e2 + 1);
+              const float ds0 = __shfl_sync(0xffffffffu, dq[i], g * 8 + 2 * e2);
+              const float ds1 = __shfl_sync(0xffffffffu, dq[i], g * 8 + 2 * e2 + 1);
               f[2 * e2] = p2.x * (__uint_as_float(wv[g * 8 + 2 * e2]) - ds0) * A.scale;
               f[2 * e2 + 1] = p2.y * (__uint_as_float(wv[g * 8 + 2 * e2 + 1]) - ds1) * A.scale;
             }
@@ -585,7 +592,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t br = grow / A.qkv.bh, bc = gcol / A.qkv.bw;
         bf16* dst = dqkv + A.qkv.block_base((int32_t)br, (int32_t)bc) + (grow - br * A.qkv.bh) * A.qkv.bw +
                     (gcol - bc * A.qkv.bw);
-        for (int cc = 0; cc < (int)(A.d / 32); ++cc) {
+        const int nd = (int)(A.d / 64);  // this warp's 32-column chunks: its half of the d columns
+        for (int cc = half * nd; cc < half * nd + nd; ++cc) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(tmem_row(tmem, quarter, 256u + (uint32_t)(which * A.d) + cc * 32), v);
           tmem_ld_wait();
@@ -608,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // item w: query tile nq-1-(w / Z) of (batch, head) w % Z
 // smem: Q | dO | K0 V0 | K1 V1 | dS (32 KiB each)
 // TMEM: S [0,128) dP [128,256) dQ [256,256+d)
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap mqkv, const __grid_constant__ CUtensorMap mo,
                        const AttnProblem A, const float* __restrict__ lse, const float* __restrict__ delta,
                        bf16* __restrict__ dqkv) {
@@ -630,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t dbytes = (uint32_t)(A.d * TR * 2);
 
   if (threadIdx.x == 0) {
-    for (int k = 0; k < 13; ++k) mbar_init(bar(k), (k == 3 || k == 4 || k == 7) ? kComputeWarps : 1);
+    for (int k = 0; k < 13; ++k) mbar_init(bar(k), (k == 3 || k == 4 || k == 7) ? kBwdComputeWarps : 1);
     *c.abort_flag = 0;
     fence_barrier_init();
   }
@@ -699,6 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ query rows
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;  // key columns [64 half, +64) of the tile
     const int r = quarter * 32 + lane;
     const float sl2 = A.scale * kLog2e;
     uint32_t n = 0, ic = 0;
@@ -714,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const bool diag = it == niter - 1;
 #pragma unroll 1
-        for (int cc = 0; cc < TR / 32; ++cc) {
+        for (int cc = 2 * half; cc < 2 * half + 2; ++cc) {
           uint32_t v[32], wv[32];
           tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(cc * 32)), v);
           tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(128 + cc * 32)), wv);
@@ -743,7 +752,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t br = grow / A.qkv.bh, bc = gcol / A.qkv.bw;
       bf16* dst = dqkv + A.qkv.block_base((int32_t)br, (int32_t)bc) + (grow - br * A.qkv.bh) * A.qkv.bw +
                   (gcol - bc * A.qkv.bw);
-      for (int cc = 0; cc < (int)(A.d / 32); ++cc) {
+      const int nd = (int)(A.d / 64);  // this warp's half of the d columns
+      for (int cc = half * nd; cc < half * nd + nd; ++cc) {
         uint32_t v[32];
         tmem_ld_32x32b_x32(tmem_row(tmem, quarter, 256u + cc * 32), v);
         tmem_ld_wait();
@@ -855,9 +865,9 @@ tp3d_status launch_attn_bwd(const tp3d_ctx* ctx, const AttnProblem& A, const voi
   TP3D_CUDA_TRY(cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem));
   const int64_t items = A.Z * (A.s / TR);
   const unsigned grid = (unsigned)(items < ctx->num_sms ? items : ctx->num_sms);
-  attn_bwd_dkdv_kernel<<<grid, kThreads, kSmem, s>>>(mq, mo, A, lse, delta, static_cast<bf16*>(dqkv));
+  attn_bwd_dkdv_kernel<<<grid, kBwdThreads, kSmem, s>>>(mq, mo, A, lse, delta, static_cast<bf16*>(dqkv));
   TP3D_CUDA_TRY(cudaGetLastError());
-  attn_bwd_dq_kernel<<<grid, kThreads, kSmem, s>>>(mq, mo, A, lse, delta, static_cast<bf16*>(dqkv));
+  attn_bwd_dq_kernel<<<grid, kBwdThreads, kSmem, s>>>(mq, mo, A, lse, delta, static_cast<bf16*>(dqkv));
   return cudaGetLastError() == cudaSuccess ? TP3D_OK : TP3D_ECUDA;
 }
 
