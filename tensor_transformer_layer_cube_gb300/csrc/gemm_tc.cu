@@ -691,7 +691,7 @@ template <int KD>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                     const __grid_constant__ CUtensorMap mapC, const __grid_constant__ CUtensorMap mapZ,
-                    const __grid_constant__ CUtensorMap mapX, const GemmProblem P) {
+                    const __grid_constant__ CUtensorMap mapX, const GemmProblem P, const uint32_t wide) {
   using Cfg = Tc2Cfg<KD>;
   constexpr int S = Cfg::STAGES;
   constexpr int BKP = Cfg::BKP;
@@ -826,7 +826,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             // (the transaction count goes negative, the phase cannot end before this arrival)
             if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * Cfg::STAGE_BYTES);
             const int kofs = kt * BKP;
-            if (!a_mn) {
+            // a wide map moves an operand's whole stage in one box (its 64-column
+            // chunks land KCHUNK or MNBOX apart, as the separate boxes would)
+            if (wide & 1u) {
+              if (!a_mn)
+                tma_load_4d_pair(a_stage(s), &mapA, fb, a_c1, (a_k + kofs) >> 6, a_sh);
+              else
+                tma_load_4d_pair(a_stage(s), &mapA, fb, a_k + kofs, a_c0[0] >> 6, a_shh[0]);
+            } else if (!a_mn) {
 #pragma unroll
               for (int c = 0; c < BKP / 64; ++c)
                 tma_load_3d_pair(a_stage(s) + c * Cfg::KCHUNK, &mapA, fb, a_k + kofs + 64 * c, a_c1, a_sh);
@@ -835,7 +842,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int h = 0; h < 2; ++h)
                 tma_load_3d_pair(a_stage(s) + h * Cfg::MNBOX, &mapA, fb, a_c0[h], a_k + kofs, a_shh[h]);
             }
-            if (!b_mn) {
+            if (wide & 2u) {
+              if (!b_mn)
+                tma_load_4d_pair(b_stage(s), &mapB, fb, b_c1, (b_k + kofs) >> 6, b_sh);
+              else
+                tma_load_4d_pair(b_stage(s), &mapB, fb, b_k + kofs, b_c0[0] >> 6, b_shh[0]);
+            } else if (!b_mn) {
 #pragma unroll
               for (int c = 0; c < BKP / 64; ++c)
                 tma_load_3d_pair(b_stage(s) + c * Cfg::KCHUNK, &mapB, fb, b_k + kofs + 64 * c, b_c1, b_sh);
@@ -963,6 +975,23 @@ tp3d_status make_map(CUtensorMap* m, const Grid& g, const void* ptr, uint32_t bo
   return r == CUDA_SUCCESS ? TP3D_OK : TP3D_ECUDA;
 }
 
+// 4-D map over a stored bf16 matrix whose shard width is a multiple of 64:
+// (column in a 64-column chunk, row in shard, chunk, shard).  A box of
+// `chunks` chunks x `box_rows` rows lands in shared memory chunk after chunk,
+// each chunk box_rows x 128 bytes with the 128-byte swizzle.  Returns false
+// (and the caller keeps 3-D maps) if the driver rejects the encoding.
+bool make_map_wide(CUtensorMap* m, const Grid& g, const void* ptr, uint32_t box_rows, uint32_t chunks) {
+  auto fn = encode_fn();
+  if (!fn || g.bw % 64 != 0) return false;
+  cuuint64_t dims[4] = {64, (cuuint64_t)g.bh, (cuuint64_t)(g.bw / 64), (cuuint64_t)g.nshards()};
+  cuuint64_t strides[3] = {(cuuint64_t)g.bw * 2, 128, (cuuint64_t)(g.bh * g.bw * 2)};
+  cuuint32_t box[4] = {64, box_rows, chunks, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int BN>
 tp3d_status launch(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t s) {
   using Cfg = TcCfg<BN>;
@@ -1025,8 +1054,22 @@ template <int KD>
 tp3d_status launch_pair(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t s) {
   using Cfg = Tc2Cfg<KD>;
   CUtensorMap ma, mb, mc, mz, mx;
-  TP3D_TRY(make_map(&ma, P.a.g, P.a.ptr, 64, P.a.mn_major ? KD : 128));
-  TP3D_TRY(make_map(&mb, P.b.g, P.b.ptr, 64, P.b.mn_major ? KD : 128));
+  // One box per operand and stage where every stage's chunks lie in one
+  // shard: K-major, the contraction segment (a multiple of KD) inside a
+  // block row; MN-major, the CTA's 128 columns (128-aligned in a segment
+  // that is a multiple of 128) inside a block whose width is a multiple of 128.
+  uint32_t wide = 0;
+  auto wide_ok = [&](const Operand& o, int64_t seg_mn) {
+    return o.mn_major ? (o.g.bw % 128 == 0 && seg_mn % 128 == 0) : (o.g.bw % 64 == 0);
+  };
+  if (wide_ok(P.a, P.segM) && make_map_wide(&ma, P.a.g, P.a.ptr, P.a.mn_major ? KD : 128, P.a.mn_major ? 2 : KD / 64))
+    wide |= 1u;
+  else
+    TP3D_TRY(make_map(&ma, P.a.g, P.a.ptr, 64, P.a.mn_major ? KD : 128));
+  if (wide_ok(P.b, P.segN) && make_map_wide(&mb, P.b.g, P.b.ptr, P.b.mn_major ? KD : 128, P.b.mn_major ? 2 : KD / 64))
+    wide |= 2u;
+  else
+    TP3D_TRY(make_map(&mb, P.b.g, P.b.ptr, 64, P.b.mn_major ? KD : 128));
   if (P.epi.out_f32)
     TP3D_TRY(make_map(&mc, P.c.g, P.c.ptr, 32, 32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, CU_TENSOR_MAP_SWIZZLE_128B));
   else
@@ -1058,7 +1101,7 @@ tp3d_status launch_pair(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t 
   cfg.numAttrs = 1;
   const int64_t nc = ntiles < max_clusters ? ntiles : max_clusters;
   cfg.gridDim = dim3(2 * (unsigned)nc);
-  TP3D_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<KD>, ma, mb, mc, mz, mx, P));
+  TP3D_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<KD>, ma, mb, mc, mz, mx, P, wide));
   return TP3D_OK;
 }
 
