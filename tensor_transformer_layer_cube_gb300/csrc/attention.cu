@@ -771,30 +771,49 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
-// delta[z*s + r] = sum over the head's d columns of dO * O (one warp per row)
+// delta[z*s + r] = sum over the head's d columns of dO * O.  One warp per
+// token row: 16-byte loads, 256 columns (every head in them) per step, four
+// steps in flight; the G = d/8 lanes that hold one head reduce with shuffles.
+template <int G>
 __global__ void __launch_bounds__(256) attn_delta_kernel(const AttnProblem A, const bf16* __restrict__ O,
                                                          const bf16* __restrict__ dO, float* __restrict__ delta) {
+  constexpr int U = 4;
   const int lane = threadIdx.x & 31;
-  const int64_t rows = A.Z * A.s;
-  for (int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); row < rows; row += (int64_t)gridDim.x * 8) {
-    const int64_t z = row / A.s, rr = row - z * A.s;
-    const int64_t b = z / A.H, t = z % A.H;
-    const int64_t grow = b * A.s + rr, gcol = t * A.d;
-    const int64_t br = grow / A.o.bh, bc = gcol / A.o.bw;
-    const int64_t off = A.o.block_base((int32_t)br, (int32_t)bc) + (grow - br * A.o.bh) * A.o.bw + (gcol - bc * A.o.bw);
-    float acc = 0.0f;
-    for (int64_t cidx = lane * 4; cidx < A.d; cidx += 128) {
-      const uint2 a = *reinterpret_cast<const uint2*>(O + off + cidx);
-      const uint2 g = *reinterpret_cast<const uint2*>(dO + off + cidx);
-      const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a.x));
-      const float2 a1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a.y));
-      const float2 g0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g.x));
-      const float2 g1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g.y));
-      acc += a0.x * g0.x + a0.y * g0.y + a1.x * g1.x + a1.y * g1.y;
-    }
+  const int64_t M = A.Z / A.H * A.s;  // token rows
+  const int64_t nw = (int64_t)gridDim.x * 8;
+  for (int64_t tok = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); tok < M; tok += nw) {
+    const int64_t b = tok / A.s, rr = tok - b * A.s;
+    const int64_t br = tok / A.o.bh, rin = tok - br * A.o.bh;
+    for (int64_t c0 = 0; c0 < A.h; c0 += 256 * U) {
+      uint4 a[U], g[U];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) delta[row] = acc;
+      for (int u = 0; u < U; ++u) {
+        const int64_t col = c0 + u * 256 + lane * 8;
+        if (col < A.h) {
+          const int64_t bc = col / A.o.bw;
+          const int64_t off = A.o.block_base((int32_t)br, (int32_t)bc) + rin * A.o.bw + (col - bc * A.o.bw);
+          a[u] = __ldg(reinterpret_cast<const uint4*>(O + off));
+          g[u] = __ldg(reinterpret_cast<const uint4*>(dO + off));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t col = c0 + u * 256 + lane * 8;
+        float acc = 0.0f;
+        if (col < A.h) {
+          const __nv_bfloat162* ah = reinterpret_cast<const __nv_bfloat162*>(&a[u]);
+          const __nv_bfloat162* gh = reinterpret_cast<const __nv_bfloat162*>(&g[u]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 x = __bfloat1622float2(ah[e]), y = __bfloat1622float2(gh[e]);
+            acc += x.x * y.x + x.y * y.y;
+          }
+        }
+#pragma unroll
+        for (int o = G / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if ((lane & (G - 1)) == 0 && col < A.h) delta[(b * A.H + col / A.d) * A.s + rr] = acc;
+      }
+    }
   }
 }
 
@@ -855,11 +874,15 @@ tp3d_status launch_attn_bwd(const tp3d_ctx* ctx, const AttnProblem& A, const voi
   CUtensorMap mq, mo;
   TP3D_TRY(tile_map(&mq, A.qkv, qkv));
   TP3D_TRY(tile_map(&mo, A.o, dO));
-  const int64_t rows = A.Z * A.s;
-  int64_t dgrid = (rows + 7) / 8;
-  if (dgrid > (int64_t)ctx->num_sms * 16) dgrid = (int64_t)ctx->num_sms * 16;
-  attn_delta_kernel<<<(unsigned)dgrid, 256, 0, s>>>(A, static_cast<const bf16*>(o), static_cast<const bf16*>(dO),
-                                                    delta);
+  const int64_t tokens = A.Z / A.H * A.s;
+  int64_t dgrid = (tokens + 7) / 8;
+  if (dgrid > (int64_t)ctx->num_sms * 8) dgrid = (int64_t)ctx->num_sms * 8;
+  if (A.d == 128)
+    attn_delta_kernel<16><<<(unsigned)dgrid, 256, 0, s>>>(A, static_cast<const bf16*>(o), static_cast<const bf16*>(dO),
+                                                          delta);
+  else
+    attn_delta_kernel<8><<<(unsigned)dgrid, 256, 0, s>>>(A, static_cast<const bf16*>(o), static_cast<const bf16*>(dO),
+                                                         delta);
   TP3D_CUDA_TRY(cudaGetLastError());
   TP3D_CUDA_TRY(cudaFuncSetAttribute(attn_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem));
   TP3D_CUDA_TRY(cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem));

@@ -154,10 +154,72 @@ __global__ void __launch_bounds__(kThreads) ln_bwd_kernel(const Grid g, const bf
   }
 }
 
+// LayerNorm forward with the whole row in registers: C = NV * 256, lane l holds
+// columns 8 (l + 32 i) .. +7 for i < NV.  Every load of a row is issued
+// before the first use, so a warp spends one memory round trip per row, and
+// the statistics are taken from registers (two passes over them, no reload).
+template <int NV>
+__device__ __forceinline__ int64_t row_vec_off(const Grid& g, int64_t br, int64_t rr, int lane, int i) {
+  const int32_t col = (lane + 32 * i) * 8;
+  const int32_t bc = col / (int32_t)g.bw;
+  return g.block_base((int32_t)br, bc) + rr * g.bw + (col - (int64_t)bc * g.bw);
+}
+
+template <int NV>
+__global__ void __launch_bounds__(kThreads) ln_fwd_row_kernel(const Grid g, const bf16* __restrict__ x,
+                                                              const bf16* __restrict__ gamma,
+                                                              const bf16* __restrict__ beta, bf16* __restrict__ y,
+                                                              float* __restrict__ mean, float* __restrict__ rstd,
+                                                              float eps) {
+  constexpr float invC = 1.0f / (float)(NV * 256);
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * kWarps;
+  for (int64_t r = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); r < g.R; r += nwarps) {
+    const int64_t br = r / g.bh, rr = r - br * g.bh;
+    uint4 xv[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) xv[i] = __ldg(reinterpret_cast<const uint4*>(x + row_vec_off<NV>(g, br, rr, lane, i)));
+    float s1 = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      float f[8];
+      unpack8(xv[i], f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) s1 += f[e];
+    }
+    const float mu = warp_sum(s1) * invC;
+    float s2 = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      float f[8];
+      unpack8(xv[i], f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) s2 += (f[e] - mu) * (f[e] - mu);
+    }
+    const float rs = rsqrtf(warp_sum(s2) * invC + eps);
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int32_t col = (lane + 32 * i) * 8;
+      float f[8], gg[8], bb[8], o[8];
+      unpack8(xv[i], f);
+      unpack8(__ldg(reinterpret_cast<const uint4*>(gamma + col)), gg);
+      unpack8(__ldg(reinterpret_cast<const uint4*>(beta + col)), bb);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = (f[e] - mu) * rs * gg[e] + bb[e];
+      *reinterpret_cast<uint4*>(y + row_vec_off<NV>(g, br, rr, lane, i)) = pack8(o);
+    }
+    if (lane == 0) {
+      mean[r] = mu;
+      rstd[r] = rs;
+    }
+  }
+}
+
 // ------------------------------------------------------------------ column sums
 // CTA (x, y): columns [256 x, +256) over the rows of part y (rows_per_part
 // rows inside one row block); lane l of every warp holds columns 8l..8l+7,
-// warps stride over rows with eight rows' loads in flight; the 8 warps are
+// warps stride over rows with U rows' loads in flight (16, or 8 when each
+// row brings two inputs); the 8 warps are
 // summed in shared memory into the part's partial row.  The last CTA of a
 // column strip to finish (an atomic count per strip, reset to zero after)
 // adds the partial rows of all parts and writes the bf16 sums.
@@ -171,7 +233,7 @@ __global__ void __launch_bounds__(kThreads) colsum_kernel(const Grid g, const bf
                                                           float* __restrict__ part2, int64_t rows_per_part,
                                                           int* __restrict__ counters, bf16* __restrict__ out,
                                                           bf16* __restrict__ out2) {
-  constexpr int U = 8;  // rows in flight per warp
+  constexpr int U = LN ? 8 : 16;  // rows in flight per warp
   __shared__ float red[kWarps][257];
   __shared__ int is_last;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -304,7 +366,13 @@ tp3d_status launch_ln_fwd(const tp3d_ctx* ctx, const Grid& g, const void* x, con
   const bf16 *xb = static_cast<const bf16*>(x), *gb = static_cast<const bf16*>(gamma),
              *bb = static_cast<const bf16*>(beta);
   bf16* yb = static_cast<bf16*>(y);
-  ln_fwd_kernel<<<grid, kThreads, 0, s>>>(g, xb, gb, bb, yb, mean, rstd, eps);
+  switch (g.C % 256 == 0 ? g.C / 256 : 0) {  // whole rows in registers where C = 256 NV
+    case 2: ln_fwd_row_kernel<2><<<grid, kThreads, 0, s>>>(g, xb, gb, bb, yb, mean, rstd, eps); break;
+    case 4: ln_fwd_row_kernel<4><<<grid, kThreads, 0, s>>>(g, xb, gb, bb, yb, mean, rstd, eps); break;
+    case 8: ln_fwd_row_kernel<8><<<grid, kThreads, 0, s>>>(g, xb, gb, bb, yb, mean, rstd, eps); break;
+    case 16: ln_fwd_row_kernel<16><<<grid, kThreads, 0, s>>>(g, xb, gb, bb, yb, mean, rstd, eps); break;
+    default: ln_fwd_kernel<<<grid, kThreads, 0, s>>>(g, xb, gb, bb, yb, mean, rstd, eps);
+  }
   return last_error();
 }
 
@@ -321,18 +389,29 @@ tp3d_status launch_ln_bwd(const tp3d_ctx* ctx, const Grid& g, const void* dy, co
 int64_t colsum_strips(const Grid& g) { return (g.C + 255) / 256; }
 // the most parts any launch uses (64-row parts), for sizing the scratch
 int64_t colsum_parts(const Grid& g) { return g.R / gcd64(g.bh, 64); }
-// rows per part: a power of two (64..1024, dividing the row block) that
-// gives about three CTAs per SM
+// rows per part: the smallest power of two (64..1024, dividing the row
+// block) for which every CTA is resident at once (one round, no tail wave)
+template <bool LN>
 int64_t colsum_rows(const tp3d_ctx* ctx, const Grid& g) {
-  const int64_t want = colsum_strips(g) * g.R / (3 * (int64_t)ctx->num_sms);
+  static int per_sm[64] = {};
+  const int dev = ctx->device & 63;
+  if (per_sm[dev] == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, colsum_kernel<LN>, kThreads, 0) != cudaSuccess || n < 1) {
+      (void)cudaGetLastError();
+      n = 1;
+    }
+    per_sm[dev] = n;
+  }
+  const int64_t slots = (int64_t)per_sm[dev] * ctx->num_sms;
   int64_t p = 64;
-  while (p < 1024 && p * 2 <= want) p *= 2;
+  while (p < 1024 && colsum_strips(g) * ((g.R + p - 1) / p) > slots) p *= 2;
   return gcd64(g.bh, p);
 }
 
 tp3d_status launch_colsum(const tp3d_ctx* ctx, const Grid& g, const void* x, float* part, int* counters, void* out,
                           cudaStream_t s) {
-  const int64_t rpp = colsum_rows(ctx, g);
+  const int64_t rpp = colsum_rows<false>(ctx, g);
   const dim3 grid((unsigned)colsum_strips(g), (unsigned)(g.R / rpp));
   if (grid.y > 65535u) return TP3D_EUNSUPPORTED;
   colsum_kernel<false><<<grid, kThreads, 0, s>>>(g, static_cast<const bf16*>(x), nullptr, nullptr, nullptr, part,
@@ -343,7 +422,7 @@ tp3d_status launch_colsum(const tp3d_ctx* ctx, const Grid& g, const void* x, flo
 tp3d_status launch_ln_param_grads(const tp3d_ctx* ctx, const Grid& g, const void* dy, const void* x,
                                   const float* mean, const float* rstd, float* part, int* counters, void* out_g,
                                   void* out_b, cudaStream_t s) {
-  const int64_t rpp = colsum_rows(ctx, g);
+  const int64_t rpp = colsum_rows<true>(ctx, g);
   const dim3 grid((unsigned)colsum_strips(g), (unsigned)(g.R / rpp));
   if (grid.y > 65535u) return TP3D_EUNSUPPORTED;
   colsum_kernel<true><<<grid, kThreads, 0, s>>>(g, static_cast<const bf16*>(x), static_cast<const bf16*>(dy), mean,
