@@ -15,8 +15,10 @@
 //    shared memory, O += P V in TMEM, O rescaled only when the row maximum
 //    grows by more than 2^8); the row's log-sum-exp is saved for the backward.
 //  * backward dK/dV: per key tile, over the query tiles at or above the
-//    diagonal: S^T = K Q^T, dP^T = V dO^T, P^T = exp(S^T - lse), then
-//    dV += P^T dO and dK += dS^T Q with dS = P (dP - rowsum(dO O)) / sqrt(d).
+//    diagonal: S = Q K^T, dP = dO V^T, P = exp(S - lse) (one query row per
+//    thread, so lse and rowsum(dO O) are per-thread values), then
+//    dV += P^T dO and dK += dS^T Q with dS = P (dP - rowsum(dO O)) / sqrt(d),
+//    P and dS read transposed out of shared memory by the MMA.
 //  * backward dQ: per query tile, over the key tiles at or below the
 //    diagonal: S, dP, dS as above, dQ += dS K.
 // The score and probability matrices never leave the SM.  Every mbarrier
@@ -409,8 +411,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
 // ------------------------------------------------------------------ backward: dK, dV
 // item w: key tile w / Z of (batch, head) w % Z (the most query tiles first)
-// smem: K | V | Q0 dO0 | Q1 dO1 | PdS (32 KiB each); PdS holds P^T, then dS^T
-// TMEM: S^T [0,128) dP^T [128,256) dV [256,256+d) dK [256+d, 256+2d)
+// smem: K | V | Q0 dO0 | Q1 dO1 | PdS (32 KiB each); PdS holds P, then dS,
+// [query][key] (the MN-major A operand of the dV and dK products)
+// TMEM: S [0,128) dP [128,256) (lanes = queries), dV [256,256+d) dK
+// [256+d, 256+2d) (lanes = keys)
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mqkv, const __grid_constant__ CUtensorMap mo,
                          const AttnProblem A, const float* __restrict__ lse, const float* __restrict__ delta,
@@ -471,7 +475,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16_f32(TR, TR, 0, 0);
-      const uint32_t id_acc = idesc_bf16_f32(TR, (int)A.d, 0, 1);
+      const uint32_t id_acc = idesc_bf16_f32(TR, (int)A.d, 1, 1);  // A = P^T or dS^T, read transposed
       const int ks_d = (int)(A.d / 16);
       uint32_t n = 0, ic = 0;
       bool ok = true;
@@ -483,18 +487,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!(ok = mbar_wait(r_full(s), (n >> 1) & 1, c.abort_flag, A.err))) break;
           if (!(ok = mbar_wait(st_empty, (n & 1) ^ 1, c.abort_flag, A.err))) break;
           tc_fence_after();
-          mma_tile(tmem, sK, false, sQ[s], false, ks_d, id_s, false);          // S^T = K Q^T
-          mma_tile(tmem + 128u, sV, false, sdO[s], false, ks_d, id_s, false);  // dP^T = V dO^T
+          mma_tile(tmem, sQ[s], false, sK, false, ks_d, id_s, false);          // S = Q K^T
+          mma_tile(tmem + 128u, sdO[s], false, sV, false, ks_d, id_s, false);  // dP = dO V^T
           if (it == niter - 1) umma_commit(kv_empty);
           umma_commit(st_full);
           if (!(ok = mbar_wait(pds_full, 0, c.abort_flag, A.err))) break;
           if (it == 0 && !(ok = mbar_wait(acc_empty, (ic & 1) ^ 1, c.abort_flag, A.err))) break;
           tc_fence_after();
-          mma_tile(tmem + 256u, sPdS, false, sdO[s], true, TR / 16, id_acc, it > 0);  // dV += P^T dO
+          mma_tile(tmem + 256u, sPdS, true, sdO[s], true, TR / 16, id_acc, it > 0);  // dV += P^T dO
           umma_commit(pds_empty);
           if (!(ok = mbar_wait(pds_full, 1, c.abort_flag, A.err))) break;
           tc_fence_after();
-          mma_tile(tmem + 256u + (uint32_t)A.d, sPdS, false, sQ[s], true, TR / 16, id_acc, it > 0);  // dK += dS^T Q
+          mma_tile(tmem + 256u + (uint32_t)A.d, sPdS, true, sQ[s], true, TR / 16, id_acc, it > 0);  // dK += dS^T Q
           umma_commit(pds_empty);
           umma_commit(r_empty(s));
         }
@@ -504,9 +508,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       drain(final_bar, 0);
     }
   } else {
-    // ------------------------------------------------------------ key rows
+    // ---------------------------------------- query rows of S and dP (then key rows of dV, dK)
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;  // query columns [64 half, +64) of the tile
+    const int half = (warp - 2) >> 2;  // key columns [64 half, +64) of the tile
     const int r = quarter * 32 + lane;
     const float sl2 = A.scale * kLog2e;
     uint32_t n = 0, ic = 0;
@@ -515,37 +519,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int64_t jk = w / A.Z, z = w % A.Z, b = z / A.H, t = z % A.H;
       const int niter = (int)(nq - jk);
       for (int it = 0; it < niter && ok; ++it, ++n) {
+        // this thread's query row: its log-sum-exp and delta, read before the waits
+        const int64_t qrow = z * A.s + (jk + it) * TR + r;
+        const float l2 = lse[qrow] * kLog2e, dr = delta[qrow];
         if (!(ok = warp_wait(st_full, n & 1, c, A.err, lane))) break;
         if (!(ok = warp_wait(pds_empty, 1, c, A.err, lane))) break;  // previous dK product done
         tc_fence_after();
         const bool diag = it == 0;
-        const int64_t q0 = z * A.s + (jk + it) * TR;  // first query row of this tile in lse / delta
-        // lane l holds lse (pre-scaled by log2 e) and delta of queries
-        // 32 cc + l of the tile; query 32 cc + j is read with a shuffle from lane j
-        float lq[2], dq[2];
+        // P = exp2(S sl2 - lse), zero where the key follows the query; stored
+        // [query][key], the layout the dV product reads transposed
+        {
+          uint32_t v[2][32];
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int cc = 2 * half + i;
-          lq[i] = lse[q0 + cc * 32 + lane] * kLog2e;
-          dq[i] = delta[q0 + cc * 32 + lane];
-        }
-        // P^T = exp(S^T - lse), zero where the query precedes the key
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int cc = 2 * half + i;
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(cc * 32)), v);
+          for (int i = 0; i < 2; ++i) tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)((2 * half + i) * 32)), v[i]);
           tmem_ld_wait();
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            float f[8];
+          for (int i = 0; i < 2; ++i) {
+            const int cc = 2 * half + i;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int q = cc * 32 + g * 8 + e;
-              const float ls = __shfl_sync(0xffffffffu, lq[i], g * 8 + e);
-              f[e] = (!diag || q >= r) ? exp2f(__uint_as_float(v[g * 8 + e]) * sl2 - ls) : 0.0f;
+            for (int g = 0; g < 4; ++g) {
+              float f[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const int k = cc * 32 + g * 8 + e;
+                f[e] = (!diag || k <= r) ? exp2f(__uint_as_float(v[i][g * 8 + e]) * sl2 - l2) : 0.0f;
+              }
+              st_tile8(pPdS, r, cc * 4 + g, pack8f(f));
             }
-            st_tile8(pPdS, r, cc * 4 + g, pack8f(f));
           }
         }
         fence_proxy_async_smem();
@@ -553,30 +553,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         warp_arrive(pds_full, lane);
         if (!(ok = warp_wait(pds_empty, 0, c, A.err, lane))) break;  // dV product has read P^T
         tc_fence_after();
-        // dS^T = P^T (dP^T - delta) * scale, P^T read back (bf16) from this
-        // thread's own row of the buffer and overwritten in place
+        // dS = P (dP - delta) * scale, P read back (bf16) from this thread's
+        // own row of the buffer and overwritten in place
+        {
+          uint32_t wv[2][32];
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int cc = 2 * half + i;
-          uint32_t wv[32];
-          tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(128 + cc * 32)), wv);
+          for (int i = 0; i < 2; ++i)
+            tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(128 + (2 * half + i) * 32)), wv[i]);
           tmem_ld_wait();
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            uint4* slot = reinterpret_cast<uint4*>(pPdS + ((cc * 4 + g) >> 3) * kChunk + r * 128 +
-                                                   ((((cc * 4 + g) & 7) ^ (r & 7)) << 4));
-            const uint4 pv = *slot;
-            const __nv_bfloat162* ph = reinterpret_cast<const __nv_bfloat162*>(&pv);
-            float f[8];
+          for (int i = 0; i < 2; ++i) {
+            const int cc = 2 * half + i;
 #pragma unroll
-            for (int e2 = 0; e2 < 4; ++e2) {
-              const float2 p2 = __bfloat1622float2(ph[e2]);
-              const float ds0 = __shfl_sync(0xffffffffu, dq[i], g * 8 + 2 * e2);
-              const float ds1 = __shfl_sync(0xffffffffu, dq[i], g * 8 + 2 * e2 + 1);
-              f[2 * e2] = p2.x * (__uint_as_float(wv[g * 8 + 2 * e2]) - ds0) * A.scale;
-              f[2 * e2 + 1] = p2.y * (__uint_as_float(wv[g * 8 + 2 * e2 + 1]) - ds1) * A.scale;
+            for (int g = 0; g < 4; ++g) {
+              uint4* slot = reinterpret_cast<uint4*>(pPdS + ((cc * 4 + g) >> 3) * kChunk + r * 128 +
+                                                     ((((cc * 4 + g) & 7) ^ (r & 7)) << 4));
+              const uint4 pv = *slot;
+              const __nv_bfloat162* ph = reinterpret_cast<const __nv_bfloat162*>(&pv);
+              float f[8];
+#pragma unroll
+              for (int e2 = 0; e2 < 4; ++e2) {
+                const float2 p2 = __bfloat1622float2(ph[e2]);
+                f[2 * e2] = p2.x * (__uint_as_float(wv[i][g * 8 + 2 * e2]) - dr) * A.scale;
+                f[2 * e2 + 1] = p2.y * (__uint_as_float(wv[i][g * 8 + 2 * e2 + 1]) - dr) * A.scale;
+              }
+              *slot = pack8f(f);
             }
-            *slot = pack8f(f);
           }
         }
         fence_proxy_async_smem();
