@@ -479,23 +479,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int ks_d = (int)(A.d / 16);
       uint32_t n = 0, ic = 0;
       bool ok = true;
+      // S = Q K^T and dP = dO V^T of global query-tile iteration m (slot m & 1)
+      auto issue_sdp = [&](uint32_t m, bool last) -> bool {
+        const int sm = (int)(m & 1u);
+        if (!mbar_wait(r_full(sm), (m >> 1) & 1, c.abort_flag, A.err)) return false;
+        if (!mbar_wait(st_empty, (m & 1) ^ 1, c.abort_flag, A.err)) return false;
+        tc_fence_after();
+        mma_tile(tmem, sQ[sm], false, sK, false, ks_d, id_s, false);
+        mma_tile(tmem + 128u, sdO[sm], false, sV, false, ks_d, id_s, false);
+        if (last) umma_commit(kv_empty);  // the item's K and V are no longer read
+        umma_commit(st_full);
+        return true;
+      };
       for (int64_t w = blockIdx.x; w < items && ok; w += gridDim.x, ++ic) {
         const int niter = (int)(nq - w / A.Z);
         if (!(ok = mbar_wait(kv_full, ic & 1, c.abort_flag, A.err))) break;
+        if (!(ok = issue_sdp(n, niter == 1))) break;
         for (int it = 0; it < niter && ok; ++it, ++n) {
           const int s = n & 1;
-          if (!(ok = mbar_wait(r_full(s), (n >> 1) & 1, c.abort_flag, A.err))) break;
-          if (!(ok = mbar_wait(st_empty, (n & 1) ^ 1, c.abort_flag, A.err))) break;
-          tc_fence_after();
-          mma_tile(tmem, sQ[s], false, sK, false, ks_d, id_s, false);          // S = Q K^T
-          mma_tile(tmem + 128u, sdO[s], false, sV, false, ks_d, id_s, false);  // dP = dO V^T
-          if (it == niter - 1) umma_commit(kv_empty);
-          umma_commit(st_full);
           if (!(ok = mbar_wait(pds_full, 0, c.abort_flag, A.err))) break;
           if (it == 0 && !(ok = mbar_wait(acc_empty, (ic & 1) ^ 1, c.abort_flag, A.err))) break;
           tc_fence_after();
           mma_tile(tmem + 256u, sPdS, true, sdO[s], true, TR / 16, id_acc, it > 0);  // dV += P^T dO
           umma_commit(pds_empty);
+          // the next query tile's S and dP go ahead of this tile's dK, so they
+          // are computed while the element-wise warps form dS
+          if (it + 1 < niter && !(ok = issue_sdp(n + 1, it + 2 == niter))) break;
           if (!(ok = mbar_wait(pds_full, 1, c.abort_flag, A.err))) break;
           tc_fence_after();
           mma_tile(tmem + 256u + (uint32_t)A.d, sPdS, true, sQ[s], true, TR / 16, id_acc, it > 0);  // dK += dS^T Q
@@ -523,11 +532,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int64_t qrow = z * A.s + (jk + it) * TR + r;
         const float l2 = lse[qrow] * kLog2e, dr = delta[qrow];
         if (!(ok = warp_wait(st_full, n & 1, c, A.err, lane))) break;
-        if (!(ok = warp_wait(pds_empty, 1, c, A.err, lane))) break;  // previous dK product done
         tc_fence_after();
         const bool diag = it == 0;
-        // P = exp2(S sl2 - lse), zero where the key follows the query; stored
-        // [query][key], the layout the dV product reads transposed
+        // P = exp2(S sl2 - lse), zero where the key follows the query, kept as
+        // bf16 pairs: computed before the buffer is free, stored [query][key]
+        // (the layout the dV product reads transposed) once it is
+        uint32_t pk[2][16];
         {
           uint32_t v[2][32];
 #pragma unroll
@@ -535,56 +545,55 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
-            const int cc = 2 * half + i;
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-              float f[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const int k = cc * 32 + g * 8 + e;
-                f[e] = (!diag || k <= r) ? exp2f(__uint_as_float(v[i][g * 8 + e]) * sl2 - l2) : 0.0f;
-              }
-              st_tile8(pPdS, r, cc * 4 + g, pack8f(f));
+            for (int e2 = 0; e2 < 16; ++e2) {
+              const int k = (2 * half + i) * 32 + 2 * e2;
+              const float f0 = (!diag || k <= r) ? exp2f(__uint_as_float(v[i][2 * e2]) * sl2 - l2) : 0.0f;
+              const float f1 = (!diag || k + 1 <= r) ? exp2f(__uint_as_float(v[i][2 * e2 + 1]) * sl2 - l2) : 0.0f;
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(f0, f1);
+              pk[i][e2] = *reinterpret_cast<const uint32_t*>(&h2);
             }
           }
         }
+        if (!(ok = warp_wait(pds_empty, 1, c, A.err, lane))) break;  // previous dK product has read dS
+        auto store_pk = [&]() {
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+              st_tile8(pPdS, r, (2 * half + i) * 4 + g,
+                       make_uint4(pk[i][4 * g], pk[i][4 * g + 1], pk[i][4 * g + 2], pk[i][4 * g + 3]));
+        };
+        store_pk();
         fence_proxy_async_smem();
         tc_fence_before();
         warp_arrive(pds_full, lane);
-        if (!(ok = warp_wait(pds_empty, 0, c, A.err, lane))) break;  // dV product has read P^T
-        tc_fence_after();
-        // dS = P (dP - delta) * scale, P read back (bf16) from this thread's
-        // own row of the buffer and overwritten in place
+        // dS = P (dP - delta) * scale from the bf16 P in registers
         {
           uint32_t wv[2][32];
 #pragma unroll
           for (int i = 0; i < 2; ++i)
             tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(128 + (2 * half + i) * 32)), wv[i]);
           tmem_ld_wait();
+          tc_fence_before();
+          warp_arrive(st_empty, lane);  // S and dP are read: the next tile's may overwrite them
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
-            const int cc = 2 * half + i;
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-              uint4* slot = reinterpret_cast<uint4*>(pPdS + ((cc * 4 + g) >> 3) * kChunk + r * 128 +
-                                                     ((((cc * 4 + g) & 7) ^ (r & 7)) << 4));
-              const uint4 pv = *slot;
-              const __nv_bfloat162* ph = reinterpret_cast<const __nv_bfloat162*>(&pv);
-              float f[8];
-#pragma unroll
-              for (int e2 = 0; e2 < 4; ++e2) {
-                const float2 p2 = __bfloat1622float2(ph[e2]);
-                f[2 * e2] = p2.x * (__uint_as_float(wv[i][g * 8 + 2 * e2]) - dr) * A.scale;
-                f[2 * e2 + 1] = p2.y * (__uint_as_float(wv[i][g * 8 + 2 * e2 + 1]) - dr) * A.scale;
-              }
-              *slot = pack8f(f);
+            for (int e2 = 0; e2 < 16; ++e2) {
+              const float2 p2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[i][e2]));
+              const float d0 = p2.x * (__uint_as_float(wv[i][2 * e2]) - dr) * A.scale;
+              const float d1 = p2.y * (__uint_as_float(wv[i][2 * e2 + 1]) - dr) * A.scale;
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(d0, d1);
+              pk[i][e2] = *reinterpret_cast<const uint32_t*>(&h2);
             }
           }
         }
+        if (!(ok = warp_wait(pds_empty, 0, c, A.err, lane))) break;  // dV product has read P
+        store_pk();
         fence_proxy_async_smem();
         tc_fence_before();
         warp_arrive(pds_full, lane);
-        warp_arrive(st_empty, lane);
       }
       if (!ok || !(ok = warp_wait(acc_full, ic & 1, c, A.err, lane))) break;
       tc_fence_after();
