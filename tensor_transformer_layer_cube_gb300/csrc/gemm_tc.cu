@@ -668,19 +668,25 @@ struct Tc2Cfg {
   static constexpr int SMEM = STAGES * STAGE_BYTES + kEpiWarps * STAGE_OUT + BAR_BYTES + 1024;
 };
 
-// Tile t for CTA r of the pair.
+// Tile t for CTA r of the pair.  32-bit arithmetic (the launcher checks that
+// every extent and the tile count fit): a 64-bit division is a long software
+// sequence, and this runs at every tile change of the producer.
+__device__ __forceinline__ uint32_t udiv32(int64_t a, int64_t b) { return (uint32_t)a / (uint32_t)b; }
 __device__ __forceinline__ void decode_pair_tile(const GemmProblem& P, int64_t t, uint32_t r, TileInfo& T) {
-  const int64_t tpsM = ceil_div(P.segM, 256), tpsN = ceil_div(P.segN, 256);
-  const int64_t tiles_m = (P.M / P.segM) * tpsM;
-  const int64_t per_z = tiles_m * (P.N / P.segN) * tpsN;
-  T.z = (int32_t)(t / per_z);
-  const int64_t rem = t - (int64_t)T.z * per_z;
-  const int64_t tn = rem / tiles_m, tm = rem - tn * tiles_m;
-  const int64_t sm = tm / tpsM, sn = tn / tpsN;
-  T.m0 = sm * P.segM + (tm - sm * tpsM) * 256 + 128 * (int64_t)r;
-  T.n0 = sn * P.segN + (tn - sn * tpsN) * 256;
-  T.m_end = sm * P.segM + P.segM;
-  T.n_end = sn * P.segN + P.segN;
+  const uint32_t segM = (uint32_t)P.segM, segN = (uint32_t)P.segN;
+  const uint32_t tpsM = (segM + 255u) / 256u, tpsN = (segN + 255u) / 256u;
+  const uint32_t tiles_m = udiv32(P.M, segM) * tpsM;
+  const uint32_t per_z = tiles_m * udiv32(P.N, segN) * tpsN;
+  const uint32_t tt = (uint32_t)t;
+  const uint32_t z = tt / per_z;
+  const uint32_t rem = tt - z * per_z;
+  const uint32_t tn = rem / tiles_m, tm = rem - tn * tiles_m;
+  const uint32_t sm = tm / tpsM, sn = tn / tpsN;
+  T.z = (int32_t)z;
+  T.m0 = (int64_t)sm * segM + (int64_t)(tm - sm * tpsM) * 256 + 128 * (int64_t)r;
+  T.n0 = (int64_t)sn * segN + (int64_t)(tn - sn * tpsN) * 256;
+  T.m_end = (int64_t)sm * segM + segM;
+  T.n_end = (int64_t)sn * segN + segN;
 }
 
 __device__ __forceinline__ int64_t total_pair_tiles(const GemmProblem& P) {
@@ -757,59 +763,73 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------------- producer
-      uint32_t it = 0;
-      bool ok = true;
-      for (int64_t t = cid; t < ntiles && ok; t += nclusters) {
+      // Where a tile's operand boxes start (block row or columns and offsets
+      // inside the block).  The next tile's are worked out while the current
+      // tile's first stage is in flight, so a tile change costs no arithmetic.
+      struct TileLd {
+        int64_t ak, bk;
+        int32_t a_br, b_br, a_c1, b_c1;
+        int32_t a_bc[2], b_bc[2], a_c0[2], b_c0[2];
+      };
+      auto setup = [&](int64_t t, TileLd& L) {
         TileInfo T;
         decode_pair_tile(P, t, rank, T);
         const int64_t am = T.m0 + op_off(P.a.hi1, P.a.lo1, P.a.base1, T.z, P.Hz);
-        const int64_t ak = op_off(P.a.hi2, P.a.lo2, P.a.base2, T.z, P.Hz);
-        const int64_t bk = op_off(P.b.hi1, P.b.lo1, P.b.base1, T.z, P.Hz);
+        L.ak = op_off(P.a.hi2, P.a.lo2, P.a.base2, T.z, P.Hz);
+        L.bk = op_off(P.b.hi1, P.b.lo1, P.b.base1, T.z, P.Hz);
         const int64_t bn = T.n0 + 128 * (int64_t)rank + op_off(P.b.hi2, P.b.lo2, P.b.base2, T.z, P.Hz);
-        int64_t a_br = 0, b_br = 0;
-        int a_c1 = 0, b_c1 = 0;
-        int64_t a_bc[2], b_bc[2];
-        int a_c0[2], b_c0[2];
         if (!a_mn) {
-          a_br = am / P.a.g.bh;
-          a_c1 = (int)(am - a_br * P.a.g.bh);
+          L.a_br = (int32_t)udiv32(am, P.a.g.bh);
+          L.a_c1 = (int32_t)(am - (int64_t)L.a_br * P.a.g.bh);
         } else {
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            a_bc[h] = (am + 64 * h) / P.a.g.bw;
-            a_c0[h] = (int)(am + 64 * h - a_bc[h] * P.a.g.bw);
+            L.a_bc[h] = (int32_t)udiv32(am + 64 * h, P.a.g.bw);
+            L.a_c0[h] = (int32_t)(am + 64 * h - (int64_t)L.a_bc[h] * P.a.g.bw);
           }
         }
         if (!b_mn) {
-          b_br = bn / P.b.g.bh;
-          b_c1 = (int)(bn - b_br * P.b.g.bh);
+          L.b_br = (int32_t)udiv32(bn, P.b.g.bh);
+          L.b_c1 = (int32_t)(bn - (int64_t)L.b_br * P.b.g.bh);
         } else {
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            b_bc[h] = (bn + 64 * h) / P.b.g.bw;
-            b_c0[h] = (int)(bn + 64 * h - b_bc[h] * P.b.g.bw);
+            L.b_bc[h] = (int32_t)udiv32(bn + 64 * h, P.b.g.bw);
+            L.b_c0[h] = (int32_t)(bn + 64 * h - (int64_t)L.b_bc[h] * P.b.g.bw);
           }
         }
+      };
+      uint32_t it = 0;
+      bool ok = true;
+      TileLd cur = {}, nxt = {};
+      if (cid < ntiles) setup(cid, cur);
+      for (int64_t t = cid; t < ntiles && ok; t += nclusters) {
+        const int64_t ak = cur.ak, bk = cur.bk;
+        const int64_t a_br = cur.a_br, b_br = cur.b_br;
+        const int a_c1 = cur.a_c1, b_c1 = cur.b_c1;
+        const int64_t a_bc[2] = {cur.a_bc[0], cur.a_bc[1]}, b_bc[2] = {cur.b_bc[0], cur.b_bc[1]};
+        const int a_c0[2] = {cur.a_c0[0], cur.a_c0[1]}, b_c0[2] = {cur.b_c0[0], cur.b_c0[1]};
+        bool next_ready = false;
         for (int32_t sg = 0; sg < nsegK && ok; ++sg) {
           const int64_t ks = (int64_t)sg * segK;
           int a_k = 0, b_k = 0, a_sh = 0, b_sh = 0;
           int a_shh[2], b_shh[2];
           if (!a_mn) {
-            const int64_t bc = (ak + ks) / P.a.g.bw;
+            const int64_t bc = udiv32(ak + ks, P.a.g.bw);
             a_k = (int)(ak + ks - bc * P.a.g.bw);
             a_sh = shard_or_oob(P.a.g, a_br, bc);
           } else {
-            const int64_t br = (ak + ks) / P.a.g.bh;
+            const int64_t br = udiv32(ak + ks, P.a.g.bh);
             a_k = (int)(ak + ks - br * P.a.g.bh);
 #pragma unroll
             for (int h = 0; h < 2; ++h) a_shh[h] = shard_or_oob(P.a.g, br, a_bc[h]);
           }
           if (!b_mn) {
-            const int64_t bc = (bk + ks) / P.b.g.bw;
+            const int64_t bc = udiv32(bk + ks, P.b.g.bw);
             b_k = (int)(bk + ks - bc * P.b.g.bw);
             b_sh = shard_or_oob(P.b.g, b_br, bc);
           } else {
-            const int64_t br = (bk + ks) / P.b.g.bh;
+            const int64_t br = udiv32(bk + ks, P.b.g.bh);
             b_k = (int)(bk + ks - br * P.b.g.bh);
 #pragma unroll
             for (int h = 0; h < 2; ++h) b_shh[h] = shard_or_oob(P.b.g, br, b_bc[h]);
@@ -857,8 +877,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_3d_pair(b_stage(s) + h * Cfg::MNBOX, &mapB, fb, b_c0[h], b_k + kofs, b_shh[h]);
             }
             ++it;
+            if (!next_ready) {  // the first stage is in flight: prepare the next tile
+              next_ready = true;
+              if (t + nclusters < ntiles) setup(t + nclusters, nxt);
+            }
           }
         }
+        cur = nxt;
       }
       if (!ok && leader) {
         // drain: every load of both CTAs completes on the even CTA's full barriers
@@ -1088,6 +1113,11 @@ tp3d_status launch_pair(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t 
   if (ntiles <= 0) return TP3D_OK;
   const int max_clusters = pair_clusters<KD>(ctx);
   if (max_clusters < 1) return TP3D_ECUDA;
+  // the kernel decodes tiles and shard coordinates in 32-bit arithmetic
+  const int64_t lim = INT32_MAX;
+  if (P.M > lim || P.N > lim || P.K > lim || ntiles > lim || P.a.g.R > lim || P.a.g.C > lim || P.b.g.R > lim ||
+      P.b.g.C > lim || P.c.g.R > lim || P.c.g.C > lim)
+    return TP3D_EUNSUPPORTED;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
