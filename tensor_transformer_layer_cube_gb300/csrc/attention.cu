@@ -71,7 +71,8 @@ __device__ __forceinline__ Ctx setup_smem(uint8_t* smem_raw) {
 // grid g (the window lies inside one shard): d / 64 boxes of 64 columns.
 __device__ __forceinline__ void load_tile(const CUtensorMap* m, const Grid& g, int64_t row0, int64_t col0, int nch,
                                           uint32_t dst, uint32_t bar) {
-  const int64_t br = row0 / g.bh, bc = col0 / g.bw;
+  // 32-bit division (the launchers check the extents): this runs for every tile loaded
+  const int64_t br = (uint32_t)row0 / (uint32_t)g.bh, bc = (uint32_t)col0 / (uint32_t)g.bw;
   const int sh = g.shard((int32_t)br, (int32_t)bc);
   const int c1 = (int)(row0 - br * g.bh), c0 = (int)(col0 - bc * g.bw);
   for (int c = 0; c < nch; ++c) tma_load_3d(dst + c * kChunk, m, bar, c0 + 64 * c, c1, sh);
@@ -856,6 +857,7 @@ tp3d_status tile_map(CUtensorMap* m, const Grid& g, const void* ptr) {
 
 tp3d_status check(const AttnProblem& A) {
   if (A.d != 64 && A.d != 128) return TP3D_EUNSUPPORTED;
+  if (A.qkv.R > INT32_MAX || A.qkv.C > INT32_MAX || A.o.R > INT32_MAX || A.o.C > INT32_MAX) return TP3D_EUNSUPPORTED;
   if (A.s % TR || A.qkv.bh % TR || A.o.bh % TR || A.qkv.bw % A.d || A.o.bw % A.d) return TP3D_EUNSUPPORTED;
   if (A.Z * (A.s / TR) > 0x7fffffff) return TP3D_EUNSUPPORTED;
   return TP3D_OK;

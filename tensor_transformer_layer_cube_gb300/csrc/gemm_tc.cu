@@ -198,12 +198,13 @@ __device__ __forceinline__ void epilogue_tile(const GemmProblem& P, const TileIn
   const bool rows_full = T.m0 + quarter * 32 + 31 < T.m_end;
   const int64_t gm = m + op_off(P.c.hi1, P.c.lo1, P.c.base1, T.z, P.Hz);
   const int64_t gn0 = T.n0 + op_off(P.c.hi2, P.c.lo2, P.c.base2, T.z, P.Hz);
-  const int64_t cbr = (gm - lane) / cg.bh, cbc = gn0 / cg.bw;  // C block of the warp's rows
+  // 32-bit divisions (every launcher checks the extents)
+  const int64_t cbr = (uint32_t)(gm - lane) / (uint32_t)cg.bh, cbc = (uint32_t)gn0 / (uint32_t)cg.bw;  // C block of the warp's rows
   const int c1 = (int)(gm - lane - cbr * cg.bh);
   const int c2 = cg.shard((int32_t)cbr, (int32_t)cbc);
   int64_t row_base = 0;
   if (row_ok) {
-    const int64_t br = gm / cg.bh;
+    const int64_t br = (uint32_t)gm / (uint32_t)cg.bh;
     row_base = cg.block_base((int32_t)br, (int32_t)cbc) + (gm - br * cg.bh) * cg.bw + (gn0 - cbc * cg.bw);
   }
   auto chunk_n = [&](int cc) { return T.n0 + (half * CH + cc) * 32; };
@@ -1146,6 +1147,10 @@ tp3d_status gemm_bf16_tc(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t
   for (const Grid* g : gs)
     if (g->bw % 8 != 0) return TP3D_EALIGN;
   if (P.segM % 8 || P.segN % 8) return TP3D_EUNSUPPORTED;
+  // tile decode and the epilogue's block arithmetic run in 32 bits
+  for (const Grid* g : gs)
+    if (g->R > INT32_MAX || g->C > INT32_MAX) return TP3D_EUNSUPPORTED;
+  if (P.M > INT32_MAX || P.N > INT32_MAX || P.K > INT32_MAX) return TP3D_EUNSUPPORTED;
   // a ragged contraction tile is exact only if one operand's block ends at the segment end
   if (P.segK % BK != 0) {
     const int64_t ka = P.a.mn_major ? P.a.g.bh : P.a.g.bw;
