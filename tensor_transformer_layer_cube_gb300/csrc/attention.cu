@@ -549,8 +549,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
             for (int e2 = 0; e2 < 16; ++e2) {
               const int k = (2 * half + i) * 32 + 2 * e2;
-              const float f0 = (!diag || k <= r) ? exp2f(__uint_as_float(v[i][2 * e2]) * sl2 - l2) : 0.0f;
-              const float f1 = (!diag || k + 1 <= r) ? exp2f(__uint_as_float(v[i][2 * e2 + 1]) * sl2 - l2) : 0.0f;
+              const float f0 = (!diag || k <= r) ? ex2_approx(fmaf(__uint_as_float(v[i][2 * e2]), sl2, -l2)) : 0.0f;
+              const float f1 = (!diag || k + 1 <= r) ? ex2_approx(fmaf(__uint_as_float(v[i][2 * e2 + 1]), sl2, -l2)) : 0.0f;
               const __nv_bfloat162 h2 = __floats2bfloat162_rn(f0, f1);
               pk[i][e2] = *reinterpret_cast<const uint32_t*>(&h2);
             }
@@ -746,7 +746,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               const int k = cc * 32 + g * 8 + e;
-              const float p = (!diag || k <= r) ? exp2f(__uint_as_float(v[g * 8 + e]) * sl2 - l2) : 0.0f;
+              const float p = (!diag || k <= r) ? ex2_approx(fmaf(__uint_as_float(v[g * 8 + e]), sl2, -l2)) : 0.0f;
               f[e] = p * (__uint_as_float(wv[g * 8 + e]) - dr) * A.scale;
             }
             st_tile8(pdS, r, cc * 4 + g, pack8f(f));
