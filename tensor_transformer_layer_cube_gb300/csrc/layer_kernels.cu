@@ -9,6 +9,8 @@
 // warp that reads its q pieces, so the statistics are those of the whole
 // row.  All of these kernels are HBM-bound: 16-byte vector accesses, fp32
 // arithmetic, one pass over the data where possible.
+#include <cudaTypedefs.h>
+
 #include "layer_kernels.cuh"
 
 namespace tp3d {
@@ -350,6 +352,270 @@ __global__ void __launch_bounds__(kThreads) colsum_kernel(const Grid g, const bf
   if (threadIdx.x == 0) counters[blockIdx.x] = 0;
 }
 
+// ---------------------------------------------------- column sums fed by TMA
+// The same sums as colsum_kernel, with the rows streamed through shared
+// memory: warp 8 issues 256-column x 32-row TMA boxes into a ring of kSkStages
+// stages (the data in flight takes no registers, so a CTA keeps up to
+// kSkStages x 16 KiB per input moving), warps 0-7 read rows w, w + 8, w + 16,
+// w + 24 of each box, lane l columns 8l..8l+7.  Then the partial rows and the
+// last-CTA reduction of colsum_kernel.
+constexpr int kSkStages = 6;               // boxes in flight (LN: 3, two inputs per box)
+constexpr int kBoxRows = 32;
+constexpr uint32_t kBoxBytes = kBoxRows * 256 * 2;
+constexpr int kSkThreads = 288;
+
+template <bool LN>
+TP3D_HD constexpr int sk_stages() { return LN ? kSkStages / 2 : kSkStages; }
+template <bool LN>
+TP3D_HD constexpr int sk_smem() { return sk_stages<LN>() * (LN ? 2 : 1) * (int)kBoxBytes + kWarps * 257 * 4 + 256 + 128; }
+
+template <bool LN>
+__global__ void __launch_bounds__(kSkThreads) colsum_tma_kernel(const __grid_constant__ CUtensorMap mx,
+                                                                const __grid_constant__ CUtensorMap mdy, const Grid g,
+                                                                const float* __restrict__ mean,
+                                                                const float* __restrict__ rstd,
+                                                                float* __restrict__ part, float* __restrict__ part2,
+                                                                int64_t rows_per_part, int* __restrict__ counters,
+                                                                bf16* __restrict__ out, bf16* __restrict__ out2,
+                                                                int* err) {
+  constexpr int NS = sk_stages<LN>();
+  constexpr uint32_t STAGE = (LN ? 2u : 1u) * kBoxBytes;
+  extern __shared__ __align__(128) uint8_t sk_smem_raw[];
+  uint8_t* ring = sk_smem_raw;
+  float(*red)[257] = reinterpret_cast<float(*)[257]>(ring + NS * STAGE);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ring + NS * STAGE + kWarps * 257 * 4);
+  int* is_last = reinterpret_cast<int*>(bars + 2 * NS);
+  volatile int* abort_flag = is_last + 1;
+  const uint32_t bar0 = smem_u32(bars);
+  auto full = [&](int st) { return bar0 + 8u * st; };
+  auto empty = [&](int st) { return bar0 + 8u * (NS + st); };
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t c0 = (int64_t)blockIdx.x * 256;
+  const int64_t r0 = (int64_t)blockIdx.y * rows_per_part;
+  const int nb = (int)(rows_per_part / kBoxRows);
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < NS; ++st) {
+      mbar_init(full(st), 1);
+      mbar_init(empty(st), kWarps);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0}, acc2[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  bool ok = true;
+  if (w == kWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const int32_t br = (int32_t)((uint32_t)r0 / (uint32_t)g.bh), bc = (int32_t)((uint32_t)c0 / (uint32_t)g.bw);
+      const int sh = g.shard(br, bc);
+      const int cin = (int)(c0 - (int64_t)bc * g.bw), rin0 = (int)(r0 - (int64_t)br * g.bh);
+      int b = 0;
+      for (; b < nb && ok; ++b) {
+        const int st = b % NS;
+        if (!(ok = mbar_wait(empty(st), ((b / NS) & 1) ^ 1, abort_flag, err))) break;
+        mbar_arrive_expect_tx(full(st), STAGE);
+        tma_load_3d(smem_u32(ring + st * STAGE), &mx, full(st), cin, rin0 + b * kBoxRows, sh);
+        if (LN) tma_load_3d(smem_u32(ring + st * STAGE + kBoxBytes), &mdy, full(st), cin, rin0 + b * kBoxRows, sh);
+      }
+      if (!ok) {  // every issued box lands before the CTA may leave
+        for (int j = b - NS > 0 ? b - NS : 0; j < b; ++j) {
+          const unsigned long long t0 = globaltimer_ns();
+          while (!mbar_try_wait(full(j % NS), (j / NS) & 1))
+            if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ consumers
+    for (int b = 0; b < nb && ok; ++b) {
+      const int st = b % NS;
+      float mu[4], rs[4];
+      if (LN) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int64_t r = r0 + (int64_t)b * kBoxRows + w + 8 * k;
+          mu[k] = __ldg(mean + r);
+          rs[k] = __ldg(rstd + r);
+        }
+      }
+      bool got = lane == 0 ? mbar_wait(full(st), (b / NS) & 1, abort_flag, err) : false;
+      got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+      if (!(ok = got)) break;
+      const uint8_t* box = ring + st * STAGE;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int row = w + 8 * k;
+        float f[8];
+        unpack8(*reinterpret_cast<const uint4*>(box + row * 512 + lane * 16), f);
+        if (!LN) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[e] += f[e];
+        } else {
+          float d[8];
+          unpack8(*reinterpret_cast<const uint4*>(box + kBoxBytes + row * 512 + lane * 16), d);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            acc[e] += d[e] * (f[e] - mu[k]) * rs[k];
+            acc2[e] += d[e];
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty(st));
+    }
+  }
+  // every role reaches here: an aborted CTA leaves without writing
+  ok = __syncthreads_and(ok ? 1 : 0) != 0;
+  if (!ok) return;
+  const int tid = threadIdx.x;
+  if (w < kWarps) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) red[w][lane * 8 + e] = acc[e];
+  }
+  __syncthreads();
+  if (tid < 256) {
+    float sum = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kWarps; ++k) sum += red[k][tid];
+    part[(int64_t)blockIdx.y * g.C + c0 + tid] = sum;
+  }
+  if (LN) {
+    __syncthreads();
+    if (w < kWarps) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) red[w][lane * 8 + e] = acc2[e];
+    }
+    __syncthreads();
+    if (tid < 256) {
+      float sum = 0.0f;
+#pragma unroll
+      for (int k = 0; k < kWarps; ++k) sum += red[k][tid];
+      part2[(int64_t)blockIdx.y * g.C + c0 + tid] = sum;
+    }
+  }
+  // the last part of this strip to finish reduces all of them (as colsum_kernel)
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    *is_last = atomicAdd(&counters[blockIdx.x], 1) == (int)gridDim.y - 1;
+  }
+  __syncthreads();
+  if (!*is_last) return;
+  __threadfence();
+  for (int which = 0; which < (LN ? 2 : 1); ++which) {
+    const float* src = which == 0 ? part : part2;
+    float t[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (w < kWarps) {
+      const int64_t np = gridDim.y, c = c0 + lane * 8;
+      for (int64_t p0 = w; p0 < np; p0 += (int64_t)kWarps * 4) {
+        float4 v[4][2];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int64_t pp = p0 + (int64_t)u * kWarps;
+          if (pp < np) {
+            v[u][0] = __ldcg(reinterpret_cast<const float4*>(src + pp * g.C + c));
+            v[u][1] = __ldcg(reinterpret_cast<const float4*>(src + pp * g.C + c + 4));
+          } else {
+            v[u][0] = v[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          t[0] += v[u][0].x;
+          t[1] += v[u][0].y;
+          t[2] += v[u][0].z;
+          t[3] += v[u][0].w;
+          t[4] += v[u][1].x;
+          t[5] += v[u][1].y;
+          t[6] += v[u][1].z;
+          t[7] += v[u][1].w;
+        }
+      }
+    }
+    __syncthreads();
+    if (w < kWarps) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) red[w][lane * 8 + e] = t[e];
+    }
+    __syncthreads();
+    if (tid < 256) {
+      float u = 0.0f;
+#pragma unroll
+      for (int k = 0; k < kWarps; ++k) u += red[k][tid];
+      (which == 0 ? out : out2)[c0 + tid] = __float2bfloat16_rn(u);
+    }
+  }
+  if (tid == 0) counters[blockIdx.x] = 0;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 sk_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// (column in shard, row in shard, shard) map with 256 x 32 boxes, unswizzled
+bool sk_map(CUtensorMap* m, const Grid& g, const void* ptr) {
+  auto fn = sk_encode();
+  if (!fn || !aligned16(ptr)) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)g.bw, (cuuint64_t)g.bh, (cuuint64_t)g.nshards()};
+  cuuint64_t strides[2] = {(cuuint64_t)g.bw * 2, (cuuint64_t)(g.bh * g.bw * 2)};
+  cuuint32_t box[3] = {256, (cuuint32_t)kBoxRows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The TMA-fed column sums, when every 256-column strip lies in one shard
+// column and the parts divide the row blocks; false = use colsum_kernel.
+template <bool LN>
+bool launch_colsum_tma(const tp3d_ctx* ctx, const Grid& g, const void* x, const void* dy, const float* mean,
+                       const float* rstd, float* part, float* part2, int* counters, void* out, void* out2,
+                       cudaStream_t s, tp3d_status* st) {
+  if (g.C % 256 || g.bw % 256 || g.bh % kBoxRows || g.R > INT32_MAX || g.C > INT32_MAX) return false;
+  static int per_sm[64] = {};
+  const int dev = ctx->device & 63;
+  if (per_sm[dev] == 0) {
+    int n = 0;
+    if (cudaFuncSetAttribute(colsum_tma_kernel<LN>, cudaFuncAttributeMaxDynamicSharedMemorySize, sk_smem<LN>()) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, colsum_tma_kernel<LN>, kSkThreads, sk_smem<LN>()) !=
+            cudaSuccess ||
+        n < 1) {
+      (void)cudaGetLastError();
+      n = -1;
+    }
+    per_sm[dev] = n;
+  }
+  if (per_sm[dev] < 1) return false;
+  const int64_t strips = g.C / 256, slots = (int64_t)per_sm[dev] * ctx->num_sms;
+  // rows per part: the smallest power of two from 64 with one resident round
+  int64_t rpp = 64;
+  while (rpp < g.bh && strips * ((g.R + rpp - 1) / rpp) > slots) rpp *= 2;
+  if (g.bh % rpp || g.R % rpp || g.R / rpp > 65535) return false;
+  CUtensorMap mx, mdy;
+  if (!sk_map(&mx, g, x)) return false;
+  if (LN) {
+    if (!sk_map(&mdy, g, dy)) return false;
+  } else {
+    mdy = mx;
+  }
+  const dim3 grid((unsigned)strips, (unsigned)(g.R / rpp));
+  colsum_tma_kernel<LN><<<grid, kSkThreads, sk_smem<LN>(), s>>>(mx, mdy, g, mean, rstd, part, part2, rpp, counters,
+                                                                static_cast<bf16*>(out), static_cast<bf16*>(out2),
+                                                                ctx->d_err);
+  *st = cudaGetLastError() == cudaSuccess ? TP3D_OK : TP3D_ECUDA;
+  return true;
+}
+
 unsigned grid_for_rows(const tp3d_ctx* ctx, int64_t rows, int per_sm) {
   int64_t g = (rows + kWarps - 1) / kWarps;
   const int64_t cap = (int64_t)ctx->num_sms * per_sm;
@@ -411,6 +677,9 @@ int64_t colsum_rows(const tp3d_ctx* ctx, const Grid& g) {
 
 tp3d_status launch_colsum(const tp3d_ctx* ctx, const Grid& g, const void* x, float* part, int* counters, void* out,
                           cudaStream_t s) {
+  tp3d_status st;
+  if (launch_colsum_tma<false>(ctx, g, x, nullptr, nullptr, nullptr, part, nullptr, counters, out, nullptr, s, &st))
+    return st;
   const int64_t rpp = colsum_rows<false>(ctx, g);
   const dim3 grid((unsigned)colsum_strips(g), (unsigned)(g.R / rpp));
   if (grid.y > 65535u) return TP3D_EUNSUPPORTED;
@@ -422,6 +691,12 @@ tp3d_status launch_colsum(const tp3d_ctx* ctx, const Grid& g, const void* x, flo
 tp3d_status launch_ln_param_grads(const tp3d_ctx* ctx, const Grid& g, const void* dy, const void* x,
                                   const float* mean, const float* rstd, float* part, int* counters, void* out_g,
                                   void* out_b, cudaStream_t s) {
+  {
+    const int64_t np = g.R / gcd64(g.bh, 64);  // parts the scratch is sized for
+    tp3d_status st;
+    if (launch_colsum_tma<true>(ctx, g, x, dy, mean, rstd, part, part + np * g.C, counters, out_g, out_b, s, &st))
+      return st;
+  }
   const int64_t rpp = colsum_rows<true>(ctx, g);
   const dim3 grid((unsigned)colsum_strips(g), (unsigned)(g.R / rpp));
   if (grid.y > 65535u) return TP3D_EUNSUPPORTED;
