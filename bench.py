@@ -67,6 +67,8 @@ def parse():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU baseline sample budget")
     ap.add_argument("--no-extras", action="store_true", help="skip the other workloads and the CPU baseline")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time direct C-ABI calls instead of replaying a CUDA graph of the step")
     ap.add_argument("--probe-only", action="store_true",
                     help="only launch the dominant kernel three times (for profiler captures)")
     return ap.parse_args()
@@ -338,6 +340,23 @@ def time_steps(torch, fn, steps, warmup, flush, stream):
     return [a.elapsed_time(b) for a, b in evs]
 
 
+def capture(torch, fn, stream):
+    """A CUDA graph of one call of fn (C-ABI launches on the current stream),
+    for the timed loop to replay: the same kernels on the same buffers, without
+    the host's per-launch work between them."""
+    s = torch.cuda.Stream()
+    s.wait_stream(stream)
+    with torch.cuda.stream(s):
+        fn()
+    stream.wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
 def cpu_baseline_mlp(w, seconds):
     """The oracle (plain numpy fp64) on a bounded sample: the MLP is
     row-separable, so the sample is a block of rows run repeatedly."""
@@ -593,7 +612,15 @@ def run_ours(args, rank, world, dist):
         dist.barrier()
     torch.cuda.synchronize()
     t0 = time.time()
-    durs = time_steps(torch, wb.step, args.steps, args.warmup, flush, stream)
+    use_graph = not args.no_graph and w["kind"] in ("layer", "mlp", "linear_f32")
+    step_fn = wb.step
+    if use_graph:
+        for _ in range(args.warmup):  # one-time host work (attributes, occupancy) before the capture
+            wb.step()
+        torch.cuda.synchronize()
+        graph = capture(torch, wb.step, stream)
+        step_fn = graph.replay
+    durs = time_steps(torch, step_fn, args.steps, args.warmup, flush, stream)
     torch.cuda.synchronize()
     t1 = time.time()
     if world > 1:
@@ -616,13 +643,18 @@ def run_ours(args, rank, world, dist):
         "vs_baseline": None, "dtype": "bf16" if w["kind"] != "linear_f32" else "f32",
         "data": "synthetic (seeded device RNG; N(0,1) inputs, N(0,0.02) weights)",
         "config": {"workload": w["name"], "l2": "flushed between timed steps (256 MiB write outside the events)",
+                   "launch": "one CUDA graph per step (the step's C-ABI calls captured once, replayed)" if use_graph
+                   else "direct C-ABI calls",
                    "parallelism": "replicas (no data-path collective)" if world > 1
                    else "single GPU, q^3 virtual devices in HBM"},
         "gpu_launches": wb.launches * args.steps,
     }
     if w["kind"] == "layer":
-        fd = time_steps(torch, wb.fwd, max(5, args.steps // 2), 2, flush, stream)
-        bd = time_steps(torch, wb.bwd, max(5, args.steps // 2), 2, flush, stream)
+        ffn, bfn = wb.fwd, wb.bwd
+        if use_graph:
+            ffn, bfn = capture(torch, wb.fwd, stream).replay, capture(torch, wb.bwd, stream).replay
+        fd = time_steps(torch, ffn, max(5, args.steps // 2), 2, flush, stream)
+        bd = time_steps(torch, bfn, max(5, args.steps // 2), 2, flush, stream)
         fwd_ms, bwd_ms = statistics.mean(fd), statistics.mean(bd)
         line["layer"] = {"fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
                          "avg_step_time_ms_per_sequence": (fwd_ms + bwd_ms) / w["batch"],
