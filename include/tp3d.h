@@ -21,9 +21,14 @@
  *
  * Ownership.  The caller allocates every tensor and workspace (PyTorch in the
  * bundled binding).  The library allocates only its context: one device
- * error word and host-side caches.  All compute calls are asynchronous on
- * the given CUDA stream (a cudaStream_t passed as void*; NULL = the legacy
- * default stream).  Inputs are read-only; outputs must not alias inputs.
+ * error word, two side streams with three events, and host-side caches.  All
+ * compute calls are asynchronous on the given CUDA stream (a cudaStream_t
+ * passed as void*; NULL = the legacy default stream).  A call that runs
+ * independent launches on the context's side streams (tp3d_layer_bwd) forks
+ * them from the given stream and joins them back into it before returning,
+ * so its work is ordered on the given stream as a whole; calls of one context
+ * must not run concurrently on different streams.  Inputs are read-only;
+ * outputs must not alias inputs.
  *
  * Errors.  Arguments are validated on the host before anything is launched;
  * a failed check returns its status and launches nothing.  There are no

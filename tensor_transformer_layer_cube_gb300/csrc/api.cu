@@ -102,6 +102,16 @@ tp3d_status tp3d_create(int device, tp3d_ctx** out) {
     free(c);
     return TP3D_ECUDA;
   }
+  bool ok = true;
+  for (int k = 0; k < 2; ++k) {
+    ok = ok && cudaStreamCreateWithFlags(&c->side[k], cudaStreamNonBlocking) == cudaSuccess;
+    ok = ok && cudaEventCreateWithFlags(&c->ev_join[k], cudaEventDisableTiming) == cudaSuccess;
+  }
+  ok = ok && cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming) == cudaSuccess;
+  if (!ok) {
+    tp3d_destroy(c);
+    return TP3D_ECUDA;
+  }
   *out = c;
   return TP3D_OK;
 }
@@ -109,6 +119,11 @@ tp3d_status tp3d_create(int device, tp3d_ctx** out) {
 void tp3d_destroy(tp3d_ctx* ctx) {
   if (!ctx) return;
   if (ctx->d_err) cudaFree(ctx->d_err);
+  for (int k = 0; k < 2; ++k) {
+    if (ctx->side[k]) cudaStreamDestroy(ctx->side[k]);
+    if (ctx->ev_join[k]) cudaEventDestroy(ctx->ev_join[k]);
+  }
+  if (ctx->ev_fork) cudaEventDestroy(ctx->ev_fork);
   free(ctx);
 }
 

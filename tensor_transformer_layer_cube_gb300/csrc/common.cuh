@@ -13,6 +13,11 @@ struct tp3d_ctx {
   int device;
   int num_sms;
   int* d_err;  // device error word: 0, or the first TP3D_* code a kernel raised
+  // two side streams and their events, for independent launches of one call
+  // that run beside the caller's stream (forked from it and joined back into
+  // it before the call returns)
+  cudaStream_t side[2];
+  cudaEvent_t ev_fork, ev_join[2];
 };
 
 namespace tp3d {

@@ -18,6 +18,8 @@
 // place from the CUBE_C shards of the QKV matrix (attention.cu).
 #include <math.h>
 
+#include <algorithm>
+
 #include "attention.cuh"
 #include "gemm.cuh"
 #include "layer_kernels.cuh"
@@ -44,6 +46,7 @@ struct Plan {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 constexpr int64_t kCounters = 1024;  // column-sum arrival counters in the workspace
+constexpr int64_t kStripSlot = 256;  // counters of one of up to four concurrent column sums
 
 tp3d_status make_plan(const tp3d_layer_cfg* c, Plan* p) {
   if (!c) return TP3D_EINVAL;
@@ -95,15 +98,19 @@ tp3d_status make_plan(const tp3d_layer_cfg* c, Plan* p) {
   x.dH = take(M * h * 2);
   x.dO = take(M * h * 2);
   x.dqkv = take(M * 3 * h * 2);
-  // column-sum partials: the largest of the bias sums and the two LayerNorm sums
-  Grid gc;
+  // column-sum partials, for the sums that run at the same time: db1 alone;
+  // the LN2 gamma/beta sums with dbo and db2; the LN1 gamma/beta sums with dbqkv
+  Grid gc, ga, gq;
   TP3D_TRY(make_grid(cube(TP3D_CUBE_C, x.q), M, f, &gc));
-  const int64_t pc = colsum_parts(gc) * (f > 3 * h ? f : 3 * h);
-  const int64_t pl = colsum_parts(gc) * 2 * h;
-  x.part_floats = (size_t)(pc > pl ? pc : pl);
+  TP3D_TRY(make_grid(cube(TP3D_CUBE_A, x.q), M, h, &ga));
+  TP3D_TRY(make_grid(cube(TP3D_CUBE_C, x.q), M, 3 * h, &gq));
+  const int64_t p1 = colsum_parts(gc) * f;
+  const int64_t p2 = 4 * colsum_parts(ga) * h;
+  const int64_t p3 = 2 * colsum_parts(ga) * h + colsum_parts(gq) * 3 * h;
+  x.part_floats = (size_t)std::max(p1, std::max(p2, p3));
   x.part = take(x.part_floats * 4);
-  // one arrival counter per 256-column strip of the widest column sum
-  if ((f > 3 * h ? f : 3 * h) / 256 + 1 > kCounters) return TP3D_EUNSUPPORTED;
+  // arrival counters: one per 256-column strip, kStripSlot apart for the sums that run together
+  if ((f > 3 * h ? f : 3 * h) / 256 + 1 > kStripSlot) return TP3D_EUNSUPPORTED;
   x.counters = take(kCounters * 4);
   x.total = o;
   *p = x;
@@ -275,8 +282,25 @@ tp3d_status tp3d_layer_bwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_
   Grid gA;
   TP3D_TRY(make_grid(cube(TP3D_CUBE_A, q), M, h, &gA));
 
+  // Column sums that nothing later reads run beside the main stream, two or
+  // three at once (each with its own partials and counters): their launch and
+  // reduction tails overlap.  The main stream waits for them before its next
+  // launch that could overwrite what they read, and before returning.
+  auto fork = [&](int n) -> tp3d_status {
+    TP3D_CUDA_TRY(cudaEventRecord(ctx->ev_fork, st));
+    for (int k = 0; k < n; ++k) TP3D_CUDA_TRY(cudaStreamWaitEvent(ctx->side[k], ctx->ev_fork, 0));
+    return TP3D_OK;
+  };
+  auto join = [&](int n) -> tp3d_status {
+    for (int k = 0; k < n; ++k) {
+      TP3D_CUDA_TRY(cudaEventRecord(ctx->ev_join[k], ctx->side[k]));
+      TP3D_CUDA_TRY(cudaStreamWaitEvent(st, ctx->ev_join[k], 0));
+    }
+    return TP3D_OK;
+  };
+  const int64_t pa = colsum_parts(gA) * h;  // floats of one M x h partial set
+
   // ---- MLP block
-  TP3D_TRY(colsum(ctx, TP3D_CUBE_A, q, M, h, dY, part, counters, g->b_2, st));            // db2
   TP3D_TRY(plan_wgrad(ctx, q, 1, M, f, h, W(p.y1), dY, g->w_2, &G));                       // dW2 = Y1^T dY
   TP3D_TRY(run(ctx, G, st));
   TP3D_TRY(plan_dgrad(ctx, q, 1, M, f, h, dY, w->w_2, W(p.dz1), &G));                      // dZ1 = (dY W2^T) GELU'(Z1)
@@ -290,11 +314,17 @@ tp3d_status tp3d_layer_bwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_
   TP3D_TRY(run(ctx, G, st));
   TP3D_TRY(launch_ln_bwd(ctx, gA, W(p.dxn), W(p.Hres), (const float*)W(p.mean2), (const float*)W(p.rstd2),
                          w->ln2_g, dY, W(p.dH), st));                                                  // dH
+  // dgamma2, dbeta2 | dbo | db2 at once (dLN2 in dxn is overwritten later: joined before then)
+  TP3D_TRY(fork(2));
   TP3D_TRY(launch_ln_param_grads(ctx, gA, W(p.dxn), W(p.Hres), (const float*)W(p.mean2), (const float*)W(p.rstd2),
                                  part, counters, g->ln2_g, g->ln2_b, st));
+  TP3D_TRY(colsum(ctx, TP3D_CUBE_A, q, M, h, W(p.dH), part + 2 * pa, counters + kStripSlot, g->b_o,
+                  ctx->side[0]));                                                                        // dbo
+  TP3D_TRY(colsum(ctx, TP3D_CUBE_A, q, M, h, dY, part + 3 * pa, counters + 2 * kStripSlot, g->b_2,
+                  ctx->side[1]));                                                                        // db2
+  TP3D_TRY(join(2));
 
   // ---- attention block
-  TP3D_TRY(colsum(ctx, TP3D_CUBE_A, q, M, h, W(p.dH), part, counters, g->b_o, st));       // dbo
   TP3D_TRY(plan_wgrad(ctx, q, 1, M, h, h, W(p.O), W(p.dH), g->w_o, &G));                   // dWo = O^T dH
   TP3D_TRY(run(ctx, G, st));
   TP3D_TRY(plan_dgrad(ctx, q, 1, M, h, h, W(p.dH), w->w_o, W(p.dO), &G));                  // dO = dH Wo^T
@@ -302,15 +332,19 @@ tp3d_status tp3d_layer_bwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_
   // attention backward, fused: dQ, dK, dV into dQKV (MP3D's C = A B^T and C = A^T B forms)
   TP3D_TRY(launch_attn_bwd(ctx, attn_problem(p, ctx->d_err), W(p.qkv), W(p.O), W(p.dO), (const float*)W(p.lse),
                            (float*)W(p.delta), W(p.dqkv), st));
-  TP3D_TRY(colsum(ctx, TP3D_CUBE_C, q, M, 3 * h, W(p.dqkv), part, counters, g->b_qkv, st));  // dbqkv
   TP3D_TRY(plan_wgrad(ctx, q, 0, M, h, 3 * h, W(p.xn1), W(p.dqkv), g->w_qkv, &G));         // dWqkv = LN1(X)^T dQKV
   TP3D_TRY(run(ctx, G, st));
   TP3D_TRY(plan_dgrad(ctx, q, 0, M, h, 3 * h, W(p.dqkv), w->w_qkv, W(p.dxn), &G));         // dLN1 = dQKV Wqkv^T
   TP3D_TRY(run(ctx, G, st));
   TP3D_TRY(launch_ln_bwd(ctx, gA, W(p.dxn), X, (const float*)W(p.mean1), (const float*)W(p.rstd1), w->ln1_g,
                          W(p.dH), dX, st));                                                            // dX
-  return launch_ln_param_grads(ctx, gA, W(p.dxn), X, (const float*)W(p.mean1), (const float*)W(p.rstd1), part,
-                               counters, g->ln1_g, g->ln1_b, st);
+  // dgamma1, dbeta1 | dbqkv at once, joined before returning
+  TP3D_TRY(fork(1));
+  TP3D_TRY(launch_ln_param_grads(ctx, gA, W(p.dxn), X, (const float*)W(p.mean1), (const float*)W(p.rstd1), part,
+                                 counters, g->ln1_g, g->ln1_b, st));
+  TP3D_TRY(colsum(ctx, TP3D_CUBE_C, q, M, 3 * h, W(p.dqkv), part + 2 * pa, counters + kStripSlot, g->b_qkv,
+                  ctx->side[0]));                                                                        // dbqkv
+  return join(1);
 }
 
 }  // extern "C"
