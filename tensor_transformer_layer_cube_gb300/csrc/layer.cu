@@ -40,7 +40,7 @@ struct Plan {
   // workspace offsets (bytes)
   size_t xn1, mean1, rstd1, qkv, lse, O, Hres, xn2, mean2, rstd2, z1, y1;  // saved by the forward
   size_t delta, dz1, dxn, dH, dO, dqkv, part, counters;                    // scratch
-  size_t part_floats, total;
+  size_t part_floats, part_db1, total;  // part_db1: float offset of db1's partials
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -98,8 +98,9 @@ tp3d_status make_plan(const tp3d_layer_cfg* c, Plan* p) {
   x.dH = take(M * h * 2);
   x.dO = take(M * h * 2);
   x.dqkv = take(M * 3 * h * 2);
-  // column-sum partials, for the sums that run at the same time: db1 alone;
-  // the LN2 gamma/beta sums with dbo and db2; the LN1 gamma/beta sums with dbqkv
+  // column-sum partials, for the sums that run at the same time: the LN2
+  // gamma/beta sums with dbo and db2; the LN1 gamma/beta sums with dbqkv; db1
+  // beside the GEMMs and sums that follow it
   Grid gc, ga, gq;
   TP3D_TRY(make_grid(cube(TP3D_CUBE_C, x.q), M, f, &gc));
   TP3D_TRY(make_grid(cube(TP3D_CUBE_A, x.q), M, h, &ga));
@@ -107,7 +108,8 @@ tp3d_status make_plan(const tp3d_layer_cfg* c, Plan* p) {
   const int64_t p1 = colsum_parts(gc) * f;
   const int64_t p2 = 4 * colsum_parts(ga) * h;
   const int64_t p3 = 2 * colsum_parts(ga) * h + colsum_parts(gq) * 3 * h;
-  x.part_floats = (size_t)std::max(p1, std::max(p2, p3));
+  x.part_db1 = (size_t)std::max(p2, p3);  // db1's partials after the others: it runs beside them
+  x.part_floats = x.part_db1 + (size_t)p1;
   x.part = take(x.part_floats * 4);
   // arrival counters: one per 256-column strip, kStripSlot apart for the sums that run together
   if ((f > 3 * h ? f : 3 * h) / 256 + 1 > kStripSlot) return TP3D_EUNSUPPORTED;
@@ -307,7 +309,10 @@ tp3d_status tp3d_layer_bwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_
   G.epi.act = EPI_GELU_BWD;
   G.epi.gin = W(p.z1);
   TP3D_TRY(run(ctx, G, st));
-  TP3D_TRY(colsum(ctx, TP3D_CUBE_C, q, M, f, W(p.dz1), part, counters, g->b_1, st));      // db1
+  // db1 on a side stream, beside everything up to the end of the call
+  TP3D_TRY(fork(1));
+  TP3D_TRY(colsum(ctx, TP3D_CUBE_C, q, M, f, W(p.dz1), part + p.part_db1,
+                  counters + 3 * kStripSlot, g->b_1, ctx->side[0]));                                      // db1
   TP3D_TRY(plan_wgrad(ctx, q, 0, M, h, f, W(p.xn2), W(p.dz1), g->w_1, &G));                // dW1 = LN2(H)^T dZ1
   TP3D_TRY(run(ctx, G, st));
   TP3D_TRY(plan_dgrad(ctx, q, 0, M, h, f, W(p.dz1), w->w_1, W(p.dxn), &G));                // dLN2 = dZ1 W1^T
