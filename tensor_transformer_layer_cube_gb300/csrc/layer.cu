@@ -319,7 +319,10 @@ tp3d_status tp3d_layer_bwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_
   TP3D_TRY(run(ctx, G, st));
   TP3D_TRY(launch_ln_bwd(ctx, gA, W(p.dxn), W(p.Hres), (const float*)W(p.mean2), (const float*)W(p.rstd2),
                          w->ln2_g, dY, W(p.dH), st));                                                  // dH
-  // dgamma2, dbeta2 | dbo | db2 at once (dLN2 in dxn is overwritten later: joined before then)
+  // dgamma2, dbeta2 on the main stream (dLN2 in dxn is overwritten later) |
+  // dbo | db2 and then dWo on the side streams, joined at the end of the call
+  // (nothing later writes what they read; later sums that reuse their
+  // partials run after them on the same side stream)
   TP3D_TRY(fork(2));
   TP3D_TRY(launch_ln_param_grads(ctx, gA, W(p.dxn), W(p.Hres), (const float*)W(p.mean2), (const float*)W(p.rstd2),
                                  part, counters, g->ln2_g, g->ln2_b, st));
@@ -327,11 +330,10 @@ tp3d_status tp3d_layer_bwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_
                   ctx->side[0]));                                                                        // dbo
   TP3D_TRY(colsum(ctx, TP3D_CUBE_A, q, M, h, dY, part + 3 * pa, counters + 2 * kStripSlot, g->b_2,
                   ctx->side[1]));                                                                        // db2
-  TP3D_TRY(join(2));
 
   // ---- attention block
   TP3D_TRY(plan_wgrad(ctx, q, 1, M, h, h, W(p.O), W(p.dH), g->w_o, &G));                   // dWo = O^T dH
-  TP3D_TRY(run(ctx, G, st));
+  TP3D_TRY(run(ctx, G, ctx->side[1]));
   TP3D_TRY(plan_dgrad(ctx, q, 1, M, h, h, W(p.dH), w->w_o, W(p.dO), &G));                  // dO = dH Wo^T
   TP3D_TRY(run(ctx, G, st));
   // attention backward, fused: dQ, dK, dV into dQKV (MP3D's C = A B^T and C = A^T B forms)
@@ -343,13 +345,13 @@ tp3d_status tp3d_layer_bwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_
   TP3D_TRY(run(ctx, G, st));
   TP3D_TRY(launch_ln_bwd(ctx, gA, W(p.dxn), X, (const float*)W(p.mean1), (const float*)W(p.rstd1), w->ln1_g,
                          W(p.dH), dX, st));                                                            // dX
-  // dgamma1, dbeta1 | dbqkv at once, joined before returning
+  // dgamma1, dbeta1 | dbqkv at once; every side stream joined before returning
   TP3D_TRY(fork(1));
   TP3D_TRY(launch_ln_param_grads(ctx, gA, W(p.dxn), X, (const float*)W(p.mean1), (const float*)W(p.rstd1), part,
                                  counters, g->ln1_g, g->ln1_b, st));
   TP3D_TRY(colsum(ctx, TP3D_CUBE_C, q, M, 3 * h, W(p.dqkv), part + 2 * pa, counters + kStripSlot, g->b_qkv,
                   ctx->side[0]));                                                                        // dbqkv
-  return join(1);
+  return join(2);
 }
 
 }  // extern "C"
