@@ -288,9 +288,14 @@ tp3d_status tp3d_layer_bwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_
   // three at once (each with its own partials and counters): their launch and
   // reduction tails overlap.  The main stream waits for them before its next
   // launch that could overwrite what they read, and before returning.
-  auto fork = [&](int n) -> tp3d_status {
+  auto fork = [&](int n) -> tp3d_status {  // side streams 0..n-1 start after everything on st so far
     TP3D_CUDA_TRY(cudaEventRecord(ctx->ev_fork, st));
     for (int k = 0; k < n; ++k) TP3D_CUDA_TRY(cudaStreamWaitEvent(ctx->side[k], ctx->ev_fork, 0));
+    return TP3D_OK;
+  };
+  auto fork_to = [&](int k) -> tp3d_status {  // side stream k alone
+    TP3D_CUDA_TRY(cudaEventRecord(ctx->ev_fork, st));
+    TP3D_CUDA_TRY(cudaStreamWaitEvent(ctx->side[k], ctx->ev_fork, 0));
     return TP3D_OK;
   };
   auto join = [&](int n) -> tp3d_status {
@@ -302,19 +307,23 @@ tp3d_status tp3d_layer_bwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_
   };
   const int64_t pa = colsum_parts(gA) * h;  // floats of one M x h partial set
 
+  // The weight gradients (nothing in the call reads them) go to side stream 1,
+  // beside the chain of data gradients on the main stream.
+
   // ---- MLP block
+  TP3D_TRY(fork_to(1));
   TP3D_TRY(plan_wgrad(ctx, q, 1, M, f, h, W(p.y1), dY, g->w_2, &G));                       // dW2 = Y1^T dY
-  TP3D_TRY(run(ctx, G, st));
+  TP3D_TRY(run(ctx, G, ctx->side[1]));
   TP3D_TRY(plan_dgrad(ctx, q, 1, M, f, h, dY, w->w_2, W(p.dz1), &G));                      // dZ1 = (dY W2^T) GELU'(Z1)
   G.epi.act = EPI_GELU_BWD;
   G.epi.gin = W(p.z1);
   TP3D_TRY(run(ctx, G, st));
-  // db1 on a side stream, beside everything up to the end of the call
-  TP3D_TRY(fork(1));
+  // db1 on side stream 0 (its own partials and counters), dW1 on side stream 1
+  TP3D_TRY(fork(2));
   TP3D_TRY(colsum(ctx, TP3D_CUBE_C, q, M, f, W(p.dz1), part + p.part_db1,
                   counters + 3 * kStripSlot, g->b_1, ctx->side[0]));                                      // db1
   TP3D_TRY(plan_wgrad(ctx, q, 0, M, h, f, W(p.xn2), W(p.dz1), g->w_1, &G));                // dW1 = LN2(H)^T dZ1
-  TP3D_TRY(run(ctx, G, st));
+  TP3D_TRY(run(ctx, G, ctx->side[1]));
   TP3D_TRY(plan_dgrad(ctx, q, 0, M, h, f, W(p.dz1), w->w_1, W(p.dxn), &G));                // dLN2 = dZ1 W1^T
   TP3D_TRY(run(ctx, G, st));
   TP3D_TRY(launch_ln_bwd(ctx, gA, W(p.dxn), W(p.Hres), (const float*)W(p.mean2), (const float*)W(p.rstd2),
@@ -339,8 +348,9 @@ tp3d_status tp3d_layer_bwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_
   // attention backward, fused: dQ, dK, dV into dQKV (MP3D's C = A B^T and C = A^T B forms)
   TP3D_TRY(launch_attn_bwd(ctx, attn_problem(p, ctx->d_err), W(p.qkv), W(p.O), W(p.dO), (const float*)W(p.lse),
                            (float*)W(p.delta), W(p.dqkv), st));
+  TP3D_TRY(fork_to(1));
   TP3D_TRY(plan_wgrad(ctx, q, 0, M, h, 3 * h, W(p.xn1), W(p.dqkv), g->w_qkv, &G));         // dWqkv = LN1(X)^T dQKV
-  TP3D_TRY(run(ctx, G, st));
+  TP3D_TRY(run(ctx, G, ctx->side[1]));
   TP3D_TRY(plan_dgrad(ctx, q, 0, M, h, 3 * h, W(p.dqkv), w->w_qkv, W(p.dxn), &G));         // dLN1 = dQKV Wqkv^T
   TP3D_TRY(run(ctx, G, st));
   TP3D_TRY(launch_ln_bwd(ctx, gA, W(p.dxn), X, (const float*)W(p.mean1), (const float*)W(p.rstd1), w->ln1_g,
