@@ -40,13 +40,13 @@ struct Plan {
   // workspace offsets (bytes)
   size_t xn1, mean1, rstd1, qkv, lse, O, Hres, xn2, mean2, rstd2, z1, y1;  // saved by the forward
   size_t delta, dz1, dxn, dH, dO, dqkv, part, counters;                    // scratch
-  size_t part_floats, part_db1, total;  // part_db1: float offset of db1's partials
+  size_t part_floats, part_db1, part_dbqkv, total;  // float offsets of db1's and dbqkv's partials
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-constexpr int64_t kCounters = 1024;  // column-sum arrival counters in the workspace
-constexpr int64_t kStripSlot = 256;  // counters of one of up to four concurrent column sums
+constexpr int64_t kCounters = 2048;  // column-sum arrival counters in the workspace
+constexpr int64_t kStripSlot = 256;  // counters of one column sum (slots 0..4)
 
 tp3d_status make_plan(const tp3d_layer_cfg* c, Plan* p) {
   if (!c) return TP3D_EINVAL;
@@ -98,18 +98,15 @@ tp3d_status make_plan(const tp3d_layer_cfg* c, Plan* p) {
   x.dH = take(M * h * 2);
   x.dO = take(M * h * 2);
   x.dqkv = take(M * 3 * h * 2);
-  // column-sum partials, for the sums that run at the same time: the LN2
-  // gamma/beta sums with dbo and db2; the LN1 gamma/beta sums with dbqkv; db1
-  // beside the GEMMs and sums that follow it
+  // column-sum partials: a region for each sum that may run beside another
+  // (the gamma/beta sums [2 sets], dbo, db2, db1, dbqkv)
   Grid gc, ga, gq;
   TP3D_TRY(make_grid(cube(TP3D_CUBE_C, x.q), M, f, &gc));
   TP3D_TRY(make_grid(cube(TP3D_CUBE_A, x.q), M, h, &ga));
   TP3D_TRY(make_grid(cube(TP3D_CUBE_C, x.q), M, 3 * h, &gq));
-  const int64_t p1 = colsum_parts(gc) * f;
-  const int64_t p2 = 4 * colsum_parts(ga) * h;
-  const int64_t p3 = 2 * colsum_parts(ga) * h + colsum_parts(gq) * 3 * h;
-  x.part_db1 = (size_t)std::max(p2, p3);  // db1's partials after the others: it runs beside them
-  x.part_floats = x.part_db1 + (size_t)p1;
+  x.part_db1 = (size_t)(4 * colsum_parts(ga) * h);
+  x.part_dbqkv = x.part_db1 + (size_t)(colsum_parts(gc) * f);
+  x.part_floats = x.part_dbqkv + (size_t)(colsum_parts(gq) * 3 * h);
   x.part = take(x.part_floats * 4);
   // arrival counters: one per 256-column strip, kStripSlot apart for the sums that run together
   if ((f > 3 * h ? f : 3 * h) / 256 + 1 > kStripSlot) return TP3D_EUNSUPPORTED;
@@ -328,15 +325,13 @@ tp3d_status tp3d_layer_bwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_
   TP3D_TRY(run(ctx, G, st));
   TP3D_TRY(launch_ln_bwd(ctx, gA, W(p.dxn), W(p.Hres), (const float*)W(p.mean2), (const float*)W(p.rstd2),
                          w->ln2_g, dY, W(p.dH), st));                                                  // dH
-  // dgamma2, dbeta2 on the main stream (dLN2 in dxn is overwritten later) |
-  // dbo | db2 and then dWo on the side streams, joined at the end of the call
-  // (nothing later writes what they read; later sums that reuse their
-  // partials run after them on the same side stream)
+  // dbo, then dgamma2 and dbeta2 on side stream 0 (dLN2 in dxn is overwritten
+  // by dLN1: joined before then); db2, then dWo on side stream 1
   TP3D_TRY(fork(2));
-  TP3D_TRY(launch_ln_param_grads(ctx, gA, W(p.dxn), W(p.Hres), (const float*)W(p.mean2), (const float*)W(p.rstd2),
-                                 part, counters, g->ln2_g, g->ln2_b, st));
   TP3D_TRY(colsum(ctx, TP3D_CUBE_A, q, M, h, W(p.dH), part + 2 * pa, counters + kStripSlot, g->b_o,
                   ctx->side[0]));                                                                        // dbo
+  TP3D_TRY(launch_ln_param_grads(ctx, gA, W(p.dxn), W(p.Hres), (const float*)W(p.mean2), (const float*)W(p.rstd2),
+                                 part, counters, g->ln2_g, g->ln2_b, ctx->side[0]));
   TP3D_TRY(colsum(ctx, TP3D_CUBE_A, q, M, h, dY, part + 3 * pa, counters + 2 * kStripSlot, g->b_2,
                   ctx->side[1]));                                                                        // db2
 
@@ -348,20 +343,24 @@ tp3d_status tp3d_layer_bwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_
   // attention backward, fused: dQ, dK, dV into dQKV (MP3D's C = A B^T and C = A^T B forms)
   TP3D_TRY(launch_attn_bwd(ctx, attn_problem(p, ctx->d_err), W(p.qkv), W(p.O), W(p.dO), (const float*)W(p.lse),
                            (float*)W(p.delta), W(p.dqkv), st));
+  // dWqkv, then dbqkv on side stream 1
   TP3D_TRY(fork_to(1));
   TP3D_TRY(plan_wgrad(ctx, q, 0, M, h, 3 * h, W(p.xn1), W(p.dqkv), g->w_qkv, &G));         // dWqkv = LN1(X)^T dQKV
   TP3D_TRY(run(ctx, G, ctx->side[1]));
+  TP3D_TRY(colsum(ctx, TP3D_CUBE_C, q, M, 3 * h, W(p.dqkv), part + p.part_dbqkv, counters + 4 * kStripSlot,
+                  g->b_qkv, ctx->side[1]));                                                              // dbqkv
+  // dgamma2 and dbeta2 have read dLN2 before dLN1 takes its place
+  TP3D_CUDA_TRY(cudaEventRecord(ctx->ev_join[0], ctx->side[0]));
+  TP3D_CUDA_TRY(cudaStreamWaitEvent(st, ctx->ev_join[0], 0));
   TP3D_TRY(plan_dgrad(ctx, q, 0, M, h, 3 * h, W(p.dqkv), w->w_qkv, W(p.dxn), &G));         // dLN1 = dQKV Wqkv^T
   TP3D_TRY(run(ctx, G, st));
+  // dgamma1, dbeta1 on side stream 0 beside the LN1 backward (both only read dLN1)
+  TP3D_TRY(fork_to(0));
+  TP3D_TRY(launch_ln_param_grads(ctx, gA, W(p.dxn), X, (const float*)W(p.mean1), (const float*)W(p.rstd1), part,
+                                 counters, g->ln1_g, g->ln1_b, ctx->side[0]));
   TP3D_TRY(launch_ln_bwd(ctx, gA, W(p.dxn), X, (const float*)W(p.mean1), (const float*)W(p.rstd1), w->ln1_g,
                          W(p.dH), dX, st));                                                            // dX
-  // dgamma1, dbeta1 | dbqkv at once; every side stream joined before returning
-  TP3D_TRY(fork(1));
-  TP3D_TRY(launch_ln_param_grads(ctx, gA, W(p.dxn), X, (const float*)W(p.mean1), (const float*)W(p.rstd1), part,
-                                 counters, g->ln1_g, g->ln1_b, st));
-  TP3D_TRY(colsum(ctx, TP3D_CUBE_C, q, M, 3 * h, W(p.dqkv), part + 2 * pa, counters + kStripSlot, g->b_qkv,
-                  ctx->side[0]));                                                                        // dbqkv
-  return join(2);
+  return join(2);  // every side stream joined before returning
 }
 
 }  // extern "C"
