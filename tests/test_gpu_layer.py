@@ -135,3 +135,49 @@ def test_layer_errors_before_launch(ctx):
     p2["w_o"] = None
     assert t.tp3d_layer_fwd(ctx, ok, p2, x, x, x) == 1
     assert t.tp3d_sync_status(ctx) == 0
+
+
+def test_layer_step_in_a_cuda_graph(ctx):
+    # The forward and the backward (whose independent launches fork onto the
+    # context's side streams and join back) can be captured in one CUDA graph;
+    # replaying it gives the bits of direct calls.
+    cfg = OY.LayerConfig(p=2, batch=2, seq=256, hidden=512, heads=4, ffn=2048)
+    I = S.layer_inputs(cfg.batch, cfg.seq, cfg.hidden, cfg.heads, cfg.ffn, 4242, perturb=True)
+    q, M, h = cfg.p, cfg.M, cfg.hidden
+    params = {k: to_dev_bf16(I[k], lay(q)) for k, lay in OY.WEIGHT_LAYOUTS.items()}
+    params.update({k: I[k].to(device()) for k in OY.VECTORS})
+    X = to_dev_bf16(I["X"], L.CUBE_A(q))
+    dY = to_dev_bf16(I["dY"], L.CUBE_A(q))
+    c = t.tp3d_layer_cfg(q, cfg.batch, cfg.seq, h, cfg.heads, cfg.ffn, t.TP3D_BF16, cfg.eps)
+    ws = torch.empty(t.tp3d_layer_workspace_bytes(c), dtype=torch.uint8, device=device())
+    Y = torch.empty(M * h, dtype=torch.bfloat16, device=device())
+    dX = torch.empty(M * h, dtype=torch.bfloat16, device=device())
+    grads = {k: torch.empty_like(v) for k, v in params.items()}
+
+    def step():
+        assert t.tp3d_layer_fwd(ctx, c, params, X, Y, ws) == 0
+        assert t.tp3d_layer_bwd(ctx, c, params, X, ws, dY, dX, grads) == 0
+
+    step()
+    torch.cuda.synchronize()
+    assert t.tp3d_sync_status(ctx) == 0
+    direct = [Y.clone(), dX.clone()] + [v.clone() for v in grads.values()]
+    for v in [Y, dX] + list(grads.values()):
+        v.fill_(float("nan"))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for v in [Y, dX] + list(grads.values()):
+        v.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert t.tp3d_sync_status(ctx) == 0
+    replayed = [Y, dX] + list(grads.values())
+    for a, b in zip(direct, replayed):
+        assert torch.equal(a, b)
