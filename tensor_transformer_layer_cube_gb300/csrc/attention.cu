@@ -133,14 +133,23 @@ __device__ __forceinline__ void mma_tile(uint32_t d_tmem, uint32_t a_tile, bool 
   }
 }
 
+// The persistent CTAs take the work items (numbered longest first) in rounds
+// of gridDim.x, each round in the opposite CTA order to the one before: the
+// CTA given a round's longest item gets the next round's shortest, which
+// evens out the CTAs' total work.  Every role of a CTA walks the same list.
+__device__ __forceinline__ int64_t snake_item(int64_t r) {
+  const int64_t g = gridDim.x;
+  return r * g + ((r & 1) ? g - 1 - (int64_t)blockIdx.x : (int64_t)blockIdx.x);
+}
+
 __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) {
   const unsigned long long t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity))
     if (globaltimer_ns() - t0 > kWaitLimitNs) return;
 }
 
-// All three kernels are persistent: CTA c takes work items c, c + grid, ...
-// in longest-first order, and the producer loads the next item's tiles while
+// All three kernels are persistent: the CTAs take the work items in longest-first
+// order, in rounds (snake_item), and the producer loads the next item's tiles while
 // the current one finishes (phase counters run across items).
 
 // ------------------------------------------------------------------ forward
@@ -217,7 +226,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // ------------------------------------------------------------ producer
       uint32_t n = 0, ic = 0;
       bool ok = true;
-      for (int64_t w = blockIdx.x; w < items && ok; w += gridDim.x, ++ic) {
+      for (int64_t rd = 0, w = snake_item(0); w < items && ok; w = snake_item(++rd), ++ic) {
         const int64_t k = npair - 1 - w / A.Z, z = w % A.Z, b = z / A.H, t = z % A.H;
         const int64_t iq0 = 2 * k;
         const bool two = iq0 + 1 < nq;
@@ -265,7 +274,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         ++pc[sl];
         return true;
       };
-      for (int64_t w = blockIdx.x; w < items && ok; w += gridDim.x, ++ic) {
+      for (int64_t rd = 0, w = snake_item(0); w < items && ok; w = snake_item(++rd), ++ic) {
         const int64_t iq0 = 2 * (npair - 1 - w / A.Z);
         const bool two = iq0 + 1 < nq;
         const int nkv0 = (int)iq0 + 1, nkv1 = two ? nkv0 + 1 : 0, nmax = two ? nkv1 : nkv0;
@@ -314,7 +323,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t s_col = (uint32_t)(sl * TR), o_col = 256u + (uint32_t)(sl * A.d);
     uint32_t sc = 0, pc = 0, oc = 0;
     bool ok = true;
-    for (int64_t w = blockIdx.x; w < items && ok; w += gridDim.x) {
+    for (int64_t rd = 0, w = snake_item(0); w < items && ok; w = snake_item(++rd)) {
       const int64_t k = npair - 1 - w / A.Z, z = w % A.Z, b = z / A.H, t = z % A.H;
       const int64_t iq = 2 * k + sl;
       if (iq >= nq) continue;  // an odd tile count leaves the last item's slot 1 empty
@@ -455,7 +464,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0) {
       uint32_t n = 0, ic = 0;
       bool ok = true;
-      for (int64_t w = blockIdx.x; w < items && ok; w += gridDim.x, ++ic) {
+      for (int64_t rd = 0, w = snake_item(0); w < items && ok; w = snake_item(++rd), ++ic) {
         const int64_t jk = w / A.Z, z = w % A.Z, b = z / A.H, t = z % A.H;
         const int niter = (int)(nq - jk);
         if (!(ok = mbar_wait(kv_empty, (ic & 1) ^ 1, c.abort_flag, A.err))) break;
@@ -492,7 +501,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         umma_commit(st_full);
         return true;
       };
-      for (int64_t w = blockIdx.x; w < items && ok; w += gridDim.x, ++ic) {
+      for (int64_t rd = 0, w = snake_item(0); w < items && ok; w = snake_item(++rd), ++ic) {
         const int niter = (int)(nq - w / A.Z);
         if (!(ok = mbar_wait(kv_full, ic & 1, c.abort_flag, A.err))) break;
         if (!(ok = issue_sdp(n, niter == 1))) break;
@@ -525,7 +534,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float sl2 = A.scale * kLog2e;
     uint32_t n = 0, ic = 0;
     bool ok = true;
-    for (int64_t w = blockIdx.x; w < items && ok; w += gridDim.x, ++ic) {
+    for (int64_t rd = 0, w = snake_item(0); w < items && ok; w = snake_item(++rd), ++ic) {
       const int64_t jk = w / A.Z, z = w % A.Z, b = z / A.H, t = z % A.H;
       const int niter = (int)(nq - jk);
       for (int it = 0; it < niter && ok; ++it, ++n) {
@@ -667,7 +676,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0) {
       uint32_t n = 0, ic = 0;
       bool ok = true;
-      for (int64_t w = blockIdx.x; w < items && ok; w += gridDim.x, ++ic) {
+      for (int64_t rd = 0, w = snake_item(0); w < items && ok; w = snake_item(++rd), ++ic) {
         const int64_t iq = nq - 1 - w / A.Z, z = w % A.Z, b = z / A.H, t = z % A.H;
         const int niter = (int)iq + 1;
         if (!(ok = mbar_wait(qo_empty, (ic & 1) ^ 1, c.abort_flag, A.err))) break;
@@ -692,7 +701,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int ks_d = (int)(A.d / 16);
       uint32_t n = 0, ic = 0;
       bool ok = true;
-      for (int64_t w = blockIdx.x; w < items && ok; w += gridDim.x, ++ic) {
+      for (int64_t rd = 0, w = snake_item(0); w < items && ok; w = snake_item(++rd), ++ic) {
         const int niter = (int)(nq - 1 - w / A.Z) + 1;
         if (!(ok = mbar_wait(qo_full, ic & 1, c.abort_flag, A.err))) break;
         for (int it = 0; it < niter && ok; ++it, ++n) {
@@ -724,7 +733,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float sl2 = A.scale * kLog2e;
     uint32_t n = 0, ic = 0;
     bool ok = true;
-    for (int64_t w = blockIdx.x; w < items && ok; w += gridDim.x, ++ic) {
+    for (int64_t rd = 0, w = snake_item(0); w < items && ok; w = snake_item(++rd), ++ic) {
       const int64_t iq = nq - 1 - w / A.Z, z = w % A.Z, b = z / A.H, t = z % A.H;
       const int niter = (int)iq + 1;
       const int64_t qrow = z * A.s + iq * TR + r;
