@@ -793,12 +793,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // delta[z*s + r] = sum over the head's d columns of dO * O.  One warp per
-// token row: 16-byte loads, 256 columns (every head in them) per step, four
+// token row: 16-byte loads, 256 columns (every head in them) per step, eight
 // steps in flight; the G = d/8 lanes that hold one head reduce with shuffles.
 template <int G>
 __global__ void __launch_bounds__(256) attn_delta_kernel(const AttnProblem A, const bf16* __restrict__ O,
                                                          const bf16* __restrict__ dO, float* __restrict__ delta) {
-  constexpr int U = 4;
+  constexpr int U = 8;
   const int lane = threadIdx.x & 31;
   const int64_t M = A.Z / A.H * A.s;  // token rows
   const int64_t nw = (int64_t)gridDim.x * 8;
