@@ -332,22 +332,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       for (int j = 0; j < nkv && ok; ++j) {
         if (!(ok = warp_wait(s_full(sl), sc & 1, c, A.err, lane))) break;
         tc_fence_after();
-        // the whole row of scores into registers (four loads, one wait)
+        // the row of scores, 32 columns at a time (the loop over the chunks is
+        // kept rolled: a compact body the instruction cache holds); read twice,
+        // for the maximum and then for P
         const bool diag = j == nkv - 1;
-        uint32_t v[TR / 32][32];
-#pragma unroll
-        for (int cc = 0; cc < TR / 32; ++cc) tmem_ld_32x32b_x32(tmem_row(tmem, quarter, s_col + (uint32_t)(cc * 32)), v[cc]);
-        tmem_ld_wait();
-        tc_fence_before();
-        warp_arrive(s_empty(sl), lane);
-        ++sc;
         // eight independent partial maxima (short dependency chains)
         float mx[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+#pragma unroll 1
+        for (int cc = 0; cc < TR / 32; ++cc) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem_row(tmem, quarter, s_col + (uint32_t)(cc * 32)), v);
+          tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < TR; ++e)
-          if (!diag || e <= r) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(v[e >> 5][e & 31]));
+          for (int e = 0; e < 32; ++e)
+            if (!diag || cc * 32 + e <= r) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(v[e]));
+        }
         float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         mt *= sl2;
         // the product of the previous tile has finished: P is free and O current
@@ -373,17 +374,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         float ps[8];  // eight partial row sums
 #pragma unroll
         for (int i = 0; i < 8; ++i) ps[i] = 0.0f;
+#pragma unroll 1
+        for (int cc = 0; cc < TR / 32; ++cc) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem_row(tmem, quarter, s_col + (uint32_t)(cc * 32)), v);
+          tmem_ld_wait();
 #pragma unroll
-        for (int g = 0; g < TR / 8; ++g) {
-          float f[8];
+          for (int g = 0; g < 4; ++g) {
+            float f[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int col = g * 8 + e;
-            f[e] = (!diag || col <= r) ? ex2_approx(fmaf(__uint_as_float(v[col >> 5][col & 31]), sl2, -m)) : 0.0f;
-            ps[e] += f[e];
+            for (int e = 0; e < 8; ++e) {
+              const int col = cc * 32 + g * 8 + e;
+              f[e] = (!diag || col <= r) ? ex2_approx(fmaf(__uint_as_float(v[g * 8 + e]), sl2, -m)) : 0.0f;
+              ps[e] += f[e];
+            }
+            st_tile8(c.base_ptr + (2 + sl) * kTile, r, cc * 4 + g, pack8f(f));
           }
-          st_tile8(c.base_ptr + (2 + sl) * kTile, r, g, pack8f(f));
         }
+        // S is read for the last time: the next tile's scores may overwrite it
+        tc_fence_before();
+        warp_arrive(s_empty(sl), lane);
+        ++sc;
         l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
         fence_proxy_async_smem();
         tc_fence_before();
