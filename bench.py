@@ -434,7 +434,7 @@ def cpu_baseline_layer(w, seconds):
 # DRAM bytes (read + write) of one launch of the layer's linear-1 probe, from
 # the ncu capture summarised in profiles/gemm_tc2_layer_w1.md; valid only
 # while the GEMM sources hash to the value they had when it was taken.
-GEMM_TRAFFIC = {"workload": "layer_q2", "bytes": 50558208 + 27396864, "sources_sha256_16": "36bd04366272f951",
+GEMM_TRAFFIC = {"workload": "layer_q2", "bytes": 50565888 + 27478784, "sources_sha256_16": "87c2d320b204b556",
                 "note": "ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch; output lines still in "
                         "L2 when the kernel ends are not counted (reads equal the algorithmic inputs)"}
 

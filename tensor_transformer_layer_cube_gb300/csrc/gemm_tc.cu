@@ -896,6 +896,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && leader) {
       // ---------------------------------------------------------- MMA issuer (even CTA)
       const uint32_t idesc = idesc_bf16_f32(256, BN, a_mn ? 1 : 0, b_mn ? 1 : 0);
+      // Stage 0's operand descriptors, built once: a stage, chunk or row step
+      // adds its byte offset / 16 to the 14-bit address field (shared
+      // addresses stay below 256 KiB, so the field never carries).  Fewer
+      // instructions per stage for this warp, which shares its scheduler with
+      // two epilogue warps, keep the tensor pipe fed.
+      const uint64_t adesc0 =
+          a_mn ? smem_desc_sw128(a_stage(0), Cfg::MNBOX, 1024u) : smem_desc_sw128(a_stage(0), 16u, 1024u);
+      const uint64_t bdesc0 =
+          b_mn ? smem_desc_sw128(b_stage(0), Cfg::MNBOX, 1024u) : smem_desc_sw128(b_stage(0), 16u, 1024u);
       uint32_t it = 0, tc = 0;
       bool ok = true;
       for (int64_t t = cid; t < ntiles && ok; t += nclusters) {
@@ -917,15 +926,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc_fence_after();
+            const uint64_t as0 = adesc0 + (uint64_t)((s * Cfg::A_BYTES) >> 4);
+            const uint64_t bs0 = bdesc0 + (uint64_t)((s * Cfg::B_BYTES) >> 4);
 #pragma unroll
             for (int k16 = 0; k16 < BKP / 16; ++k16) {
               // K-major: 64-column chunks of 128 rows, +32 B per 16 columns;
               // MN-major: 64-wide boxes of BKP rows, +16 rows per step
               const uint32_t kk = (uint32_t)(k16 >> 2) * Cfg::KCHUNK + (uint32_t)(k16 & 3) * 32u;
-              const uint64_t ad = a_mn ? smem_desc_sw128(a_stage(s) + k16 * 2048u, Cfg::MNBOX, 1024u)
-                                       : smem_desc_sw128(a_stage(s) + kk, 16u, 1024u);
-              const uint64_t bd = b_mn ? smem_desc_sw128(b_stage(s) + k16 * 2048u, Cfg::MNBOX, 1024u)
-                                       : smem_desc_sw128(b_stage(s) + kk, 16u, 1024u);
+              const uint64_t ad = as0 + (uint64_t)((a_mn ? k16 * 2048u : kk) >> 4);
+              const uint64_t bd = bs0 + (uint64_t)((b_mn ? k16 * 2048u : kk) >> 4);
               umma_bf16_pair(d_tmem, ad, bd, idesc, (first && k16 == 0) ? 0u : 1u);
             }
             first = false;
