@@ -24,7 +24,7 @@ baseline may import this module; the library never does.
   instances), and greedy search with randomisation (rounds of mutually
   non-overlapping tasks, the largest of several random orders per round).
 
-Readings where the page is silent (also listed in the design doc): the size of a
+Readings where the page is silent: the size of a
 round is the number of hosts it involves; a task joining a round is sent by
 its free holder host with the least send load so far (ties: lowest host);
 ties between equal candidate rounds keep the first trial; random orders sort

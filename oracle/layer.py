@@ -13,7 +13,7 @@ position.  The attention core and the statistics of LayerNorm are not
 described on the page (its figures are lost); every partition of them
 reaches the unpartitioned layer, which is what the oracle computes.
 
-Readings (listed in the design doc): pre-LN (as GPT-2), biased variance with
+Readings where the pages are silent: pre-LN (as GPT-2), biased variance with
 eps = 1e-5, exact-erf GELU, QKV columns packed [Q | K | V] with head t using
 columns t*d .. t*d+d-1 of each, causal mask (key position > query position
 excluded), no dropout, softmax over keys in float64.

@@ -13,7 +13,7 @@ a sharded tensor is one flat buffer holding every device's shard back to
 back, in device order; each shard is dense and row-major.  A replicated
 layout stores every replica.
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
 
 * Virtual-device linear order: device (i, j, l) of the p x p x p cube is
   number (i*p + j)*p + l.  MP3D §2.3 names processors by (i, j, l) on the
