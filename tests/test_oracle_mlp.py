@@ -46,3 +46,30 @@ def test_cube_mlp_equals_two_cube_linears(p, M, h, f):
     # the output is back in the input's direction (CUBE_A) and equals the dense MLP
     want = OM.mlp_dense(X, W1, b1, W2, b2)[0]
     assert np.allclose(L.from_sharded(Ym, L.CUBE_A(p), M, h), want, rtol=1e-12, atol=1e-12)
+
+
+def test_mlp_is_row_separable():
+    # the sampled-row parity of large MLPs relies on it: any subset of rows
+    # through the MLP equals the same rows of the full output (up to the
+    # summation order a matrix library picks for a different height)
+    rng = np.random.default_rng(11)
+    X, W1, b1, W2, b2 = _inputs(rng, 24, 8, 32)
+    rows = np.array([0, 5, 6, 17, 23])
+    full = OM.mlp_dense(X, W1, b1, W2, b2)[0]
+    got = OM.mlp_rows_dense(X[rows], W1, b1, W2, b2)
+    assert np.max(np.abs(got - full[rows])) <= 1e-13 * np.max(np.abs(full))
+
+
+def test_mlp_bias_paths():
+    # W2 = 0: every output row is b2; W1 = 0 and b1 = 0: the hidden
+    # activation is GELU(0) = 0, so again every row is b2; b1 alone reaches
+    # the output as GELU(b1) W2 + b2 in every row
+    rng = np.random.default_rng(12)
+    X, W1, b1, W2, b2 = _inputs(rng, 6, 8, 16)
+    Y = OM.mlp_dense(X, W1, b1, np.zeros_like(W2), b2)[0]
+    assert np.array_equal(Y, np.broadcast_to(b2, Y.shape))
+    Y, Z1, Y1 = OM.mlp_dense(X, np.zeros_like(W1), np.zeros_like(b1), W2, b2)
+    assert not Y1.any() and np.array_equal(Y, np.broadcast_to(b2, Y.shape))
+    Y = OM.mlp_dense(X, np.zeros_like(W1), b1, W2, b2)[0]
+    want = OL.gelu(b1) @ W2 + b2
+    assert np.allclose(Y, np.broadcast_to(want, Y.shape), rtol=0, atol=1e-15)
