@@ -50,3 +50,16 @@ def test_struct_sizes_match_the_header(lib):
     assert ctypes.sizeof(t.tp3d_layout) == 16
     assert ctypes.sizeof(t.tp3d_layer_cfg) == 32
     assert ctypes.sizeof(t.tp3d_layer_params) == 12 * ctypes.sizeof(ctypes.c_void_p)
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    # no fallback path: without the built library, loading and every compute
+    # entry point raise instead of computing anything on the host
+    monkeypatch.setattr(t, "_lib", None)
+    monkeypatch.setattr(t, "LIB_PATH", str(tmp_path / "absent" / "libtp3d.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        t.lib()
+    with pytest.raises(RuntimeError, match="missing"):
+        t.tp3d_linear(None, 2, 0, 64, 64, 64, 1, None, None, None, 0, None)
+    with pytest.raises(RuntimeError, match="missing"):
+        t.tp3d_reshard(None, 8, 8, 2, t.tp3d_layout(), None, t.tp3d_layout(), None)
