@@ -434,17 +434,31 @@ def cpu_baseline_layer(w, seconds):
 # DRAM bytes (read + write) of one launch of the layer's linear-1 probe, from
 # the ncu capture summarised in profiles/gemm_tc2_layer_w1.md; valid only
 # while the GEMM sources hash to the value they had when it was taken.
-GEMM_TRAFFIC = {"workload": "layer_q2", "bytes": 50565888 + 27478784, "sources_sha256_16": "87c2d320b204b556",
+GEMM_TRAFFIC = {"workload": "layer_q2", "bytes": 50565888 + 27478784, "sources_sha256_16": "74303bdfe64ab924",
                 "note": "ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch; output lines still in "
                         "L2 when the kernel ends are not counted (reads equal the algorithmic inputs)"}
 
 
-def gemm_sources_hash():
+def strip_comments(src):
+    """C/C++ source without its comments and blank lines: an edit to a
+    comment does not change the kernel the traffic figure was taken on."""
+    import re
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(ln.rstrip() for ln in src.split("\n") if ln.strip())
+
+
+def gemm_sources_hash(read=None):
     import hashlib
     h = hashlib.sha256()
     for f in ("gemm_tc.cu", "gemm.cuh", "common.cuh", "layout.cuh", "api.cu"):
-        with open(os.path.join(ROOT, "tensor_transformer_layer_cube_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        path = os.path.join("tensor_transformer_layer_cube_gb300", "csrc", f)
+        if read is None:
+            with open(os.path.join(ROOT, path), encoding="utf-8") as fh:
+                text = fh.read()
+        else:
+            text = read(path)
+        h.update(strip_comments(text).encode())
     return h.hexdigest()[:16]
 
 

@@ -25,11 +25,11 @@ Sources (cited by page title and section):
 
 Modules:
 
-* ``layouts``  - O1/O7: the cube layouts, the diagonal vector layout, the
+* ``layouts``  - the cube layouts, the diagonal vector layout, the
   mesh sharding specs, sharded storage, resharding and unit tasks.
-* ``linear``   - O2: the 3-D linear (C = A.B [+ b] [GELU]) and its gradients.
-* ``mlp``      - O3: the Megatron / cube MLP.
-* ``layer``    - O4/O5: the pre-LN GPT decoder layer, forward and backward.
+* ``linear``   - the 3-D linear (C = A.B [+ b] [GELU]) and its gradients.
+* ``mlp``      - the Megatron / cube MLP.
+* ``layer``    - the pre-LN GPT decoder layer, forward and backward.
 * ``metrics``  - the error metric the parity tests use.
 
 Parity status per function is stated in each module header.

@@ -1,4 +1,4 @@
-"""O4 / O5 - the pre-LN GPT decoder layer on the cube, forward and backward
+"""The pre-LN GPT decoder layer on the cube, forward and backward
 (oracle).
 
 TEST INFRASTRUCTURE ONLY (see ``oracle/__init__``).

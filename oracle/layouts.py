@@ -1,4 +1,4 @@
-"""O1 / O7 - layout maps, sharded storage, resharding and unit tasks (oracle).
+"""Layout maps, sharded storage, resharding and unit tasks (oracle).
 
 TEST INFRASTRUCTURE ONLY (see ``oracle/__init__``).  Plain numpy, written
 from the pages' index formulas; nothing here is shared with the GPU path.
@@ -226,7 +226,7 @@ def sharded_size(layout, R: int, C: int) -> int:
 
 
 def reshard(buf: np.ndarray, src, dst, R: int, C: int) -> np.ndarray:
-    """O7: every destination element takes the bits of the same global
+    """Resharding: every destination element takes the bits of the same global
     element of the source (CMR §2, cross-mesh resharding).  Bits are copied
     as they are; dtype is preserved."""
     return to_sharded(from_sharded(buf, src, R, C), dst)

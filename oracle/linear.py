@@ -1,4 +1,4 @@
-"""O2 - the 3-D linear C = A.B (+ b) (GELU), forward and backward (oracle).
+"""The 3-D linear C = A.B (+ b) (GELU), forward and backward (oracle).
 
 TEST INFRASTRUCTURE ONLY (see ``oracle/__init__``).
 

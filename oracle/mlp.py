@@ -1,4 +1,4 @@
-"""O3 - the MLP block on the cube: Y = GELU(X W1 + b1) W2 + b2 (oracle).
+"""The MLP block on the cube: Y = GELU(X W1 + b1) W2 + b2 (oracle).
 
 TEST INFRASTRUCTURE ONLY (see ``oracle/__init__``).
 

@@ -1,4 +1,4 @@
-// gemm_simt.cu - K3: the sharded, batched GEMM in fp32 on the CUDA cores
+// gemm_simt.cu - the sharded, batched GEMM in fp32 on the CUDA cores
 // (FFMA, no TF32), for fp32 problems.
 //
 // Same problem description as the tensor-core kernel (gemm.cuh); every

@@ -1,4 +1,4 @@
-// gemm_tc.cu - K2: the sharded, batched bf16 GEMM on the sm_103a tensor cores.
+// gemm_tc.cu - the sharded, batched bf16 GEMM on the sm_103a tensor cores.
 //
 // Persistent, warp-specialised kernel, one CTA per SM:
 //   warp 0      TMA producer: 3-D tensor maps (shard column, shard row,

@@ -1,4 +1,4 @@
-// reshard.cu - K1: bit-exact layout conversion between the ABI layouts
+// reshard.cu - bit-exact layout conversion between the ABI layouts
 // ("On Optimizing the Communication of Model Parallelism", §2, cross-mesh
 // resharding; the cube layouts of "Maximizing Parallelism in Distributed
 // Training for Huge Neural Networks", §3.1.1).

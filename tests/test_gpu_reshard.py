@@ -1,4 +1,4 @@
-"""GPU parity of tp3d_reshard (K1) against the oracle: bit-exact.
+"""GPU parity of tp3d_reshard against the oracle: bit-exact.
 
 Resharding is the layout conversion of "On Optimizing the Communication of
 Model Parallelism" §2 among row-split, column-split, 2-D block, cube and

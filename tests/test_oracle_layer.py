@@ -1,4 +1,4 @@
-"""Pins of the oracle's GPT layer (O4 forward, O5 backward), CPU only.
+"""Pins of the oracle's GPT layer (forward and backward), CPU only.
 
 The page ("Maximizing Parallelism ..." §3.2) fixes the structure (two 3-D
 linears per block, LayerNorm as matrix-vector ops, direction restored per

@@ -1,4 +1,4 @@
-"""Pins of the oracle's layout maps (O1) and resharding (O7), CPU only.
+"""Pins of the oracle's layout maps and resharding, CPU only.
 
 What pins them (none of it re-types the oracle's formulas):
 * hand-worked shard ranges from the index formulas of "Maximizing

@@ -1,4 +1,4 @@
-"""Pins of the oracle's 3-D linear (O2), CPU only.
+"""Pins of the oracle's 3-D linear, CPU only.
 
 "Maximizing Parallelism in Distributed Training for Huge Neural Networks":
 * §2.3: the unbalanced 2x2x2 algorithm and its printed block formula;

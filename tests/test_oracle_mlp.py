@@ -1,4 +1,4 @@
-"""Pins of the oracle's MLP (O3), CPU only.
+"""Pins of the oracle's MLP, CPU only.
 
 "Transformer Training 11: Model Parallelism", section "Tensor parallelism":
 the first FFN matrix split by columns with GELU applied per part, the second
