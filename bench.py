@@ -606,6 +606,23 @@ def make_bench(t, ctx, dev, name):
     return BENCHES[w["kind"]](t, ctx, dev, w)
 
 
+def slowest_rank_ms(total_ms, world, dist, device):
+    """The job's timed total: every rank runs the same replica, so the job
+    takes as long as its slowest rank (a MAX all-reduce over the ranks)."""
+    if world <= 1 or dist is None:
+        return total_ms
+    import torch
+    tt = torch.tensor([total_ms], device=device, dtype=torch.float64)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_value(world, units, steps, total_ms, scale):
+    """Whole-job throughput: the work of all ranks' steps over the slowest
+    rank's time (units per second, divided by the metric's scale)."""
+    return world * units * steps / (total_ms / 1e3) / scale
+
+
 def run_ours(args, rank, world, dist):
     import torch
 
@@ -653,13 +670,9 @@ def run_ours(args, rank, world, dist):
     st = t.tp3d_sync_status(ctx)
     if st != 0:
         raise SystemExit(f"device error after the timed region: {t.STATUS[st]}")
-    total_ms = sum(durs)
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = slowest_rank_ms(sum(durs), world, dist, dev)
     ms = total_ms / args.steps
-    value = world * wb.units * args.steps / (total_ms / 1e3) / wb.scale
+    value = job_value(world, wb.units, args.steps, total_ms, wb.scale)
 
     line = {
         "metric": METRIC, "value": value, "unit": wb.unit, "n_gpus": world, "steps": args.steps,
