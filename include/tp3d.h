@@ -24,8 +24,9 @@
  * error word, two side streams with three events, and host-side caches.  All
  * compute calls are asynchronous on the given CUDA stream (a cudaStream_t
  * passed as void*; NULL = the legacy default stream).  A call that runs
- * independent launches on the context's side streams (tp3d_layer_bwd) forks
- * them from the given stream and joins them back into it before returning,
+ * independent launches on the context's side streams (tp3d_layer_fwd,
+ * tp3d_layer_bwd) forks them from the given stream and joins them back into
+ * it before returning,
  * so its work is ordered on the given stream as a whole; calls of one context
  * must not run concurrently on different streams.  Inputs are read-only;
  * outputs must not alias inputs.
@@ -55,7 +56,10 @@ typedef enum {
   TP3D_ECUDA = 5,        /* a CUDA runtime or driver call failed                  */
   TP3D_ETIMEOUT = 6,     /* a bounded device-side wait ran out                    */
   TP3D_EUNSUPPORTED = 7, /* valid request outside what the kernels implement      */
-  TP3D_EOVERLAP = 8      /* output buffer overlaps an input buffer               */
+  TP3D_EOVERLAP = 8,     /* output buffer overlaps an input buffer               */
+  TP3D_ERANGE = 9        /* a value on the layer's fp16 score path (LN1 output,
+                            Q, K) beyond fp16's finite range; raised by a kernel
+                            and reported by tp3d_sync_status                     */
 } tp3d_status;
 
 typedef enum { TP3D_F32 = 0, TP3D_BF16 = 1 } tp3d_dtype;
@@ -103,7 +107,8 @@ void tp3d_destroy(tp3d_ctx* ctx);
 const char* tp3d_status_string(tp3d_status s);
 
 /* Synchronises `stream`, then reads and clears the device error word:
- * TP3D_ETIMEOUT if a bounded wait ran out since the last call, TP3D_ECUDA if
+ * TP3D_ETIMEOUT if a bounded wait ran out since the last call, TP3D_ERANGE
+ * if a layer call met a value its fp16 score path cannot hold, TP3D_ECUDA if
  * the stream reported an error, else TP3D_OK.                               */
 tp3d_status tp3d_sync_status(tp3d_ctx* ctx, void* stream);
 
@@ -195,8 +200,22 @@ tp3d_status tp3d_mlp_noalloc(tp3d_ctx* ctx, int q, int64_t M, int64_t h, int64_t
  * t*d .. t*d+d-1 of each; GELU exact.  Token row = batch*seq + position.
  * Layouts: X, Y, dX, dY in CUBE_A (M x hidden, M = batch*seq); W_qkv
  * (hidden x 3 hidden) and W_1 (hidden x ffn) in CUBE_B; W_o (hidden x hidden)
- * and W_2 (ffn x hidden) in CUBE_B_SWAP; vectors plain.  bf16 throughout;
- * LN and softmax statistics in fp32.                                         */
+ * and W_2 (ffn x hidden) in CUBE_B_SWAP; vectors plain.  Parameters,
+ * activations and gradients are bf16; LN and softmax statistics fp32.
+ *
+ * Score path in fp16.  The softmax backward amplifies a relative error u of
+ * the scores' inputs by about the scores' own magnitude, so with sharply
+ * peaked attention (|scores| of 5 and more) bf16's u = 2^-9 on the LN1
+ * output and on Q and K alone puts dQ, dK and everything upstream of them
+ * beyond 1e-2 of the exact layer.  The layer therefore keeps the inputs of
+ * the scores in fp16 (u = 2^-11): the LN1 output feeding the QKV product,
+ * a copy of W_qkv scaled by a power of two (2^k |w|max in [2^14, 2^15),
+ * undone in the product's epilogue), Q and K, and the score gradients dS
+ * (scaled by a power of two from a bound on max_r |dO_r| max |V|, undone in
+ * the dQ and dK epilogues).  V, P, O and every gradient stay bf16.  A value
+ * of the LN1 output or of Q or K beyond 65504 in magnitude raises
+ * TP3D_ERANGE (read with tp3d_sync_status); magnitudes below fp16's normal
+ * range (2^-14) keep an absolute precision of 2^-25 there.                   */
 typedef struct {
   int32_t q, batch, seq, hidden, heads, ffn;
   int32_t dtype; /* tp3d_dtype; TP3D_BF16 only */

@@ -16,8 +16,15 @@ layer, whose activations and gradients are stored in bf16 between steps
 (unit roundoff u = 2^-9), the element-wise metric of a tensor with n
 elements and k independent roundings on its path grows like
 sqrt(2 ln n) * sqrt(k) * u (about 1-3e-2 for n = 1e5..1e7, k = 2..4) from
-rounding alone; it is bounded at LAYER_ELEM_TOL there as a detector of
-localised errors, while max_rel_err and fro_err carry the 1e-2 bar.
+rounding alone; max_rel_err and fro_err carry the 1e-2 bar there, and the
+element-wise metric is a detector of localised errors, bounded at what the
+layer measures plus a margin of 1.3x:
+  LAYER_ELEM_TOL: 0.035 is the largest over the ordinary layer cases (on
+    dW_qkv, whose columns sum the most rounded products), so 0.045;
+  LAYER_ELEM_TOL_PEAKED: with sharply peaked attention (scores of rms 6 and
+    more) dX is heavy-tailed (max |dX| / rms(dX) about 9) and its largest
+    absolute error, 0.0062 max |dX|, falls on an element below the RMS
+    floor, which reads as 0.058; so 0.075.
 """
 from __future__ import annotations
 
@@ -53,4 +60,5 @@ def fro_err(got, want) -> float:
 
 BF16_TOL = 1e-2
 F32_TOL = 1e-4
-LAYER_ELEM_TOL = 5e-2
+LAYER_ELEM_TOL = 0.045
+LAYER_ELEM_TOL_PEAKED = 0.075

@@ -39,7 +39,8 @@ __all__ = [
 ]
 
 STATUS = {0: "TP3D_OK", 1: "TP3D_EINVAL", 2: "TP3D_ESHAPE", 3: "TP3D_EALIGN", 4: "TP3D_EDTYPE",
-          5: "TP3D_ECUDA", 6: "TP3D_ETIMEOUT", 7: "TP3D_EUNSUPPORTED", 8: "TP3D_EOVERLAP"}
+          5: "TP3D_ECUDA", 6: "TP3D_ETIMEOUT", 7: "TP3D_EUNSUPPORTED", 8: "TP3D_EOVERLAP",
+          9: "TP3D_ERANGE"}
 TP3D_F32, TP3D_BF16 = 0, 1
 CUBE_A, CUBE_B, CUBE_C, CUBE_B_SWAP, ROW, COL, BLOCK2D, REPLICATED = range(8)
 TP3D_SPEC_R, TP3D_SPEC_S0, TP3D_SPEC_S1, TP3D_SPEC_S01 = range(4)

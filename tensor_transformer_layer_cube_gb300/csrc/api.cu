@@ -138,6 +138,7 @@ const char* tp3d_status_string(tp3d_status s) {
     case TP3D_ETIMEOUT: return "a bounded device-side wait ran out";
     case TP3D_EUNSUPPORTED: return "unsupported configuration";
     case TP3D_EOVERLAP: return "output overlaps an input";
+    case TP3D_ERANGE: return "a value on the fp16 score path beyond fp16's range";
   }
   return "unknown status";
 }

@@ -7,6 +7,14 @@
 // first linear): head t of sequence b is the window rows [b*s, +s) x columns
 // [t*d, +d) (Q), [h + t*d, +d) (K), [2h + t*d, +d) (V).
 //
+// Q and K arrive in fp16 (the layer writes them so: the softmax's
+// sensitivity to its scores' inputs grows with the scores' magnitude, and
+// fp16 carries 3 more significant bits than bf16); V, O and dO are bf16.
+// Every product takes both operands in one type: S = Q K^T in fp16, the score
+// gradients dS in fp16 for dQ = dS K and dK = dS^T Q (scaled by a power of
+// two sigma that keeps them inside fp16's range, undone when dQ and dK are
+// stored), P in bf16 for O = P V and dV = P^T dO, dP = dO V^T in bf16.
+//
 // Three persistent tcgen05 kernels, 128-row tiles, warp 0 = TMA
 // producer, warp 1 = MMA issuer (and TMEM owner), then one thread per tile
 // row (TMEM lane) for the softmax arithmetic:
@@ -98,6 +106,31 @@ __device__ __forceinline__ uint4 pack8f(const float* f) {
   for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
   return v;
 }
+__device__ __forceinline__ uint4 pack8h(const float* f) {
+  uint4 v;
+  __half2* h = reinterpret_cast<__half2*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+  return v;
+}
+
+// The scale sigma of the fp16 score gradients.  With P <= 1 (up to rounding),
+// |dP_rk| <= |dO_r| |V_k| and |delta_r| = |dO_r . O_r| <= |dO_r| max_k |V_k|
+// (O_r is a convex combination of the V rows), and |V_k| <= sqrt(d) max |V|,
+// so (Euclidean norms over a head's d columns)
+//   |dS_rk| <= B = 2.1 scale sqrt(d) max_r |dO_r| max |V|.
+// sigma = 2^(13 - e) for B < 2^e keeps sigma |dS| below 2^13, a factor 8
+// inside fp16's range, and its largest values far above fp16's normal
+// minimum; sigma = 1 when B is 0 or not finite.  dmax[0] holds max |dO_r|^2
+// (rows and heads), dmax[1] max |V| over every element, as the bits of
+// non-negative floats.
+__device__ __forceinline__ float ds_sigma(const unsigned* dmax, float scale, int64_t d) {
+  const float b = 2.1f * scale * sqrtf((float)d) * sqrtf(__uint_as_float(dmax[0])) * __uint_as_float(dmax[1]);
+  if (!(b > 0.0f) || !(b <= 3.0e38f)) return 1.0f;
+  int e;
+  frexpf(b, &e);  // b = m 2^e, m in [0.5, 1)
+  return ldexpf(1.0f, 13 - e);
+}
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Ctx& c, int* err, int lane) {
   bool ok = lane == 0 ? mbar_wait(bar, parity, c.abort_flag, err) : false;
@@ -113,13 +146,13 @@ __device__ __forceinline__ uint32_t tmem_row(uint32_t tmem, int quarter, uint32_
   return tmem + ((uint32_t)(quarter * 32) << 16) + col;
 }
 
-// store 32 fp32 values as bf16 to global row pointer + column offset (16-byte aligned)
-__device__ __forceinline__ void store_row32(bf16* dst, const uint32_t (&r)[32]) {
+// store 32 fp32 values times mul as bf16 to global row pointer + column offset (16-byte aligned)
+__device__ __forceinline__ void store_row32(bf16* dst, const uint32_t (&r)[32], float mul = 1.0f) {
 #pragma unroll
   for (int v = 0; v < 4; ++v) {
     float f[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(r[v * 8 + e]);
+    for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(r[v * 8 + e]) * mul;
     *reinterpret_cast<uint4*>(dst + v * 8) = pack8f(f);
   }
 }
@@ -247,8 +280,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
     } else if (warp == 1 && lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      const uint32_t id_s = idesc_bf16_f32(TR, TR, 0, 0);
-      const uint32_t id_o = idesc_bf16_f32(TR, (int)A.d, 0, 1);
+      const uint32_t id_s = idesc_f16_f32(TR, TR, 0, 0);       // S = Q K^T, fp16
+      const uint32_t id_o = idesc_bf16_f32(TR, (int)A.d, 0, 1);  // O += P V, bf16
       const int ks_d = (int)(A.d / 16);
       uint32_t n = 0, ic = 0;
       uint32_t sc[2] = {0, 0}, pc[2] = {0, 0}, oc[2] = {0, 0};
@@ -439,7 +472,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mqkv, const __grid_constant__ CUtensorMap mo,
                          const AttnProblem A, const float* __restrict__ lse, const float* __restrict__ delta,
-                         bf16* __restrict__ dqkv) {
+                         const unsigned* __restrict__ dmax, bf16* __restrict__ dqkv) {
   extern __shared__ uint8_t smem_raw[];
   const Ctx c = setup_smem(smem_raw);
   const uint32_t sK = c.base, sV = c.base + kTile;
@@ -495,8 +528,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t id_s = idesc_bf16_f32(TR, TR, 0, 0);
-      const uint32_t id_acc = idesc_bf16_f32(TR, (int)A.d, 1, 1);  // A = P^T or dS^T, read transposed
+      const uint32_t id_s = idesc_f16_f32(TR, TR, 0, 0);           // S = Q K^T, fp16
+      const uint32_t id_dp = idesc_bf16_f32(TR, TR, 0, 0);          // dP = dO V^T, bf16
+      const uint32_t id_dv = idesc_bf16_f32(TR, (int)A.d, 1, 1);    // dV += P^T dO, bf16 (P^T read transposed)
+      const uint32_t id_dk = idesc_f16_f32(TR, (int)A.d, 1, 1);     // dK += dS^T Q, fp16 (dS^T read transposed)
       const int ks_d = (int)(A.d / 16);
       uint32_t n = 0, ic = 0;
       bool ok = true;
@@ -507,7 +542,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!mbar_wait(st_empty, (m & 1) ^ 1, c.abort_flag, A.err)) return false;
         tc_fence_after();
         mma_tile(tmem, sQ[sm], false, sK, false, ks_d, id_s, false);
-        mma_tile(tmem + 128u, sdO[sm], false, sV, false, ks_d, id_s, false);
+        mma_tile(tmem + 128u, sdO[sm], false, sV, false, ks_d, id_dp, false);
         if (last) umma_commit(kv_empty);  // the item's K and V are no longer read
         umma_commit(st_full);
         return true;
@@ -521,14 +556,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!(ok = mbar_wait(pds_full, 0, c.abort_flag, A.err))) break;
           if (it == 0 && !(ok = mbar_wait(acc_empty, (ic & 1) ^ 1, c.abort_flag, A.err))) break;
           tc_fence_after();
-          mma_tile(tmem + 256u, sPdS, true, sdO[s], true, TR / 16, id_acc, it > 0);  // dV += P^T dO
+          mma_tile(tmem + 256u, sPdS, true, sdO[s], true, TR / 16, id_dv, it > 0);  // dV += P^T dO
           umma_commit(pds_empty);
           // the next query tile's S and dP go ahead of this tile's dK, so they
           // are computed while the element-wise warps form dS
           if (it + 1 < niter && !(ok = issue_sdp(n + 1, it + 2 == niter))) break;
           if (!(ok = mbar_wait(pds_full, 1, c.abort_flag, A.err))) break;
           tc_fence_after();
-          mma_tile(tmem + 256u + (uint32_t)A.d, sPdS, true, sQ[s], true, TR / 16, id_acc, it > 0);  // dK += dS^T Q
+          mma_tile(tmem + 256u + (uint32_t)A.d, sPdS, true, sQ[s], true, TR / 16, id_dk, it > 0);  // dK += dS^T Q
           umma_commit(pds_empty);
           umma_commit(r_empty(s));
         }
@@ -543,6 +578,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int half = (warp - 2) >> 2;  // key columns [64 half, +64) of the tile
     const int r = quarter * 32 + lane;
     const float sl2 = A.scale * kLog2e;
+    const float sigma = ds_sigma(dmax, A.scale, A.d), dscale = A.scale * sigma;
     uint32_t n = 0, ic = 0;
     bool ok = true;
     for (int64_t rd = 0, w = snake_item(0); w < items && ok; w = snake_item(++rd), ++ic) {
@@ -589,7 +625,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         warp_arrive(pds_full, lane);
-        // dS = P (dP - delta) * scale from the bf16 P in registers
+        // sigma dS = P (dP - delta) * scale * sigma from the bf16 P in registers, as fp16
         {
           uint32_t wv[2][32];
 #pragma unroll
@@ -603,9 +639,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
             for (int e2 = 0; e2 < 16; ++e2) {
               const float2 p2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[i][e2]));
-              const float d0 = p2.x * (__uint_as_float(wv[i][2 * e2]) - dr) * A.scale;
-              const float d1 = p2.y * (__uint_as_float(wv[i][2 * e2 + 1]) - dr) * A.scale;
-              const __nv_bfloat162 h2 = __floats2bfloat162_rn(d0, d1);
+              const float d0 = p2.x * (__uint_as_float(wv[i][2 * e2]) - dr) * dscale;
+              const float d1 = p2.y * (__uint_as_float(wv[i][2 * e2 + 1]) - dr) * dscale;
+              const __half2 h2 = __floats2half2_rn(d0, d1);
               pk[i][e2] = *reinterpret_cast<const uint32_t*>(&h2);
             }
           }
@@ -625,11 +661,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bf16* dst = dqkv + A.qkv.block_base((int32_t)br, (int32_t)bc) + (grow - br * A.qkv.bh) * A.qkv.bw +
                     (gcol - bc * A.qkv.bw);
         const int nd = (int)(A.d / 64);  // this warp's 32-column chunks: its half of the d columns
+        const float mul = which == 0 ? 1.0f : 1.0f / sigma;  // dK was accumulated from sigma dS
         for (int cc = half * nd; cc < half * nd + nd; ++cc) {
           uint32_t v[32];
           tmem_ld_32x32b_x32(tmem_row(tmem, quarter, 256u + (uint32_t)(which * A.d) + cc * 32), v);
           tmem_ld_wait();
-          store_row32(dst + cc * 32, v);
+          store_row32(dst + cc * 32, v, mul);
         }
       }
       tc_fence_before();
@@ -651,7 +688,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap mqkv, const __grid_constant__ CUtensorMap mo,
                        const AttnProblem A, const float* __restrict__ lse, const float* __restrict__ delta,
-                       bf16* __restrict__ dqkv) {
+                       const unsigned* __restrict__ dmax, bf16* __restrict__ dqkv) {
   extern __shared__ uint8_t smem_raw[];
   const Ctx c = setup_smem(smem_raw);
   const uint32_t sQ = c.base, sdO = c.base + kTile;
@@ -707,8 +744,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t id_s = idesc_bf16_f32(TR, TR, 0, 0);
-      const uint32_t id_acc = idesc_bf16_f32(TR, (int)A.d, 0, 1);
+      const uint32_t id_s = idesc_f16_f32(TR, TR, 0, 0);           // S = Q K^T, fp16
+      const uint32_t id_dp = idesc_bf16_f32(TR, TR, 0, 0);          // dP = dO V^T, bf16
+      const uint32_t id_acc = idesc_f16_f32(TR, (int)A.d, 0, 1);    // dQ += dS K, fp16
       const int ks_d = (int)(A.d / 16);
       uint32_t n = 0, ic = 0;
       bool ok = true;
@@ -721,7 +759,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!(ok = mbar_wait(s_empty, (n & 1) ^ 1, c.abort_flag, A.err))) break;
           tc_fence_after();
           mma_tile(tmem, sQ, false, sK[s], false, ks_d, id_s, false);          // S = Q K^T
-          mma_tile(tmem + 128u, sdO, false, sV[s], false, ks_d, id_s, false);  // dP = dO V^T
+          mma_tile(tmem + 128u, sdO, false, sV[s], false, ks_d, id_dp, false);  // dP = dO V^T
           if (it == niter - 1) umma_commit(qo_empty);
           umma_commit(s_full);
           if (!(ok = mbar_wait(ds_full, n & 1, c.abort_flag, A.err))) break;
@@ -742,6 +780,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int half = (warp - 2) >> 2;  // key columns [64 half, +64) of the tile
     const int r = quarter * 32 + lane;
     const float sl2 = A.scale * kLog2e;
+    const float sigma = ds_sigma(dmax, A.scale, A.d), dscale = A.scale * sigma;
     uint32_t n = 0, ic = 0;
     bool ok = true;
     for (int64_t rd = 0, w = snake_item(0); w < items && ok; w = snake_item(++rd), ++ic) {
@@ -767,9 +806,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int e = 0; e < 8; ++e) {
               const int k = cc * 32 + g * 8 + e;
               const float p = (!diag || k <= r) ? ex2_approx(fmaf(__uint_as_float(v[g * 8 + e]), sl2, -l2)) : 0.0f;
-              f[e] = p * (__uint_as_float(wv[g * 8 + e]) - dr) * A.scale;
+              f[e] = p * (__uint_as_float(wv[g * 8 + e]) - dr) * dscale;
             }
-            st_tile8(pdS, r, cc * 4 + g, pack8f(f));
+            st_tile8(pdS, r, cc * 4 + g, pack8h(f));  // sigma dS, fp16
           }
         }
         fence_proxy_async_smem();
@@ -785,11 +824,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       bf16* dst = dqkv + A.qkv.block_base((int32_t)br, (int32_t)bc) + (grow - br * A.qkv.bh) * A.qkv.bw +
                   (gcol - bc * A.qkv.bw);
       const int nd = (int)(A.d / 64);  // this warp's half of the d columns
+      const float inv_sigma = 1.0f / sigma;  // dQ was accumulated from sigma dS
       for (int cc = half * nd; cc < half * nd + nd; ++cc) {
         uint32_t v[32];
         tmem_ld_32x32b_x32(tmem_row(tmem, quarter, 256u + cc * 32), v);
         tmem_ld_wait();
-        store_row32(dst + cc * 32, v);
+        store_row32(dst + cc * 32, v, inv_sigma);
       }
       tc_fence_before();
       warp_arrive(acc_empty, lane);
@@ -806,13 +846,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // delta[z*s + r] = sum over the head's d columns of dO * O.  One warp per
 // token row: 16-byte loads, 256 columns (every head in them) per step, eight
 // steps in flight; the G = d/8 lanes that hold one head reduce with shuffles.
+// The same pass takes dmax0 = max over rows and heads of |dO_r|^2 for the
+// bound that scales the score gradients (ds_sigma): each warp keeps a
+// running maximum, the CTA combines its warps' in shared memory and takes
+// one atomic max (non-negative floats order as their bits; zero on entry).
 template <int G>
 __global__ void __launch_bounds__(256) attn_delta_kernel(const AttnProblem A, const bf16* __restrict__ O,
-                                                         const bf16* __restrict__ dO, float* __restrict__ delta) {
+                                                         const bf16* __restrict__ dO, float* __restrict__ delta,
+                                                         unsigned* __restrict__ dmax0) {
   constexpr int U = 8;
+  __shared__ float red[8];
   const int lane = threadIdx.x & 31;
   const int64_t M = A.Z / A.H * A.s;  // token rows
   const int64_t nw = (int64_t)gridDim.x * 8;
+  float mdo = 0.0f;
   for (int64_t tok = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); tok < M; tok += nw) {
     const int64_t b = tok / A.s, rr = tok - b * A.s;
     const int64_t br = tok / A.o.bh, rin = tok - br * A.o.bh;
@@ -831,7 +878,7 @@ __global__ void __launch_bounds__(256) attn_delta_kernel(const AttnProblem A, co
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int64_t col = c0 + u * 256 + lane * 8;
-        float acc = 0.0f;
+        float acc = 0.0f, sg = 0.0f;
         if (col < A.h) {
           const __nv_bfloat162* ah = reinterpret_cast<const __nv_bfloat162*>(&a[u]);
           const __nv_bfloat162* gh = reinterpret_cast<const __nv_bfloat162*>(&g[u]);
@@ -839,13 +886,27 @@ __global__ void __launch_bounds__(256) attn_delta_kernel(const AttnProblem A, co
           for (int e = 0; e < 4; ++e) {
             const float2 x = __bfloat1622float2(ah[e]), y = __bfloat1622float2(gh[e]);
             acc += x.x * y.x + x.y * y.y;
+            sg += y.x * y.x + y.y * y.y;
           }
         }
 #pragma unroll
-        for (int o = G / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        for (int o = G / 2; o > 0; o >>= 1) {
+          acc += __shfl_xor_sync(0xffffffffu, acc, o);
+          sg += __shfl_xor_sync(0xffffffffu, sg, o);
+        }
         if ((lane & (G - 1)) == 0 && col < A.h) delta[(b * A.H + col / A.d) * A.s + rr] = acc;
+        mdo = fmaxf(mdo, sg);
       }
     }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mdo = fmaxf(mdo, __shfl_xor_sync(0xffffffffu, mdo, o));
+  if (lane == 0) red[threadIdx.x >> 5] = mdo;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int k = 1; k < 8; ++k) mdo = fmaxf(mdo, red[k]);
+    atomicMax(dmax0, __float_as_uint(mdo));
   }
 }
 
@@ -902,7 +963,8 @@ tp3d_status launch_attn_fwd(const tp3d_ctx* ctx, const AttnProblem& A, const voi
 }
 
 tp3d_status launch_attn_bwd(const tp3d_ctx* ctx, const AttnProblem& A, const void* qkv, const void* o,
-                            const void* dO, const float* lse, float* delta, void* dqkv, cudaStream_t s) {
+                            const void* dO, const float* lse, float* delta, unsigned* dmax, void* dqkv,
+                            cudaStream_t s) {
   TP3D_TRY(check(A));
   CUtensorMap mq, mo;
   TP3D_TRY(tile_map(&mq, A.qkv, qkv));
@@ -910,20 +972,20 @@ tp3d_status launch_attn_bwd(const tp3d_ctx* ctx, const AttnProblem& A, const voi
   const int64_t tokens = A.Z / A.H * A.s;
   int64_t dgrid = (tokens + 7) / 8;
   if (dgrid > (int64_t)ctx->num_sms * 8) dgrid = (int64_t)ctx->num_sms * 8;
+  TP3D_CUDA_TRY(cudaMemsetAsync(dmax, 0, sizeof(unsigned), s));  // dmax[0]; dmax[1] came with Q, K, V
+  const bf16 *ob = static_cast<const bf16*>(o), *gb = static_cast<const bf16*>(dO);
   if (A.d == 128)
-    attn_delta_kernel<16><<<(unsigned)dgrid, 256, 0, s>>>(A, static_cast<const bf16*>(o), static_cast<const bf16*>(dO),
-                                                          delta);
+    attn_delta_kernel<16><<<(unsigned)dgrid, 256, 0, s>>>(A, ob, gb, delta, dmax);
   else
-    attn_delta_kernel<8><<<(unsigned)dgrid, 256, 0, s>>>(A, static_cast<const bf16*>(o), static_cast<const bf16*>(dO),
-                                                         delta);
+    attn_delta_kernel<8><<<(unsigned)dgrid, 256, 0, s>>>(A, ob, gb, delta, dmax);
   TP3D_CUDA_TRY(cudaGetLastError());
   TP3D_CUDA_TRY(cudaFuncSetAttribute(attn_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem));
   TP3D_CUDA_TRY(cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem));
   const int64_t items = A.Z * (A.s / TR);
   const unsigned grid = (unsigned)(items < ctx->num_sms ? items : ctx->num_sms);
-  attn_bwd_dkdv_kernel<<<grid, kBwdThreads, kSmem, s>>>(mq, mo, A, lse, delta, static_cast<bf16*>(dqkv));
+  attn_bwd_dkdv_kernel<<<grid, kBwdThreads, kSmem, s>>>(mq, mo, A, lse, delta, dmax, static_cast<bf16*>(dqkv));
   TP3D_CUDA_TRY(cudaGetLastError());
-  attn_bwd_dq_kernel<<<grid, kBwdThreads, kSmem, s>>>(mq, mo, A, lse, delta, static_cast<bf16*>(dqkv));
+  attn_bwd_dq_kernel<<<grid, kBwdThreads, kSmem, s>>>(mq, mo, A, lse, delta, dmax, static_cast<bf16*>(dqkv));
   return cudaGetLastError() == cudaSuccess ? TP3D_OK : TP3D_ECUDA;
 }
 

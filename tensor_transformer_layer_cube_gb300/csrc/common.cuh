@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -340,5 +341,15 @@ TP3D_HD constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn_major, int b_mn
          (static_cast<uint32_t>(b_mn_major) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
 }
+// The same with fp16 A and B (format code 0 in bits 7-9 and 10-12).  A and B
+// of one product always share a type: both codes come from one descriptor.
+TP3D_HD constexpr uint32_t idesc_f16_f32(int M, int N, int a_mn_major, int b_mn_major) {
+  return (1u << 4) | (static_cast<uint32_t>(a_mn_major) << 15) | (static_cast<uint32_t>(b_mn_major) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Largest finite fp16 magnitude.  Values headed for an fp16 buffer beyond it
+// raise TP3D_ERANGE.
+constexpr float kHalfMax = 65504.0f;
 
 }  // namespace tp3d

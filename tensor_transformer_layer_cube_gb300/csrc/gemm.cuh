@@ -55,6 +55,12 @@ struct Epilogue {
   int32_t act;          // EpiAct
   int32_t out_f32;      // C stored as fp32 instead of the input dtype
   float alpha;          // scale of the product
+  const float* alpha_dev;  // or null: a device scalar that multiplies alpha
+  int64_t f16_cols;     // C's columns below this are written as fp16 (a value
+                        // beyond fp16's range raises TP3D_ERANGE), the rest as
+                        // bf16; a multiple of 32
+  unsigned* amax_out;   // or null: atomic max of |C| over the columns from
+                        // f16_cols on, as the bits of a non-negative float
   const void* bias;     // vector indexed by C's stored column, or null
   const void* resid;    // matrix in C's layout added after the activation, or null
   const void* gin;      // EPI_GELU_BWD: the GELU input, in C's layout
@@ -63,6 +69,7 @@ struct Epilogue {
 
 struct GemmProblem {
   int32_t Z, Hz;
+  int32_t in_f16;             // A and B hold fp16 (else bf16); both always share a type
   int64_t M, N, K;            // per-batch extents
   int64_t segM, segN, segK;   // segment lengths (divide M, N, K)
   int32_t causal;             // Causal

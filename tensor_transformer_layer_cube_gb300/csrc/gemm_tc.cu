@@ -160,6 +160,26 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
   for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
   return v;
 }
+// max over the warp, then one atomic max (non-negative floats order as their bits)
+__device__ __forceinline__ void warp_amax(float m, unsigned* out, int lane) {
+  if (!out) return;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) atomicMax(out, __float_as_uint(m));
+}
+// fp16 form; a value beyond fp16's finite range raises TP3D_ERANGE
+__device__ __forceinline__ uint4 pack8h(const float* f, int* err) {
+  uint4 v;
+  __half2* h = reinterpret_cast<__half2*>(&v);
+  float mx = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    h[i] = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+    mx = fmaxf(mx, fmaxf(fabsf(f[2 * i]), fabsf(f[2 * i + 1])));
+  }
+  if (mx > kHalfMax) raise_error(err, TP3D_ERANGE);
+  return v;
+}
 
 
 // One tile's epilogue for the calling epilogue warp (32 rows x BN/2 columns
@@ -177,13 +197,16 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
 // A chunk crossing the segment's edge is written element-wise under a mask.
 // After its last TMEM load the warp arrives on `tempty` (in the peer CTA when
 // `tempty_remote`, a shared::cluster address).
-template <int BN>
+// H16: the problem has fp16 output columns or a device-resident scale
+// (instantiated apart, so the plain epilogue's code is left as it is: its
+// speed answers to code layout).
+template <int BN, bool H16>
 __device__ __forceinline__ void epilogue_tile(const GemmProblem& P, const TileInfo& T, bool any_k, int buf,
                                               uint32_t tmem_base, int warp, int lane, uint8_t* stg,
                                               const CUtensorMap* mapC, const CUtensorMap* mapZ,
                                               const CUtensorMap* mapX, uint32_t aux_bar, uint32_t& aux_phase,
                                               volatile int* abort_flag, uint32_t tempty, bool tempty_remote,
-                                              uint32_t& stores) {
+                                              uint32_t& stores, float& cmax) {
   const void* aux = P.epi.resid ? P.epi.resid : P.epi.gin;
   const bool aux_ok = aux != nullptr && P.epi.zsave == nullptr && !P.epi.out_f32;
   const int quarter = warp & 3;
@@ -218,7 +241,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmProblem& P, const TileIn
   };
   if (aux_ok && fast(0)) aux_issue(0);
   const __nv_bfloat16* bias = static_cast<const __nv_bfloat16*>(P.epi.bias);
-  const bool scaled = P.epi.alpha != 1.0f;
+  const float alpha = H16 && P.epi.alpha_dev ? P.epi.alpha * *P.epi.alpha_dev : P.epi.alpha;
+  const bool scaled = alpha != 1.0f;
 #pragma unroll 1
   for (int cc = 0; cc < CH; ++cc) {
     const int ch = half * CH + cc;
@@ -243,6 +267,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmProblem& P, const TileIn
     }
     const int64_t n = chunk_n(cc);
     if (n >= T.n_end) continue;
+    // fp16 output for the chunk's 32 columns (the bound is a multiple of 32)
+    const bool h16 = H16 && gn0 + (n - T.n0) < P.epi.f16_cols;
     if (fast(cc)) {
       // ---------------------------------------------------------- fast path
       // sv: the auxiliary input read from staging, or the pre-activation to
@@ -275,7 +301,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmProblem& P, const TileIn
         for (int e = 0; e < 8; ++e) x[e] = any_k ? __uint_as_float(r[v * 8 + e]) : 0.0f;
         if (scaled) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] *= P.epi.alpha;
+          for (int e = 0; e < 8; ++e) x[e] *= alpha;
         }
         if (bias) {
           float bb[8];
@@ -300,7 +326,11 @@ __device__ __forceinline__ void epilogue_tile(const GemmProblem& P, const TileIn
           for (int e = 0; e < 8; ++e) x[e] += rr[e];
         }
         if (!f32) {
-          yv[v] = pack8(x);
+          yv[v] = h16 ? pack8h(x, P.err) : pack8(x);
+          if (H16 && !h16) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) cmax = fmaxf(cmax, fabsf(x[e]));
+          }
         } else {
           *reinterpret_cast<float4*>(stg + lane * 128 + (((2 * v) ^ (lane & 7)) << 4)) = make_float4(x[0], x[1], x[2], x[3]);
           *reinterpret_cast<float4*>(stg + lane * 128 + (((2 * v + 1) ^ (lane & 7)) << 4)) = make_float4(x[4], x[5], x[6], x[7]);
@@ -342,7 +372,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmProblem& P, const TileIn
         const int64_t off = row_base + (nv - T.n0);
         float x[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = any_k ? __uint_as_float(r[v * 8 + e]) * P.epi.alpha : 0.0f;
+        for (int e = 0; e < 8; ++e) x[e] = any_k ? __uint_as_float(r[v * 8 + e]) * alpha : 0.0f;
         if (bias) {
           float bb[8];
           unpack8(*reinterpret_cast<const uint4*>(bias + (gn0 + (nv - T.n0))), bb);
@@ -366,7 +396,12 @@ __device__ __forceinline__ void epilogue_tile(const GemmProblem& P, const TileIn
           for (int e = 0; e < 8; ++e) x[e] += rr[e];
         }
         if (!f32) {
-          *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(const_cast<void*>(P.c.ptr)) + off) = pack8(x);
+          *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(const_cast<void*>(P.c.ptr)) + off) =
+              h16 ? pack8h(x, P.err) : pack8(x);
+          if (H16 && !h16) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) cmax = fmaxf(cmax, fabsf(x[e]));
+          }
         } else {
           float4* o = reinterpret_cast<float4*>(static_cast<float*>(const_cast<void*>(P.c.ptr)) + off);
           o[0] = make_float4(x[0], x[1], x[2], x[3]);
@@ -377,7 +412,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmProblem& P, const TileIn
   }
 }
 
-template <int BN>
+template <int BN, bool H16>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                    const __grid_constant__ CUtensorMap mapC, const __grid_constant__ CUtensorMap mapZ,
@@ -546,7 +581,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      const uint32_t idesc = idesc_bf16_f32(BM, BN, a_mn ? 1 : 0, b_mn ? 1 : 0);
+      const uint32_t idesc = P.in_f16 ? idesc_f16_f32(BM, BN, a_mn ? 1 : 0, b_mn ? 1 : 0)
+                                      : idesc_bf16_f32(BM, BN, a_mn ? 1 : 0, b_mn ? 1 : 0);
       uint32_t it = 0, tc = 0;
       bool ok = true;
       for (int64_t t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
@@ -605,6 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t stores = 0;  // TMA stores this warp has issued from its staging buffer
     uint32_t aux_phase = 0;
     uint8_t* stg = stage_out + (warp - 2) * Cfg::STAGE_OUT;
+    float cmax = 0.0f;  // H16: the largest |C| of the bf16 columns this warp stored
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
       TileInfo T;
       decode_tile<BN>(P, t, T);
@@ -620,12 +657,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       tc_fence_after();
-      epilogue_tile<BN>(P, T, any_k, buf, tmem_base, warp, lane, stg, &mapC, &mapZ, &mapX, aux_bar(warp - 2),
-                        aux_phase, abort_flag, tempty_bar(buf), false, stores);
+      epilogue_tile<BN, H16>(P, T, any_k, buf, tmem_base, warp, lane, stg, &mapC, &mapZ, &mapX, aux_bar(warp - 2),
+                             aux_phase, abort_flag, tempty_bar(buf), false, stores, cmax);
       ++tc;
     }
     if (lane == 0) bulk_wait_all();
     __syncwarp();
+    if (H16) warp_amax(cmax, P.epi.amax_out, lane);
   }
 
   tc_fence_before();
@@ -694,7 +732,7 @@ __device__ __forceinline__ int64_t total_pair_tiles(const GemmProblem& P) {
   return (int64_t)P.Z * (P.M / P.segM) * ceil_div(P.segM, 256) * (P.N / P.segN) * ceil_div(P.segN, 256);
 }
 
-template <int KD>
+template <int KD, bool H16>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                     const __grid_constant__ CUtensorMap mapC, const __grid_constant__ CUtensorMap mapZ,
@@ -895,7 +933,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       // ---------------------------------------------------------- MMA issuer (even CTA)
-      const uint32_t idesc = idesc_bf16_f32(256, BN, a_mn ? 1 : 0, b_mn ? 1 : 0);
+      const uint32_t idesc = P.in_f16 ? idesc_f16_f32(256, BN, a_mn ? 1 : 0, b_mn ? 1 : 0)
+                                      : idesc_bf16_f32(256, BN, a_mn ? 1 : 0, b_mn ? 1 : 0);
       // Stage 0's operand descriptors, built once: a stage, chunk or row step
       // adds its byte offset / 16 to the 14-bit address field (shared
       // addresses stay below 256 KiB, so the field never carries).  Fewer
@@ -956,6 +995,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t stores = 0;
     uint32_t aux_phase = 0;
     uint8_t* stg = stage_out + (warp - 2) * Cfg::STAGE_OUT;
+    float cmax = 0.0f;  // H16: the largest |C| of the bf16 columns this warp stored
     for (int64_t t = cid; t < ntiles; t += nclusters) {
       TileInfo T;
       decode_pair_tile(P, t, rank, T);
@@ -965,12 +1005,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       tc_fence_after();
-      epilogue_tile<BN>(P, T, true, buf, tmem_base, warp, lane, stg, &mapC, &mapZ, &mapX, aux_bar(warp - 2),
-                        aux_phase, abort_flag, map_to_cta(tempty_bar(buf), 0), true, stores);
+      epilogue_tile<BN, H16>(P, T, true, buf, tmem_base, warp, lane, stg, &mapC, &mapZ, &mapX, aux_bar(warp - 2),
+                             aux_phase, abort_flag, map_to_cta(tempty_bar(buf), 0), true, stores, cmax);
       ++tc;
     }
     if (lane == 0) bulk_wait_all();
     __syncwarp();
+    if (H16) warp_amax(cmax, P.epi.amax_out, lane);
   }
 
   tc_fence_before();
@@ -1027,7 +1068,7 @@ bool make_map_wide(CUtensorMap* m, const Grid& g, const void* ptr, uint32_t box_
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN>
+template <int BN, bool H16>
 tp3d_status launch(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t s) {
   using Cfg = TcCfg<BN>;
   CUtensorMap ma, mb, mc, mz, mx;
@@ -1047,17 +1088,17 @@ tp3d_status launch(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t s) {
     TP3D_TRY(make_map(&mx, P.c.g, aux, 32, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, CU_TENSOR_MAP_SWIZZLE_64B));
   else
     mx = mc;
-  TP3D_CUDA_TRY(cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM));
+  TP3D_CUDA_TRY(cudaFuncSetAttribute(gemm_tc_kernel<BN, H16>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM));
   const int64_t tpsM = (P.segM + BM - 1) / BM, tpsN = (P.segN + BN - 1) / BN;
   const int64_t ntiles = (int64_t)P.Z * (P.M / P.segM) * tpsM * (P.N / P.segN) * tpsN;
   if (ntiles <= 0) return TP3D_OK;
   const int grid = (int)(ntiles < ctx->num_sms ? ntiles : ctx->num_sms);
-  gemm_tc_kernel<BN><<<grid, kThreads, Cfg::SMEM, s>>>(ma, mb, mc, mz, mx, P);
+  gemm_tc_kernel<BN, H16><<<grid, kThreads, Cfg::SMEM, s>>>(ma, mb, mc, mz, mx, P);
   return cudaGetLastError() == cudaSuccess ? TP3D_OK : TP3D_ECUDA;
 }
 
 // CTA pairs that fit on the device at once (0 if the query fails).
-template <int KD>
+template <int KD, bool H16>
 int pair_clusters(const tp3d_ctx* ctx) {
   static int cached[64] = {};
   const int dev = ctx->device & 63;
@@ -1074,9 +1115,9 @@ int pair_clusters(const tp3d_ctx* ctx) {
   cfg.numAttrs = 1;
   cfg.gridDim = dim3(2 * (unsigned)(ctx->num_sms / 2));
   int n = 0;
-  if (cudaFuncSetAttribute(gemm_tc2_kernel<KD>, cudaFuncAttributeMaxDynamicSharedMemorySize, Tc2Cfg<KD>::SMEM) !=
-          cudaSuccess ||
-      cudaOccupancyMaxActiveClusters(&n, gemm_tc2_kernel<KD>, &cfg) != cudaSuccess || n < 1) {
+  if (cudaFuncSetAttribute(gemm_tc2_kernel<KD, H16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Tc2Cfg<KD>::SMEM) != cudaSuccess ||
+      cudaOccupancyMaxActiveClusters(&n, gemm_tc2_kernel<KD, H16>, &cfg) != cudaSuccess || n < 1) {
     (void)cudaGetLastError();
     cached[dev] = -1;
     return 0;
@@ -1085,7 +1126,7 @@ int pair_clusters(const tp3d_ctx* ctx) {
   return n;
 }
 
-template <int KD>
+template <int KD, bool H16>
 tp3d_status launch_pair(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t s) {
   using Cfg = Tc2Cfg<KD>;
   CUtensorMap ma, mb, mc, mz, mx;
@@ -1121,7 +1162,7 @@ tp3d_status launch_pair(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t 
   const int64_t ntiles = (int64_t)P.Z * (P.M / P.segM) * ((P.segM + 255) / 256) * (P.N / P.segN) *
                          ((P.segN + 255) / 256);
   if (ntiles <= 0) return TP3D_OK;
-  const int max_clusters = pair_clusters<KD>(ctx);
+  const int max_clusters = pair_clusters<KD, H16>(ctx);
   if (max_clusters < 1) return TP3D_ECUDA;
   // the kernel decodes tiles and shard coordinates in 32-bit arithmetic
   const int64_t lim = INT32_MAX;
@@ -1141,7 +1182,7 @@ tp3d_status launch_pair(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t 
   cfg.numAttrs = 1;
   const int64_t nc = ntiles < max_clusters ? ntiles : max_clusters;
   cfg.gridDim = dim3(2 * (unsigned)nc);
-  TP3D_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<KD>, ma, mb, mc, mz, mx, P, wide));
+  TP3D_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_tc2_kernel<KD, H16>, ma, mb, mc, mz, mx, P, wide));
   return TP3D_OK;
 }
 
@@ -1156,6 +1197,11 @@ tp3d_status gemm_bf16_tc(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t
   for (const Grid* g : gs)
     if (g->bw % 8 != 0) return TP3D_EALIGN;
   if (P.segM % 8 || P.segN % 8) return TP3D_EUNSUPPORTED;
+  // fp16 output columns: whole 32-column chunks, plain outputs only
+  if (P.epi.f16_cols < 0 || P.epi.f16_cols % 32 ||
+      ((P.epi.f16_cols > 0 || P.epi.amax_out) &&
+       (P.epi.out_f32 || P.epi.zsave || P.epi.resid || P.epi.gin || P.epi.act != EPI_NONE)))
+    return TP3D_EINVAL;
   // tile decode and the epilogue's block arithmetic run in 32 bits
   for (const Grid* g : gs)
     if (g->R > INT32_MAX || g->C > INT32_MAX) return TP3D_EUNSUPPORTED;
@@ -1179,9 +1225,13 @@ tp3d_status gemm_bf16_tc(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t
   const double c128 = waves(tiles(BM, 128), sms) * 0.5 / 0.45;
   const bool pairs_ok = P.causal == CAUSAL_NONE && P.segM >= 256 && P.segN >= 256;
   const double cpair = pairs_ok ? waves(tiles(256, 256), sms / 2) / 0.80 : 1e30;
-  if (cpair <= c256 && cpair <= c128)
-    return P.segK % 128 == 0 ? launch_pair<128>(ctx, P, s) : launch_pair<64>(ctx, P, s);
-  return c256 <= c128 ? launch<256>(ctx, P, s) : launch<128>(ctx, P, s);
+  const bool h16 = P.epi.f16_cols > 0 || P.epi.alpha_dev != nullptr || P.epi.amax_out != nullptr;
+  if (cpair <= c256 && cpair <= c128) {
+    if (P.segK % 128 == 0) return h16 ? launch_pair<128, true>(ctx, P, s) : launch_pair<128, false>(ctx, P, s);
+    return h16 ? launch_pair<64, true>(ctx, P, s) : launch_pair<64, false>(ctx, P, s);
+  }
+  if (c256 <= c128) return h16 ? launch<256, true>(ctx, P, s) : launch<256, false>(ctx, P, s);
+  return h16 ? launch<128, true>(ctx, P, s) : launch<128, false>(ctx, P, s);
 }
 
 tp3d_status plan_segments(GemmProblem& P) {

@@ -10,11 +10,22 @@
 // read by its definition (bias gradient = column sums over every row) and
 // §3.1.3's gamma gradient sum(dC * A-hat).
 //
-// Everything runs on the caller's stream: LayerNorm, the four linear GEMMs
-// (QKV, output projection + residual, W1 + GELU, W2 + residual) and the fused
-// causal attention forward; the backward's eight linear GEMMs, the fused
-// attention backward, LayerNorm backward and the column sums of the bias /
-// gamma / beta gradients.  Attention reads each (batch, head) window in
+// The scores' inputs are carried in fp16 (11 significant bits against bf16's
+// 8): the softmax backward magnifies their rounding by about the scores'
+// magnitude, which for sharply peaked attention takes bf16 storage of the LN1
+// output and of Q and K past 1e-2 of the exact layer.  So LN1 also writes an
+// fp16 copy of its output, W_qkv is converted to fp16 scaled by a power of
+// two (undone in the QKV product's epilogue), and that product stores Q and K
+// in fp16, V in bf16; the attention kernels take it from there.
+//
+// The forward launches LayerNorm, the four linear GEMMs (QKV, output
+// projection + residual, W1 + GELU, W2 + residual) and the fused causal
+// attention forward; the backward its eight linear GEMMs, the fused attention
+// backward, LayerNorm backward and the column sums of the bias / gamma / beta
+// gradients.  They run on the caller's stream, except independent work that
+// is forked onto the context's two side streams and joined back before the
+// call returns (the forward's W_qkv conversion; the backward's weight
+// gradients and column sums).  Attention reads each (batch, head) window in
 // place from the CUBE_C shards of the QKV matrix (attention.cu).
 #include <math.h>
 
@@ -39,6 +50,7 @@ struct Plan {
   float eps;
   // workspace offsets (bytes)
   size_t xn1, mean1, rstd1, qkv, lse, O, Hres, xn2, mean2, rstd2, z1, y1;  // saved by the forward
+  size_t xn1h, wqkvh, misc;  // fp16 score-path operands; misc: max |W_qkv|, 1/scale, max |dO_r|^2, max |V|
   size_t delta, dz1, dxn, dH, dO, dqkv, part, counters;                    // scratch
   size_t part_floats, part_db1, part_dbqkv, total;  // float offsets of db1's and dbqkv's partials
 };
@@ -92,6 +104,9 @@ tp3d_status make_plan(const tp3d_layer_cfg* c, Plan* p) {
   x.rstd2 = take(M * 4);
   x.z1 = take(M * f * 2);
   x.y1 = take(M * f * 2);
+  x.xn1h = take(M * h * 2);
+  x.wqkvh = take(3 * h * h * 2);
+  x.misc = take(256);
   x.delta = take(Z * s * 4);
   x.dz1 = take(M * f * 2);
   x.dxn = take(M * h * 2);
@@ -227,11 +242,29 @@ tp3d_status tp3d_layer_fwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_
 
   Grid gA;
   TP3D_TRY(make_grid(cube(TP3D_CUBE_A, q), M, h, &gA));
+  // The score path in fp16: W_qkv scaled by a power of two 2^k, the LN1
+  // output in bf16 (for the weight gradient) and fp16, Q and K in fp16.  The
+  // conversion of W_qkv runs on side stream 0 beside LN1 and is joined before
+  // the QKV product.
+  unsigned* misc = (unsigned*)W(p.misc);
+  float* inv_scale = (float*)(misc + 1);
+  TP3D_CUDA_TRY(cudaEventRecord(ctx->ev_fork, st));
+  TP3D_CUDA_TRY(cudaStreamWaitEvent(ctx->side[0], ctx->ev_fork, 0));
+  TP3D_TRY(launch_to_f16_scaled(ctx, w->w_qkv, 3 * h * h, misc, W(p.wqkvh), inv_scale, ctx->side[0]));
+  TP3D_CUDA_TRY(cudaEventRecord(ctx->ev_join[0], ctx->side[0]));
   // LN1
-  TP3D_TRY(launch_ln_fwd(ctx, gA, X, w->ln1_g, w->ln1_b, W(p.xn1), (float*)W(p.mean1), (float*)W(p.rstd1), p.eps, st));
-  // QKV = LN1(X) W_qkv + b_qkv   (y = 0: CUBE_A -> CUBE_C)
+  TP3D_TRY(launch_ln_fwd(ctx, gA, X, w->ln1_g, w->ln1_b, W(p.xn1), W(p.xn1h), (float*)W(p.mean1),
+                         (float*)W(p.rstd1), p.eps, st));
+  TP3D_CUDA_TRY(cudaStreamWaitEvent(st, ctx->ev_join[0], 0));
+  // QKV = LN1(X) W_qkv + b_qkv   (y = 0: CUBE_A -> CUBE_C): fp16 product, 2^-k applied
+  // in the epilogue, Q and K (columns below 2h) stored in fp16, V in bf16
   GemmProblem G;
-  TP3D_TRY(plan_linear(ctx, q, 0, M, h, 3 * h, W(p.xn1), w->w_qkv, w->b_qkv, 0, W(p.qkv), &G));
+  TP3D_TRY(plan_linear(ctx, q, 0, M, h, 3 * h, W(p.xn1h), W(p.wqkvh), w->b_qkv, 0, W(p.qkv), &G));
+  G.in_f16 = 1;
+  G.epi.alpha_dev = inv_scale;
+  G.epi.f16_cols = 2 * h;
+  G.epi.amax_out = misc + 3;  // max |V|, for the backward's bound on the score gradients
+  TP3D_CUDA_TRY(cudaMemsetAsync(misc + 3, 0, sizeof(unsigned), st));
   TP3D_TRY(gemm_bf16_tc(ctx, G, st));
   // causal attention per (batch, head), fused: O = softmax(Q K^T / sqrt(d)) V
   TP3D_TRY(launch_attn_fwd(ctx, attn_problem(p, ctx->d_err), W(p.qkv), W(p.O), (float*)W(p.lse), st));
@@ -240,8 +273,8 @@ tp3d_status tp3d_layer_fwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_
   G.epi.resid = X;
   TP3D_TRY(gemm_bf16_tc(ctx, G, st));
   // LN2, then Y1 = GELU(Z1), Z1 = LN2(H) W_1 + b_1 saved
-  TP3D_TRY(launch_ln_fwd(ctx, gA, W(p.Hres), w->ln2_g, w->ln2_b, W(p.xn2), (float*)W(p.mean2), (float*)W(p.rstd2),
-                         p.eps, st));
+  TP3D_TRY(launch_ln_fwd(ctx, gA, W(p.Hres), w->ln2_g, w->ln2_b, W(p.xn2), nullptr, (float*)W(p.mean2),
+                         (float*)W(p.rstd2), p.eps, st));
   TP3D_TRY(plan_linear(ctx, q, 0, M, h, f, W(p.xn2), w->w_1, w->b_1, 1, W(p.y1), &G));
   G.epi.zsave = W(p.z1);
   TP3D_TRY(gemm_bf16_tc(ctx, G, st));
@@ -342,7 +375,7 @@ tp3d_status tp3d_layer_bwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_
   TP3D_TRY(run(ctx, G, st));
   // attention backward, fused: dQ, dK, dV into dQKV (MP3D's C = A B^T and C = A^T B forms)
   TP3D_TRY(launch_attn_bwd(ctx, attn_problem(p, ctx->d_err), W(p.qkv), W(p.O), W(p.dO), (const float*)W(p.lse),
-                           (float*)W(p.delta), W(p.dqkv), st));
+                           (float*)W(p.delta), (unsigned*)W(p.misc) + 2, W(p.dqkv), st));
   // dWqkv, then dbqkv on side stream 1
   TP3D_TRY(fork_to(1));
   TP3D_TRY(plan_wgrad(ctx, q, 0, M, h, 3 * h, W(p.xn1), W(p.dqkv), g->w_qkv, &G));         // dWqkv = LN1(X)^T dQKV

@@ -43,12 +43,28 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
   return v;
 }
 
+// fp16 form of 8 values; a value beyond fp16's finite range raises TP3D_ERANGE
+__device__ __forceinline__ uint4 pack8h(const float* f, int* err) {
+  uint4 v;
+  __half2* h = reinterpret_cast<__half2*>(&v);
+  float mx = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    h[i] = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+    mx = fmaxf(mx, fmaxf(fabsf(f[2 * i]), fabsf(f[2 * i + 1])));
+  }
+  if (mx > kHalfMax) raise_error(err, TP3D_ERANGE);
+  return v;
+}
+
 using bf16 = __nv_bfloat16;
 
 // ------------------------------------------------------------------ LayerNorm
+// y16 (or null): the same output in fp16, in y's layout
 __global__ void __launch_bounds__(kThreads) ln_fwd_kernel(const Grid g, const bf16* __restrict__ x,
                                                           const bf16* __restrict__ gamma,
                                                           const bf16* __restrict__ beta, bf16* __restrict__ y,
+                                                          __half* __restrict__ y16, int* err,
                                                           float* __restrict__ mean, float* __restrict__ rstd,
                                                           float eps) {
   const int lane = threadIdx.x & 31;
@@ -93,6 +109,7 @@ __global__ void __launch_bounds__(kThreads) ln_fwd_kernel(const Grid g, const bf
 #pragma unroll
         for (int e = 0; e < 8; ++e) o[e] = (f[e] - mu) * rs * gg[e] + bb[e];
         q[v] = pack8(o);
+        if (y16) reinterpret_cast<uint4*>(y16 + off)[v] = pack8h(o, err);
       }
     }
     if (lane == 0) {
@@ -171,6 +188,7 @@ template <int NV>
 __global__ void __launch_bounds__(kThreads) ln_fwd_row_kernel(const Grid g, const bf16* __restrict__ x,
                                                               const bf16* __restrict__ gamma,
                                                               const bf16* __restrict__ beta, bf16* __restrict__ y,
+                                                              __half* __restrict__ y16, int* err,
                                                               float* __restrict__ mean, float* __restrict__ rstd,
                                                               float eps) {
   constexpr float invC = 1.0f / (float)(NV * 256);
@@ -208,12 +226,73 @@ __global__ void __launch_bounds__(kThreads) ln_fwd_row_kernel(const Grid g, cons
       unpack8(__ldg(reinterpret_cast<const uint4*>(beta + col)), bb);
 #pragma unroll
       for (int e = 0; e < 8; ++e) o[e] = (f[e] - mu) * rs * gg[e] + bb[e];
-      *reinterpret_cast<uint4*>(y + row_vec_off<NV>(g, br, rr, lane, i)) = pack8(o);
+      const int64_t off = row_vec_off<NV>(g, br, rr, lane, i);
+      *reinterpret_cast<uint4*>(y + off) = pack8(o);
+      if (y16) *reinterpret_cast<uint4*>(y16 + off) = pack8h(o, err);
     }
     if (lane == 0) {
       mean[r] = mu;
       rstd[r] = rs;
     }
+  }
+}
+
+// ------------------------------------------------------------------ bf16 -> scaled fp16
+// amax = max |x| over n bf16 values (n a multiple of 8), as the bits of a
+// non-negative float (integer order = float order), by an atomic max per CTA.
+__global__ void __launch_bounds__(kThreads) absmax_kernel(const bf16* __restrict__ x, int64_t n,
+                                                          unsigned* __restrict__ amax) {
+  __shared__ float red[kWarps];
+  float m = 0.0f;
+  const int64_t nv = n / 8;
+  for (int64_t v = (int64_t)blockIdx.x * kThreads + threadIdx.x; v < nv; v += (int64_t)gridDim.x * kThreads) {
+    float f[8];
+    unpack8(__ldg(reinterpret_cast<const uint4*>(x) + v), f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(f[e]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int k = 1; k < kWarps; ++k) m = fmaxf(m, red[k]);
+    atomicMax(amax, __float_as_uint(m));
+  }
+}
+
+// The power of two 2^k that puts amax in [2^14, 2^15) (1 for amax 0 or not
+// finite).  Every finite bf16 value w then has |w 2^k| <= 2^15, and w 2^k is
+// exact in fp16 when |w| >= amax 2^-28 (fp16's normal range holds bf16's 8
+// significant bits); smaller magnitudes keep an absolute error below
+// amax 2^-39.
+__device__ __forceinline__ int f16_scale_exp(float amax) {
+  if (!(amax > 0.0f) || !(amax <= 3.0e38f)) return 0;
+  int e;
+  frexpf(amax, &e);  // amax = m 2^e, m in [0.5, 1)
+  return 15 - e;
+}
+
+// y = fp16(x 2^k) with k from amax; inv_scale = 2^-k (written by one thread).
+// A non-finite amax raises TP3D_ERANGE.
+__global__ void __launch_bounds__(kThreads) to_f16_scaled_kernel(const bf16* __restrict__ x, int64_t n,
+                                                                 const unsigned* __restrict__ amax,
+                                                                 __half* __restrict__ y,
+                                                                 float* __restrict__ inv_scale, int* err) {
+  const float am = __uint_as_float(*amax);
+  const int k = f16_scale_exp(am);
+  const float sc = ldexpf(1.0f, k);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    *inv_scale = ldexpf(1.0f, -k);
+    if (!(am <= 3.0e38f)) raise_error(err, TP3D_ERANGE);
+  }
+  const int64_t nv = n / 8;
+  for (int64_t v = (int64_t)blockIdx.x * kThreads + threadIdx.x; v < nv; v += (int64_t)gridDim.x * kThreads) {
+    float f[8];
+    unpack8(__ldg(reinterpret_cast<const uint4*>(x) + v), f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] *= sc;
+    reinterpret_cast<uint4*>(y)[v] = pack8h(f, nullptr);
   }
 }
 
@@ -627,18 +706,33 @@ tp3d_status last_error() { return cudaGetLastError() == cudaSuccess ? TP3D_OK : 
 }  // namespace
 
 tp3d_status launch_ln_fwd(const tp3d_ctx* ctx, const Grid& g, const void* x, const void* gamma, const void* beta,
-                          void* y, float* mean, float* rstd, float eps, cudaStream_t s) {
+                          void* y, void* y16, float* mean, float* rstd, float eps, cudaStream_t s) {
   const unsigned grid = grid_for_rows(ctx, g.R, 16);
   const bf16 *xb = static_cast<const bf16*>(x), *gb = static_cast<const bf16*>(gamma),
              *bb = static_cast<const bf16*>(beta);
   bf16* yb = static_cast<bf16*>(y);
+  __half* yh = static_cast<__half*>(y16);
+  int* err = ctx->d_err;
   switch (g.C % 256 == 0 ? g.C / 256 : 0) {  // whole rows in registers where C = 256 NV
-    case 2: ln_fwd_row_kernel<2><<<grid, kThreads, 0, s>>>(g, xb, gb, bb, yb, mean, rstd, eps); break;
-    case 4: ln_fwd_row_kernel<4><<<grid, kThreads, 0, s>>>(g, xb, gb, bb, yb, mean, rstd, eps); break;
-    case 8: ln_fwd_row_kernel<8><<<grid, kThreads, 0, s>>>(g, xb, gb, bb, yb, mean, rstd, eps); break;
-    case 16: ln_fwd_row_kernel<16><<<grid, kThreads, 0, s>>>(g, xb, gb, bb, yb, mean, rstd, eps); break;
-    default: ln_fwd_kernel<<<grid, kThreads, 0, s>>>(g, xb, gb, bb, yb, mean, rstd, eps);
+    case 2: ln_fwd_row_kernel<2><<<grid, kThreads, 0, s>>>(g, xb, gb, bb, yb, yh, err, mean, rstd, eps); break;
+    case 4: ln_fwd_row_kernel<4><<<grid, kThreads, 0, s>>>(g, xb, gb, bb, yb, yh, err, mean, rstd, eps); break;
+    case 8: ln_fwd_row_kernel<8><<<grid, kThreads, 0, s>>>(g, xb, gb, bb, yb, yh, err, mean, rstd, eps); break;
+    case 16: ln_fwd_row_kernel<16><<<grid, kThreads, 0, s>>>(g, xb, gb, bb, yb, yh, err, mean, rstd, eps); break;
+    default: ln_fwd_kernel<<<grid, kThreads, 0, s>>>(g, xb, gb, bb, yb, yh, err, mean, rstd, eps);
   }
+  return last_error();
+}
+
+tp3d_status launch_to_f16_scaled(const tp3d_ctx* ctx, const void* x, int64_t n, unsigned* amax, void* y,
+                                 float* inv_scale, cudaStream_t s) {
+  if (n <= 0 || n % 8) return TP3D_EINVAL;
+  TP3D_CUDA_TRY(cudaMemsetAsync(amax, 0, sizeof(unsigned), s));
+  const int64_t blocks = (n / 8 + kThreads - 1) / kThreads, cap = (int64_t)ctx->num_sms * 8;
+  const unsigned grid = (unsigned)(blocks < cap ? blocks : cap);
+  absmax_kernel<<<grid, kThreads, 0, s>>>(static_cast<const bf16*>(x), n, amax);
+  TP3D_CUDA_TRY(cudaGetLastError());
+  to_f16_scaled_kernel<<<grid, kThreads, 0, s>>>(static_cast<const bf16*>(x), n, amax, static_cast<__half*>(y),
+                                                 inv_scale, ctx->d_err);
   return last_error();
 }
 

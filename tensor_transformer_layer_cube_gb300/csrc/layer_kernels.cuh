@@ -9,9 +9,17 @@
 namespace tp3d {
 
 // y = (x - mean) * rstd * gamma + beta per row of the R x C matrix x (layout g,
-// y in the same layout); mean / rstd (fp32, R each) are saved.
+// y in the same layout); mean / rstd (fp32, R each) are saved.  y16, if not
+// null, receives the same values in fp16 (a value beyond fp16's range raises
+// TP3D_ERANGE in the context's error word).
 tp3d_status launch_ln_fwd(const tp3d_ctx* ctx, const Grid& g, const void* x, const void* gamma, const void* beta,
-                          void* y, float* mean, float* rstd, float eps, cudaStream_t s);
+                          void* y, void* y16, float* mean, float* rstd, float eps, cudaStream_t s);
+
+// y = fp16(x 2^k) for n bf16 values (n a multiple of 8), 2^k the power of two
+// that puts max |x| in [2^14, 2^15); *inv_scale = 2^-k (device float).  `amax`
+// is one device word of scratch.  Two launches and a 4-byte memset on s.
+tp3d_status launch_to_f16_scaled(const tp3d_ctx* ctx, const void* x, int64_t n, unsigned* amax, void* y,
+                                 float* inv_scale, cudaStream_t s);
 
 // dx = dres + rstd * (dxh - mean(dxh) - xh * mean(dxh * xh)), dxh = dy * gamma,
 // xh = (x - mean) * rstd, per row (dy, x, dres, dx in layout g).
