@@ -7,7 +7,8 @@
 Prints ONE JSON line (rank 0).  A step is one pass of the workload's whole
 hot path over one batch of synthetic input already resident in HBM; every
 timed step is bracketed by CUDA events on the launching stream and followed,
-outside the events, by a 256 MiB write that flushes L2.  `value` is the
+outside the events, by a 256 MiB write that flushes L2 and a 256 MiB read
+that writes the flush's dirty lines back before the next step.  `value` is the
 whole-job throughput (all ranks' work / the slowest rank's time).  `e2e` is
 the same metric through the public C-ABI call with the step's input copied
 from pinned host memory and its result copied back inside the timed region.
@@ -55,6 +56,9 @@ WORKLOADS = {
                    name="MLP on a q=4 cube (64 virtual devices): tokens 8192, hidden 4096, ffn 16384, bf16"),
     "reshard": dict(kind="reshard", R=8192, C=8192,
                     name="resharding sweep, 8192x8192 bf16, 20 ordered pairs of ROW4 COL4 BLK2x2 CUBE_A(q=2) REP4"),
+    "reshard_q3": dict(kind="reshard", R=8190, C=8190, q3=True,
+                       name="resharding sweep, 8190x8190 bf16, 30 ordered pairs of CUBE_A CUBE_B CUBE_C (q=3) "
+                            "ROW3 COL3 REP3 (block rows of 5460, 1820 and 16380 bytes: not 16-byte aligned)"),
 }
 
 
@@ -306,8 +310,13 @@ class ReshardBench:
         g = torch.Generator(device=dev)
         g.manual_seed(seed)
         L = t.layout
-        self.lays = [("ROW4", L(t.ROW, 0, 4), 1), ("COL4", L(t.COL, 0, 4), 1), ("BLK2x2", L(t.BLOCK2D, 0, 2, 2), 1),
-                     ("CUBE_A", L(t.CUBE_A, 2), 1), ("REP4", L(t.REPLICATED, 0, 4), 4)]
+        if w.get("q3"):
+            self.lays = [("CUBE_A", L(t.CUBE_A, 3), 1), ("CUBE_B", L(t.CUBE_B, 3), 1), ("CUBE_C", L(t.CUBE_C, 3), 1),
+                         ("ROW3", L(t.ROW, 0, 3), 1), ("COL3", L(t.COL, 0, 3), 1), ("REP3", L(t.REPLICATED, 0, 3), 3)]
+        else:
+            self.lays = [("ROW4", L(t.ROW, 0, 4), 1), ("COL4", L(t.COL, 0, 4), 1),
+                         ("BLK2x2", L(t.BLOCK2D, 0, 2, 2), 1), ("CUBE_A", L(t.CUBE_A, 2), 1),
+                         ("REP4", L(t.REPLICATED, 0, 4), 4)]
         vals = torch.randint(-256, 257, (R * C,), device=dev, generator=g).to(torch.bfloat16)
         self.src = {}
         for name, lay, copies in self.lays:
@@ -334,18 +343,28 @@ class ReshardBench:
 BENCHES = {"mlp": MlpBench, "layer": LayerBench, "linear_f32": LinearF32Bench, "reshard": ReshardBench}
 
 
+def flush_l2(flush):
+    """Flush L2 between timed steps: write 256 MiB (the first half of the
+    buffer), then read the other 256 MiB, so that the write's dirty lines are
+    written back here, outside the timed region, and not by the next step's
+    kernels."""
+    h = flush.numel() // 2
+    flush[:h].add_(1)
+    flush[h:].sum()
+
+
 def time_steps(torch, fn, steps, warmup, flush, stream):
     """Per-step CUDA-event durations (ms), L2 flushed between steps (outside the events)."""
     for _ in range(warmup):
         fn()
-        flush.add_(1)
+        flush_l2(flush)
     torch.cuda.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for a, b in evs:
         a.record(stream)
         fn()
         b.record(stream)
-        flush.add_(1)
+        flush_l2(flush)
     torch.cuda.synchronize()
     return [a.elapsed_time(b) for a, b in evs]
 
@@ -432,33 +451,27 @@ def cpu_baseline_layer(w, seconds):
 
 
 # DRAM bytes (read + write) of one launch of the layer's linear-1 probe, from
-# the ncu capture summarised in profiles/gemm_tc2_layer_w1.md; valid only
-# while the GEMM sources hash to the value they had when it was taken.
+# an ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of that
+# launch; valid only while the GEMM sources, byte for byte as written, hash
+# to the value they had when it was taken (any edit voids it until the
+# figure is captured again).
 GEMM_TRAFFIC = {"workload": "layer_q2", "bytes": 50565888 + 27478784, "sources_sha256_16": "74303bdfe64ab924",
                 "note": "ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch; output lines still in "
                         "L2 when the kernel ends are not counted (reads equal the algorithmic inputs)"}
-
-
-def strip_comments(src):
-    """C/C++ source without its comments and blank lines: an edit to a
-    comment does not change the kernel the traffic figure was taken on."""
-    import re
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    src = re.sub(r"//[^\n]*", "", src)
-    return "\n".join(ln.rstrip() for ln in src.split("\n") if ln.strip())
+GEMM_SOURCES = ("gemm_tc.cu", "gemm.cuh", "common.cuh", "layout.cuh", "api.cu")
 
 
 def gemm_sources_hash(read=None):
     import hashlib
     h = hashlib.sha256()
-    for f in ("gemm_tc.cu", "gemm.cuh", "common.cuh", "layout.cuh", "api.cu"):
+    for f in GEMM_SOURCES:
         path = os.path.join("tensor_transformer_layer_cube_gb300", "csrc", f)
         if read is None:
             with open(os.path.join(ROOT, path), encoding="utf-8") as fh:
                 text = fh.read()
         else:
             text = read(path)
-        h.update(strip_comments(text).encode())
+        h.update(text.encode())
     return h.hexdigest()[:16]
 
 
@@ -474,23 +487,33 @@ def roofline_probe(torch, wb, steps, flush, stream, pk, workload=None):
             "peak_source": f"bf16_tflops ({pk['source']}, burst)", "launch_ms": statistics.mean(kd)}
 
 
-def reshard_summary(torch, rb, flush, stream, pk, reps=5):
+def reshard_summary(torch, rb, flush, stream, pk, name="reshard", reps=5):
     per = []
     for k in range(len(rb.pairs)):
         d = time_steps(torch, lambda k=k: rb.launch_pair(k), reps, 2, flush, stream)
         per.append(statistics.median(d))
     gbs = [rb.pair_bytes[k] / (per[k] / 1e3) / 1e9 for k in range(len(per))]
     tot = rb.units / (sum(per) / 1e3) / 1e9
-    k_best = max(range(len(per)), key=lambda k: gbs[k])
+    # a plain device copy of the same 128 MiB (torch), the practical ceiling for one launch of this size
+    a = torch.empty(rb.R * rb.C, device=flush.device, dtype=torch.bfloat16)
+    b = torch.empty_like(a)
+    cd = time_steps(torch, lambda: b.copy_(a), reps, 2, flush, stream)
+    copy_gbs = 2 * a.numel() * 2 / (statistics.median(cd) / 1e3) / 1e9
+    del a, b
+    kern = ("reshard_vec_kernel" if not WORKLOADS[name].get("q3") else
+            "reshard_staged_kernel (rows staged through shared memory by bulk copies and realigned)")
     return {
         "value": tot, "unit": "GB/s", "frac_of_measured_hbm": tot / pk["hbm"], "frac_of_8TBs": tot / 8000.0,
-        "min_pair_gbs": min(gbs), "max_pair_gbs": max(gbs), "ms_per_sweep": sum(per),
-        "pairs": {f"{rb.pairs[k][0][0]}->{rb.pairs[k][1][0]}": round(gbs[k], 1) for k in range(len(gbs))},
+        "min_pair_gbs": min(gbs), "min_pair_frac": min(gbs) / pk["hbm"], "max_pair_gbs": max(gbs),
+        "ms_per_sweep": sum(per), "torch_copy_same_bytes_gbs": copy_gbs,
+        "pairs": {f"{rb.pairs[k][0][0]}->{rb.pairs[k][1][0]}": {"gbs": round(gbs[k], 1),
+                                                                 "frac": round(gbs[k] / pk["hbm"], 4)}
+                  for k in range(len(gbs))},
         "roofline": {"bound": "hbm", "achieved": tot, "peak": pk["hbm"], "unit": "GB/s", "frac": tot / pk["hbm"],
-                     "traffic": None, "kernel": "reshard_vec_kernel (sweep average; bytes = read once + every "
-                                                "destination copy written)",
+                     "traffic": None, "kernel": f"{kern} (sweep average; bytes = read once + every destination "
+                                                "copy written)",
                      "peak_source": f"hbm_gbs ({pk['source']})"},
-        "workload": WORKLOADS["reshard"]["name"]}
+        "workload": WORKLOADS[name]["name"]}
 
 
 def host_planner_summary(t):
@@ -633,7 +656,7 @@ def run_ours(args, rank, world, dist):
     torch.cuda.set_device(dev)
     ctx = t.tp3d_create(local)
     stream = torch.cuda.current_stream()
-    flush = torch.empty(256 * 1024 * 1024 // 4, device=dev, dtype=torch.float32)
+    flush = torch.zeros(512 * 1024 * 1024 // 4, device=dev, dtype=torch.float32)  # 256 MiB written + 256 MiB read
     w = WORKLOADS[args.workload]
     pk = peaks()
     wb = make_bench(t, ctx, dev, args.workload)
@@ -679,7 +702,8 @@ def run_ours(args, rank, world, dist):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w["kind"] != "linear_f32" else "f32",
         "data": "synthetic (seeded device RNG; N(0,1) inputs, N(0,0.02) weights)",
-        "config": {"workload": w["name"], "l2": "flushed between timed steps (256 MiB write outside the events)",
+        "config": {"workload": w["name"], "l2": "flushed between timed steps outside the events: a 256 MiB write, "
+                                                  "then a 256 MiB read that writes its dirty lines back",
                    "launch": "one CUDA graph per step (the step's C-ABI calls captured once, replayed)" if use_graph
                    else "direct C-ABI calls",
                    "parallelism": "replicas (no data-path collective)" if world > 1
@@ -692,7 +716,8 @@ def run_ours(args, rank, world, dist):
             ffn, bfn = capture(torch, wb.fwd, stream).replay, capture(torch, wb.bwd, stream).replay
         fd = time_steps(torch, ffn, max(5, args.steps // 2), 2, flush, stream)
         bd = time_steps(torch, bfn, max(5, args.steps // 2), 2, flush, stream)
-        fwd_ms, bwd_ms = statistics.mean(fd), statistics.mean(bd)
+        fwd_ms = slowest_rank_ms(sum(fd), world, dist, dev) / len(fd)
+        bwd_ms = slowest_rank_ms(sum(bd), world, dist, dev) / len(bd)
         line["layer"] = {"fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
                          "avg_step_time_ms_per_sequence": (fwd_ms + bwd_ms) / w["batch"],
                          "fwd_tflops": wb.fwd_flops / (fwd_ms / 1e3) / 1e12,
@@ -701,13 +726,16 @@ def run_ours(args, rank, world, dist):
     if hasattr(wb, "e2e_step"):
         edurs = time_steps(torch, wb.e2e_step, max(3, args.steps // 2), 2, flush, stream)
         bi, bo, what = wb.e2e_bytes()
-        line["e2e"] = {"value": world * wb.units / (statistics.mean(edurs) / 1e3) / wb.scale, "unit": wb.unit,
+        e_ms = slowest_rank_ms(sum(edurs), world, dist, dev)
+        line["e2e"] = {"value": job_value(world, wb.units, len(edurs), e_ms, wb.scale), "unit": wb.unit,
                        "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-                       "ms_per_step": statistics.mean(edurs), "what": what + ", per step"}
+                       "ms_per_step": e_ms / len(edurs), "what": what + ", per step"}
     if hasattr(wb, "kernel_probe"):
         line["roofline"] = roofline_probe(torch, wb, args.steps, flush, stream, pk, args.workload)
     elif w["kind"] == "reshard":
-        line["roofline"] = reshard_summary(torch, wb, flush, stream, pk)["roofline"]
+        sweep = reshard_summary(torch, wb, flush, stream, pk, args.workload)
+        line["roofline"] = sweep["roofline"]
+        line["sweep"] = sweep
 
     if rank == 0 and not args.no_extras:
         extras = {}
@@ -716,7 +744,7 @@ def run_ours(args, rank, world, dist):
                 continue
             eb = make_bench(t, ctx, dev, name)
             if WORKLOADS[name]["kind"] == "reshard":
-                extras[name] = reshard_summary(torch, eb, flush, stream, pk)
+                extras[name] = reshard_summary(torch, eb, flush, stream, pk, name)
             else:
                 d = time_steps(torch, eb.step, 10, 3, flush, stream)
                 e = {"value": eb.units / (statistics.mean(d) / 1e3) / eb.scale, "unit": eb.unit,
@@ -727,18 +755,27 @@ def run_ours(args, rank, world, dist):
                 extras[name] = e
             del eb
             torch.cuda.empty_cache()
-        line["configs"] = extras
-        line["host_planners"] = host_planner_summary(t)
-        line["layout_comparison"] = layout_comparison(torch, t, ctx, dev, flush, stream)
+        host = host_planner_summary(t)
+        layouts = layout_comparison(torch, t, ctx, dev, flush, stream)
         torch.cuda.empty_cache()
         st = t.tp3d_sync_status(ctx)
         if st != 0:
             raise SystemExit(f"device error in the extra workloads: {t.STATUS[st]}")
+        # a compact resharding summary near the top of the line; the full
+        # objects follow, with `configs` (every other workload) last
+        line["reshard"] = {k: {"gbs": round(extras[k]["value"], 1), "frac": round(extras[k]["frac_of_measured_hbm"], 4),
+                               "min_pair_frac": round(extras[k]["min_pair_frac"], 4),
+                               "frac_of_8TBs": round(extras[k]["frac_of_8TBs"], 4)}
+                           for k in extras if WORKLOADS[k]["kind"] == "reshard"}
     if rank == 0:
         line["clocks"] = ClockSampler.summarize(rows, t0, t1) if isinstance(rows, list) else rows
         if not args.no_extras and w["kind"] in ("mlp", "layer"):
             line["cpu_baseline"] = (cpu_baseline_layer if w["kind"] == "layer" else cpu_baseline_mlp)(
                 w, args.cpu_seconds)
+        if not args.no_extras:
+            line["host_planners"] = host
+            line["layout_comparison"] = layouts
+            line["configs"] = extras
         print(json.dumps(line), flush=True)
     t.tp3d_destroy(ctx)
 

@@ -35,3 +35,24 @@ def bits_u16(t: torch.Tensor):
 
 def as_np64(t: torch.Tensor):
     return t.float().cpu().numpy().astype(np.float64)
+
+
+GUARD_BYTES = 64 * 1024
+SENTINEL = 0xFF
+
+
+def guarded(n: int, dtype) -> tuple:
+    """An output buffer of n elements between two 64 KiB guard bands, every
+    byte 0xFF (the interior too: NaN in bf16 and fp32, so an element never
+    written shows as well).  Returns (whole buffer, interior view); the
+    interior starts 64 KiB in, so it keeps the allocation's alignment."""
+    esz = torch.empty(0, dtype=dtype).element_size()
+    whole = torch.full((2 * GUARD_BYTES + n * esz,), SENTINEL, dtype=torch.uint8, device=device())
+    return whole, whole[GUARD_BYTES:GUARD_BYTES + n * esz].view(dtype)
+
+
+def assert_guards_intact(whole: torch.Tensor, what="") -> None:
+    """Both guard bands still hold the sentinel: nothing was stored outside the output."""
+    head = whole[:GUARD_BYTES]
+    tail = whole[whole.numel() - GUARD_BYTES:]
+    assert bool((head == SENTINEL).all()) and bool((tail == SENTINEL).all()), f"store outside the output {what}"

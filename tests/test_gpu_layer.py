@@ -22,7 +22,7 @@ import tensor_transformer_layer_cube_gb300 as t
 from oracle import layer as OY
 from oracle import layouts as L
 from oracle.metrics import BF16_TOL, LAYER_ELEM_TOL, LAYER_ELEM_TOL_PEAKED, fro_err, max_rel_err, rel_err
-from tests.gpu_util import as_np64, device, to_dev_bf16
+from tests.gpu_util import as_np64, assert_guards_intact, device, guarded, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -50,16 +50,22 @@ def _run(ctx, cfg: OY.LayerConfig, seed, perturb, wqkv_mult=1, forward_only=Fals
     wsb = t.tp3d_layer_workspace_bytes(c)
     assert wsb > 0
     ws = torch.empty(wsb, dtype=torch.uint8, device=device())
-    Y = torch.full((M * h,), float("nan"), dtype=torch.bfloat16, device=device())
+    # outputs NaN-filled between 64 KiB guard bands (checked after each call)
+    wY, Y = guarded(M * h, torch.bfloat16)
     st = t.tp3d_layer_fwd(ctx, c, params, X, Y, ws)
     assert st == 0, t.STATUS[st]
     assert t.tp3d_sync_status(ctx) == 0
-    grads = {k: torch.full_like(v, float("nan")) for k, v in params.items()}
-    dX = torch.full((M * h,), float("nan"), dtype=torch.bfloat16, device=device())
+    assert_guards_intact(wY, "layer Y")
+    gw = {k: guarded(v.numel(), torch.bfloat16) for k, v in params.items()}
+    grads = {k: g[1] for k, g in gw.items()}
+    wdX, dX = guarded(M * h, torch.bfloat16)
     if not forward_only:
         st = t.tp3d_layer_bwd(ctx, c, params, X, ws, dY, dX, grads)
         assert st == 0, t.STATUS[st]
         assert t.tp3d_sync_status(ctx) == 0
+        assert_guards_intact(wdX, "layer dX")
+        for k, g in gw.items():
+            assert_guards_intact(g[0], f"layer d{k}")
     # oracle on the same bf16 values, sharded by its own layout maps
     P64 = {k: S.as_f64(v) for k, v in I.items() if k not in ("X", "dY")}
     Ps = OY.shard_params(P64, cfg)

@@ -18,7 +18,7 @@ from oracle import layouts as L
 from oracle import linear as OL
 from oracle import mlp as OM
 from oracle.metrics import BF16_TOL, F32_TOL, rel_err
-from tests.gpu_util import as_np64, device, sharded_f64, to_dev_bf16, to_dev_f32
+from tests.gpu_util import as_np64, assert_guards_intact, device, guarded, sharded_f64, to_dev_bf16, to_dev_f32
 
 pytestmark = pytest.mark.gpu
 
@@ -35,11 +35,12 @@ def _linear_case(ctx, q, y, M, N, K, bias, act, seed, wstd=0.05):
     B = S.normal((N, K), wstd, seed + 1)
     b = S.normal((K,), 0.1, seed + 2) if bias else None
     la, lb, lc = OL.linear_layouts(q, y)
-    dC = torch.full((M * K,), float("nan"), dtype=torch.bfloat16, device=device())
+    whole, dC = guarded(M * K, torch.bfloat16)  # NaN-filled, between 64 KiB guard bands
     st = t.tp3d_linear(ctx, q, y, M, N, K, t.TP3D_BF16, to_dev_bf16(A, la), to_dev_bf16(B, lb),
                        b.to(device()) if bias else None, 1 if act else 0, dC)
     assert st == 0, t.STATUS[st]
     assert t.tp3d_sync_status(ctx) == 0
+    assert_guards_intact(whole, f"linear q={q} y={y} {M}x{N}x{K}")
     want = OL.linear3d(sharded_f64(A, la), sharded_f64(B, lb), q, M, N, K,
                        bias=S.as_f64(b) if bias else None, act="gelu" if act else None, y=y)
     got = as_np64(dC)
@@ -99,11 +100,13 @@ def _mlp_case(ctx, q, M, h, f, seed, bias_std, sample_rows=None):
     dX = to_dev_bf16(I["X"], L.CUBE_A(q))
     dW1 = to_dev_bf16(I["W1"], L.CUBE_B(q))
     dW2 = to_dev_bf16(I["W2"], L.CUBE_B_SWAP(q))
-    dY1 = torch.empty(M * f, dtype=torch.bfloat16, device=device())
-    dY = torch.full((M * h,), float("nan"), dtype=torch.bfloat16, device=device())
+    whole1, dY1 = guarded(M * f, torch.bfloat16)
+    whole, dY = guarded(M * h, torch.bfloat16)
     st = t.tp3d_mlp(ctx, q, M, h, f, t.TP3D_BF16, dX, dW1, I["b1"].to(device()), dW2, I["b2"].to(device()), dY1, dY)
     assert st == 0, t.STATUS[st]
     assert t.tp3d_sync_status(ctx) == 0
+    assert_guards_intact(whole1, "MLP Y1")
+    assert_guards_intact(whole, "MLP Y")
     Yg = L.from_sharded(as_np64(dY), L.CUBE_A(q), M, h)
     X, W1, W2 = S.as_f64(I["X"]), S.as_f64(I["W1"]), S.as_f64(I["W2"])
     b1, b2 = S.as_f64(I["b1"]), S.as_f64(I["b2"])

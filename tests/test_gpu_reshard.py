@@ -3,7 +3,12 @@
 Resharding is the layout conversion of "On Optimizing the Communication of
 Model Parallelism" §2 among row-split, column-split, 2-D block, cube and
 replicated layouts; every destination word must equal the oracle's bit for
-bit, for every ordered pair of layouts.
+bit, for every ordered pair of layouts.  Every destination buffer sits between
+two 64 KiB guard bands that must come back unchanged (a store outside the
+output would show there).  The cases cover the three kernels: cells whose
+rows are whole 16-byte vectors, cells of 64 bytes and more whose rows are not
+16-byte aligned (staged through shared memory and realigned), and narrow
+cells.
 """
 import itertools
 
@@ -14,7 +19,7 @@ import torch
 import synth_inputs as S
 import tensor_transformer_layer_cube_gb300 as t
 from oracle import layouts as L
-from tests.gpu_util import bits_u16, device
+from tests.gpu_util import assert_guards_intact, bits_u16, device, guarded
 
 pytestmark = pytest.mark.gpu
 
@@ -44,11 +49,12 @@ def _run(ctx, R, C, G_bits, src, dst, esz=2):
     want = L.reshard(sbuf, src[1], dst[1], R, C)
     sview = {1: np.uint8, 2: np.int16, 4: np.int32, 8: np.int64}[esz]
     d_src = torch.from_numpy(np.ascontiguousarray(sbuf.astype(npdt)).view(sview)).to(device())
-    d_dst = torch.full((want.size,), -1, dtype=dt, device=device())
+    whole, d_dst = guarded(want.size, dt)
     assert t.tp3d_reshard(ctx, R, C, esz, src[2], d_src, dst[2], d_dst) == 0
     assert t.tp3d_sync_status(ctx) == 0
     got = d_dst.cpu().numpy().view(npdt)
     assert np.array_equal(got, want.astype(npdt)), (src[0], dst[0])
+    assert_guards_intact(whole, f"{src[0]} -> {dst[0]}")
 
 
 @pytest.mark.parametrize("R,C", [(64, 64), (256, 512), (1024, 96)])
@@ -69,8 +75,38 @@ def test_cube_layouts_all_kinds(ctx):
         _run(ctx, R, C, G, a, b)
 
 
+def _q3_lays(q=3, rep=3):
+    return [("CUBE_A", L.CUBE_A(q), t.layout(t.CUBE_A, q)), ("CUBE_B", L.CUBE_B(q), t.layout(t.CUBE_B, q)),
+            ("CUBE_C", L.CUBE_C(q), t.layout(t.CUBE_C, q)), ("COL3", L.COL(3), t.layout(t.COL, 0, 3)),
+            ("ROW3", L.ROW(3), t.layout(t.ROW, 0, 3)), ("REP3", L.REP(rep), t.layout(t.REPLICATED, 0, rep))]
+
+
+@pytest.mark.parametrize("esz,R,C", [(2, 1170, 1170), (1, 630, 630), (4, 450, 450), (8, 99, 99)])
+def test_unaligned_rows_staged_path(ctx, esz, R, C):
+    # q = 3 cube layouts whose block widths are not whole 16-byte vectors
+    # (bf16 1170: 390 / 130 columns = 780 / 260 bytes), cells of 64 bytes and
+    # more: the shared-memory staged kernel (rows of 2340 bytes take two jobs);
+    # a replicated destination whose copies
+    # start at other alignments (R C esz not a multiple of 16)
+    rng = np.random.default_rng(esz + 100)
+    npdt = {1: np.uint8, 2: np.uint16, 4: np.uint32, 8: np.uint64}[esz]
+    G = rng.integers(0, np.iinfo(npdt).max, size=(R, C), dtype=npdt)
+    for a, b in itertools.permutations(_q3_lays(), 2):
+        _run(ctx, R, C, G, a, b, esz=esz)
+
+
+def test_full_size_unaligned_8190(ctx):
+    # 8190 x 8190 bf16 (128 MiB) on the q = 3 cube: 2730- and 910-column
+    # blocks (5460 and 1820 bytes, not 16-byte multiples)
+    R = C = 8190
+    G = S.bf16_bits(S.random_bits16((R, C), S.SEED_BASE + 51).view(torch.bfloat16)).reshape(R, C)
+    lays = _q3_lays()
+    for a, b in [(lays[0], lays[1]), (lays[1], lays[3]), (lays[4], lays[2]), (lays[0], lays[5])]:
+        _run(ctx, R, C, G, a, b)
+
+
 def test_unaligned_cells_take_the_element_path(ctx):
-    R, C = 36, 36  # q = 3 cube: 4-row blocks and 12-column blocks; ROW(3): 12 rows
+    R, C = 36, 36  # q = 3 cube: 4-row blocks and 12-column blocks; ROW(3): 12 rows (8-byte cells)
     G = S.bf16_bits(S.random_bits16((R, C), 9).view(torch.bfloat16)).reshape(R, C)
     a = ("CUBE_B", L.CUBE_B(3), t.layout(t.CUBE_B, 3))
     b = ("COL3", L.COL(3), t.layout(t.COL, 0, 3))

@@ -5,10 +5,14 @@ where cudaMalloc is not allowed (it would synchronise the device, or all
 device memory belongs to another pool) or they only own the tensors they
 read and write.  tp3d_mlp_noalloc keeps the hidden activation in the
 library's own fixed device array instead.  This test calls it through the C
-ABI twice in a row, with different inputs, and checks each output against
-tp3d_mlp's on the same inputs, within the bf16 tolerance of the other GPU
-tests.  It lives in its own file, collected last, and sets up everything it
-uses itself, so it passes alone in a fresh process or after the other tests.
+ABI twice in a row at the array's full size, with different inputs, then
+once with a much smaller hidden activation (which must not pick up what the
+larger call left in the array), and checks each output against tp3d_mlp's
+on the same inputs: bit for bit (both run the same deterministic kernels in
+the same order; only the hidden buffer's address differs), and within the
+bf16 tolerance of the other GPU tests.  It lives in its own file, collected
+last, and sets up everything it uses itself, so it passes alone in a fresh
+process or after the other tests.
 """
 import numpy as np
 import pytest
@@ -26,8 +30,9 @@ pytestmark = pytest.mark.gpu
 def test_mlp_noalloc_matches_tp3d_mlp_on_two_calls():
     ctx = t.tp3d_create(0)
     try:
-        q, M, h, f = 2, 2048, 1024, 4096  # M * f = 8 Mi: the whole static array
-        for call, seed in enumerate((611, 733)):
+        # M * f = 8 Mi (the whole static array) twice, then 512 x 1024 = 0.5 Mi
+        for call, (q, M, h, f, seed) in enumerate(((2, 2048, 1024, 4096, 611), (2, 2048, 1024, 4096, 733),
+                                                   (2, 512, 256, 1024, 857))):
             I = S.mlp_inputs(M, h, f, seed, bias_std=0.05)
             X = to_dev_bf16(I["X"], L.CUBE_A(q))
             W1 = to_dev_bf16(I["W1"], L.CUBE_B(q))
@@ -41,6 +46,7 @@ def test_mlp_noalloc_matches_tp3d_mlp_on_two_calls():
             assert t.tp3d_sync_status(ctx) == 0
             got, want = as_np64(Y), as_np64(Y_ref)
             assert not np.isnan(got).any()
+            assert torch.equal(Y.view(torch.int16), Y_ref.view(torch.int16)), call
             assert rel_err(got, want) <= BF16_TOL, call
     finally:
         t.tp3d_destroy(ctx)
