@@ -34,8 +34,9 @@
  * Errors.  Arguments are validated on the host before anything is launched;
  * a failed check returns its status and launches nothing.  There are no
  * exceptions, aborts or prints.  A failed launch returns TP3D_ECUDA.  Kernel
- * waits are bounded: a wait that runs out sets the context's device error
- * word, the kernel returns, and tp3d_sync_status() reports TP3D_ETIMEOUT.
+ * waits are bounded (tp3d_set_wait_limit_ns): a wait that runs out sets the
+ * context's device error word, the kernel returns, and tp3d_sync_status()
+ * reports TP3D_ETIMEOUT.
  */
 #ifndef TP3D_H
 #define TP3D_H
@@ -111,6 +112,24 @@ const char* tp3d_status_string(tp3d_status s);
  * if a layer call met a value its fp16 score path cannot hold, TP3D_ECUDA if
  * the stream reported an error, else TP3D_OK.                               */
 tp3d_status tp3d_sync_status(tp3d_ctx* ctx, void* stream);
+
+/* Failure detection (no counterpart on the pages; the bounded waits are this
+ * library's own).  Every wait inside a kernel gives up after the context's
+ * wait limit, 4 s unless set here; a wait that runs out sets TP3D_ETIMEOUT in
+ * the device error word, the kernel's CTAs let everything they issued land
+ * (loads, products, stores), free their tensor memory and return, and the
+ * context stays usable.  `ns` = 0 restores 4 s.  The limit lives in device
+ * memory and is written synchronously: it applies to kernels launched after
+ * the call returns; do not call it while this context's work is in flight
+ * or during stream capture.  TP3D_ECUDA if the write fails.                 */
+tp3d_status tp3d_set_wait_limit_ns(tp3d_ctx* ctx, uint64_t ns);
+
+/* Test hook for the timeout path: from now on, the GEMM kernels of this
+ * context's calls stop loading operands after `stages` contraction stages of
+ * each launch (after letting the loads they issued land), so the tensor-core
+ * issuer's next wait can only run out (-1 turns the hook off; the default).
+ * Host-side state only; TP3D_EINVAL for stages < -1.                         */
+tp3d_status tp3d_inject_load_stall(tp3d_ctx* ctx, int64_t stages);
 
 /* Resharding (CMR §2, cross-mesh resharding; MP3D §3.1.1 cube layouts):
  * writes into `dst` (layout dst_l) the same R x C matrix that `src` holds in

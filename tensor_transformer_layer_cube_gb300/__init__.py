@@ -27,6 +27,7 @@ from .build import build
 __all__ = [
     "build", "lib", "Tp3dError", "check", "STATUS", "layout",
     "tp3d_create", "tp3d_destroy", "tp3d_status_string", "tp3d_sync_status", "tp3d_reshard",
+    "tp3d_set_wait_limit_ns", "tp3d_inject_load_stall",
     "tp3d_linear", "tp3d_mlp", "tp3d_mlp_noalloc", "tp3d_layer_workspace_bytes", "tp3d_layer_fwd", "tp3d_layer_bwd",
     "tp3d_layout", "tp3d_layer_cfg", "tp3d_layer_params", "tp3d_layer_grads",
     "TP3D_F32", "TP3D_BF16", "CUBE_A", "CUBE_B", "CUBE_C", "CUBE_B_SWAP", "ROW", "COL", "BLOCK2D", "REPLICATED",
@@ -127,6 +128,8 @@ _SIGS = {
     "tp3d_destroy": (None, [ctypes.c_void_p]),
     "tp3d_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "tp3d_sync_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
+    "tp3d_set_wait_limit_ns": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_uint64]),
+    "tp3d_inject_load_stall": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64]),
     "tp3d_reshard": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_size_t, tp3d_layout,
                                     ctypes.c_void_p, tp3d_layout, ctypes.c_void_p, ctypes.c_void_p]),
     "tp3d_linear": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
@@ -225,6 +228,14 @@ def tp3d_status_string(status: int) -> str:
 
 def tp3d_sync_status(ctx: int, stream=None) -> int:
     return lib().tp3d_sync_status(ctx, _s(stream))
+
+
+def tp3d_set_wait_limit_ns(ctx: int, ns: int) -> int:
+    return lib().tp3d_set_wait_limit_ns(ctx, ns)
+
+
+def tp3d_inject_load_stall(ctx: int, stages: int) -> int:
+    return lib().tp3d_inject_load_stall(ctx, stages)
 
 
 def tp3d_reshard(ctx, R, C, elem_bytes, src_l: tp3d_layout, src, dst_l: tp3d_layout, dst, stream=None) -> int:

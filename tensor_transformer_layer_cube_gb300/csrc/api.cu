@@ -1,6 +1,7 @@
 // api.cu - the extern "C" entry points declared in include/tp3d.h: argument
 // validation (all of it before any launch), problem planning, dispatch.
 #include <stdlib.h>
+#include <string.h>
 
 #include "gemm.cuh"
 
@@ -96,8 +97,13 @@ tp3d_status tp3d_create(int device, tp3d_ctx** out) {
   tp3d_ctx* c = static_cast<tp3d_ctx*>(calloc(1, sizeof(tp3d_ctx)));
   if (!c) return TP3D_ECUDA;
   c->device = device;
+  c->stall_after = -1;
+  int init[kErrWords] = {0, 0, 0, 0};
+  const unsigned long long lim = kWaitLimitNs;
+  memcpy(init + 2, &lim, sizeof(lim));
   if (cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
-      cudaMalloc(&c->d_err, sizeof(int)) != cudaSuccess || cudaMemset(c->d_err, 0, sizeof(int)) != cudaSuccess) {
+      cudaMalloc(&c->d_err, sizeof(init)) != cudaSuccess ||
+      cudaMemcpy(c->d_err, init, sizeof(init), cudaMemcpyHostToDevice) != cudaSuccess) {
     if (c->d_err) cudaFree(c->d_err);
     free(c);
     return TP3D_ECUDA;
@@ -150,6 +156,21 @@ tp3d_status tp3d_sync_status(tp3d_ctx* ctx, void* stream) {
   if (cudaMemcpy(&e, ctx->d_err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return TP3D_ECUDA;
   if (e != 0 && cudaMemset(ctx->d_err, 0, sizeof(int)) != cudaSuccess) return TP3D_ECUDA;
   return static_cast<tp3d_status>(e);
+}
+
+tp3d_status tp3d_set_wait_limit_ns(tp3d_ctx* ctx, uint64_t ns) {
+  if (!ctx) return TP3D_EINVAL;
+  const unsigned long long lim = ns ? (unsigned long long)ns : kWaitLimitNs;
+  if (cudaSetDevice(ctx->device) != cudaSuccess ||
+      cudaMemcpy(ctx->d_err + 2, &lim, sizeof(lim), cudaMemcpyHostToDevice) != cudaSuccess)
+    return TP3D_ECUDA;
+  return TP3D_OK;
+}
+
+tp3d_status tp3d_inject_load_stall(tp3d_ctx* ctx, int64_t stages) {
+  if (!ctx || stages < -1) return TP3D_EINVAL;
+  ctx->stall_after = stages;
+  return TP3D_OK;
 }
 
 tp3d_status tp3d_reshard(tp3d_ctx* ctx, int64_t R, int64_t C, size_t elem_bytes, tp3d_layout src_l, const void* src,

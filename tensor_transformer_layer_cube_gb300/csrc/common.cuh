@@ -13,7 +13,12 @@
 struct tp3d_ctx {
   int device;
   int num_sms;
-  int* d_err;  // device error word: 0, or the first TP3D_* code a kernel raised
+  // device words: d_err[0] = 0, or the first TP3D_* code a kernel raised;
+  // d_err[2..3] = the bounded waits' limit in nanoseconds (a uint64)
+  int* d_err;
+  // test hook: the GEMM producers stop loading after this many contraction
+  // stages of each launch (-1: never), so that the issuer's next wait runs out
+  int64_t stall_after;
   // two side streams and their events, for independent launches of one call
   // that run beside the caller's stream (forked from it and joined back into
   // it before the call returns)
@@ -23,8 +28,11 @@ struct tp3d_ctx {
 
 namespace tp3d {
 
-// A bounded wait gives up after this many nanoseconds of wall time.
+// A bounded wait gives up after this many nanoseconds of wall time, unless
+// the context sets another limit (tp3d_set_wait_limit_ns); the drains of an
+// aborting CTA always allow this long.
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;
+constexpr int kErrWords = 4;  // ints of the device error area (error code, pad, 64-bit limit)
 
 #define TP3D_CUDA_TRY(expr)                       \
   do {                                            \
@@ -102,17 +110,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The context's wait limit, read from its error area (err[2..3]) on a wait's
+// slow path only.
+__device__ __forceinline__ unsigned long long wait_limit_ns(const int* err) {
+  return err ? *reinterpret_cast<const volatile unsigned long long*>(err + 2) : kWaitLimitNs;
+}
+
 // Bounded wait on phase `parity` of an mbarrier.  Returns false if the wait
 // ran out (the error word and the CTA's abort flag are then set) or if
 // another role of the CTA already aborted.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err) {
   if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
+  const unsigned long long t0 = globaltimer_ns(), lim = wait_limit_ns(err);
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 7u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > lim) {
         *abort_flag = 1;
         raise_error(err, TP3D_ETIMEOUT);
         return false;
@@ -248,33 +262,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t cluster_ad
   asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_addr),
                "r"(bytes)
                : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
-      : "memory");
-  return ok != 0;
-}
-// bounded wait with cluster-scope acquire (arrivals may come from the peer CTA)
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if ((it & 7u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
-        *abort_flag = 1;
-        raise_error(err, TP3D_ETIMEOUT);
-        return false;
-      }
-    }
-  }
 }
 // TMA load into this CTA's shared memory that completes on an mbarrier of
 // either CTA of the pair (cluster address)

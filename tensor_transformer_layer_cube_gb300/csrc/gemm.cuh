@@ -75,7 +75,8 @@ struct GemmProblem {
   int32_t causal;             // Causal
   Operand a, b, c;
   Epilogue epi;
-  int* err;                   // device error word
+  int* err;                   // device error area (error word, wait limit)
+  int64_t stall_after;        // test hook: the producer stops after this many stages (-1: never)
 };
 
 TP3D_HD int64_t op_off(int64_t hi, int64_t lo, int64_t base, int32_t z, int32_t Hz) {

@@ -277,8 +277,13 @@ __device__ __forceinline__ void epilogue_tile(const GemmProblem& P, const TileIn
       if (aux_ok) {
         bool ok = lane == 0 ? mbar_wait(aux_bar, aux_phase & 1u, abort_flag, P.err) : false;
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) {
+          // the load into the staging buffer may still be in flight: let it land first
+          if (lane == 0) mbar_wait_drain(aux_bar, aux_phase & 1u);
+          __syncwarp();
+          return;
+        }
         ++aux_phase;
-        if (!ok) return;
 #pragma unroll
         for (int v = 0; v < 4; ++v)
           sv[v] = *reinterpret_cast<const uint4*>(stg + 2048 + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4));
@@ -548,6 +553,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (k0 < klo || k0 >= khi) continue;
             const int s = (int)(it % S);
             const uint32_t ph = (it / S) & 1u;
+            // test hook: stop loading (and drain what is in flight, below)
+            if (P.stall_after >= 0 && (int64_t)it >= P.stall_after) {
+              ok = false;
+              break;
+            }
             if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, P.err)) {
               ok = false;
               break;
@@ -876,6 +886,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int32_t kt = 0; kt < tpsK; ++kt) {
             const int s = (int)(it % S);
             const uint32_t ph = (it / S) & 1u;
+            // test hook: both CTAs stop loading after the same stage (the even
+            // CTA then drains every load in flight, below)
+            if (P.stall_after >= 0 && (int64_t)it >= P.stall_after) {
+              ok = false;
+              break;
+            }
             if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, P.err)) {
               ok = false;
               break;
@@ -1188,7 +1204,9 @@ tp3d_status launch_pair(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t 
 
 }  // namespace
 
-tp3d_status gemm_bf16_tc(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t s) {
+tp3d_status gemm_bf16_tc(const tp3d_ctx* ctx, const GemmProblem& P0, cudaStream_t s) {
+  GemmProblem P = P0;
+  P.stall_after = ctx->stall_after;
   if (P.Z < 1 || P.Hz < 1 || P.M < 1 || P.N < 1 || P.K < 1) return TP3D_EINVAL;
   if (P.segM < 1 || P.segN < 1 || P.segK < 1 || P.M % P.segM || P.N % P.segN || P.K % P.segK) return TP3D_EINVAL;
   // every operand block must be at least one TMA box wide and tall enough
