@@ -188,28 +188,44 @@ __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) {
 // ------------------------------------------------------------------ forward
 // One pass with an online softmax over two query tiles at once (slots 0 and
 // 1: query tiles 2k and 2k+1 of one (batch, head); item w = (k, z) with the
-// longest k first).  Both slots share every K and V tile.  The MMA issuer
-// interleaves the slots so that one slot's softmax overlaps the other's
-// products: S0(0) S1(0) | PV0(j) S0(j+1) PV1(j) S1(j+1) | ...
+// longest k first).  Both slots share every K and V tile.
 //
 // Softmax rows (one thread per query row, four warps per slot): each key
 // tile's scores are read from TMEM, the row maximum updated, and
-// P = 2^(S log2e / sqrt d - m) written to shared memory (bf16, unnormalised)
-// together with the running row sum l.  The exponent base m only moves when
-// the row maximum exceeds it by more than 8 (2^8: P and l stay far from
-// overflow); then l and the row of O already accumulated in TMEM are scaled
-// by 2^(m_old - m_new) before the next product adds to it.  At the end
-// O / l is stored and the row's log-sum-exp (m + log2 l) ln 2 saved.
+// P = 2^(S log2e / sqrt d - m) (bf16, unnormalised) written back into tensor
+// memory over the tile's own scores, together with the running row sum l.
+// From a row's second key tile on this is one optimistic pass against the
+// current base m (P held in registers until the tile's maximum is known to
+// stay within m + 8); the first tile, and any tile that breaks that bound,
+// takes the two passes (maximum, then P).
+// The exponent base m only moves when the row maximum exceeds it by more than
+// 8 (2^8: P and l stay far from overflow); then l and the row of O already
+// accumulated in TMEM are scaled by 2^(m_old - m_new) before the next product
+// adds to it.  At the end O / l is stored and the row's log-sum-exp
+// (m + log2 l) ln 2 saved.
+//
+// P stays in tensor memory: O += P V takes its A operand from there (P as
+// bf16 pairs in the upper 64 columns of the slot's 128 score columns), so P
+// costs neither shared memory nor its bandwidth, and shared memory holds the
+// two query tiles and a ring of five K / V tiles.  P overwrites the scores,
+// so the issuer starts a slot's next S = Q K^T only once that slot's P V has
+// finished: PV0(j) S0(j+1) PV1(j) S1(j+1) per key tile, each S issued after
+// its slot's PV completes (the other slot's work keeps the tensor pipe busy
+// meanwhile).  A slot's new scores therefore imply its previous product is
+// done: the softmax warps may rescale O and overwrite the scores with P
+// without waiting for it.  The P chunks are written in descending column
+// order into the upper half, so every write lands on scores already read.
 //
 // warps: 0 TMA producer, 1 MMA issuer + TMEM owner, 2-3 idle (warpgroup 0);
 // 4-7 slot 0 rows (warpgroup 1); 8-11 slot 1 rows (warpgroup 2).  Warpgroup 0
-// gives registers to the two row warpgroups (setmaxnreg) so that each row
-// thread holds its whole 128-score row in registers.
-// smem: Q0 | Q1 | P0 | P1 | R0 R1 R2 (a ring of K_0 V_0 K_1 V_1 ...), 32 KiB each
-// TMEM: S0 [0,128) S1 [128,256) O0 [256, 256+d) O1 [256+d, 256+2d)
+// gives registers to the two row warpgroups (setmaxnreg).
+// smem: Q0 | Q1 | R0 .. R4 (a ring of K_0 V_0 K_1 V_1 ...), 32 KiB each
+// TMEM: S0 [0,128) (P0 in [64,128)) S1 [128,256) (P1 in [192,256))
+//       O0 [256, 256+d) O1 [256+d, 256+2d)
 constexpr int kFwdThreads = 384;
 constexpr int kFwdRegsLow = 64, kFwdRegsHigh = 216;  // 128 x 64 + 256 x 216 <= 384 x 168
 constexpr float kRescaleLog2 = 8.0f;
+constexpr uint32_t kFwdRing = 5;
 
 __global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap mqkv, const AttnProblem A, bf16* __restrict__ O,
@@ -217,19 +233,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const Ctx c = setup_smem(smem_raw);
   auto sQ = [&](int sl) { return c.base + (uint32_t)sl * kTile; };
-  auto sP = [&](int sl) { return c.base + (uint32_t)(2 + sl) * kTile; };
-  auto sR = [&](uint32_t i) { return c.base + (4u + i) * kTile; };
+  auto sR = [&](uint32_t i) { return c.base + (2u + i) * kTile; };
   auto bar = [&](int k) { return c.bar0 + 8u * k; };
   const uint32_t q_full = bar(0), q_empty = bar(1);
   auto r_full = [&](uint32_t i) { return bar(2 + (int)i); };
-  auto r_empty = [&](uint32_t i) { return bar(5 + (int)i); };
-  auto s_full = [&](int sl) { return bar(8 + sl); };
-  auto s_empty = [&](int sl) { return bar(10 + sl); };
-  auto p_full = [&](int sl) { return bar(12 + sl); };
-  auto p_empty = [&](int sl) { return bar(14 + sl); };
-  auto o_full = [&](int sl) { return bar(16 + sl); };
-  auto o_empty = [&](int sl) { return bar(18 + sl); };
-  const uint32_t final_bar = bar(20);
+  auto r_empty = [&](uint32_t i) { return bar(2 + (int)kFwdRing + (int)i); };
+  auto s_full = [&](int sl) { return bar(12 + sl); };
+  auto p_full = [&](int sl) { return bar(14 + sl); };
+  auto p_empty = [&](int sl) { return bar(16 + sl); };
+  auto o_full = [&](int sl) { return bar(18 + sl); };
+  auto o_empty = [&](int sl) { return bar(20 + sl); };
+  const uint32_t final_bar = bar(22);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t nq = A.s / TR, npair = (nq + 1) / 2, items = A.Z * npair;
@@ -237,13 +251,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const uint32_t dbytes = (uint32_t)(A.d * TR * 2);
 
   if (threadIdx.x == 0) {
-    for (int k = 0; k < 21; ++k) {
-      const bool four = (k >= 10 && k <= 13) || k == 18 || k == 19;  // s_empty, p_full, o_empty
+    for (int k = 0; k < 23; ++k) {
+      const bool four = k == 14 || k == 15 || k == 20 || k == 21;  // p_full, o_empty: one arrival per row warp
       mbar_init(bar(k), four ? kComputeWarps : 1);
     }
     *c.abort_flag = 0;
     fence_barrier_init();
   }
+  if (warp == 0 && lane == 0) tma_prefetch_map(&mqkv);
   if (warp == 1) {
     tmem_alloc(smem_u32(c.tmem_holder), 512);
     tmem_relinquish();
@@ -270,8 +285,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (two) load_tile(&mqkv, A.qkv, b * A.s + (iq0 + 1) * TR, t * A.d, nch, sQ(1), q_full);
         for (int j = 0; j < nmax && ok; ++j) {
           for (int kv = 0; kv < 2; ++kv, ++n) {
-            const uint32_t slot = n % 3;
-            if (!(ok = mbar_wait(r_empty(slot), ((n / 3) & 1) ^ 1, c.abort_flag, A.err))) break;
+            const uint32_t slot = n % kFwdRing;
+            if (!(ok = mbar_wait(r_empty(slot), ((n / kFwdRing) & 1) ^ 1, c.abort_flag, A.err))) break;
             mbar_arrive_expect_tx(r_full(slot), dbytes);
             load_tile(&mqkv, A.qkv, b * A.s + (int64_t)j * TR, (kv == 0 ? A.h : 2 * A.h) + t * A.d, nch, sR(slot),
                       r_full(slot));
@@ -280,29 +295,32 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
     } else if (warp == 1 && lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      const uint32_t id_s = idesc_f16_f32(TR, TR, 0, 0);       // S = Q K^T, fp16
-      const uint32_t id_o = idesc_bf16_f32(TR, (int)A.d, 0, 1);  // O += P V, bf16
+      const uint32_t id_s = idesc_f16_f32(TR, TR, 0, 0);         // S = Q K^T, fp16
+      const uint32_t id_o = idesc_bf16_f32(TR, (int)A.d, 0, 1);  // O += P V, bf16 (P from TMEM, V MN-major)
       const int ks_d = (int)(A.d / 16);
       uint32_t n = 0, ic = 0;
-      uint32_t sc[2] = {0, 0}, pc[2] = {0, 0}, oc[2] = {0, 0};
+      uint32_t pc[2] = {0, 0}, oc[2] = {0, 0};  // P V products issued, items finished, per slot
       bool ok = true;
       auto ring = [&](uint32_t idx, uint32_t& slot) -> bool {
-        slot = idx % 3;
-        return mbar_wait(r_full(slot), (idx / 3) & 1, c.abort_flag, A.err);
+        slot = idx % kFwdRing;
+        return mbar_wait(r_full(slot), (idx / kFwdRing) & 1, c.abort_flag, A.err);
       };
-      auto issue_s = [&](int sl, uint32_t kslot) -> bool {  // S_sl = Q_sl K^T
-        if (!mbar_wait(s_empty(sl), (sc[sl] & 1) ^ 1, c.abort_flag, A.err)) return false;
+      // S_sl = Q_sl K^T, once the slot's previous P V has read its P
+      auto issue_s = [&](int sl, uint32_t kslot) -> bool {
+        if (pc[sl] > 0 && !mbar_wait(p_empty(sl), (pc[sl] - 1) & 1, c.abort_flag, A.err)) return false;
         tc_fence_after();
         mma_tile(tmem + (uint32_t)(sl * TR), sQ(sl), false, sR(kslot), false, ks_d, id_s, false);
         umma_commit(s_full(sl));
-        ++sc[sl];
         return true;
       };
-      auto issue_pv = [&](int sl, uint32_t vslot, bool first) -> bool {  // O_sl += P_sl V
+      // O_sl += P_sl V, P from tensor memory
+      auto issue_pv = [&](int sl, uint32_t vslot, bool first) -> bool {
         if (!mbar_wait(p_full(sl), pc[sl] & 1, c.abort_flag, A.err)) return false;
         if (first && !mbar_wait(o_empty(sl), (oc[sl] & 1) ^ 1, c.abort_flag, A.err)) return false;
         tc_fence_after();
-        mma_tile(tmem + 256u + (uint32_t)(sl * A.d), sP(sl), false, sR(vslot), true, TR / 16, id_o, !first);
+        const uint32_t pt = tmem + (uint32_t)(sl * TR + 64), ot = tmem + 256u + (uint32_t)(sl * A.d);
+        for (int k = 0; k < TR / 16; ++k)
+          umma_ts(ot, pt + 8u * (uint32_t)k, desc_mnmajor(sR(vslot), k), id_o, (!first || k > 0) ? 1u : 0u);
         umma_commit(p_empty(sl));
         ++pc[sl];
         return true;
@@ -319,20 +337,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         umma_commit(r_empty(ks));
         for (int j = 0; j < nmax && ok; ++j) {
           uint32_t vs = 0, kn = 0;
-          if (!(ok = ring(n0 + 2 * j + 1, vs))) break;
-          if (j < nkv0 && !(ok = issue_pv(0, vs, j == 0))) break;
           const bool more = j + 1 < nmax;
-          if (more) {
-            if (!(ok = ring(n0 + 2 * j + 2, kn))) break;
+          if (!(ok = ring(n0 + 2 * j + 1, vs))) break;
+          if (more && !(ok = ring(n0 + 2 * j + 2, kn))) break;
+          if (j < nkv0) {
+            if (!(ok = issue_pv(0, vs, j == 0))) break;
             if (j + 1 < nkv0 && !(ok = issue_s(0, kn))) break;
           }
-          if (j < nkv1 && !(ok = issue_pv(1, vs, j == 0))) break;
-          if (more) {
+          if (j < nkv1) {
+            if (!(ok = issue_pv(1, vs, j == 0))) break;
             if (j + 1 < nkv1 && !(ok = issue_s(1, kn))) break;
+          }
+          umma_commit(r_empty(vs));
+          if (more) {
             if (j + 2 == nmax) umma_commit(q_empty);  // the item's last product with Q issued
             umma_commit(r_empty(kn));
           }
-          umma_commit(r_empty(vs));
         }
         if (!ok) break;
         umma_commit(o_full(0));
@@ -353,8 +373,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const float sl2 = A.scale * kLog2e;
-    const uint32_t s_col = (uint32_t)(sl * TR), o_col = 256u + (uint32_t)(sl * A.d);
-    uint32_t sc = 0, pc = 0, oc = 0;
+    const uint32_t s_col = (uint32_t)(sl * TR), p_col = s_col + 64u, o_col = 256u + (uint32_t)(sl * A.d);
+    uint32_t sc = 0, oc = 0;
     bool ok = true;
     for (int64_t rd = 0, w = snake_item(0); w < items && ok; w = snake_item(++rd)) {
       const int64_t k = npair - 1 - w / A.Z, z = w % A.Z, b = z / A.H, t = z % A.H;
@@ -363,76 +383,126 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int nkv = (int)iq + 1;
       float m = -INFINITY, l = 0.0f;
       for (int j = 0; j < nkv && ok; ++j) {
+        // new scores; they also mean the slot's previous P V has finished
         if (!(ok = warp_wait(s_full(sl), sc & 1, c, A.err, lane))) break;
+        ++sc;
         tc_fence_after();
-        // the row of scores, 32 columns at a time (the loop over the chunks is
-        // kept rolled: a compact body the instruction cache holds); read twice,
-        // for the maximum and then for P
         const bool diag = j == nkv - 1;
-        // eight independent partial maxima (short dependency chains)
-        float mx[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
-#pragma unroll 1
-        for (int cc = 0; cc < TR / 32; ++cc) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tmem_row(tmem, quarter, s_col + (uint32_t)(cc * 32)), v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (!diag || cc * 32 + e <= r) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(v[e]));
-        }
-        float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-        mt *= sl2;
-        // the product of the previous tile has finished: P is free and O current
-        if (!(ok = warp_wait(p_empty(sl), (pc & 1) ^ 1, c, A.err, lane))) break;
-        tc_fence_after();
-        // the TMEM accesses are warp-collective (.sync.aligned): the warp
-        // rescales when any of its rows needs it, each row by its own factor
-        const bool move = mt > m + kRescaleLog2;
-        if (j > 0 && __any_sync(0xffffffffu, move)) {
-          const float f = move ? ex2_approx(m - mt) : 1.0f;
-          l *= f;
-          for (int cc = 0; cc < (int)(A.d / 32); ++cc) {
-            uint32_t ov[32];
-            tmem_ld_32x32b_x32(tmem_row(tmem, quarter, o_col + (uint32_t)(cc * 32)), ov);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
-            tmem_st_32x32b_x32(tmem_row(tmem, quarter, o_col + (uint32_t)(cc * 32)), ov);
-          }
-          tmem_st_wait();
-        }
-        if (move) m = mt;
         float ps[8];  // eight partial row sums
 #pragma unroll
         for (int i = 0; i < 8; ++i) ps[i] = 0.0f;
-#pragma unroll 1
-        for (int cc = 0; cc < TR / 32; ++cc) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tmem_row(tmem, quarter, s_col + (uint32_t)(cc * 32)), v);
-          tmem_ld_wait();
+        // From the second key tile on, one optimistic pass: P against the
+        // current base m while the tile's maximum is tracked, P held in
+        // registers.  If no row's maximum passed m + 8, P is stored and the
+        // tile is done; otherwise (rare once the first tiles have set m) the
+        // two passes below run on the scores, still intact in TMEM.
+        bool two_pass = j == 0;
+        if (!two_pass) {
+          uint32_t pk[64];
+          float mx[8];
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            float f[8];
+          for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int col = cc * 32 + g * 8 + e;
-              f[e] = (!diag || col <= r) ? ex2_approx(fmaf(__uint_as_float(v[g * 8 + e]), sl2, -m)) : 0.0f;
-              ps[e] += f[e];
+          for (int cc = 0; cc < TR / 32; cc += 2) {
+            uint32_t v[2][32];
+            tmem_ld_32x32b_x32(tmem_row(tmem, quarter, s_col + (uint32_t)(cc * 32)), v[0]);
+            tmem_ld_32x32b_x32(tmem_row(tmem, quarter, s_col + (uint32_t)(cc * 32 + 32)), v[1]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+              for (int e2 = 0; e2 < 16; ++e2) {
+                const int col = (cc + h) * 32 + 2 * e2;
+                const bool k0 = !diag || col <= r, k1 = !diag || col + 1 <= r;
+                const float x0 = __uint_as_float(v[h][2 * e2]), x1 = __uint_as_float(v[h][2 * e2 + 1]);
+                if (k0) mx[(2 * e2) & 7] = fmaxf(mx[(2 * e2) & 7], x0);
+                if (k1) mx[(2 * e2 + 1) & 7] = fmaxf(mx[(2 * e2 + 1) & 7], x1);
+                const float f0 = k0 ? ex2_approx(fmaf(x0, sl2, -m)) : 0.0f;
+                const float f1 = k1 ? ex2_approx(fmaf(x1, sl2, -m)) : 0.0f;
+                ps[(2 * e2) & 7] += f0;
+                ps[(2 * e2 + 1) & 7] += f1;
+                const __nv_bfloat162 hh = __floats2bfloat162_rn(f0, f1);
+                pk[(cc + h) * 16 + e2] = *reinterpret_cast<const uint32_t*>(&hh);
+              }
             }
-            st_tile8(c.base_ptr + (2 + sl) * kTile, r, cc * 4 + g, pack8f(f));
+          }
+          const float mt = sl2 * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+          if (__any_sync(0xffffffffu, mt > m + kRescaleLog2)) {
+            two_pass = true;  // P above 2^8 somewhere in the warp: start over
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ps[i] = 0.0f;
+          } else {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint32_t w16[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) w16[i] = pk[q4 * 16 + i];
+              tmem_st_32x32b_x16(tmem_row(tmem, quarter, p_col + (uint32_t)(q4 * 16)), w16);
+            }
           }
         }
-        // S is read for the last time: the next tile's scores may overwrite it
-        tc_fence_before();
-        warp_arrive(s_empty(sl), lane);
-        ++sc;
+        if (two_pass) {
+          // the row maximum: the four 32-column chunks in two pairs of loads
+          float mx[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+#pragma unroll 1
+          for (int cc = 0; cc < TR / 32; cc += 2) {
+            uint32_t v[2][32];
+            tmem_ld_32x32b_x32(tmem_row(tmem, quarter, s_col + (uint32_t)(cc * 32)), v[0]);
+            tmem_ld_32x32b_x32(tmem_row(tmem, quarter, s_col + (uint32_t)(cc * 32 + 32)), v[1]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                if (!diag || (cc + h) * 32 + e <= r) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(v[h][e]));
+          }
+          float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+          mt *= sl2;
+          // the TMEM accesses are warp-collective (.sync.aligned): the warp
+          // rescales when any of its rows needs it, each row by its own factor
+          const bool move = mt > m + kRescaleLog2;
+          if (j > 0 && __any_sync(0xffffffffu, move)) {
+            const float f = move ? ex2_approx(m - mt) : 1.0f;
+            l *= f;
+            for (int cc = 0; cc < (int)(A.d / 32); ++cc) {
+              uint32_t ov[32];
+              tmem_ld_32x32b_x32(tmem_row(tmem, quarter, o_col + (uint32_t)(cc * 32)), ov);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
+              tmem_st_32x32b_x32(tmem_row(tmem, quarter, o_col + (uint32_t)(cc * 32)), ov);
+            }
+          }
+          if (move) m = mt;
+          // P, chunk by chunk from the highest columns down: chunk cc's 32
+          // scores become 16 columns of bf16 pairs at p_col + 16 cc, over
+          // scores read before
+#pragma unroll 1
+          for (int cc = TR / 32 - 1; cc >= 0; --cc) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tmem_row(tmem, quarter, s_col + (uint32_t)(cc * 32)), v);
+            tmem_ld_wait();
+            uint32_t pk[16];
+#pragma unroll
+            for (int e2 = 0; e2 < 16; ++e2) {
+              const int col = cc * 32 + 2 * e2;
+              const float f0 = (!diag || col <= r) ? ex2_approx(fmaf(__uint_as_float(v[2 * e2]), sl2, -m)) : 0.0f;
+              const float f1 = (!diag || col + 1 <= r) ? ex2_approx(fmaf(__uint_as_float(v[2 * e2 + 1]), sl2, -m)) : 0.0f;
+              ps[(2 * e2) & 7] += f0;
+              ps[(2 * e2 + 1) & 7] += f1;
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(f0, f1);
+              pk[e2] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            tmem_st_32x32b_x16(tmem_row(tmem, quarter, p_col + (uint32_t)(cc * 16)), pk);
+          }
+        }
+        tmem_st_wait();
         l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-        fence_proxy_async_smem();
         tc_fence_before();
         warp_arrive(p_full(sl), lane);
-        ++pc;
       }
       if (!ok || !(ok = warp_wait(o_full(sl), oc & 1, c, A.err, lane))) break;
       tc_fence_after();
