@@ -114,25 +114,39 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
 // 7.1.26 (Hastings' rational approximation, |error| <= 1.5e-7 for z >= 0):
 //   erf(z) = 1 - t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-z^2),
 //   t = 1 / (1 + p z),
-// extended to z < 0 by odd symmetry.  Branch-free: one reciprocal and one
-// exponential per element; exp(-z^2) = exp(-x^2 / 2) is also the Gaussian
-// density the backward needs.  The lower tail Phi(x) = erfc(|x| / sqrt 2) / 2
-// (x < 0) is taken directly, without the cancellation of 1 - erf.
+// extended to z < 0 by odd symmetry.  The lower tail Phi(x) = erfc(|x| / sqrt 2) / 2
+// (x < 0) is taken directly, without the cancellation of 1 - erf; the 1/2
+// rides in the coefficients (exact: a power of two).  exp(-z^2) is
+// 2^(-z^2 log2 e) on the special-function unit, and is also the Gaussian
+// density the backward needs.  Branch-free: one reciprocal and one
+// exponential per element.
+//
+// Two forms, with the same operations in the same order (so the same bits):
+// one value at a time, and two at once on the paired fp32 pipe (fma / mul
+// .f32x2: one instruction for both halves), which the epilogue's fast path
+// uses - GELU is bound by instruction issue there.
 __device__ __forceinline__ float rcp_approx(float x) {
   float r;
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
   return r;
 }
+namespace gelu_c {
+constexpr float kRsqrt2 = 0.70710678118654752f, kP = 0.3275911f, kNegLog2e = -1.44269504088896341f;
+constexpr float kA1 = 0.5f * 0.254829592f, kA2 = 0.5f * -0.284496736f, kA3 = 0.5f * 1.421413741f,
+                kA4 = 0.5f * -1.453152027f, kA5 = 0.5f * 1.061405429f;
+constexpr float kRsqrt2pi = 0.39894228040143268f;
+}  // namespace gelu_c
 __device__ __forceinline__ float gauss_cdf(float x, float& e) {
-  const float z = fabsf(x) * 0.70710678118654752f;
-  const float t = rcp_approx(fmaf(0.3275911f, z, 1.0f));
-  float p = fmaf(t, 1.061405429f, -1.453152027f);
-  p = fmaf(t, p, 1.421413741f);
-  p = fmaf(t, p, -0.284496736f);
-  p = fmaf(t, p, 0.254829592f);
-  e = __expf(-z * z);
-  const float tail = 0.5f * (p * t) * e;  // erfc(|x| / sqrt 2) / 2
-  return x < 0.0f ? tail : 1.0f - tail;
+  using namespace gelu_c;
+  const float z = fabsf(x) * kRsqrt2;
+  const float t = rcp_approx(fmaf(z, kP, 1.0f));
+  float p = fmaf(t, kA5, kA4);
+  p = fmaf(t, p, kA3);
+  p = fmaf(t, p, kA2);
+  p = fmaf(t, p, kA1);
+  e = ex2_approx(z * (z * kNegLog2e));
+  const float tail = (p * t) * e;  // erfc(|x| / sqrt 2) / 2
+  return x < 0.0f ? tail : fmaf(tail, -1.0f, 1.0f);
 }
 __device__ __forceinline__ float gelu_f(float x) {
   float e;
@@ -141,7 +155,77 @@ __device__ __forceinline__ float gelu_f(float x) {
 __device__ __forceinline__ float gelu_grad_f(float x) {
   float e;
   const float cdf = gauss_cdf(x, e);
-  return fmaf(x * 0.39894228040143268f, e, cdf);  // Phi(x) + x phi(x)
+  return fmaf(x * gelu_c::kRsqrt2pi, e, cdf);  // Phi(x) + x phi(x)
+}
+
+// two fp32 values in one 64-bit register pair
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 pk2(float a, float b) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void upk2(f32x2 v, float& a, float& b) { asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v)); }
+__device__ __forceinline__ f32x2 splat2(float a) { return pk2(a, a); }
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// gauss_cdf of both halves of X: the cdfs and exp(-x^2 / 2)
+__device__ __forceinline__ void gauss_cdf2(f32x2 X, f32x2& C, f32x2& E) {
+  using namespace gelu_c;
+  const f32x2 Z = mul2(X & 0x7fffffff7fffffffull, splat2(kRsqrt2));
+  float d0, d1;
+  upk2(fma2(Z, splat2(kP), splat2(1.0f)), d0, d1);
+  const f32x2 T = pk2(rcp_approx(d0), rcp_approx(d1));
+  f32x2 Pp = fma2(T, splat2(kA5), splat2(kA4));
+  Pp = fma2(T, Pp, splat2(kA3));
+  Pp = fma2(T, Pp, splat2(kA2));
+  Pp = fma2(T, Pp, splat2(kA1));
+  float q0, q1;
+  upk2(mul2(Z, mul2(Z, splat2(kNegLog2e))), q0, q1);
+  E = pk2(ex2_approx(q0), ex2_approx(q1));
+  const f32x2 TL = mul2(mul2(Pp, T), E);
+  float t0, t1, o0, o1, x0, x1;
+  upk2(TL, t0, t1);
+  upk2(fma2(TL, splat2(-1.0f), splat2(1.0f)), o0, o1);
+  upk2(X, x0, x1);
+  C = pk2(x0 < 0.0f ? t0 : o0, x1 < 0.0f ? t1 : o1);
+}
+// x[e], x[e + 1] = GELU of themselves
+__device__ __forceinline__ void gelu_pair(float& a, float& b) {
+  const f32x2 X = pk2(a, b);
+  f32x2 C, E;
+  gauss_cdf2(X, C, E);
+  upk2(mul2(X, C), a, b);
+}
+// a, b *= GELU'(za), GELU'(zb)
+__device__ __forceinline__ void gelu_grad_mul_pair(float za, float zb, float& a, float& b) {
+  const f32x2 Zv = pk2(za, zb);
+  f32x2 C, E;
+  gauss_cdf2(Zv, C, E);
+  const f32x2 G = fma2(mul2(Zv, splat2(gelu_c::kRsqrt2pi)), E, C);
+  upk2(mul2(pk2(a, b), G), a, b);
+}
+// x[0..7] (+)= and *= on pairs
+__device__ __forceinline__ void add8_pairs(float* x, const float* y) {
+#pragma unroll
+  for (int e = 0; e < 8; e += 2) upk2(add2(pk2(x[e], x[e + 1]), pk2(y[e], y[e + 1])), x[e], x[e + 1]);
+}
+__device__ __forceinline__ void scale8_pairs(float* x, float s) {
+#pragma unroll
+  for (int e = 0; e < 8; e += 2) upk2(mul2(pk2(x[e], x[e + 1]), splat2(s)), x[e], x[e + 1]);
 }
 
 __device__ __forceinline__ void unpack8(const uint4& v, float* f) {
@@ -304,31 +388,27 @@ __device__ __forceinline__ void epilogue_tile(const GemmProblem& P, const TileIn
         float x[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) x[e] = any_k ? __uint_as_float(r[v * 8 + e]) : 0.0f;
-        if (scaled) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] *= alpha;
-        }
+        // the arithmetic on pairs of columns (the paired fp32 pipe)
+        if (scaled) scale8_pairs(x, alpha);
         if (bias) {
           float bb[8];
           unpack8(bv[v], bb);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] += bb[e];
+          add8_pairs(x, bb);
         }
         if (P.epi.zsave) sv[v] = pack8(x);
         if (P.epi.act == EPI_GELU) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = gelu_f(x[e]);
+          for (int e = 0; e < 8; e += 2) gelu_pair(x[e], x[e + 1]);
         } else if (P.epi.act == EPI_GELU_BWD) {
           float zz[8];
           unpack8(sv[v], zz);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] *= gelu_grad_f(zz[e]);
+          for (int e = 0; e < 8; e += 2) gelu_grad_mul_pair(zz[e], zz[e + 1], x[e], x[e + 1]);
         }
         if (P.epi.resid) {
           float rr[8];
           unpack8(sv[v], rr);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] += rr[e];
+          add8_pairs(x, rr);
         }
         if (!f32) {
           yv[v] = h16 ? pack8h(x, P.err) : pack8(x);
