@@ -162,7 +162,10 @@ class MlpBench:
         self.Y1 = torch.empty(M * f, device=dev, dtype=bf)
         self.Y = torch.empty(M * h, device=dev, dtype=bf)
         self.units = 4.0 * M * h * f
-        self.launches = 2
+        # one chained launch for a small block, else two GEMM launches
+        st, n, splits = t.tp3d_mlp_plan(ctx, q, M, h, f)
+        t.check(st, "tp3d_mlp_plan")
+        self.launches, self.splits = n, splits
         self.unit, self.scale = "TFLOP/s", 1e12
         self.X_host = self.X.cpu().pin_memory()
         self.Y_host = torch.empty(M * h, dtype=bf).pin_memory()
@@ -182,6 +185,12 @@ class MlpBench:
 
     def kernel_probe(self):
         w = self.w
+        if self.launches == 1:  # the whole block is the one kernel
+            fl = 4.0 * w["M"] * w["h"] * w["f"]
+            return self.step, fl, (f"gemm_chain_kernel (the MLP block as one persistent launch of CTA pairs: "
+                                   f"linear 1 + bias + GELU feeding linear 2 + bias, second contraction in "
+                                   f"{self.splits} part(s); M={w['M']}, h={w['h']}, f={w['f']}, q={w['q']}), "
+                                   f"{fl / 1e9:.2f} GFLOP per launch")
 
         def launch():
             self.t.check(self.t.tp3d_linear(self.ctx, w["q"], 0, w["M"], w["h"], w["f"], self.t.TP3D_BF16, self.X,

@@ -165,10 +165,31 @@ tp3d_status tp3d_linear(tp3d_ctx* ctx, int q, int y, int64_t M, int64_t N, int64
  *   Y  = Y1.W2 + b2        (3-D linear with y = 1: W2 CUBE_B_SWAP, Y CUBE_A)
  * X: M x h, W1: h x f, W2: f x h, b1: f, b2: h (either bias may be NULL).
  * Y1 (M x f, CUBE_C) is caller-owned scratch that also returns the hidden
- * activation.  bf16 only.                                                    */
+ * activation.  bf16 only.
+ *
+ * A block whose operands (X, W1, Y1, W2) total at most 64 MiB runs as ONE
+ * persistent launch (the row tiles of the first GEMM feed the second's
+ * contraction as soon as they are stored; the second GEMM's contraction may
+ * be cut in two halves whose fp32 partial sums are added in a fixed order);
+ * a larger block runs as two GEMM launches.  tp3d_mlp_plan says which.  The
+ * one launch uses a device scratch owned by the context (counters and, with
+ * two halves, M x h fp32 partial sums): the first call that needs it, or
+ * more of it, allocates it (cudaMalloc, after a cudaDeviceSynchronize if it
+ * replaces a smaller one), so make that call before any stream capture, and
+ * order the context's tp3d_mlp calls on one stream (they share the scratch).
+ * The launch's clusters wait on each other's progress with bounded waits; a
+ * wait that runs out (only possible if the device cannot keep its clusters
+ * resident, e.g. beside another such launch) raises TP3D_ETIMEOUT.          */
 tp3d_status tp3d_mlp(tp3d_ctx* ctx, int q, int64_t M, int64_t h, int64_t f, tp3d_dtype dtype,
                      const void* X, const void* W1, const void* b1, const void* W2,
                      const void* b2, void* Y1, void* Y, void* stream);
+
+/* How tp3d_mlp (and tp3d_mlp_noalloc) run a bf16 block of these sizes on
+ * this context's device: *launches = 1 for the one chained launch, with
+ * *splits = 1 or 2 (the second GEMM's contraction halves), or 2 for two GEMM
+ * launches (*splits = 0).  Launches nothing; errors as tp3d_mlp's shape
+ * checks.                                                                    */
+tp3d_status tp3d_mlp_plan(tp3d_ctx* ctx, int q, int64_t M, int64_t h, int64_t f, int* launches, int* splits);
 
 /* The same MLP block in the layouts the pages compare the cube with
  * ("Maximizing Parallelism in Distributed Training for Huge Neural
@@ -200,11 +221,13 @@ tp3d_status tp3d_mlp_layout(tp3d_ctx* ctx, int scheme, int p, int64_t M, int64_t
  * Y1 lives in a fixed array of 8 Mi bf16 elements (16 MiB) in this
  * library's device memory, which every GPU that loads the library keeps
  * until the process exits; M * f must be <= 8388608, else TP3D_EUNSUPPORTED
- * and nothing is launched.  The call allocates nothing.
+ * and nothing is launched.  The chained launch's scratch is a second fixed
+ * array (32 MiB: M * h <= 8388608 when that launch cuts the contraction in
+ * two, else TP3D_EUNSUPPORTED).  The call allocates nothing.
  *   - The first call on a device looks up the array's device address (one
  *     cudaGetSymbolAddress with that device current) and caches it; make
  *     that first call before any stream capture.
- *   - Every call, on every stream, shares the one array, which keeps the last
+ *   - Every call, on every stream, shares the arrays, which keep the last
  *     call's contents; calls that overlap on the GPU race.  Y1 is fully
  *     written before it is read, so nothing needs clearing between calls.
  * Other arguments, layouts and errors as tp3d_mlp.                           */

@@ -6,8 +6,8 @@ relative error" the bars below apply to.
 
 rel_err = max_i |g_i - o_i| / max(|o_i|, rms(o)): element-wise relative error
 with a floor at the RMS of the oracle's output; stricter, and the bar for the
-single-GEMM paths (3-D linear, MLP), which keep no bf16 intermediate between
-their fp32 accumulation and the output.
+single-GEMM paths (the 3-D linear, and the MLP's hidden activation Y1), which
+keep no bf16 intermediate between their fp32 accumulation and the output.
 
 fro_err: Frobenius-norm relative error, reported and bounded beside them.
 
@@ -25,6 +25,13 @@ layer measures plus a margin of 1.3x:
     more) dX is heavy-tailed (max |dX| / rms(dX) about 9) and its largest
     absolute error, 0.0062 max |dX|, falls on an element below the RMS
     floor, which reads as 0.058; so 0.075.
+The MLP's output Y is downstream of one bf16 intermediate: the hidden
+activation Y1 is stored in bf16 and read back by the second GEMM (the oracle
+keeps it exact), and Y is rounded again.  Two roundings of unit roundoff
+u = 2^-9 on the path of each of n outputs give an element-wise metric of up
+to about sqrt(2 ln n) * sqrt(2) * u = 0.015 for n = 2^21 (the q = 2 block's
+2048 x 1024 output): MLP_ELEM_TOL.  Measured: up to 0.0119 on that block.
+Y's max-normalised and Frobenius errors keep the 1e-2 bar.
 """
 from __future__ import annotations
 
@@ -62,3 +69,4 @@ BF16_TOL = 1e-2
 F32_TOL = 1e-4
 LAYER_ELEM_TOL = 0.045
 LAYER_ELEM_TOL_PEAKED = 0.075
+MLP_ELEM_TOL = 0.015

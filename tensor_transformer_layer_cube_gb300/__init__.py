@@ -28,7 +28,7 @@ __all__ = [
     "build", "lib", "Tp3dError", "check", "STATUS", "layout",
     "tp3d_create", "tp3d_destroy", "tp3d_status_string", "tp3d_sync_status", "tp3d_reshard",
     "tp3d_set_wait_limit_ns", "tp3d_inject_load_stall",
-    "tp3d_linear", "tp3d_mlp", "tp3d_mlp_noalloc", "tp3d_layer_workspace_bytes", "tp3d_layer_fwd", "tp3d_layer_bwd",
+    "tp3d_linear", "tp3d_mlp", "tp3d_mlp_plan", "tp3d_mlp_noalloc", "tp3d_layer_workspace_bytes", "tp3d_layer_fwd", "tp3d_layer_bwd",
     "tp3d_layout", "tp3d_layer_cfg", "tp3d_layer_params", "tp3d_layer_grads",
     "TP3D_F32", "TP3D_BF16", "CUBE_A", "CUBE_B", "CUBE_C", "CUBE_B_SWAP", "ROW", "COL", "BLOCK2D", "REPLICATED",
     "tp3d_rect", "tp3d_mesh_spec", "tp3d_cmr_options", "tp3d_cmr_result", "tp3d_pipe_cfg", "tp3d_pipe_op",
@@ -138,6 +138,8 @@ _SIGS = {
     "tp3d_mlp": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                 ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "tp3d_mlp_plan": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                     ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
     "tp3d_mlp_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
                                         ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
@@ -248,6 +250,13 @@ def tp3d_linear(ctx, q, y, M, N, K, dtype, A, B, bias, act, C, stream=None) -> i
 
 def tp3d_mlp(ctx, q, M, h, f, dtype, X, W1, b1, W2, b2, Y1, Y, stream=None) -> int:
     return lib().tp3d_mlp(ctx, q, M, h, f, dtype, _p(X), _p(W1), _p(b1), _p(W2), _p(b2), _p(Y1), _p(Y), _s(stream))
+
+
+def tp3d_mlp_plan(ctx, q, M, h, f):
+    """(status, launches, splits): how tp3d_mlp runs a block of these sizes."""
+    n, s = ctypes.c_int(0), ctypes.c_int(0)
+    st = lib().tp3d_mlp_plan(ctx, q, M, h, f, ctypes.byref(n), ctypes.byref(s))
+    return st, n.value, s.value
 
 
 def tp3d_mlp_noalloc(ctx, q, M, h, f, dtype, X, W1, b1, W2, b2, Y, stream=None) -> int:

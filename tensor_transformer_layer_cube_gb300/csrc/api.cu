@@ -84,6 +84,29 @@ static tp3d_layout layout_of(int kind, int a, int b) {
   return l;
 }
 
+// The context's scratch, at least `bytes` long.  Growing it waits for the
+// device (an earlier launch may still use the old one) and zeroes the new one.
+tp3d_status ctx_scratch(tp3d_ctx* ctx, size_t bytes, void** out) {
+  if (ctx->scratch_bytes < bytes) {
+    if (ctx->scratch) {
+      TP3D_CUDA_TRY(cudaDeviceSynchronize());
+      TP3D_CUDA_TRY(cudaFree(ctx->scratch));
+      ctx->scratch = nullptr;
+      ctx->scratch_bytes = 0;
+    }
+    void* p = nullptr;
+    TP3D_CUDA_TRY(cudaMalloc(&p, bytes));
+    if (cudaMemset(p, 0, bytes) != cudaSuccess) {
+      cudaFree(p);
+      return TP3D_ECUDA;
+    }
+    ctx->scratch = p;
+    ctx->scratch_bytes = bytes;
+  }
+  *out = ctx->scratch;
+  return TP3D_OK;
+}
+
 }  // namespace tp3d
 
 using namespace tp3d;
@@ -130,6 +153,7 @@ void tp3d_destroy(tp3d_ctx* ctx) {
     if (ctx->ev_join[k]) cudaEventDestroy(ctx->ev_join[k]);
   }
   if (ctx->ev_fork) cudaEventDestroy(ctx->ev_fork);
+  if (ctx->scratch) cudaFree(ctx->scratch);
   free(ctx);
 }
 
@@ -219,8 +243,36 @@ tp3d_status tp3d_mlp(tp3d_ctx* ctx, int q, int64_t M, int64_t h, int64_t f, tp3d
     if (overlaps(Y1, y1b, in.p, in.n) || overlaps(Y, yb, in.p, in.n)) return TP3D_EOVERLAP;
   if (overlaps(Y, yb, Y1, y1b)) return TP3D_EOVERLAP;
   const cudaStream_t s = as_stream(stream);
+  // one chained launch where the block is small enough for it, else the two GEMMs
+  ChainShape sh;
+  if (chain_plan(ctx, P1, P2, &sh)) {
+    void* scratch = nullptr;
+    TP3D_TRY(ctx_scratch(ctx, sh.scratch_bytes, &scratch));
+    return gemm_chain_tc(ctx, P1, P2, sh, scratch, s);
+  }
   TP3D_TRY(gemm_bf16_tc(ctx, P1, s));
   return gemm_bf16_tc(ctx, P2, s);
+}
+
+tp3d_status tp3d_mlp_plan(tp3d_ctx* ctx, int q, int64_t M, int64_t h, int64_t f, int* launches, int* splits) {
+  if (!ctx || !launches || !splits) return TP3D_EINVAL;
+  if (q < 1 || q > 16 || M <= 0 || h <= 0 || f <= 0) return TP3D_EINVAL;
+  // planning reads only the layouts: stand-in addresses (Y1's the same in both)
+  static const uint8_t x = 0, w1 = 0, w2 = 0, y1 = 0, y = 0;
+  GemmProblem P1, P2;
+  TP3D_TRY(plan_linear(ctx, q, 0, M, h, f, &x, &w1, nullptr, 1, (void*)&y1, &P1));
+  TP3D_TRY(plan_linear(ctx, q, 1, M, f, h, &y1, &w2, nullptr, 0, (void*)&y, &P2));
+  for (const GemmProblem* P : {&P1, &P2})
+    if (P->a.g.bw % 8 || P->b.g.bw % 8 || P->c.g.bw % 8) return TP3D_ESHAPE;
+  ChainShape sh;
+  if (chain_plan(ctx, P1, P2, &sh)) {
+    *launches = 1;
+    *splits = sh.splits;
+  } else {
+    *launches = 2;
+    *splits = 0;
+  }
+  return TP3D_OK;
 }
 
 tp3d_status tp3d_mlp_layout(tp3d_ctx* ctx, int scheme, int p, int64_t M, int64_t h, int64_t f, tp3d_dtype dtype,

@@ -24,6 +24,11 @@ struct tp3d_ctx {
   // it before the call returns)
   cudaStream_t side[2];
   cudaEvent_t ev_fork, ev_join[2];
+  // device scratch of the chained MLP launch (counters, then fp32 partial
+  // sums), grown on demand by a call that needs more; its counters are zero
+  // between calls
+  void* scratch;
+  size_t scratch_bytes;
 };
 
 namespace tp3d {
@@ -173,6 +178,38 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 // make this thread's generic-proxy shared-memory writes visible to the async (TMA) proxy
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// order this thread's async-proxy (TMA) global accesses with its generic ones
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// global counters between CTAs of one launch: a release add, and a bounded
+// acquire wait until the counter reaches `target` (false: the wait ran out or
+// the CTA aborted; the error word and abort flag are then set as mbar_wait does)
+__device__ __forceinline__ void counter_add_release(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int counter_load_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ bool counter_wait_geq(const int* p, int target, volatile int* abort_flag, int* err) {
+  if (counter_load_acquire(p) >= target) return true;
+  const unsigned long long t0 = globaltimer_ns(), lim = wait_limit_ns(err);
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(128);
+    if (counter_load_acquire(p) >= target) return true;
+    if ((it & 7u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > lim) {
+        *abort_flag = 1;
+        raise_error(err, TP3D_ETIMEOUT);
+        return false;
+      }
+    }
+  }
 }
 
 // ---------------------------------------------------------------- tcgen05

@@ -87,6 +87,20 @@ TP3D_HD int64_t op_off(int64_t hi, int64_t lo, int64_t base, int32_t z, int32_t 
 tp3d_status gemm_bf16_tc(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t s);
 tp3d_status gemm_f32_simt(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t s);
 
+// Two GEMMs in one launch, the second's A being the first's output (the MLP
+// block; gemm_tc.cu).  chain_plan says whether (P0, P1) qualify and how the
+// launch divides them; gemm_chain_tc runs it on a device scratch of
+// scratch_bytes whose first counter_bytes hold counters that start at zero
+// (each launch leaves them zero again).
+struct ChainShape {
+  int64_t units0, units1, n_ready, n_fix;
+  int32_t splits, ready_target, clusters;
+  size_t counter_bytes, scratch_bytes;
+};
+bool chain_plan(const tp3d_ctx* ctx, const GemmProblem& P0, const GemmProblem& P1, ChainShape* sh);
+tp3d_status gemm_chain_tc(const tp3d_ctx* ctx, const GemmProblem& P0, const GemmProblem& P1, const ChainShape& sh,
+                          void* scratch, cudaStream_t s);
+
 // Fills segment lengths from the operand grids; returns TP3D_ESHAPE if the
 // blocks of the operands do not nest or the extents do not divide.
 tp3d_status plan_segments(GemmProblem& P);

@@ -266,6 +266,12 @@ __device__ __forceinline__ uint4 pack8h(const float* f, int* err) {
 }
 
 
+// arrive on a peer's mbarrier without a memory release: what it orders is the
+// warp's tensor-memory reads, which tcgen05.fence::before_thread_sync covers
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 // One tile's epilogue for the calling epilogue warp (32 rows x BN/2 columns
 // of the tile's TMEM accumulator `buf`).  Warp w may read TMEM lanes
 // 32*(w%4) .. +31 only: two warps share each lane quarter (= 32 rows of the
@@ -344,7 +350,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmProblem& P, const TileIn
       __syncwarp();
       if (lane == 0) {
         if (tempty_remote)
-          mbar_arrive_remote(tempty);
+          mbar_arrive_remote_relaxed(tempty);
         else
           mbar_arrive(tempty);
       }
@@ -373,10 +379,6 @@ __device__ __forceinline__ void epilogue_tile(const GemmProblem& P, const TileIn
           sv[v] = *reinterpret_cast<const uint4*>(stg + 2048 + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4));
         __syncwarp();
         if (cc + 1 < CH && fast(cc + 1)) aux_issue(cc + 1);
-      }
-      if (f32 && stores) {  // fp32 rows fill the whole staging buffer: wait before writing
-        if (lane == 0) bulk_wait_read_all();
-        __syncwarp();
       }
       // bf16 output without an auxiliary input or saved pre-activation uses
       // both 2 KiB halves of the staging buffer in turn
@@ -417,10 +419,29 @@ __device__ __forceinline__ void epilogue_tile(const GemmProblem& P, const TileIn
             for (int e = 0; e < 8; ++e) cmax = fmaxf(cmax, fabsf(x[e]));
           }
         } else {
-          *reinterpret_cast<float4*>(stg + lane * 128 + (((2 * v) ^ (lane & 7)) << 4)) = make_float4(x[0], x[1], x[2], x[3]);
-          *reinterpret_cast<float4*>(stg + lane * 128 + (((2 * v + 1) ^ (lane & 7)) << 4)) = make_float4(x[4], x[5], x[6], x[7]);
+          // fp32: each 16-column half (two groups) goes out by its own TMA
+          // store from the staging half the store before last used
+          if ((v & 1) == 0 && stores) {
+            if (lane == 0) bulk_wait_read_1();
+            __syncwarp();
+          }
+          uint8_t* hb = stg + (stores & 1u) * 2048u;
+          const int u0 = 2 * (v & 1);
+          *reinterpret_cast<float4*>(hb + lane * 64 + ((u0 ^ ((lane >> 1) & 3)) << 4)) = make_float4(x[0], x[1], x[2], x[3]);
+          *reinterpret_cast<float4*>(hb + lane * 64 + (((u0 + 1) ^ ((lane >> 1) & 3)) << 4)) =
+              make_float4(x[4], x[5], x[6], x[7]);
+          if (v & 1) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(mapC, smem_u32(hb), chunk_c0(cc) + 16 * (v >> 1), c1, c2);
+              bulk_commit();
+            }
+            ++stores;
+          }
         }
       }
+      if (f32) continue;  // stored half by half above
       if (!f32) {
         if (stores) {
           // double-buffered: the store that last used this half was issued two chunks ago
@@ -1119,6 +1140,495 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------- chained GEMMs
+// Two GEMMs in one persistent launch of CTA pairs, the second (job 1) reading
+// the first's output (job 0) as its A operand: the MLP block of "Maximizing
+// Parallelism in Distributed Training for Huge Neural Networks" §3.2, Y1 =
+// GELU(X W1 + b1) feeding Y = Y1 W2 + b2 (the column-then-row split of
+// Megatron's "Tensor parallelism").  The launch's work units are job 0's
+// tiles, then job 1's tiles (times its contraction splits), each kind with
+// the row tiles slowest, dealt to the clusters round-robin; every cluster
+// takes its units in increasing order.
+//  - A job-1 unit needs the rows of Y1 it contracts over: job 0's epilogue
+//    warps count each finished tile (after its TMA stores have completed)
+//    into a counter per (row tile, contraction half), and job 1's producers
+//    wait for the full count before loading (bounded waits).  Job 1's units
+//    start while job 0's last tiles are still in their epilogues.
+//  - With two contraction halves, each half's unit writes its raw fp32 sums
+//    (the plain fp32 epilogue, TMA stores) to its own slot of a scratch.  Per
+//    epilogue-warp region (32 rows x 128 columns) a counter takes one arrival
+//    from each half; the warp that arrives second adds the two slots (slot 0
+//    first, so the sums do not depend on which half finished first), applies
+//    the bias, and writes the bf16 output, reading and writing whole rows.
+// Every wait is on a lower-numbered unit, so the launch cannot deadlock while
+// its clusters are resident (a cluster not yet resident starts when any
+// other kernel on the device leaves an SM); a wait that runs out raises
+// TP3D_ETIMEOUT like every other.  The last CTA to leave zeroes the counters
+// for the next launch.
+struct ChainArgs {
+  int64_t units0, units1;  // job 0 tiles; job 1 tiles x splits
+  int32_t splits;          // 1 or 2: job 1's contraction halves
+  int32_t ready_target;    // arrivals that complete one (row tile, half) of job 0's output
+  int* ready;              // [row tile][half]
+  int* fix;                // [job-1 tile][CTA][epilogue warp]: arrivals of the two halves
+  int* exits;              // CTAs that have left
+  int32_t n_ready, n_fix;
+  const float* part;       // the halves' sums: slot s holds rows s M .. s M + M - 1 (dense, N columns)
+};
+
+// The second half to finish adds both halves' sums for its warp's region
+// (rows T.m0 + 32 quarter .. +31, columns T.n0 + 128 half .. +127): lane l
+// takes columns 4l .. 4l + 3 of each row, so every read (512 bytes of fp32)
+// and write (256 bytes of bf16) of a row is one contiguous span.  Then
+// alpha, bias, GELU and residual as the tensor-memory epilogue applies them.
+__device__ __noinline__ void chain_fixup(const float* __restrict__ part, int64_t M, int64_t N, const Grid cg,
+                                         __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ bias,
+                                         const __nv_bfloat16* __restrict__ res, float alpha, int act, int64_t m0,
+                                         int64_t n0, int warp, int lane) {
+  const int quarter = warp & 3, hf = (warp - 2) >> 2;
+  const int64_t n = n0 + hf * 128 + lane * 4;
+  const int32_t bc = (int32_t)((uint32_t)n / (uint32_t)cg.bw);  // the region lies in one block column
+  float bb[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  if (bias) {
+    const __nv_bfloat162* bp = reinterpret_cast<const __nv_bfloat162*>(bias + n);
+    const float2 b0 = __bfloat1622float2(bp[0]), b1 = __bfloat1622float2(bp[1]);
+    bb[0] = b0.x; bb[1] = b0.y; bb[2] = b1.x; bb[3] = b1.y;
+  }
+  const int64_t mr = m0 + quarter * 32;
+  const int32_t br = (int32_t)((uint32_t)mr / (uint32_t)cg.bh);  // 32 rows inside one block row
+  const int64_t base = cg.block_base(br, bc) + (mr - (int64_t)br * cg.bh) * cg.bw + (n - (int64_t)bc * cg.bw);
+#pragma unroll 1
+  for (int i = 0; i < 32; i += 8) {
+    float4 a[8], b[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int64_t m = mr + i + u;
+      a[u] = __ldcg(reinterpret_cast<const float4*>(part + m * N + n));
+      b[u] = __ldcg(reinterpret_cast<const float4*>(part + (M + m) * N + n));
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int64_t off = base + (int64_t)(i + u) * cg.bw;
+      float x[4] = {a[u].x + b[u].x, a[u].y + b[u].y, a[u].z + b[u].z, a[u].w + b[u].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        x[e] = x[e] * alpha + bb[e];
+        if (act == EPI_GELU) x[e] = gelu_f(x[e]);
+      }
+      if (res) {
+        const __nv_bfloat162* rp = reinterpret_cast<const __nv_bfloat162*>(res + off);
+        const float2 r0 = __bfloat1622float2(rp[0]), r1 = __bfloat1622float2(rp[1]);
+        x[0] += r0.x; x[1] += r0.y; x[2] += r1.x; x[3] += r1.y;
+      }
+      __nv_bfloat162 h[2] = {__floats2bfloat162_rn(x[0], x[1]), __floats2bfloat162_rn(x[2], x[3])};
+      *reinterpret_cast<uint2*>(out + off) = *reinterpret_cast<const uint2*>(h);
+    }
+  }
+}
+
+// tile -> coordinates, row tiles slowest; tm_out = the row tile
+__device__ __forceinline__ void decode_rows_slow(const GemmProblem& P, uint32_t tile, uint32_t r, TileInfo& T,
+                                                 uint32_t& tm_out) {
+  const uint32_t segM = (uint32_t)P.segM, segN = (uint32_t)P.segN;
+  const uint32_t tpsM = (segM + 255u) / 256u, tpsN = (segN + 255u) / 256u;
+  const uint32_t tiles_n = udiv32(P.N, segN) * tpsN;
+  const uint32_t tm = tile / tiles_n, tn = tile - tm * tiles_n;
+  const uint32_t sm = tm / tpsM, sn = tn / tpsN;
+  T.z = 0;
+  T.m0 = (int64_t)sm * segM + (int64_t)(tm - sm * tpsM) * 256 + 128 * (int64_t)r;
+  T.n0 = (int64_t)sn * segN + (int64_t)(tn - sn * tpsN) * 256;
+  T.m_end = (int64_t)sm * segM + segM;
+  T.n_end = (int64_t)sn * segN + segN;
+  tm_out = tm;
+}
+
+struct ChainUnit {
+  int32_t job, s;     // job; contraction half (job 1)
+  uint32_t tile;      // the job's tile
+  int32_t sg0, sg1;   // contraction segments [sg0, sg1)
+};
+__device__ __forceinline__ ChainUnit chain_unit(const GemmProblem& P0, const GemmProblem& P1, const ChainArgs& C,
+                                                int64_t u) {
+  ChainUnit U;
+  if (u < C.units0) {
+    U.job = 0;
+    U.s = 0;
+    U.tile = (uint32_t)u;
+    U.sg0 = 0;
+    U.sg1 = (int32_t)udiv32(P0.K, P0.segK);
+  } else {
+    const uint32_t v = (uint32_t)(u - C.units0);
+    U.job = 1;
+    U.tile = v / (uint32_t)C.splits;
+    U.s = (int32_t)(v - U.tile * (uint32_t)C.splits);
+    const int32_t per = (int32_t)udiv32(P1.K, P1.segK) / C.splits;
+    U.sg0 = U.s * per;
+    U.sg1 = U.sg0 + per;
+  }
+  return U;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_chain_kernel(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapB0,
+                      const __grid_constant__ CUtensorMap mapC0, const __grid_constant__ CUtensorMap mapZ0,
+                      const __grid_constant__ CUtensorMap mapX0, const __grid_constant__ CUtensorMap mapA1,
+                      const __grid_constant__ CUtensorMap mapB1, const __grid_constant__ CUtensorMap mapC1,
+                      const __grid_constant__ CUtensorMap mapZ1, const __grid_constant__ CUtensorMap mapX1,
+                      const __grid_constant__ CUtensorMap mapP, const __grid_constant__ GemmProblem P0,
+                      const __grid_constant__ GemmProblem P1, const __grid_constant__ GemmProblem P1h,
+                      const uint32_t wide0, const uint32_t wide1, const __grid_constant__ ChainArgs C) {
+  using Cfg = Tc2Cfg<128>;
+  constexpr int S = Cfg::STAGES;
+  constexpr int BKP = Cfg::BKP;
+  constexpr int BN = Cfg::BN;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  uint8_t* stage_out = base_ptr + S * Cfg::STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stage_out + kEpiWarps * Cfg::STAGE_OUT);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 5 + kEpiWarps);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* last_cta = const_cast<int*>(abort_flag) + 1;
+
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * S + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * S + 2 + b); };
+  const uint32_t final_bar = bar0 + 8u * (2 * S + 4);
+  auto aux_bar = [&](int ew) { return bar0 + 8u * (2 * S + 5 + ew); };
+  auto a_stage = [&](int s) { return base + (uint32_t)(s * Cfg::A_BYTES); };
+  auto b_stage = [&](int s) { return base + (uint32_t)(S * Cfg::A_BYTES + s * Cfg::B_BYTES); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 2 * kEpiWarps);
+    }
+    mbar_init(final_bar, 1);
+    for (int e = 0; e < kEpiWarps; ++e) mbar_init(aux_bar(e), 1);
+    *abort_flag = 0;
+    *last_cta = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_holder), Cfg::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&mapA0);
+    tma_prefetch_map(&mapB0);
+    tma_prefetch_map(&mapA1);
+    tma_prefetch_map(&mapB1);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  const int64_t nunits = C.units0 + C.units1;
+  const int64_t nclusters = gridDim.x >> 1, cid = blockIdx.x >> 1;
+  // both jobs have the same operand majors and input type (the launcher checks)
+  const bool a_mn = P0.a.mn_major != 0, b_mn = P0.b.mn_major != 0;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- producer
+      struct UnitLd {
+        int32_t job, sg0, sg1, wait_idx;
+        int64_t ak, bk;
+        int32_t a_br, b_br, a_c1, b_c1;
+        int32_t a_bc[2], b_bc[2], a_c0[2], b_c0[2];
+      };
+      auto setup = [&](int64_t u, UnitLd& L) {
+        const ChainUnit U = chain_unit(P0, P1, C, u);
+        const GemmProblem& P = U.job ? P1 : P0;
+        TileInfo T;
+        uint32_t tm;
+        decode_rows_slow(P, U.tile, rank, T, tm);
+        L.job = U.job;
+        L.sg0 = U.sg0;
+        L.sg1 = U.sg1;
+        L.wait_idx = U.job ? (int32_t)(tm * (uint32_t)C.splits) + U.s : -1;
+        const int64_t am = T.m0 + op_off(P.a.hi1, P.a.lo1, P.a.base1, T.z, P.Hz);
+        L.ak = op_off(P.a.hi2, P.a.lo2, P.a.base2, T.z, P.Hz);
+        L.bk = op_off(P.b.hi1, P.b.lo1, P.b.base1, T.z, P.Hz);
+        const int64_t bn = T.n0 + 128 * (int64_t)rank + op_off(P.b.hi2, P.b.lo2, P.b.base2, T.z, P.Hz);
+        if (!a_mn) {
+          L.a_br = (int32_t)udiv32(am, P.a.g.bh);
+          L.a_c1 = (int32_t)(am - (int64_t)L.a_br * P.a.g.bh);
+        } else {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            L.a_bc[h] = (int32_t)udiv32(am + 64 * h, P.a.g.bw);
+            L.a_c0[h] = (int32_t)(am + 64 * h - (int64_t)L.a_bc[h] * P.a.g.bw);
+          }
+        }
+        if (!b_mn) {
+          L.b_br = (int32_t)udiv32(bn, P.b.g.bh);
+          L.b_c1 = (int32_t)(bn - (int64_t)L.b_br * P.b.g.bh);
+        } else {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            L.b_bc[h] = (int32_t)udiv32(bn + 64 * h, P.b.g.bw);
+            L.b_c0[h] = (int32_t)(bn + 64 * h - (int64_t)L.b_bc[h] * P.b.g.bw);
+          }
+        }
+      };
+      uint32_t it = 0;
+      bool ok = true;
+      UnitLd cur = {}, nxt = {};
+      if (cid < nunits) setup(cid, cur);
+      for (int64_t u = cid; u < nunits && ok; u += nclusters) {
+        const GemmProblem& P = cur.job ? P1 : P0;
+        const CUtensorMap* mA = cur.job ? &mapA1 : &mapA0;
+        const CUtensorMap* mB = cur.job ? &mapB1 : &mapB0;
+        const uint32_t wide = cur.job ? wide1 : wide0;
+        if (cur.wait_idx >= 0) {
+          // job 1 reads rows of Y1 that job 0's epilogues store: wait for all of them
+          if (!counter_wait_geq(C.ready + cur.wait_idx, C.ready_target, abort_flag, P.err)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_global();  // the TMA loads below see those stores
+        }
+        const int32_t segK = (int32_t)P.segK, tpsK = segK / BKP;
+        const int64_t ak = cur.ak, bk = cur.bk;
+        const int64_t a_br = cur.a_br, b_br = cur.b_br;
+        const int a_c1 = cur.a_c1, b_c1 = cur.b_c1;
+        const int64_t a_bc[2] = {cur.a_bc[0], cur.a_bc[1]}, b_bc[2] = {cur.b_bc[0], cur.b_bc[1]};
+        const int a_c0[2] = {cur.a_c0[0], cur.a_c0[1]}, b_c0[2] = {cur.b_c0[0], cur.b_c0[1]};
+        bool next_ready = false;
+        for (int32_t sg = cur.sg0; sg < cur.sg1 && ok; ++sg) {
+          const int64_t ks = (int64_t)sg * segK;
+          int a_k = 0, b_k = 0, a_sh = 0, b_sh = 0;
+          int a_shh[2], b_shh[2];
+          if (!a_mn) {
+            const int64_t bc = udiv32(ak + ks, P.a.g.bw);
+            a_k = (int)(ak + ks - bc * P.a.g.bw);
+            a_sh = shard_or_oob(P.a.g, a_br, bc);
+          } else {
+            const int64_t br = udiv32(ak + ks, P.a.g.bh);
+            a_k = (int)(ak + ks - br * P.a.g.bh);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) a_shh[h] = shard_or_oob(P.a.g, br, a_bc[h]);
+          }
+          if (!b_mn) {
+            const int64_t bc = udiv32(bk + ks, P.b.g.bw);
+            b_k = (int)(bk + ks - bc * P.b.g.bw);
+            b_sh = shard_or_oob(P.b.g, b_br, bc);
+          } else {
+            const int64_t br = udiv32(bk + ks, P.b.g.bh);
+            b_k = (int)(bk + ks - br * P.b.g.bh);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) b_shh[h] = shard_or_oob(P.b.g, br, b_bc[h]);
+          }
+          for (int32_t kt = 0; kt < tpsK; ++kt) {
+            const int s = (int)(it % S);
+            const uint32_t ph = (it / S) & 1u;
+            if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, P.err)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = map_to_cta(full_bar(s), 0);
+            if (leader) mbar_arrive_expect_tx(full_bar(s), 2 * Cfg::STAGE_BYTES);
+            const int kofs = kt * BKP;
+            if (wide & 1u) {
+              if (!a_mn)
+                tma_load_4d_pair(a_stage(s), mA, fb, a_c1, (a_k + kofs) >> 6, a_sh);
+              else
+                tma_load_4d_pair(a_stage(s), mA, fb, a_k + kofs, a_c0[0] >> 6, a_shh[0]);
+            } else if (!a_mn) {
+#pragma unroll
+              for (int c = 0; c < BKP / 64; ++c)
+                tma_load_3d_pair(a_stage(s) + c * Cfg::KCHUNK, mA, fb, a_k + kofs + 64 * c, a_c1, a_sh);
+            } else {
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                tma_load_3d_pair(a_stage(s) + h * Cfg::MNBOX, mA, fb, a_c0[h], a_k + kofs, a_shh[h]);
+            }
+            if (wide & 2u) {
+              if (!b_mn)
+                tma_load_4d_pair(b_stage(s), mB, fb, b_c1, (b_k + kofs) >> 6, b_sh);
+              else
+                tma_load_4d_pair(b_stage(s), mB, fb, b_k + kofs, b_c0[0] >> 6, b_shh[0]);
+            } else if (!b_mn) {
+#pragma unroll
+              for (int c = 0; c < BKP / 64; ++c)
+                tma_load_3d_pair(b_stage(s) + c * Cfg::KCHUNK, mB, fb, b_k + kofs + 64 * c, b_c1, b_sh);
+            } else {
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                tma_load_3d_pair(b_stage(s) + h * Cfg::MNBOX, mB, fb, b_c0[h], b_k + kofs, b_shh[h]);
+            }
+            ++it;
+            if (!next_ready) {  // the unit's first stage is in flight: prepare the next unit
+              next_ready = true;
+              if (u + nclusters < nunits) setup(u + nclusters, nxt);
+            }
+          }
+        }
+        cur = nxt;
+      }
+      if (!ok && leader) {
+        const uint32_t first = it > (uint32_t)S ? it - S : 0u;
+        for (uint32_t j = first; j < it; ++j) mbar_wait_drain(full_bar((int)(j % S)), (j / S) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ---------------------------------------------------------- MMA issuer (even CTA)
+      const uint32_t idesc = P0.in_f16 ? idesc_f16_f32(256, BN, a_mn ? 1 : 0, b_mn ? 1 : 0)
+                                       : idesc_bf16_f32(256, BN, a_mn ? 1 : 0, b_mn ? 1 : 0);
+      const uint64_t adesc0 =
+          a_mn ? smem_desc_sw128(a_stage(0), Cfg::MNBOX, 1024u) : smem_desc_sw128(a_stage(0), 16u, 1024u);
+      const uint64_t bdesc0 =
+          b_mn ? smem_desc_sw128(b_stage(0), Cfg::MNBOX, 1024u) : smem_desc_sw128(b_stage(0), 16u, 1024u);
+      uint32_t it = 0, tc = 0;
+      bool ok = true;
+      for (int64_t u = cid; u < nunits && ok; u += nclusters) {
+        const ChainUnit U = chain_unit(P0, P1, C, u);
+        const GemmProblem& P = U.job ? P1 : P0;
+        const int32_t tpsK = (int32_t)P.segK / BKP;
+        const int buf = (int)(tc & 1u);
+        const uint32_t tph = (tc >> 1) & 1u;
+        if (!mbar_wait(tempty_bar(buf), tph ^ 1u, abort_flag, P.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+        bool first = true;
+        for (int32_t sg = U.sg0; sg < U.sg1 && ok; ++sg) {
+          for (int32_t kt = 0; kt < tpsK; ++kt) {
+            const int s = (int)(it % S);
+            const uint32_t ph = (it / S) & 1u;
+            if (!mbar_wait(full_bar(s), ph, abort_flag, P.err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t as0 = adesc0 + (uint64_t)((s * Cfg::A_BYTES) >> 4);
+            const uint64_t bs0 = bdesc0 + (uint64_t)((s * Cfg::B_BYTES) >> 4);
+#pragma unroll
+            for (int k16 = 0; k16 < BKP / 16; ++k16) {
+              const uint32_t kk = (uint32_t)(k16 >> 2) * Cfg::KCHUNK + (uint32_t)(k16 & 3) * 32u;
+              const uint64_t ad = as0 + (uint64_t)((a_mn ? k16 * 2048u : kk) >> 4);
+              const uint64_t bd = bs0 + (uint64_t)((b_mn ? k16 * 2048u : kk) >> 4);
+              umma_bf16_pair(d_tmem, ad, bd, idesc, (first && k16 == 0) ? 0u : 1u);
+            }
+            first = false;
+            umma_commit_pair_mc(empty_bar(s), 3);
+            ++it;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair_mc(tfull_bar(buf), 3);
+        ++tc;
+      }
+      umma_commit_pair_mc(final_bar, 1);
+      mbar_wait_drain(final_bar, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    uint32_t tc = 0;
+    uint32_t stores = 0;
+    uint32_t aux_phase = 0;
+    uint8_t* stg = stage_out + (warp - 2) * Cfg::STAGE_OUT;
+    float cmax = 0.0f;
+    for (int64_t u = cid; u < nunits; u += nclusters) {
+      const ChainUnit U = chain_unit(P0, P1, C, u);
+      const GemmProblem& P = U.job ? P1 : P0;
+      TileInfo T;
+      uint32_t tm;
+      decode_rows_slow(P, U.tile, rank, T, tm);
+      const int buf = (int)(tc & 1u);
+      const uint32_t tph = (tc >> 1) & 1u;
+      bool ok = lane == 0 ? mbar_wait(tfull_bar(buf), tph, abort_flag, P.err) : false;
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      tc_fence_after();
+      // a contraction half writes its raw sums into its slot (the plain fp32
+      // epilogue on rows s M + m of the scratch); every other unit its output
+      const bool split = U.job == 1 && C.splits == 2;
+      TileInfo Te = T;
+      if (split) {
+        Te.m0 += (int64_t)U.s * P1.M;
+        Te.m_end += (int64_t)U.s * P1.M;
+      }
+      const GemmProblem& Pe = split ? P1h : P;
+      const CUtensorMap* mc = split ? &mapP : U.job ? &mapC1 : &mapC0;
+      const CUtensorMap* mz = split ? &mapP : U.job ? &mapZ1 : &mapZ0;
+      const CUtensorMap* mx = split ? &mapP : U.job ? &mapX1 : &mapX0;
+      epilogue_tile<BN, false>(Pe, Te, true, buf, tmem_base, warp, lane, stg, mc, mz, mx, aux_bar(warp - 2),
+                               aux_phase, abort_flag, map_to_cta(tempty_bar(buf), 0), true, stores, cmax);
+      ++tc;
+      if (U.job == 0) {
+        // this warp's share of the tile is in memory (not just read out of
+        // shared memory) before the count says so
+        if (lane == 0) {
+          bulk_wait_all();
+          fence_proxy_async_global();
+          __threadfence();
+          const uint32_t half = (uint32_t)C.splits == 1u ? 0u : (uint32_t)T.n0 / ((uint32_t)P0.N / 2u);
+          counter_add_release(C.ready + tm * (uint32_t)C.splits + half, 1);
+        }
+        __syncwarp();
+      } else if (split) {
+        // the second of the two halves to reach this region adds them
+        int prev = 0;
+        if (lane == 0) {
+          bulk_wait_all();
+          fence_proxy_async_global();
+          __threadfence();
+          prev = atomicAdd(C.fix + ((int64_t)U.tile * 2 + rank) * kEpiWarps + (warp - 2), 1);
+          __threadfence();
+        }
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        if (prev == 1)
+          chain_fixup(C.part, P1.M, P1.N, P1.c.g, static_cast<__nv_bfloat16*>(const_cast<void*>(P1.c.ptr)),
+                      static_cast<const __nv_bfloat16*>(P1.epi.bias), static_cast<const __nv_bfloat16*>(P1.epi.resid),
+                      P1.epi.alpha, P1.epi.act, T.m0, T.n0, warp, lane);
+      }
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+  }
+  // the last CTA to leave zeroes the counters for the next launch (every
+  // wait of this launch is over once all other CTAs have left)
+  if (threadIdx.x == 0) {
+    __threadfence();
+    *last_cta = atomicAdd(C.exits, 1) == (int)gridDim.x - 1;
+  }
+  __syncthreads();
+  if (*last_cta) {
+    __threadfence();
+    for (int i = threadIdx.x; i < C.n_ready; i += blockDim.x) C.ready[i] = 0;
+    for (int i = threadIdx.x; i < C.n_fix; i += blockDim.x) C.fix[i] = 0;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) *C.exits = 0;
+  }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -1172,7 +1682,7 @@ tp3d_status launch(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t s) {
   TP3D_TRY(make_map(&mb, P.b.g, P.b.ptr, 64, P.b.mn_major ? 64 : BN));
   // output boxes: 32 rows x 32 columns (64-byte bf16 rows or 128-byte fp32 rows)
   if (P.epi.out_f32)
-    TP3D_TRY(make_map(&mc, P.c.g, P.c.ptr, 32, 32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, CU_TENSOR_MAP_SWIZZLE_128B));
+    TP3D_TRY(make_map(&mc, P.c.g, P.c.ptr, 16, 32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, CU_TENSOR_MAP_SWIZZLE_64B));
   else
     TP3D_TRY(make_map(&mc, P.c.g, P.c.ptr, 32, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, CU_TENSOR_MAP_SWIZZLE_64B));
   if (P.epi.zsave)
@@ -1243,7 +1753,7 @@ tp3d_status launch_pair(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t 
   else
     TP3D_TRY(make_map(&mb, P.b.g, P.b.ptr, 64, P.b.mn_major ? KD : 128));
   if (P.epi.out_f32)
-    TP3D_TRY(make_map(&mc, P.c.g, P.c.ptr, 32, 32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, CU_TENSOR_MAP_SWIZZLE_128B));
+    TP3D_TRY(make_map(&mc, P.c.g, P.c.ptr, 16, 32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, CU_TENSOR_MAP_SWIZZLE_64B));
   else
     TP3D_TRY(make_map(&mc, P.c.g, P.c.ptr, 32, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, CU_TENSOR_MAP_SWIZZLE_64B));
   if (P.epi.zsave)
@@ -1282,7 +1792,184 @@ tp3d_status launch_pair(const tp3d_ctx* ctx, const GemmProblem& P, cudaStream_t 
   return TP3D_OK;
 }
 
+// The tensor maps of one CTA-pair problem with 128-deep stages (as launch_pair builds them).
+struct PairMaps {
+  CUtensorMap a, b, c, z, x;
+  uint32_t wide;
+};
+tp3d_status pair_maps(const GemmProblem& P, PairMaps* m) {
+  constexpr int KD = 128;
+  m->wide = 0;
+  auto wide_ok = [&](const Operand& o, int64_t seg_mn) {
+    return o.mn_major ? (o.g.bw % 128 == 0 && seg_mn % 128 == 0) : (o.g.bw % 64 == 0);
+  };
+  if (wide_ok(P.a, P.segM) && make_map_wide(&m->a, P.a.g, P.a.ptr, P.a.mn_major ? KD : 128, P.a.mn_major ? 2 : KD / 64))
+    m->wide |= 1u;
+  else
+    TP3D_TRY(make_map(&m->a, P.a.g, P.a.ptr, 64, P.a.mn_major ? KD : 128));
+  if (wide_ok(P.b, P.segN) && make_map_wide(&m->b, P.b.g, P.b.ptr, P.b.mn_major ? KD : 128, P.b.mn_major ? 2 : KD / 64))
+    m->wide |= 2u;
+  else
+    TP3D_TRY(make_map(&m->b, P.b.g, P.b.ptr, 64, P.b.mn_major ? KD : 128));
+  if (P.epi.out_f32)
+    TP3D_TRY(make_map(&m->c, P.c.g, P.c.ptr, 16, 32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, CU_TENSOR_MAP_SWIZZLE_64B));
+  else
+    TP3D_TRY(make_map(&m->c, P.c.g, P.c.ptr, 32, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, CU_TENSOR_MAP_SWIZZLE_64B));
+  if (P.epi.zsave)
+    TP3D_TRY(make_map(&m->z, P.c.g, P.epi.zsave, 32, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, CU_TENSOR_MAP_SWIZZLE_64B));
+  else
+    m->z = m->c;
+  const void* aux = P.epi.resid ? P.epi.resid : P.epi.gin;
+  if (aux)
+    TP3D_TRY(make_map(&m->x, P.c.g, aux, 32, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, CU_TENSOR_MAP_SWIZZLE_64B));
+  else
+    m->x = m->c;
+  return TP3D_OK;
+}
+
+// CTA pairs of the chained kernel that fit on the device at once (0: none).
+int chain_clusters(const tp3d_ctx* ctx) {
+  static int cached[64] = {};
+  const int dev = ctx->device & 63;
+  if (cached[dev] != 0) return cached[dev] > 0 ? cached[dev] : 0;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Tc2Cfg<128>::SMEM;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(2 * (unsigned)(ctx->num_sms / 2));
+  int n = 0;
+  if (cudaFuncSetAttribute(gemm_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Tc2Cfg<128>::SMEM) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveClusters(&n, gemm_chain_kernel, &cfg) != cudaSuccess || n < 1) {
+    (void)cudaGetLastError();
+    cached[dev] = -1;
+    return 0;
+  }
+  cached[dev] = n;
+  return n;
+}
+
+bool same_grid(const Grid& x, const Grid& y) {
+  return x.kind == y.kind && x.q == y.q && x.rb == y.rb && x.cb == y.cb && x.R == y.R && x.C == y.C && x.bh == y.bh &&
+         x.bw == y.bw && x.copies == y.copies;
+}
+
 }  // namespace
+
+// The chained launch's shape of work, or false if (P0, P1) do not qualify:
+// the second problem's A is the first's output (same buffer and layout); whole
+// 256 x 256 tiles; 128-deep stages; no batch windows, causal masks or fp16
+// paths; and a working set (both inputs, the intermediate, the second
+// weight) of at most 64 MiB, so that the row-tiles-slowest order costs no
+// HBM re-reads (L2 is 126 MiB).  Two contraction halves for the second
+// problem when that doubles its units without passing one wave of clusters.
+bool chain_plan(const tp3d_ctx* ctx, const GemmProblem& P0, const GemmProblem& P1, ChainShape* sh) {
+  const GemmProblem* Ps[2] = {&P0, &P1};
+  for (const GemmProblem* P : Ps) {
+    if (P->Z != 1 || P->Hz != 1 || P->causal != CAUSAL_NONE || P->in_f16 || P->epi.f16_cols || P->epi.alpha_dev ||
+        P->epi.amax_out)
+      return false;
+    if (P->segM % 256 || P->segN % 256 || P->segK % 128 || P->M % P->segM || P->N % P->segN || P->K % P->segK)
+      return false;
+    if (P->M > INT32_MAX || P->N > INT32_MAX || P->K > INT32_MAX) return false;
+    const Grid* gs[3] = {&P->a.g, &P->b.g, &P->c.g};
+    for (const Grid* g : gs)
+      if (g->bw % 8 || g->R > INT32_MAX || g->C > INT32_MAX) return false;
+  }
+  if (P0.a.mn_major != P1.a.mn_major || P0.b.mn_major != P1.b.mn_major) return false;
+  if (P0.M != P1.M || P0.segM != P1.segM || P1.K != P0.N || P1.a.ptr != P0.c.ptr || P1.a.mn_major ||
+      !same_grid(P1.a.g, P0.c.g) || P0.epi.out_f32)
+    return false;
+  const double ws = 2.0 * ((double)P0.M * P0.K + (double)P0.K * P0.N + (double)P0.M * P0.N + (double)P1.K * P1.N);
+  if (ws > 64.0 * 1024 * 1024) return false;
+  const int clusters = chain_clusters(ctx);
+  if (clusters < 1) return false;
+  const int64_t rows = P0.M / 256;
+  sh->units0 = rows * (P0.N / 256);
+  const int64_t tiles1 = rows * (P1.N / 256);
+  const int64_t nseg1 = P1.K / P1.segK;
+  // the halves' fix-up writes rows of 128 columns inside one block of the output
+  const bool split_ok = nseg1 % 2 == 0 && (P0.N / 2) % P0.segN == 0 && P1.c.g.bw % 128 == 0 && !P1.epi.out_f32 &&
+                        !P1.epi.zsave && !P1.epi.gin && P1.epi.act != EPI_GELU_BWD;
+  sh->splits = (split_ok && 2 * tiles1 <= clusters) ? 2 : 1;
+  sh->units1 = tiles1 * sh->splits;
+  sh->n_ready = rows * sh->splits;
+  sh->n_fix = sh->splits == 2 ? tiles1 * 2 * kEpiWarps : 0;
+  sh->ready_target = 2 * kEpiWarps * (int32_t)((P0.N / 256) / sh->splits);
+  sh->clusters = (int)((sh->units0 + sh->units1) < clusters ? (sh->units0 + sh->units1) : clusters);
+  const size_t counters = (size_t)(sh->n_ready + sh->n_fix + 1) * sizeof(int);
+  sh->counter_bytes = (counters + 255) & ~(size_t)255;
+  sh->scratch_bytes = sh->counter_bytes + (sh->splits == 2 ? (size_t)(2 * P1.M * P1.N) * sizeof(float) : 0);
+  return true;
+}
+
+// Launch the chain on `scratch` (chain_plan's scratch_bytes, 256-byte
+// aligned; its counters zero, as every launch leaves them).
+tp3d_status gemm_chain_tc(const tp3d_ctx* ctx, const GemmProblem& P0i, const GemmProblem& P1i, const ChainShape& sh,
+                          void* scratch, cudaStream_t s) {
+  GemmProblem P0 = P0i, P1 = P1i;
+  P0.stall_after = P1.stall_after = -1;
+  PairMaps m0, m1;
+  TP3D_TRY(pair_maps(P0, &m0));
+  TP3D_TRY(pair_maps(P1, &m1));
+  ChainArgs C;
+  C.units0 = sh.units0;
+  C.units1 = sh.units1;
+  C.splits = sh.splits;
+  C.ready_target = sh.ready_target;
+  int* counters = static_cast<int*>(scratch);
+  C.ready = counters;
+  C.fix = counters + sh.n_ready;
+  C.exits = counters + sh.n_ready + sh.n_fix;
+  C.n_ready = (int32_t)sh.n_ready;
+  C.n_fix = (int32_t)sh.n_fix;
+  float* part = sh.splits == 2 ? reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + sh.counter_bytes) : nullptr;
+  C.part = part;
+  // the halves' raw sums: job 1 with a dense fp32 output of 2 M rows (slot s = rows s M ..)
+  GemmProblem P1h = P1;
+  CUtensorMap mp = m1.c;
+  if (part) {
+    Grid gp{};
+    gp.kind = TP3D_ROW;
+    gp.q = 0;
+    gp.rb = 1;
+    gp.cb = 1;
+    gp.R = 2 * P1.M;
+    gp.C = P1.N;
+    gp.bh = gp.R;
+    gp.bw = gp.C;
+    gp.copies = 1;
+    P1h.c.g = gp;
+    P1h.c.ptr = part;
+    P1h.c.hi1 = P1h.c.lo1 = P1h.c.base1 = P1h.c.hi2 = P1h.c.lo2 = P1h.c.base2 = 0;
+    P1h.epi = Epilogue{};
+    P1h.epi.act = EPI_NONE;
+    P1h.epi.out_f32 = 1;
+    P1h.epi.alpha = 1.0f;
+    TP3D_TRY(make_map(&mp, gp, part, 16, 32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, CU_TENSOR_MAP_SWIZZLE_64B));
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Tc2Cfg<128>::SMEM;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(2 * (unsigned)sh.clusters);
+  TP3D_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemm_chain_kernel, m0.a, m0.b, m0.c, m0.z, m0.x, m1.a, m1.b, m1.c, m1.z,
+                                   m1.x, mp, P0, P1, P1h, m0.wide, m1.wide, C));
+  return TP3D_OK;
+}
 
 tp3d_status gemm_bf16_tc(const tp3d_ctx* ctx, const GemmProblem& P0, cudaStream_t s) {
   GemmProblem P = P0;

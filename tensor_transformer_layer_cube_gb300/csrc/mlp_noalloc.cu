@@ -13,7 +13,8 @@
 // cudaFree or allocating library routine.
 //
 // The kernels are the same ones tp3d_mlp launches, in the same order; only
-// the address of the hidden activation differs.
+// the addresses of the hidden activation and of the chained launch's scratch
+// differ.
 #include <mutex>
 
 #include "gemm.cuh"
@@ -33,6 +34,10 @@ namespace {
 constexpr int64_t kMaxHiddenElems = int64_t(8) << 20;
 
 static __device__ __align__(256) __nv_bfloat16 g_mlp_hidden[kMaxHiddenElems];
+// The chained launch's counters and fp32 partial sums (M * h <= 8 Mi, 32 MiB);
+// zero when the library loads, and every launch leaves the counters zero.
+constexpr size_t kChainScratchBytes = (size_t(8) << 20) * sizeof(float) + (size_t(64) << 10);
+static __device__ __align__(256) unsigned char g_mlp_chain[kChainScratchBytes];
 
 // Host code may not use g_mlp_hidden's name as an address (it is a host-side
 // stand-in); its device address is looked up once per device and cached.
@@ -40,20 +45,25 @@ constexpr int kMaxDevices = 64;
 void* g_hidden_addr[kMaxDevices] = {};
 std::mutex g_hidden_mu;
 
-tp3d_status hidden_buffer(int device, void** out) {
+void* g_chain_addr[kMaxDevices] = {};
+
+tp3d_status hidden_buffer(int device, void** out, void** chain) {
   if (device < 0 || device >= kMaxDevices) return TP3D_EUNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_hidden_mu);
   if (!g_hidden_addr[device]) {
     int prev = 0;
     if (cudaGetDevice(&prev) != cudaSuccess) return TP3D_ECUDA;
     if (prev != device && cudaSetDevice(device) != cudaSuccess) return TP3D_ECUDA;
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_mlp_hidden);
+    void *p = nullptr, *c = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_mlp_hidden);
+    if (e == cudaSuccess) e = cudaGetSymbolAddress(&c, g_mlp_chain);
     if (prev != device) cudaSetDevice(prev);
-    if (e != cudaSuccess || p == nullptr) return TP3D_ECUDA;
+    if (e != cudaSuccess || p == nullptr || c == nullptr) return TP3D_ECUDA;
     g_hidden_addr[device] = p;
+    g_chain_addr[device] = c;
   }
   *out = g_hidden_addr[device];
+  *chain = g_chain_addr[device];
   return TP3D_OK;
 }
 
@@ -69,8 +79,8 @@ extern "C" tp3d_status tp3d_mlp_noalloc(tp3d_ctx* ctx, int q, int64_t M, int64_t
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return TP3D_EALIGN;
   if (M > kMaxHiddenElems / f) return TP3D_EUNSUPPORTED;  // M * f beyond the static array
-  void* hidden = nullptr;
-  TP3D_TRY(hidden_buffer(ctx->device, &hidden));
+  void *hidden = nullptr, *chain = nullptr;
+  TP3D_TRY(hidden_buffer(ctx->device, &hidden, &chain));
   GemmProblem P1, P2;
   TP3D_TRY(plan_linear(ctx, q, 0, M, h, f, X, W1, b1, 1, hidden, &P1));
   TP3D_TRY(plan_linear(ctx, q, 1, M, f, h, hidden, W2, b2, 0, Y, &P2));
@@ -83,6 +93,12 @@ extern "C" tp3d_status tp3d_mlp_noalloc(tp3d_ctx* ctx, int q, int64_t M, int64_t
   for (const auto& in : ins)
     if (overlaps(Y, yb, in.p, in.n)) return TP3D_EOVERLAP;
   const cudaStream_t s = as_stream(stream);
+  // the launches tp3d_mlp would make: the chained one on the static scratch
+  ChainShape sh;
+  if (chain_plan(ctx, P1, P2, &sh)) {
+    if (sh.scratch_bytes > kChainScratchBytes) return TP3D_EUNSUPPORTED;
+    return gemm_chain_tc(ctx, P1, P2, sh, chain, s);
+  }
   TP3D_TRY(gemm_bf16_tc(ctx, P1, s));
   return gemm_bf16_tc(ctx, P2, s);
 }

@@ -17,7 +17,7 @@ import tensor_transformer_layer_cube_gb300 as t
 from oracle import layouts as L
 from oracle import linear as OL
 from oracle import mlp as OM
-from oracle.metrics import BF16_TOL, F32_TOL, rel_err
+from oracle.metrics import BF16_TOL, F32_TOL, MLP_ELEM_TOL, fro_err, max_rel_err, rel_err
 from tests.gpu_util import as_np64, assert_guards_intact, device, guarded, sharded_f64, to_dev_bf16, to_dev_f32
 
 pytestmark = pytest.mark.gpu
@@ -113,20 +113,108 @@ def _mlp_case(ctx, q, M, h, f, seed, bias_std, sample_rows=None):
     if sample_rows is None:
         Ym, Y1m = OM.mlp3d(L.to_sharded(X, L.CUBE_A(q)), L.to_sharded(W1, L.CUBE_B(q)), b1,
                            L.to_sharded(W2, L.CUBE_B_SWAP(q)), b2, q, M, h, f)
+        got, want = as_np64(dY), Ym
         e1 = rel_err(as_np64(dY1), Y1m)
-        return rel_err(as_np64(dY), Ym), e1
-    want = OM.mlp_rows_dense(X[sample_rows], W1, b1, W2, b2)
-    return rel_err(Yg[sample_rows], want), 0.0
+    else:
+        got, want = Yg[sample_rows], OM.mlp_rows_dense(X[sample_rows], W1, b1, W2, b2)
+        e1 = 0.0
+    # Y passes through the bf16 hidden activation: the 1e-2 bar on the
+    # max-normalised and Frobenius errors, the element-wise one at MLP_ELEM_TOL
+    em, ef = max_rel_err(got, want), fro_err(got, want)
+    print(f"MLP q={q} M={M} h={h} f={f}: Y max-normalised {em:.5f} Frobenius {ef:.5f}; Y1 element-wise {e1:.5f}")
+    assert em <= BF16_TOL and ef <= BF16_TOL, (em, ef)
+    return rel_err(got, want), e1
 
 
 def test_mlp_q2_tokens2048_hidden1024_ffn4096(ctx):
     e, e1 = _mlp_case(ctx, 2, 2048, 1024, 4096, S.SEED_BASE + 2, 0.0)
-    assert e <= BF16_TOL and e1 <= BF16_TOL
+    assert e <= MLP_ELEM_TOL and e1 <= BF16_TOL
 
 
 def test_mlp_q2_with_biases(ctx):
     e, e1 = _mlp_case(ctx, 2, 1024, 512, 2048, 300, 0.05)
-    assert e <= BF16_TOL and e1 <= BF16_TOL
+    assert e <= MLP_ELEM_TOL and e1 <= BF16_TOL
+
+
+def test_mlp_plan_chains_small_blocks(ctx):
+    # config 2 (36 MiB of operands, 32 tiles in the second GEMM): one launch,
+    # the second GEMM's contraction in two halves
+    assert t.tp3d_mlp_plan(ctx, 2, 2048, 1024, 4096) == (0, 1, 2)
+    # 4096 tokens, ffn 2048 (32 MiB): one launch; 64 second-GEMM tiles, whole contractions
+    assert t.tp3d_mlp_plan(ctx, 2, 4096, 1024, 2048) == (0, 1, 1)
+    # config 4 (far beyond 64 MiB): two GEMM launches
+    assert t.tp3d_mlp_plan(ctx, 4, 8192, 4096, 16384) == (0, 2, 0)
+    # tiles that would be partial: two launches
+    assert t.tp3d_mlp_plan(ctx, 1, 200, 64, 128) == (0, 2, 0)
+
+
+def test_mlp_chain_whole_contractions(ctx):
+    # the chained launch without contraction halves, against the oracle in full
+    assert t.tp3d_mlp_plan(ctx, 2, 4096, 1024, 2048)[1:] == (1, 1)
+    e, e1 = _mlp_case(ctx, 2, 4096, 1024, 2048, 310, 0.05)
+    assert e <= MLP_ELEM_TOL and e1 <= BF16_TOL
+
+
+def _bf16_ulp(x: np.ndarray) -> np.ndarray:
+    """The spacing of bf16 numbers at |x| (8 significant bits)."""
+    e = np.floor(np.log2(np.maximum(np.abs(x), 2.0 ** -126)))
+    return 2.0 ** (e - 7)
+
+
+def _chain_vs_separate(ctx, q, M, h, f, seed, splits):
+    """tp3d_mlp (one chained launch) and the same block as two tp3d_linear
+    launches on the same inputs.  Y1 agrees bit for bit (the same products in
+    the same order).  So does Y when the chain contracts whole rows of Y1
+    (splits 1); with the contraction in two halves (splits 2) Y's fp32 sums
+    are the two halves' sums added, so Y agrees to one bf16 unit (and the
+    accumulation noise where a sum cancels)."""
+    assert t.tp3d_mlp_plan(ctx, q, M, h, f) == (0, 1, splits)
+    I = S.mlp_inputs(M, h, f, seed, bias_std=0.05)
+    dX = to_dev_bf16(I["X"], L.CUBE_A(q))
+    dW1 = to_dev_bf16(I["W1"], L.CUBE_B(q))
+    dW2 = to_dev_bf16(I["W2"], L.CUBE_B_SWAP(q))
+    b1, b2 = I["b1"].to(device()), I["b2"].to(device())
+    outs = []
+    for chained in (True, False):
+        Y1 = torch.full((M * f,), float("nan"), dtype=torch.bfloat16, device=device())
+        Y = torch.full((M * h,), float("nan"), dtype=torch.bfloat16, device=device())
+        if chained:
+            assert t.tp3d_mlp(ctx, q, M, h, f, t.TP3D_BF16, dX, dW1, b1, dW2, b2, Y1, Y) == 0
+        else:
+            assert t.tp3d_linear(ctx, q, 0, M, h, f, t.TP3D_BF16, dX, dW1, b1, 1, Y1) == 0
+            assert t.tp3d_linear(ctx, q, 1, M, f, h, t.TP3D_BF16, Y1, dW2, b2, 0, Y) == 0
+        assert t.tp3d_sync_status(ctx) == 0
+        outs.append((Y1, Y))
+    (c1, c), (s1, sy) = outs
+    assert torch.equal(c1.view(torch.int16), s1.view(torch.int16))
+    if splits == 1:
+        assert torch.equal(c.view(torch.int16), sy.view(torch.int16))
+    else:
+        # one bf16 unit, plus the fp32 accumulation's own noise where the sum
+        # cancels (1e-4 of the output's scale: a 4096-term sum of products of
+        # magnitude 1e-2 carries about 1e-5 absolute)
+        a, b = as_np64(c), as_np64(sy)
+        assert not np.isnan(a).any()
+        diff = np.abs(a - b)
+        tol = _bf16_ulp(np.maximum(np.abs(a), np.abs(b))) + 1e-4 * np.abs(b).max()
+        assert (diff <= tol).all(), float((diff / tol).max())
+        print(f"chain (two halves) vs two launches: {np.count_nonzero(diff)} of {a.size} Y elements differ")
+
+
+def test_mlp_chain_matches_two_launches(ctx):
+    _chain_vs_separate(ctx, 2, 4096, 1024, 2048, 330, 1)
+    _chain_vs_separate(ctx, 2, 2048, 1024, 4096, 331, 2)
+
+
+def test_mlp_chain_calls_in_a_row(ctx):
+    # chained calls back to back on one context, different sizes, inputs and
+    # contraction splits: each launch leaves its counters zero for the next
+    e, e1 = _mlp_case(ctx, 2, 2048, 1024, 4096, 320, 0.05)  # two contraction halves
+    assert e <= MLP_ELEM_TOL and e1 <= BF16_TOL
+    _chain_vs_separate(ctx, 2, 4096, 1024, 2048, 321, 1)  # whole contractions
+    _chain_vs_separate(ctx, 2, 2048, 1024, 4096, 322, 2)
+    e, e1 = _mlp_case(ctx, 2, 2048, 1024, 4096, 323, 0.05)
+    assert e <= MLP_ELEM_TOL and e1 <= BF16_TOL
 
 
 def test_mlp_q4_tokens8192_hidden4096_ffn16384_sampled_rows(ctx):
