@@ -137,6 +137,9 @@ tp3d_status tp3d_create(int device, tp3d_ctx** out) {
     ok = ok && cudaEventCreateWithFlags(&c->ev_join[k], cudaEventDisableTiming) == cudaSuccess;
   }
   ok = ok && cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming) == cudaSuccess;
+  ok = ok && cudaStreamCreateWithFlags(&c->gstream, cudaStreamNonBlocking) == cudaSuccess;
+  ok = ok && cudaEventCreateWithFlags(&c->gev_in, cudaEventDisableTiming) == cudaSuccess;
+  ok = ok && cudaEventCreateWithFlags(&c->gev_out, cudaEventDisableTiming) == cudaSuccess;
   if (!ok) {
     tp3d_destroy(c);
     return TP3D_ECUDA;
@@ -153,6 +156,11 @@ void tp3d_destroy(tp3d_ctx* ctx) {
     if (ctx->ev_join[k]) cudaEventDestroy(ctx->ev_join[k]);
   }
   if (ctx->ev_fork) cudaEventDestroy(ctx->ev_fork);
+  if (ctx->gstream) cudaStreamSynchronize(ctx->gstream);  // no graph of this context still running
+  graph_cache_free(ctx);
+  if (ctx->gstream) cudaStreamDestroy(ctx->gstream);
+  if (ctx->gev_in) cudaEventDestroy(ctx->gev_in);
+  if (ctx->gev_out) cudaEventDestroy(ctx->gev_out);
   if (ctx->scratch) cudaFree(ctx->scratch);
   free(ctx);
 }

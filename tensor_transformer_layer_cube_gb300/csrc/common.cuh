@@ -29,9 +29,19 @@ struct tp3d_ctx {
   // between calls
   void* scratch;
   size_t scratch_bytes;
+  // CUDA graphs of whole layer calls keyed by their arguments (graph.cu), the
+  // stream they run on, and the events that order it with the caller's stream
+  void* graphs;
+  cudaStream_t gstream;
+  cudaEvent_t gev_in, gev_out;
 };
 
 namespace tp3d {
+
+// Run enqueue(arg, stream) as a cached CUDA graph keyed by `key` (graph.cu).
+tp3d_status graph_call(tp3d_ctx* ctx, const void* key, size_t key_bytes, cudaStream_t st,
+                       tp3d_status (*enqueue)(void* arg, cudaStream_t s), void* arg);
+void graph_cache_free(tp3d_ctx* ctx);
 
 // A bounded wait gives up after this many nanoseconds of wall time, unless
 // the context sets another limit (tp3d_set_wait_limit_ns); the drains of an

@@ -28,6 +28,7 @@
 // gradients and column sums).  Attention reads each (batch, head) window in
 // place from the CUBE_C shards of the QKV matrix (attention.cu).
 #include <math.h>
+#include <string.h>
 
 #include <algorithm>
 
@@ -219,8 +220,8 @@ size_t tp3d_layer_workspace_bytes(const tp3d_layer_cfg* cfg) {
   return p.total;
 }
 
-tp3d_status tp3d_layer_fwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_layer_params* w, const void* X,
-                           void* Y, void* workspace, void* stream) {
+static tp3d_status layer_fwd_enqueue(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_layer_params* w,
+                                     const void* X, void* Y, void* workspace, cudaStream_t stream) {
   if (!ctx || !cfg || !w || !X || !Y || !workspace) return TP3D_EINVAL;
   Plan p;
   TP3D_TRY(make_plan(cfg, &p));
@@ -237,7 +238,7 @@ tp3d_status tp3d_layer_fwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_
     return TP3D_EOVERLAP;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   auto W = [&](size_t off) { return static_cast<void*>(ws + off); };
-  const cudaStream_t st = as_stream(stream);
+  const cudaStream_t st = stream;
   const int q = p.q;
 
   Grid gA;
@@ -284,8 +285,9 @@ tp3d_status tp3d_layer_fwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_
   return gemm_bf16_tc(ctx, G, st);
 }
 
-tp3d_status tp3d_layer_bwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_layer_params* w, const void* X,
-                           void* workspace, const void* dY, void* dX, const tp3d_layer_grads* g, void* stream) {
+static tp3d_status layer_bwd_enqueue(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_layer_params* w,
+                                     const void* X, void* workspace, const void* dY, void* dX,
+                                     const tp3d_layer_grads* g, cudaStream_t stream) {
   if (!ctx || !cfg || !w || !g || !X || !dY || !dX || !workspace) return TP3D_EINVAL;
   Plan p;
   TP3D_TRY(make_plan(cfg, &p));
@@ -306,7 +308,7 @@ tp3d_status tp3d_layer_bwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_
   auto W = [&](size_t off) { return static_cast<void*>(ws + off); };
   float* part = (float*)W(p.part);
   int* counters = (int*)W(p.counters);
-  const cudaStream_t st = as_stream(stream);
+  const cudaStream_t st = stream;
   // the column sums' arrival counters start at zero (each sum leaves them so)
   TP3D_CUDA_TRY(cudaMemsetAsync(counters, 0, kCounters * 4, st));
   const int q = p.q;
@@ -394,6 +396,84 @@ tp3d_status tp3d_layer_bwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_
   TP3D_TRY(launch_ln_bwd(ctx, gA, W(p.dxn), X, (const float*)W(p.mean1), (const float*)W(p.rstd1), w->ln1_g,
                          W(p.dH), dX, st));                                                            // dX
   return join(2);  // every side stream joined before returning
+}
+
+// The public calls: argument checks, then the launches above as a cached CUDA
+// graph keyed by every argument (graph.cu; a stream under capture gets the
+// launches directly).
+struct FwdCall {
+  tp3d_ctx* ctx;
+  const tp3d_layer_cfg* cfg;
+  const tp3d_layer_params* w;
+  const void* X;
+  void *Y, *workspace;
+};
+static tp3d_status fwd_thunk(void* a, cudaStream_t s) {
+  const FwdCall* c = static_cast<const FwdCall*>(a);
+  return layer_fwd_enqueue(c->ctx, c->cfg, c->w, c->X, c->Y, c->workspace, s);
+}
+struct BwdCall {
+  tp3d_ctx* ctx;
+  const tp3d_layer_cfg* cfg;
+  const tp3d_layer_params* w;
+  const void* X;
+  void* workspace;
+  const void* dY;
+  void* dX;
+  const tp3d_layer_grads* g;
+};
+static tp3d_status bwd_thunk(void* a, cudaStream_t s) {
+  const BwdCall* c = static_cast<const BwdCall*>(a);
+  return layer_bwd_enqueue(c->ctx, c->cfg, c->w, c->X, c->workspace, c->dY, c->dX, c->g, s);
+}
+struct CallKey {
+  int32_t fn;
+  tp3d_layer_cfg cfg;
+  tp3d_layer_params w;
+  tp3d_layer_grads g;
+  const void *X, *dY;
+  void *Y, *dX, *workspace, *stream;
+  int64_t stall_after;
+};
+
+tp3d_status tp3d_layer_fwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_layer_params* w, const void* X,
+                           void* Y, void* workspace, void* stream) {
+  if (!ctx || !cfg || !w || !X || !Y || !workspace) return TP3D_EINVAL;
+  Plan p;
+  TP3D_TRY(make_plan(cfg, &p));
+  CallKey k;
+  memset(&k, 0, sizeof(k));
+  k.fn = 1;
+  k.cfg = *cfg;
+  k.w = *w;
+  k.X = X;
+  k.Y = Y;
+  k.workspace = workspace;
+  k.stream = stream;
+  k.stall_after = ctx->stall_after;
+  FwdCall c{ctx, cfg, w, X, Y, workspace};
+  return graph_call(ctx, &k, sizeof(k), as_stream(stream), fwd_thunk, &c);
+}
+
+tp3d_status tp3d_layer_bwd(tp3d_ctx* ctx, const tp3d_layer_cfg* cfg, const tp3d_layer_params* w, const void* X,
+                           void* workspace, const void* dY, void* dX, const tp3d_layer_grads* g, void* stream) {
+  if (!ctx || !cfg || !w || !g || !X || !dY || !dX || !workspace) return TP3D_EINVAL;
+  Plan p;
+  TP3D_TRY(make_plan(cfg, &p));
+  CallKey k;
+  memset(&k, 0, sizeof(k));
+  k.fn = 2;
+  k.cfg = *cfg;
+  k.w = *w;
+  k.g = *g;
+  k.X = X;
+  k.dY = dY;
+  k.dX = dX;
+  k.workspace = workspace;
+  k.stream = stream;
+  k.stall_after = ctx->stall_after;
+  BwdCall c{ctx, cfg, w, X, workspace, dY, dX, g};
+  return graph_call(ctx, &k, sizeof(k), as_stream(stream), bwd_thunk, &c);
 }
 
 }  // extern "C"

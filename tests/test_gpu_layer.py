@@ -233,3 +233,88 @@ def test_layer_step_in_a_cuda_graph(ctx):
     replayed = [Y, dX] + list(grads.values())
     for a, b in zip(direct, replayed):
         assert torch.equal(a, b)
+
+
+def _device_case(cfg, seed):
+    """Device buffers (params, X, dY) of one seeded case, and its oracle inputs."""
+    I = S.layer_inputs(cfg.batch, cfg.seq, cfg.hidden, cfg.heads, cfg.ffn, seed, perturb=True)
+    q = cfg.p
+    params = {k: to_dev_bf16(I[k], lay(q)) for k, lay in OY.WEIGHT_LAYOUTS.items()}
+    params.update({k: I[k].to(device()) for k in OY.VECTORS})
+    X = to_dev_bf16(I["X"], L.CUBE_A(q))
+    dY = to_dev_bf16(I["dY"], L.CUBE_A(q))
+    P64 = {k: S.as_f64(v) for k, v in I.items() if k not in ("X", "dY")}
+    ref = (L.to_sharded(S.as_f64(I["X"]), L.CUBE_A(q)), L.to_sharded(S.as_f64(I["dY"]), L.CUBE_A(q)),
+           OY.shard_params(P64, cfg))
+    return params, X, dY, ref
+
+
+def _layer_outputs_vs_oracle(cfg, Y, dX, grads, ref):
+    Xb, dYb, Ps = ref
+    want_dX, want_g = OY.layer_backward(dYb, Xb, Ps, cfg)
+    pairs = {"Y": (as_np64(Y), OY.layer_forward(Xb, Ps, cfg)), "dX": (as_np64(dX), want_dX)}
+    pairs.update({k: (as_np64(grads[k]), want_g[k]) for k in want_g})
+    for k, (got, want) in pairs.items():
+        e = (max_rel_err(got, want), fro_err(got, want), rel_err(got, want))
+        assert e[0] <= BF16_TOL and e[1] <= BF16_TOL and e[2] <= LAYER_ELEM_TOL, (k, e)
+
+
+def test_layer_calls_again_with_new_contents(ctx):
+    # The context keeps a CUDA graph of each call, keyed by its arguments: the
+    # second forward + backward on the same buffers replays those graphs, and
+    # must read the buffers' new contents (a second seed copied in place).
+    cfg = OY.LayerConfig(p=2, batch=2, seq=256, hidden=256, heads=2, ffn=1024)
+    q, M, h = cfg.p, cfg.M, cfg.hidden
+    c = t.tp3d_layer_cfg(q, cfg.batch, cfg.seq, h, cfg.heads, cfg.ffn, t.TP3D_BF16, cfg.eps)
+    ws = torch.empty(t.tp3d_layer_workspace_bytes(c), dtype=torch.uint8, device=device())
+    params, X, dY, ref = _device_case(cfg, 530)
+    Y = torch.empty(M * h, dtype=torch.bfloat16, device=device())
+    dX = torch.empty(M * h, dtype=torch.bfloat16, device=device())
+    grads = {k: torch.empty_like(v) for k, v in params.items()}
+    for seed in (None, 531, 532):
+        if seed is not None:
+            p2, X2, dY2, ref = _device_case(cfg, seed)
+            for k in params:
+                params[k].copy_(p2[k])
+            X.copy_(X2)
+            dY.copy_(dY2)
+        Y.fill_(float("nan"))
+        dX.fill_(float("nan"))
+        assert t.tp3d_layer_fwd(ctx, c, params, X, Y, ws) == 0
+        assert t.tp3d_layer_bwd(ctx, c, params, X, ws, dY, dX, grads) == 0
+        assert t.tp3d_sync_status(ctx) == 0
+        _layer_outputs_vs_oracle(cfg, Y, dX, grads, ref)
+
+
+def test_layer_inside_a_captured_graph(ctx):
+    # Called while the caller's stream is being captured, the layer enqueues
+    # its launches into that capture; replaying it gives the same bits as the
+    # direct call.
+    cfg = OY.LayerConfig(p=2, batch=2, seq=256, hidden=256, heads=2, ffn=1024)
+    q, M, h = cfg.p, cfg.M, cfg.hidden
+    c = t.tp3d_layer_cfg(q, cfg.batch, cfg.seq, h, cfg.heads, cfg.ffn, t.TP3D_BF16, cfg.eps)
+    ws = torch.empty(t.tp3d_layer_workspace_bytes(c), dtype=torch.uint8, device=device())
+    params, X, dY, _ = _device_case(cfg, 540)
+    outs = []
+    for captured in (False, True):
+        Y = torch.full((M * h,), float("nan"), dtype=torch.bfloat16, device=device())
+        dX = torch.full((M * h,), float("nan"), dtype=torch.bfloat16, device=device())
+        grads = {k: torch.empty_like(v) for k, v in params.items()}
+
+        def step():
+            assert t.tp3d_layer_fwd(ctx, c, params, X, Y, ws) == 0
+            assert t.tp3d_layer_bwd(ctx, c, params, X, ws, dY, dX, grads) == 0
+        if captured:
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                step()
+            g.replay()
+        else:
+            step()
+        torch.cuda.synchronize()
+        assert t.tp3d_sync_status(ctx) == 0
+        outs.append([Y, dX] + [grads[k] for k in sorted(grads)])
+    for a, b in zip(*outs):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
