@@ -236,7 +236,7 @@ class LayerBench:
         # library kernels per step: forward 7 (2 LN, 4 GEMM, attention);
         # backward 19 (8 GEMM, 3 attention, 2 LN rows, 2 LN column sums, 4
         # bias column sums; each column sum finishes its own reduction)
-        self.launches = 7 + 19
+        self.launches = 9 + 19  # forward 9 (W_qkv max and fp16 copy, 2 LN, 4 GEMMs, attention), backward 19
         self.unit, self.scale = "TFLOP/s", 1e12
         self.X_host = self.X.cpu().pin_memory()
         self.dY_host = self.dY.cpu().pin_memory()
@@ -258,11 +258,12 @@ class LayerBench:
         cur = torch.cuda.current_stream()
         if not hasattr(self, "copy_stream"):
             self.copy_stream = torch.cuda.Stream()
-        # dY is needed only by the backward: its copy runs beside the forward
+        # X first, alone on the host-to-device engine (the forward waits for it);
+        # dY, needed only by the backward, then copies beside the forward
+        self.X.copy_(self.X_host, non_blocking=True)
         self.copy_stream.wait_stream(cur)
         with torch.cuda.stream(self.copy_stream):
             self.dY.copy_(self.dY_host, non_blocking=True)
-        self.X.copy_(self.X_host, non_blocking=True)
         self.fwd()
         cur.wait_stream(self.copy_stream)
         self.bwd()
@@ -270,7 +271,7 @@ class LayerBench:
 
     def e2e_bytes(self):
         return (2 * self.X.numel() * 2, self.dX.numel() * 2,
-                "X and dY copied from pinned host memory (dY's copy beside the forward), tp3d_layer_fwd + "
+                "X then dY copied from pinned host memory (dY's copy beside the forward), tp3d_layer_fwd + "
                 "tp3d_layer_bwd, dX copied back")
 
     def kernel_probe(self):

@@ -146,14 +146,28 @@ __device__ __forceinline__ uint32_t tmem_row(uint32_t tmem, int quarter, uint32_
   return tmem + ((uint32_t)(quarter * 32) << 16) + col;
 }
 
-// store 32 fp32 values times mul as bf16 to global row pointer + column offset (16-byte aligned)
+// store 32 fp32 values times mul as bf16 to global row pointer + column offset
+// (16-byte aligned): two 32-byte stores where the row is 32-byte aligned (a
+// whole sector per lane: each lane writes a different row), else four 16-byte
 __device__ __forceinline__ void store_row32(bf16* dst, const uint32_t (&r)[32], float mul = 1.0f) {
+  uint4 pk[4];
 #pragma unroll
   for (int v = 0; v < 4; ++v) {
     float f[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(r[v * 8 + e]) * mul;
-    *reinterpret_cast<uint4*>(dst + v * 8) = pack8f(f);
+    pk[v] = pack8f(f);
+  }
+  if ((reinterpret_cast<uintptr_t>(dst) & 31u) == 0) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + h * 16), "r"(pk[2 * h].x),
+                   "r"(pk[2 * h].y), "r"(pk[2 * h].z), "r"(pk[2 * h].w), "r"(pk[2 * h + 1].x), "r"(pk[2 * h + 1].y),
+                   "r"(pk[2 * h + 1].z), "r"(pk[2 * h + 1].w)
+                   : "memory");
+  } else {
+#pragma unroll
+    for (int v = 0; v < 4; ++v) *reinterpret_cast<uint4*>(dst + v * 8) = pk[v];
   }
 }
 
