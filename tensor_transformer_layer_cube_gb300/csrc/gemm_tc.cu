@@ -100,6 +100,21 @@ __device__ __forceinline__ bool tile_has_k(const GemmProblem& P, int64_t klo, in
 __device__ __forceinline__ int shard_or_oob(const Grid& g, int64_t br, int64_t bc) {
   return (br < g.rb && bc < g.cb) ? g.shard((int32_t)br, (int32_t)bc) : g.nshards();
 }
+// The same with shifts where the cube edge q is a power of two (qs = log2 q;
+// qs < 0: Grid::shard's divisions)
+__device__ __forceinline__ int shard_or_oob_q(const Grid& g, int32_t br, int32_t bc, int qs) {
+  if (br >= g.rb || bc >= g.cb) return g.nshards();
+  if (qs < 0) return g.shard(br, bc);
+  const int32_t qm = (1 << qs) - 1;
+  switch (g.kind) {
+    case TP3D_CUBE_A: return (br << qs) + bc;
+    case TP3D_CUBE_B: return ((((bc & qm) << qs) + (bc >> qs)) << qs) + br;
+    case TP3D_CUBE_C: return ((((br >> qs) << qs) + bc) << qs) + (br & qm);
+    case TP3D_CUBE_B_SWAP: return ((((bc & qm) << qs) + br) << qs) + (bc >> qs);
+    default: return g.shard(br, bc);
+  }
+}
+__device__ __forceinline__ int log2_if_pow2(int q) { return (q > 0 && (q & (q - 1)) == 0) ? __ffs(q) - 1 : -1; }
 
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
   const unsigned long long t0 = globaltimer_ns();
@@ -920,6 +935,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int64_t ak, bk;
         int32_t a_br, b_br, a_c1, b_c1;
         int32_t a_bc[2], b_bc[2], a_c0[2], b_c0[2];
+        int32_t a_k0, a_blk0, b_k0, b_blk0;  // segment 0: contraction offset in its block, and that block
       };
       auto setup = [&](int64_t t, TileLd& L) {
         TileInfo T;
@@ -948,41 +964,54 @@ __global__ void __launch_bounds__(kThreads, 1)
             L.b_c0[h] = (int32_t)(bn + 64 * h - (int64_t)L.b_bc[h] * P.b.g.bw);
           }
         }
+        // the contraction's first segment: later segments step from it by segK
+        // (which divides every block extent along the contraction)
+        const int64_t akd = a_mn ? P.a.g.bh : P.a.g.bw, bkd = b_mn ? P.b.g.bh : P.b.g.bw;
+        L.a_blk0 = (int32_t)udiv32(L.ak, akd);
+        L.a_k0 = (int32_t)(L.ak - (int64_t)L.a_blk0 * akd);
+        L.b_blk0 = (int32_t)udiv32(L.bk, bkd);
+        L.b_k0 = (int32_t)(L.bk - (int64_t)L.b_blk0 * bkd);
       };
+      const int qsa = log2_if_pow2(P.a.g.q), qsb = log2_if_pow2(P.b.g.q);
+      const int32_t akd = (int32_t)(a_mn ? P.a.g.bh : P.a.g.bw), bkd = (int32_t)(b_mn ? P.b.g.bh : P.b.g.bw);
       uint32_t it = 0;
       bool ok = true;
       TileLd cur = {}, nxt = {};
       if (cid < ntiles) setup(cid, cur);
       for (int64_t t = cid; t < ntiles && ok; t += nclusters) {
-        const int64_t ak = cur.ak, bk = cur.bk;
-        const int64_t a_br = cur.a_br, b_br = cur.b_br;
+        const int32_t a_br = cur.a_br, b_br = cur.b_br;
         const int a_c1 = cur.a_c1, b_c1 = cur.b_c1;
-        const int64_t a_bc[2] = {cur.a_bc[0], cur.a_bc[1]}, b_bc[2] = {cur.b_bc[0], cur.b_bc[1]};
+        const int32_t a_bc[2] = {cur.a_bc[0], cur.a_bc[1]}, b_bc[2] = {cur.b_bc[0], cur.b_bc[1]};
         const int a_c0[2] = {cur.a_c0[0], cur.a_c0[1]}, b_c0[2] = {cur.b_c0[0], cur.b_c0[1]};
+        // the running segment: offset in the contraction block, and the block
+        int32_t a_k = cur.a_k0, a_blk = cur.a_blk0, b_k = cur.b_k0, b_blk = cur.b_blk0;
         bool next_ready = false;
         for (int32_t sg = 0; sg < nsegK && ok; ++sg) {
-          const int64_t ks = (int64_t)sg * segK;
-          int a_k = 0, b_k = 0, a_sh = 0, b_sh = 0;
+          if (sg > 0) {  // step one segment (no division: segK divides the block extent)
+            a_k += segK;
+            if (a_k >= akd) {
+              a_k -= akd;
+              ++a_blk;
+            }
+            b_k += segK;
+            if (b_k >= bkd) {
+              b_k -= bkd;
+              ++b_blk;
+            }
+          }
+          int a_sh = 0, b_sh = 0;
           int a_shh[2], b_shh[2];
           if (!a_mn) {
-            const int64_t bc = udiv32(ak + ks, P.a.g.bw);
-            a_k = (int)(ak + ks - bc * P.a.g.bw);
-            a_sh = shard_or_oob(P.a.g, a_br, bc);
+            a_sh = shard_or_oob_q(P.a.g, a_br, a_blk, qsa);
           } else {
-            const int64_t br = udiv32(ak + ks, P.a.g.bh);
-            a_k = (int)(ak + ks - br * P.a.g.bh);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) a_shh[h] = shard_or_oob(P.a.g, br, a_bc[h]);
+            for (int h = 0; h < 2; ++h) a_shh[h] = shard_or_oob_q(P.a.g, a_blk, a_bc[h], qsa);
           }
           if (!b_mn) {
-            const int64_t bc = udiv32(bk + ks, P.b.g.bw);
-            b_k = (int)(bk + ks - bc * P.b.g.bw);
-            b_sh = shard_or_oob(P.b.g, b_br, bc);
+            b_sh = shard_or_oob_q(P.b.g, b_br, b_blk, qsb);
           } else {
-            const int64_t br = udiv32(bk + ks, P.b.g.bh);
-            b_k = (int)(bk + ks - br * P.b.g.bh);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) b_shh[h] = shard_or_oob(P.b.g, br, b_bc[h]);
+            for (int h = 0; h < 2; ++h) b_shh[h] = shard_or_oob_q(P.b.g, b_blk, b_bc[h], qsb);
           }
           for (int32_t kt = 0; kt < tpsK; ++kt) {
             const int s = (int)(it % S);
@@ -1349,6 +1378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int64_t ak, bk;
         int32_t a_br, b_br, a_c1, b_c1;
         int32_t a_bc[2], b_bc[2], a_c0[2], b_c0[2];
+        int32_t a_k0, a_blk0, b_k0, b_blk0;  // the unit's first segment: offset in its block, and the block
       };
       auto setup = [&](int64_t u, UnitLd& L) {
         const ChainUnit U = chain_unit(P0, P1, C, u);
@@ -1384,6 +1414,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             L.b_c0[h] = (int32_t)(bn + 64 * h - (int64_t)L.b_bc[h] * P.b.g.bw);
           }
         }
+        // the unit's first segment; later ones step from it by segK (which
+        // divides every block extent along the contraction)
+        const int64_t ka = L.ak + (int64_t)U.sg0 * P.segK, kb = L.bk + (int64_t)U.sg0 * P.segK;
+        const int64_t akd = a_mn ? P.a.g.bh : P.a.g.bw, bkd = b_mn ? P.b.g.bh : P.b.g.bw;
+        L.a_blk0 = (int32_t)udiv32(ka, akd);
+        L.a_k0 = (int32_t)(ka - (int64_t)L.a_blk0 * akd);
+        L.b_blk0 = (int32_t)udiv32(kb, bkd);
+        L.b_k0 = (int32_t)(kb - (int64_t)L.b_blk0 * bkd);
       };
       uint32_t it = 0;
       bool ok = true;
@@ -1403,35 +1441,40 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_global();  // the TMA loads below see those stores
         }
         const int32_t segK = (int32_t)P.segK, tpsK = segK / BKP;
-        const int64_t ak = cur.ak, bk = cur.bk;
-        const int64_t a_br = cur.a_br, b_br = cur.b_br;
+        const int32_t a_br = cur.a_br, b_br = cur.b_br;
         const int a_c1 = cur.a_c1, b_c1 = cur.b_c1;
-        const int64_t a_bc[2] = {cur.a_bc[0], cur.a_bc[1]}, b_bc[2] = {cur.b_bc[0], cur.b_bc[1]};
+        const int32_t a_bc[2] = {cur.a_bc[0], cur.a_bc[1]}, b_bc[2] = {cur.b_bc[0], cur.b_bc[1]};
         const int a_c0[2] = {cur.a_c0[0], cur.a_c0[1]}, b_c0[2] = {cur.b_c0[0], cur.b_c0[1]};
+        const int qsa = log2_if_pow2(P.a.g.q), qsb = log2_if_pow2(P.b.g.q);
+        const int32_t akd = (int32_t)(a_mn ? P.a.g.bh : P.a.g.bw), bkd = (int32_t)(b_mn ? P.b.g.bh : P.b.g.bw);
+        int32_t a_k = cur.a_k0, a_blk = cur.a_blk0, b_k = cur.b_k0, b_blk = cur.b_blk0;
         bool next_ready = false;
         for (int32_t sg = cur.sg0; sg < cur.sg1 && ok; ++sg) {
-          const int64_t ks = (int64_t)sg * segK;
-          int a_k = 0, b_k = 0, a_sh = 0, b_sh = 0;
+          if (sg > cur.sg0) {  // step one segment (no division: segK divides the block extent)
+            a_k += segK;
+            if (a_k >= akd) {
+              a_k -= akd;
+              ++a_blk;
+            }
+            b_k += segK;
+            if (b_k >= bkd) {
+              b_k -= bkd;
+              ++b_blk;
+            }
+          }
+          int a_sh = 0, b_sh = 0;
           int a_shh[2], b_shh[2];
           if (!a_mn) {
-            const int64_t bc = udiv32(ak + ks, P.a.g.bw);
-            a_k = (int)(ak + ks - bc * P.a.g.bw);
-            a_sh = shard_or_oob(P.a.g, a_br, bc);
+            a_sh = shard_or_oob_q(P.a.g, a_br, a_blk, qsa);
           } else {
-            const int64_t br = udiv32(ak + ks, P.a.g.bh);
-            a_k = (int)(ak + ks - br * P.a.g.bh);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) a_shh[h] = shard_or_oob(P.a.g, br, a_bc[h]);
+            for (int h = 0; h < 2; ++h) a_shh[h] = shard_or_oob_q(P.a.g, a_blk, a_bc[h], qsa);
           }
           if (!b_mn) {
-            const int64_t bc = udiv32(bk + ks, P.b.g.bw);
-            b_k = (int)(bk + ks - bc * P.b.g.bw);
-            b_sh = shard_or_oob(P.b.g, b_br, bc);
+            b_sh = shard_or_oob_q(P.b.g, b_br, b_blk, qsb);
           } else {
-            const int64_t br = udiv32(bk + ks, P.b.g.bh);
-            b_k = (int)(bk + ks - br * P.b.g.bh);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) b_shh[h] = shard_or_oob(P.b.g, br, b_bc[h]);
+            for (int h = 0; h < 2; ++h) b_shh[h] = shard_or_oob_q(P.b.g, b_blk, b_bc[h], qsb);
           }
           for (int32_t kt = 0; kt < tpsK; ++kt) {
             const int s = (int)(it % S);
