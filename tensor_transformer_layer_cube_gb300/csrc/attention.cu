@@ -45,7 +45,9 @@ constexpr int TR = 128;              // rows of a tile (queries or keys)
 constexpr int kComputeWarps = 4;     // forward: row warps per query tile (one per TMEM lane quarter)
 // backward: warp 0 producer, warp 1 MMA issuer, warps 2-9 element-wise work,
 // two per TMEM lane quarter, each on half of a tile row's 128 columns
-constexpr int kBwdComputeWarps = 8;
+constexpr int kBwdComputeWarps = 16;  // backward: element-wise warps, kBwdWpq per TMEM lane quarter
+constexpr int kBwdWpq = kBwdComputeWarps / 4;
+constexpr int kBwdCpw = 4 / kBwdWpq;    // 32-column chunks of a 128-key (or 128-query) row per warp
 constexpr int kBwdThreads = 32 * (2 + kBwdComputeWarps);
 constexpr uint32_t kChunk = 16384;   // 128 rows x 64 bf16 columns (one 128-byte swizzle span)
 constexpr uint32_t kTile = 2 * kChunk;  // a 128 x 128 bf16 tile
@@ -659,7 +661,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else {
     // ---------------------------------------- query rows of S and dP (then key rows of dV, dK)
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;  // key columns [64 half, +64) of the tile
+    const int cgp = (warp - 2) >> 2;  // key columns [32 kBwdCpw cgp, +32 kBwdCpw) of the tile
     const int r = quarter * 32 + lane;
     const float sl2 = A.scale * kLog2e;
     const float sigma = ds_sigma(dmax, A.scale, A.d), dscale = A.scale * sigma;
@@ -678,17 +680,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // P = exp2(S sl2 - lse), zero where the key follows the query, kept as
         // bf16 pairs: computed before the buffer is free, stored [query][key]
         // (the layout the dV product reads transposed) once it is
-        uint32_t pk[2][16];
+        uint32_t pk[kBwdCpw][16];
         {
-          uint32_t v[2][32];
+          uint32_t v[kBwdCpw][32];
 #pragma unroll
-          for (int i = 0; i < 2; ++i) tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)((2 * half + i) * 32)), v[i]);
+          for (int i = 0; i < kBwdCpw; ++i)
+            tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)((kBwdCpw * cgp + i) * 32)), v[i]);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 2; ++i) {
+          for (int i = 0; i < kBwdCpw; ++i) {
 #pragma unroll
             for (int e2 = 0; e2 < 16; ++e2) {
-              const int k = (2 * half + i) * 32 + 2 * e2;
+              const int k = (kBwdCpw * cgp + i) * 32 + 2 * e2;
               const float f0 = (!diag || k <= r) ? ex2_approx(fmaf(__uint_as_float(v[i][2 * e2]), sl2, -l2)) : 0.0f;
               const float f1 = (!diag || k + 1 <= r) ? ex2_approx(fmaf(__uint_as_float(v[i][2 * e2 + 1]), sl2, -l2)) : 0.0f;
               const __nv_bfloat162 h2 = __floats2bfloat162_rn(f0, f1);
@@ -699,10 +702,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!(ok = warp_wait(pds_empty, 1, c, A.err, lane))) break;  // previous dK product has read dS
         auto store_pk = [&]() {
 #pragma unroll
-          for (int i = 0; i < 2; ++i)
+          for (int i = 0; i < kBwdCpw; ++i)
 #pragma unroll
             for (int g = 0; g < 4; ++g)
-              st_tile8(pPdS, r, (2 * half + i) * 4 + g,
+              st_tile8(pPdS, r, (kBwdCpw * cgp + i) * 4 + g,
                        make_uint4(pk[i][4 * g], pk[i][4 * g + 1], pk[i][4 * g + 2], pk[i][4 * g + 3]));
         };
         store_pk();
@@ -711,15 +714,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         warp_arrive(pds_full, lane);
         // sigma dS = P (dP - delta) * scale * sigma from the bf16 P in registers, as fp16
         {
-          uint32_t wv[2][32];
+          uint32_t wv[kBwdCpw][32];
 #pragma unroll
-          for (int i = 0; i < 2; ++i)
-            tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(128 + (2 * half + i) * 32)), wv[i]);
+          for (int i = 0; i < kBwdCpw; ++i)
+            tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(128 + (kBwdCpw * cgp + i) * 32)), wv[i]);
           tmem_ld_wait();
           tc_fence_before();
           warp_arrive(st_empty, lane);  // S and dP are read: the next tile's may overwrite them
 #pragma unroll
-          for (int i = 0; i < 2; ++i) {
+          for (int i = 0; i < kBwdCpw; ++i) {
 #pragma unroll
             for (int e2 = 0; e2 < 16; ++e2) {
               const float2 p2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[i][e2]));
@@ -744,9 +747,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int64_t br = grow / A.qkv.bh, bc = gcol / A.qkv.bw;
         bf16* dst = dqkv + A.qkv.block_base((int32_t)br, (int32_t)bc) + (grow - br * A.qkv.bh) * A.qkv.bw +
                     (gcol - bc * A.qkv.bw);
-        const int nd = (int)(A.d / 64);  // this warp's 32-column chunks: its half of the d columns
         const float mul = which == 0 ? 1.0f : 1.0f / sigma;  // dK was accumulated from sigma dS
-        for (int cc = half * nd; cc < half * nd + nd; ++cc) {
+        for (int cc = cgp; cc < (int)(A.d / 32); cc += kBwdWpq) {  // this warp's 32-column chunks of d
           uint32_t v[32];
           tmem_ld_32x32b_x32(tmem_row(tmem, quarter, 256u + (uint32_t)(which * A.d) + cc * 32), v);
           tmem_ld_wait();
@@ -861,7 +863,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else {
     // ------------------------------------------------------------ query rows
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;  // key columns [64 half, +64) of the tile
+    const int cgp = (warp - 2) >> 2;  // key columns [32 kBwdCpw cgp, +32 kBwdCpw) of the tile
     const int r = quarter * 32 + lane;
     const float sl2 = A.scale * kLog2e;
     const float sigma = ds_sigma(dmax, A.scale, A.d), dscale = A.scale * sigma;
@@ -878,7 +880,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
         const bool diag = it == niter - 1;
 #pragma unroll 1
-        for (int cc = 2 * half; cc < 2 * half + 2; ++cc) {
+        for (int cc = kBwdCpw * cgp; cc < kBwdCpw * cgp + kBwdCpw; ++cc) {
           uint32_t v[32], wv[32];
           tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(cc * 32)), v);
           tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(128 + cc * 32)), wv);
@@ -907,9 +909,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int64_t br = grow / A.qkv.bh, bc = gcol / A.qkv.bw;
       bf16* dst = dqkv + A.qkv.block_base((int32_t)br, (int32_t)bc) + (grow - br * A.qkv.bh) * A.qkv.bw +
                   (gcol - bc * A.qkv.bw);
-      const int nd = (int)(A.d / 64);  // this warp's half of the d columns
       const float inv_sigma = 1.0f / sigma;  // dQ was accumulated from sigma dS
-      for (int cc = half * nd; cc < half * nd + nd; ++cc) {
+      for (int cc = cgp; cc < (int)(A.d / 32); cc += kBwdWpq) {  // this warp's 32-column chunks of d
         uint32_t v[32];
         tmem_ld_32x32b_x32(tmem_row(tmem, quarter, 256u + cc * 32), v);
         tmem_ld_wait();
