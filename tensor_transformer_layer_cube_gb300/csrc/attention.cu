@@ -19,16 +19,18 @@
 // producer, warp 1 = MMA issuer (and TMEM owner), then one thread per tile
 // row (TMEM lane) for the softmax arithmetic:
 //  * forward: two query tiles per CTA, one pass over the key tiles at or
-//    below the diagonal with an online softmax (S = Q K^T in TMEM, P to
-//    shared memory, O += P V in TMEM, O rescaled only when the row maximum
-//    grows by more than 2^8); the row's log-sum-exp is saved for the backward.
+//    below the diagonal with an online softmax (S = Q K^T in TMEM, P written
+//    back over it, O += P V in TMEM with P read from there, O rescaled only
+//    when the row maximum grows by more than 2^8); the row's log-sum-exp is
+//    saved for the backward.
 //  * backward dK/dV: per key tile, over the query tiles at or above the
 //    diagonal: S = Q K^T, dP = dO V^T, P = exp(S - lse) (one query row per
 //    thread, so lse and rowsum(dO O) are per-thread values), then
 //    dV += P^T dO and dK += dS^T Q with dS = P (dP - rowsum(dO O)) / sqrt(d),
 //    P and dS read transposed out of shared memory by the MMA.
 //  * backward dQ: per query tile, over the key tiles at or below the
-//    diagonal: S, dP, dS as above, dQ += dS K.
+//    diagonal: S, dP, dS as above, dQ += dS K with dS in TMEM (the next key
+//    tile's S and dP are computed while dS is formed).
 // The score and probability matrices never leave the SM.  Every mbarrier
 // wait is bounded; a wait that runs out sets the error word and the CTA
 // returns.
@@ -106,13 +108,6 @@ __device__ __forceinline__ uint4 pack8f(const float* f) {
   __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
 #pragma unroll
   for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
-  return v;
-}
-__device__ __forceinline__ uint4 pack8h(const float* f) {
-  uint4 v;
-  __half2* h = reinterpret_cast<__half2*>(&v);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
   return v;
 }
 
@@ -769,8 +764,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 // ------------------------------------------------------------------ backward: dQ
 // item w: query tile nq-1-(w / Z) of (batch, head) w % Z
-// smem: Q | dO | K0 V0 | K1 V1 | dS (32 KiB each)
-// TMEM: S [0,128) dP [128,256) dQ [256,256+d)
+// smem: Q | dO | K0 K1 K2 | V0 V1 (32 KiB each): K in a ring of three (read by
+// S and by dQ), V in a ring of two (read by dP only)
+// TMEM: S [0,128) dP [128,256) dQ [256,256+d), sigma dS as fp16 pairs in two
+// buffers of 64 columns at 384 and 448 (the A operand of dQ += dS K)
+// The element-wise warps copy a tile's S and dP into registers and release
+// them at once, so the issuer runs the next key tile's S and dP while they
+// form dS: per key tile the tensor pipe sees S(j+1), dP(j+1), dQ(j).
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap mqkv, const __grid_constant__ CUtensorMap mo,
                        const AttnProblem A, const float* __restrict__ lse, const float* __restrict__ delta,
@@ -778,14 +778,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const Ctx c = setup_smem(smem_raw);
   const uint32_t sQ = c.base, sdO = c.base + kTile;
-  const uint32_t sK[2] = {c.base + 2 * kTile, c.base + 4 * kTile}, sV[2] = {c.base + 3 * kTile, c.base + 5 * kTile};
-  const uint32_t sdS = c.base + 6 * kTile;
-  uint8_t* pdS = c.base_ptr + 6 * kTile;
+  auto sK = [&](uint32_t i) { return c.base + (2u + i) * kTile; };
+  auto sV = [&](uint32_t i) { return c.base + (5u + i) * kTile; };
   auto bar = [&](int k) { return c.bar0 + 8u * k; };
-  const uint32_t qo_full = bar(0), qo_empty = bar(1), s_full = bar(2), s_empty = bar(3), ds_full = bar(4),
-                 ds_empty = bar(5), acc_full = bar(6), acc_empty = bar(7), final_bar = bar(8);
-  auto r_full = [&](int s) { return bar(9 + s); };
-  auto r_empty = [&](int s) { return bar(11 + s); };
+  const uint32_t qo_full = bar(0), qo_empty = bar(1), s_full = bar(2), s_empty = bar(3), acc_full = bar(4),
+                 acc_empty = bar(5), final_bar = bar(6);
+  auto ds_full = [&](uint32_t b) { return bar(7 + (int)b); };    // 2
+  auto ds_empty = [&](uint32_t b) { return bar(9 + (int)b); };   // 2
+  auto k_full = [&](uint32_t i) { return bar(11 + (int)i); };    // 3
+  auto k_empty = [&](uint32_t i) { return bar(14 + (int)i); };   // 3
+  auto v_full = [&](uint32_t i) { return bar(17 + (int)i); };    // 2
+  auto v_empty = [&](uint32_t i) { return bar(19 + (int)i); };   // 2
+  constexpr int kBars = 21;
+  constexpr uint32_t kDs = 384;  // first dS buffer column
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t nq = A.s / TR, items = A.Z * nq;
@@ -793,7 +798,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t dbytes = (uint32_t)(A.d * TR * 2);
 
   if (threadIdx.x == 0) {
-    for (int k = 0; k < 13; ++k) mbar_init(bar(k), (k == 3 || k == 4 || k == 7) ? kBwdComputeWarps : 1);
+    for (int k = 0; k < kBars; ++k) {
+      // s_empty, acc_empty, ds_full: one arrival per element-wise warp
+      const bool ew = k == 3 || k == 5 || k == 7 || k == 8;
+      mbar_init(bar(k), ew ? kBwdComputeWarps : 1);
+    }
     *c.abort_flag = 0;
     fence_barrier_init();
   }
@@ -819,12 +828,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         load_tile(&mqkv, A.qkv, row_q, t * A.d, nch, sQ, qo_full);
         load_tile(&mo, A.o, row_q, t * A.d, nch, sdO, qo_full);
         for (int it = 0; it < niter; ++it, ++n) {
-          const int s = n & 1;
-          if (!(ok = mbar_wait(r_empty(s), ((n >> 1) & 1) ^ 1, c.abort_flag, A.err))) break;
-          mbar_arrive_expect_tx(r_full(s), 2 * dbytes);
+          const uint32_t ks = n % 3, vs = n & 1;
           const int64_t row_k = b * A.s + (int64_t)it * TR;
-          load_tile(&mqkv, A.qkv, row_k, A.h + t * A.d, nch, sK[s], r_full(s));
-          load_tile(&mqkv, A.qkv, row_k, 2 * A.h + t * A.d, nch, sV[s], r_full(s));
+          if (!(ok = mbar_wait(k_empty(ks), ((n / 3) & 1) ^ 1, c.abort_flag, A.err))) break;
+          mbar_arrive_expect_tx(k_full(ks), dbytes);
+          load_tile(&mqkv, A.qkv, row_k, A.h + t * A.d, nch, sK(ks), k_full(ks));
+          if (!(ok = mbar_wait(v_empty(vs), ((n >> 1) & 1) ^ 1, c.abort_flag, A.err))) break;
+          mbar_arrive_expect_tx(v_full(vs), dbytes);
+          load_tile(&mqkv, A.qkv, row_k, 2 * A.h + t * A.d, nch, sV(vs), v_full(vs));
         }
       }
     }
@@ -832,28 +843,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0) {
       const uint32_t id_s = idesc_f16_f32(TR, TR, 0, 0);           // S = Q K^T, fp16
       const uint32_t id_dp = idesc_bf16_f32(TR, TR, 0, 0);          // dP = dO V^T, bf16
-      const uint32_t id_acc = idesc_f16_f32(TR, (int)A.d, 0, 1);    // dQ += dS K, fp16
+      const uint32_t id_acc = idesc_f16_f32(TR, (int)A.d, 0, 1);    // dQ += dS K, fp16 (dS from TMEM, K MN-major)
       const int ks_d = (int)(A.d / 16);
       uint32_t n = 0, ic = 0;
       bool ok = true;
+      // S and dP of global key-tile iteration m, once the element-wise warps
+      // hold iteration m-1's; V's slot is free again when dP completes
+      auto issue_sdp = [&](uint32_t m, bool last) -> bool {
+        if (!mbar_wait(k_full(m % 3), (m / 3) & 1, c.abort_flag, A.err)) return false;
+        if (!mbar_wait(v_full(m & 1), (m >> 1) & 1, c.abort_flag, A.err)) return false;
+        if (!mbar_wait(s_empty, (m & 1) ^ 1, c.abort_flag, A.err)) return false;
+        tc_fence_after();
+        mma_tile(tmem, sQ, false, sK(m % 3), false, ks_d, id_s, false);          // S = Q K^T
+        mma_tile(tmem + 128u, sdO, false, sV(m & 1), false, ks_d, id_dp, false);  // dP = dO V^T
+        umma_commit(v_empty(m & 1));
+        if (last) umma_commit(qo_empty);  // the item's Q and dO are no longer read
+        umma_commit(s_full);
+        return true;
+      };
       for (int64_t rd = 0, w = snake_item(0); w < items && ok; w = snake_item(++rd), ++ic) {
         const int niter = (int)(nq - 1 - w / A.Z) + 1;
         if (!(ok = mbar_wait(qo_full, ic & 1, c.abort_flag, A.err))) break;
+        if (!(ok = issue_sdp(n, niter == 1))) break;
         for (int it = 0; it < niter && ok; ++it, ++n) {
-          const int s = n & 1;
-          if (!(ok = mbar_wait(r_full(s), (n >> 1) & 1, c.abort_flag, A.err))) break;
-          if (!(ok = mbar_wait(s_empty, (n & 1) ^ 1, c.abort_flag, A.err))) break;
-          tc_fence_after();
-          mma_tile(tmem, sQ, false, sK[s], false, ks_d, id_s, false);          // S = Q K^T
-          mma_tile(tmem + 128u, sdO, false, sV[s], false, ks_d, id_dp, false);  // dP = dO V^T
-          if (it == niter - 1) umma_commit(qo_empty);
-          umma_commit(s_full);
-          if (!(ok = mbar_wait(ds_full, n & 1, c.abort_flag, A.err))) break;
+          if (it + 1 < niter && !(ok = issue_sdp(n + 1, it + 2 == niter))) break;
+          const uint32_t db = n & 1;
+          if (!(ok = mbar_wait(ds_full(db), (n >> 1) & 1, c.abort_flag, A.err))) break;
           if (it == 0 && !(ok = mbar_wait(acc_empty, (ic & 1) ^ 1, c.abort_flag, A.err))) break;
           tc_fence_after();
-          mma_tile(tmem + 256u, sdS, false, sK[s], true, TR / 16, id_acc, it > 0);  // dQ += dS K
-          umma_commit(ds_empty);
-          umma_commit(r_empty(s));
+          const uint32_t dst = tmem + kDs + 64u * db;
+          for (int k = 0; k < TR / 16; ++k)  // dQ += dS K
+            umma_ts(tmem + 256u, dst + 8u * (uint32_t)k, desc_mnmajor(sK(n % 3), k), id_acc,
+                    (it > 0 || k > 0) ? 1u : 0u);
+          umma_commit(ds_empty(db));
+          umma_commit(k_empty(n % 3));
         }
         if (ok) umma_commit(acc_full);
       }
@@ -876,31 +899,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const float l2 = lse[qrow] * kLog2e, dr = delta[qrow];
       for (int it = 0; it < niter && ok; ++it, ++n) {
         if (!(ok = warp_wait(s_full, n & 1, c, A.err, lane))) break;
-        if (!(ok = warp_wait(ds_empty, (n & 1) ^ 1, c, A.err, lane))) break;
         tc_fence_after();
         const bool diag = it == niter - 1;
-#pragma unroll 1
-        for (int cc = kBwdCpw * cgp; cc < kBwdCpw * cgp + kBwdCpw; ++cc) {
-          uint32_t v[32], wv[32];
-          tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(cc * 32)), v);
-          tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(128 + cc * 32)), wv);
-          tmem_ld_wait();
+        uint32_t v[kBwdCpw][32], wv[kBwdCpw][32];
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            float f[8];
+        for (int i = 0; i < kBwdCpw; ++i) {
+          tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)((kBwdCpw * cgp + i) * 32)), v[i]);
+          tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(128 + (kBwdCpw * cgp + i) * 32)), wv[i]);
+        }
+        tmem_ld_wait();
+        tc_fence_before();
+        warp_arrive(s_empty, lane);  // S and dP are in registers: the next key tile's may overwrite them
+        // sigma dS = P (dP - delta) * scale * sigma, P = exp2(S sl2 - lse), zero where the key follows the query
+        uint32_t pk[kBwdCpw][16];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int k = cc * 32 + g * 8 + e;
-              const float p = (!diag || k <= r) ? ex2_approx(fmaf(__uint_as_float(v[g * 8 + e]), sl2, -l2)) : 0.0f;
-              f[e] = p * (__uint_as_float(wv[g * 8 + e]) - dr) * dscale;
-            }
-            st_tile8(pdS, r, cc * 4 + g, pack8h(f));  // sigma dS, fp16
+        for (int i = 0; i < kBwdCpw; ++i) {
+#pragma unroll
+          for (int e2 = 0; e2 < 16; ++e2) {
+            const int k = (kBwdCpw * cgp + i) * 32 + 2 * e2;
+            const float p0 = (!diag || k <= r) ? ex2_approx(fmaf(__uint_as_float(v[i][2 * e2]), sl2, -l2)) : 0.0f;
+            const float p1 = (!diag || k + 1 <= r) ? ex2_approx(fmaf(__uint_as_float(v[i][2 * e2 + 1]), sl2, -l2)) : 0.0f;
+            const __half2 h2 = __floats2half2_rn(p0 * (__uint_as_float(wv[i][2 * e2]) - dr) * dscale,
+                                                 p1 * (__uint_as_float(wv[i][2 * e2 + 1]) - dr) * dscale);
+            pk[i][e2] = *reinterpret_cast<const uint32_t*>(&h2);
           }
         }
-        fence_proxy_async_smem();
+        const uint32_t db = n & 1;
+        if (!(ok = warp_wait(ds_empty(db), ((n >> 1) & 1) ^ 1, c, A.err, lane))) break;  // dQ(j-2) has read it
+        tc_fence_after();
+#pragma unroll
+        for (int i = 0; i < kBwdCpw; ++i)
+          tmem_st_32x32b_x16(tmem_row(tmem, quarter, kDs + 64u * db + (uint32_t)((kBwdCpw * cgp + i) * 16)), pk[i]);
+        tmem_st_wait();
         tc_fence_before();
-        warp_arrive(ds_full, lane);
-        warp_arrive(s_empty, lane);
+        warp_arrive(ds_full(db), lane);
       }
       if (!ok || !(ok = warp_wait(acc_full, ic & 1, c, A.err, lane))) break;
       tc_fence_after();
