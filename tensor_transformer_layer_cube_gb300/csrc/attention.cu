@@ -24,10 +24,10 @@
 //    when the row maximum grows by more than 2^8); the row's log-sum-exp is
 //    saved for the backward.
 //  * backward dK/dV: per key tile, over the query tiles at or above the
-//    diagonal: S = Q K^T, dP = dO V^T, P = exp(S - lse) (one query row per
-//    thread, so lse and rowsum(dO O) are per-thread values), then
-//    dV += P^T dO and dK += dS^T Q with dS = P (dP - rowsum(dO O)) / sqrt(d),
-//    P and dS read transposed out of shared memory by the MMA.
+//    diagonal: S^T = K Q^T, dP^T = V dO^T (one key row per thread; lse and
+//    rowsum(dO O) are per-column values read from shared memory),
+//    P^T = exp(S^T - lse), dS^T = P^T (dP^T - rowsum(dO O)) / sqrt(d), then
+//    dV += P^T dO and dK += dS^T Q with P^T and dS^T read from TMEM.
 //  * backward dQ: per query tile, over the key tiles at or below the
 //    diagonal: S, dP, dS as above, dQ += dS K with dS in TMEM (the next key
 //    tile's S and dP are computed while dS is formed).
@@ -96,11 +96,6 @@ __device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int k16) {  // co
 }
 __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int k16) {  // contraction along the rows
   return smem_desc_sw128(tile + (uint32_t)k16 * 2048u, kChunk, 1024u);
-}
-
-// 8 bf16 values for columns [8 g, +8) of row r of a K-major 128 x 128 tile
-__device__ __forceinline__ void st_tile8(uint8_t* tile, int r, int g, uint4 v) {
-  *reinterpret_cast<uint4*>(tile + (g >> 3) * kChunk + r * 128 + (((g & 7) ^ (r & 7)) << 4)) = v;
 }
 
 __device__ __forceinline__ uint4 pack8f(const float* f) {
@@ -546,10 +541,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
 // ------------------------------------------------------------------ backward: dK, dV
 // item w: key tile w / Z of (batch, head) w % Z (the most query tiles first)
-// smem: K | V | Q0 dO0 | Q1 dO1 | PdS (32 KiB each); PdS holds P, then dS,
-// [query][key] (the MN-major A operand of the dV and dK products)
-// TMEM: S [0,128) dP [128,256) (lanes = queries), dV [256,256+d) dK
-// [256+d, 256+2d) (lanes = keys)
+// The key tile's rows are the TMEM lanes: S^T = K Q^T and dP^T = V dO^T, so
+// P^T and dS^T come out laid out as the A operand of dV += P^T dO and
+// dK += dS^T Q and stay in tensor memory: the bf16 (fp16) pairs of a
+// 32-query chunk go to the upper 16 columns of the chunk they were computed
+// from, which the same warp has already read.  A query tile's log-sum-exp and
+// delta arrive with its Q and dO (one 512-byte bulk copy each) and are read
+// per column from shared memory.
+// The issuer starts S^T(j+1) once dV(j) has read P^T(j), and dP^T(j+1) once
+// dK(j) has read dS^T(j): per query tile the tensor pipe sees S^T, dP^T, dV, dK,
+// and the element-wise warps form P^T while dP^T is computed.
+// smem: K | V | Q0 dO0 | Q1 dO1 (32 KiB each) | lse0 delta0 lse1 delta1 (512 B each)
+// TMEM (lanes = keys): S^T [0,128), dP^T [128,256), dV [256,256+d), dK [256+d, 256+2d)
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap mqkv, const __grid_constant__ CUtensorMap mo,
                          const AttnProblem A, const float* __restrict__ lse, const float* __restrict__ delta,
@@ -558,13 +561,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const Ctx c = setup_smem(smem_raw);
   const uint32_t sK = c.base, sV = c.base + kTile;
   const uint32_t sQ[2] = {c.base + 2 * kTile, c.base + 4 * kTile}, sdO[2] = {c.base + 3 * kTile, c.base + 5 * kTile};
-  const uint32_t sPdS = c.base + 6 * kTile;
-  uint8_t* pPdS = c.base_ptr + 6 * kTile;
+  const uint32_t sStat = c.base + 6 * kTile;  // per slot: lse [0,128), delta [128,256) as floats
+  const float* pStat = reinterpret_cast<const float*>(c.base_ptr + 6 * kTile);
   auto bar = [&](int k) { return c.bar0 + 8u * k; };
-  const uint32_t kv_full = bar(0), kv_empty = bar(1), st_full = bar(2), st_empty = bar(3), pds_full = bar(4),
-                 pds_empty = bar(5), acc_full = bar(6), acc_empty = bar(7), final_bar = bar(8);
-  auto r_full = [&](int s) { return bar(9 + s); };
-  auto r_empty = [&](int s) { return bar(11 + s); };
+  const uint32_t kv_full = bar(0), kv_empty = bar(1), s_full = bar(2), dp_full = bar(3), p_full = bar(4),
+                 ds_full = bar(5), s_free = bar(6), dp_free = bar(7), acc_full = bar(8), acc_empty = bar(9),
+                 final_bar = bar(10);
+  auto r_full = [&](int s) { return bar(11 + s); };
+  auto r_empty = [&](int s) { return bar(13 + s); };
+  constexpr int kBars = 15;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t nq = A.s / TR, items = A.Z * nq;
@@ -572,7 +577,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t dbytes = (uint32_t)(A.d * TR * 2);
 
   if (threadIdx.x == 0) {
-    for (int k = 0; k < 13; ++k) mbar_init(bar(k), (k == 3 || k == 4 || k == 7) ? kBwdComputeWarps : 1);
+    for (int k = 0; k < kBars; ++k) {
+      // p_full, ds_full, acc_empty: one arrival per element-wise warp
+      const bool ew = k == 4 || k == 5 || k == 9;
+      mbar_init(bar(k), ew ? kBwdComputeWarps : 1);
+    }
     *c.abort_flag = 0;
     fence_barrier_init();
   }
@@ -600,52 +609,55 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int it = 0; it < niter; ++it, ++n) {
           const int s = n & 1;
           if (!(ok = mbar_wait(r_empty(s), ((n >> 1) & 1) ^ 1, c.abort_flag, A.err))) break;
-          mbar_arrive_expect_tx(r_full(s), 2 * dbytes);
+          mbar_arrive_expect_tx(r_full(s), 2 * dbytes + 2 * TR * 4);
           const int64_t row_q = b * A.s + (jk + it) * TR;
           load_tile(&mqkv, A.qkv, row_q, t * A.d, nch, sQ[s], r_full(s));
           load_tile(&mo, A.o, row_q, t * A.d, nch, sdO[s], r_full(s));
+          const int64_t q0 = z * A.s + (jk + it) * TR;  // the tile's first row of lse and delta
+          bulk_load(sStat + (uint32_t)s * 1024u, lse + q0, TR * 4, r_full(s));
+          bulk_load(sStat + (uint32_t)s * 1024u + 512u, delta + q0, TR * 4, r_full(s));
         }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t id_s = idesc_f16_f32(TR, TR, 0, 0);           // S = Q K^T, fp16
-      const uint32_t id_dp = idesc_bf16_f32(TR, TR, 0, 0);          // dP = dO V^T, bf16
-      const uint32_t id_dv = idesc_bf16_f32(TR, (int)A.d, 1, 1);    // dV += P^T dO, bf16 (P^T read transposed)
-      const uint32_t id_dk = idesc_f16_f32(TR, (int)A.d, 1, 1);     // dK += dS^T Q, fp16 (dS^T read transposed)
+      const uint32_t id_s = idesc_f16_f32(TR, TR, 0, 0);           // S^T = K Q^T, fp16
+      const uint32_t id_dp = idesc_bf16_f32(TR, TR, 0, 0);          // dP^T = V dO^T, bf16
+      const uint32_t id_dv = idesc_bf16_f32(TR, (int)A.d, 0, 1);    // dV += P^T dO, bf16 (P^T from TMEM, dO MN-major)
+      const uint32_t id_dk = idesc_f16_f32(TR, (int)A.d, 0, 1);     // dK += dS^T Q, fp16 (dS^T from TMEM, Q MN-major)
       const int ks_d = (int)(A.d / 16);
+      // TMEM column of the A operand's 16 queries [16 k, +16): the upper half
+      // of their 32-query chunk
+      auto a_col = [](uint32_t base, int k) { return base + 32u * (uint32_t)(k >> 1) + 16u + 8u * (uint32_t)(k & 1); };
       uint32_t n = 0, ic = 0;
       bool ok = true;
-      // S = Q K^T and dP = dO V^T of global query-tile iteration m (slot m & 1)
-      auto issue_sdp = [&](uint32_t m, bool last) -> bool {
-        const int sm = (int)(m & 1u);
-        if (!mbar_wait(r_full(sm), (m >> 1) & 1, c.abort_flag, A.err)) return false;
-        if (!mbar_wait(st_empty, (m & 1) ^ 1, c.abort_flag, A.err)) return false;
-        tc_fence_after();
-        mma_tile(tmem, sQ[sm], false, sK, false, ks_d, id_s, false);
-        mma_tile(tmem + 128u, sdO[sm], false, sV, false, ks_d, id_dp, false);
-        if (last) umma_commit(kv_empty);  // the item's K and V are no longer read
-        umma_commit(st_full);
-        return true;
-      };
       for (int64_t rd = 0, w = snake_item(0); w < items && ok; w = snake_item(++rd), ++ic) {
         const int niter = (int)(nq - w / A.Z);
         if (!(ok = mbar_wait(kv_full, ic & 1, c.abort_flag, A.err))) break;
-        if (!(ok = issue_sdp(n, niter == 1))) break;
         for (int it = 0; it < niter && ok; ++it, ++n) {
           const int s = n & 1;
-          if (!(ok = mbar_wait(pds_full, 0, c.abort_flag, A.err))) break;
+          if (!(ok = mbar_wait(r_full(s), (n >> 1) & 1, c.abort_flag, A.err))) break;
+          if (!(ok = mbar_wait(s_free, (n & 1) ^ 1, c.abort_flag, A.err))) break;  // dV(j-1) has read P^T
+          tc_fence_after();
+          mma_tile(tmem, sK, false, sQ[s], false, ks_d, id_s, false);  // S^T = K Q^T
+          umma_commit(s_full);
+          if (!(ok = mbar_wait(dp_free, (n & 1) ^ 1, c.abort_flag, A.err))) break;  // dK(j-1) has read dS^T
+          tc_fence_after();
+          mma_tile(tmem + 128u, sV, false, sdO[s], false, ks_d, id_dp, false);  // dP^T = V dO^T
+          if (it == niter - 1) umma_commit(kv_empty);  // the item's K and V are no longer read
+          umma_commit(dp_full);
+          if (!(ok = mbar_wait(p_full, n & 1, c.abort_flag, A.err))) break;
           if (it == 0 && !(ok = mbar_wait(acc_empty, (ic & 1) ^ 1, c.abort_flag, A.err))) break;
           tc_fence_after();
-          mma_tile(tmem + 256u, sPdS, true, sdO[s], true, TR / 16, id_dv, it > 0);  // dV += P^T dO
-          umma_commit(pds_empty);
-          // the next query tile's S and dP go ahead of this tile's dK, so they
-          // are computed while the element-wise warps form dS
-          if (it + 1 < niter && !(ok = issue_sdp(n + 1, it + 2 == niter))) break;
-          if (!(ok = mbar_wait(pds_full, 1, c.abort_flag, A.err))) break;
+          for (int k = 0; k < TR / 16; ++k)  // dV += P^T dO
+            umma_ts(tmem + 256u, tmem + a_col(0u, k), desc_mnmajor(sdO[s], k), id_dv, (it > 0 || k > 0) ? 1u : 0u);
+          umma_commit(s_free);
+          if (!(ok = mbar_wait(ds_full, n & 1, c.abort_flag, A.err))) break;
           tc_fence_after();
-          mma_tile(tmem + 256u + (uint32_t)A.d, sPdS, true, sQ[s], true, TR / 16, id_dk, it > 0);  // dK += dS^T Q
-          umma_commit(pds_empty);
+          for (int k = 0; k < TR / 16; ++k)  // dK += dS^T Q
+            umma_ts(tmem + 256u + (uint32_t)A.d, tmem + a_col(128u, k), desc_mnmajor(sQ[s], k), id_dk,
+                    (it > 0 || k > 0) ? 1u : 0u);
+          umma_commit(dp_free);
           umma_commit(r_empty(s));
         }
         if (ok) umma_commit(acc_full);
@@ -654,9 +666,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       drain(final_bar, 0);
     }
   } else {
-    // ---------------------------------------- query rows of S and dP (then key rows of dV, dK)
+    // ---------------------------------------- key rows of S^T and dP^T (then of dV, dK)
     const int quarter = warp & 3;
-    const int cgp = (warp - 2) >> 2;  // key columns [32 kBwdCpw cgp, +32 kBwdCpw) of the tile
+    const int cgp = (warp - 2) >> 2;  // query columns [32 kBwdCpw cgp, +32 kBwdCpw) of the tile
     const int r = quarter * 32 + lane;
     const float sl2 = A.scale * kLog2e;
     const float sigma = ds_sigma(dmax, A.scale, A.d), dscale = A.scale * sigma;
@@ -666,73 +678,69 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int64_t jk = w / A.Z, z = w % A.Z, b = z / A.H, t = z % A.H;
       const int niter = (int)(nq - jk);
       for (int it = 0; it < niter && ok; ++it, ++n) {
-        // this thread's query row: its log-sum-exp and delta, read before the waits
-        const int64_t qrow = z * A.s + (jk + it) * TR + r;
-        const float l2 = lse[qrow] * kLog2e, dr = delta[qrow];
-        if (!(ok = warp_wait(st_full, n & 1, c, A.err, lane))) break;
+        const int s = n & 1;
+        const float* st = pStat + s * 256;  // lse [0,128), delta [128,256) of the query tile
+        if (!(ok = warp_wait(r_full(s), (n >> 1) & 1, c, A.err, lane))) break;
+        __syncwarp();  // lane 0 observed the copies of lse and delta: order the other lanes' reads after it
+        if (!(ok = warp_wait(s_full, n & 1, c, A.err, lane))) break;
         tc_fence_after();
         const bool diag = it == 0;
-        // P = exp2(S sl2 - lse), zero where the key follows the query, kept as
-        // bf16 pairs: computed before the buffer is free, stored [query][key]
-        // (the layout the dV product reads transposed) once it is
-        uint32_t pk[kBwdCpw][16];
-        {
-          uint32_t v[kBwdCpw][32];
+        // P^T = exp2(S^T sl2 - lse log2 e), zero where the key follows the query
+        float pf[kBwdCpw][32];
 #pragma unroll
-          for (int i = 0; i < kBwdCpw; ++i)
-            tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)((kBwdCpw * cgp + i) * 32)), v[i]);
+        for (int i = 0; i < kBwdCpw; ++i) {
+          const int ch = kBwdCpw * cgp + i;
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(ch * 32)), v);
           tmem_ld_wait();
+          uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < kBwdCpw; ++i) {
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(st + ch * 32 + 4 * e4);
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-            for (int e2 = 0; e2 < 16; ++e2) {
-              const int k = (kBwdCpw * cgp + i) * 32 + 2 * e2;
-              const float f0 = (!diag || k <= r) ? ex2_approx(fmaf(__uint_as_float(v[i][2 * e2]), sl2, -l2)) : 0.0f;
-              const float f1 = (!diag || k + 1 <= r) ? ex2_approx(fmaf(__uint_as_float(v[i][2 * e2 + 1]), sl2, -l2)) : 0.0f;
-              const __nv_bfloat162 h2 = __floats2bfloat162_rn(f0, f1);
-              pk[i][e2] = *reinterpret_cast<const uint32_t*>(&h2);
+            for (int e = 0; e < 4; ++e) {
+              const int j = ch * 32 + 4 * e4 + e;
+              pf[i][4 * e4 + e] =
+                  (!diag || j >= r) ? ex2_approx(fmaf(__uint_as_float(v[4 * e4 + e]), sl2, -lv[e] * kLog2e)) : 0.0f;
             }
           }
-        }
-        if (!(ok = warp_wait(pds_empty, 1, c, A.err, lane))) break;  // previous dK product has read dS
-        auto store_pk = [&]() {
 #pragma unroll
-          for (int i = 0; i < kBwdCpw; ++i)
-#pragma unroll
-            for (int g = 0; g < 4; ++g)
-              st_tile8(pPdS, r, (kBwdCpw * cgp + i) * 4 + g,
-                       make_uint4(pk[i][4 * g], pk[i][4 * g + 1], pk[i][4 * g + 2], pk[i][4 * g + 3]));
-        };
-        store_pk();
-        fence_proxy_async_smem();
-        tc_fence_before();
-        warp_arrive(pds_full, lane);
-        // sigma dS = P (dP - delta) * scale * sigma from the bf16 P in registers, as fp16
-        {
-          uint32_t wv[kBwdCpw][32];
-#pragma unroll
-          for (int i = 0; i < kBwdCpw; ++i)
-            tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(128 + (kBwdCpw * cgp + i) * 32)), wv[i]);
-          tmem_ld_wait();
-          tc_fence_before();
-          warp_arrive(st_empty, lane);  // S and dP are read: the next tile's may overwrite them
-#pragma unroll
-          for (int i = 0; i < kBwdCpw; ++i) {
-#pragma unroll
-            for (int e2 = 0; e2 < 16; ++e2) {
-              const float2 p2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[i][e2]));
-              const float d0 = p2.x * (__uint_as_float(wv[i][2 * e2]) - dr) * dscale;
-              const float d1 = p2.y * (__uint_as_float(wv[i][2 * e2 + 1]) - dr) * dscale;
-              const __half2 h2 = __floats2half2_rn(d0, d1);
-              pk[i][e2] = *reinterpret_cast<const uint32_t*>(&h2);
-            }
+          for (int e2 = 0; e2 < 16; ++e2) {
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(pf[i][2 * e2], pf[i][2 * e2 + 1]);
+            pk[e2] = *reinterpret_cast<const uint32_t*>(&h2);
           }
+          tmem_st_32x32b_x16(tmem_row(tmem, quarter, (uint32_t)(ch * 32 + 16)), pk);
         }
-        if (!(ok = warp_wait(pds_empty, 0, c, A.err, lane))) break;  // dV product has read P
-        store_pk();
-        fence_proxy_async_smem();
+        tmem_st_wait();
         tc_fence_before();
-        warp_arrive(pds_full, lane);
+        warp_arrive(p_full, lane);
+        // sigma dS^T = P^T (dP^T - delta) * scale * sigma, as fp16 pairs
+        if (!(ok = warp_wait(dp_full, n & 1, c, A.err, lane))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int i = 0; i < kBwdCpw; ++i) {
+          const int ch = kBwdCpw * cgp + i;
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem_row(tmem, quarter, (uint32_t)(128 + ch * 32)), v);
+          tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 d4 = *reinterpret_cast<const float4*>(st + 128 + ch * 32 + 4 * e4);
+            const float d0 = pf[i][4 * e4] * (__uint_as_float(v[4 * e4]) - d4.x) * dscale;
+            const float d1 = pf[i][4 * e4 + 1] * (__uint_as_float(v[4 * e4 + 1]) - d4.y) * dscale;
+            const float d2 = pf[i][4 * e4 + 2] * (__uint_as_float(v[4 * e4 + 2]) - d4.z) * dscale;
+            const float d3 = pf[i][4 * e4 + 3] * (__uint_as_float(v[4 * e4 + 3]) - d4.w) * dscale;
+            const __half2 h01 = __floats2half2_rn(d0, d1), h23 = __floats2half2_rn(d2, d3);
+            pk[2 * e4] = *reinterpret_cast<const uint32_t*>(&h01);
+            pk[2 * e4 + 1] = *reinterpret_cast<const uint32_t*>(&h23);
+          }
+          tmem_st_32x32b_x16(tmem_row(tmem, quarter, (uint32_t)(128 + ch * 32 + 16)), pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        warp_arrive(ds_full, lane);
       }
       if (!ok || !(ok = warp_wait(acc_full, ic & 1, c, A.err, lane))) break;
       tc_fence_after();
@@ -1083,6 +1091,8 @@ tp3d_status launch_attn_bwd(const tp3d_ctx* ctx, const AttnProblem& A, const voi
                             const void* dO, const float* lse, float* delta, unsigned* dmax, void* dqkv,
                             cudaStream_t s) {
   TP3D_TRY(check(A));
+  // the dK/dV kernel copies 128-row runs of lse and delta with bulk copies
+  if ((reinterpret_cast<uintptr_t>(lse) | reinterpret_cast<uintptr_t>(delta)) & 15u) return TP3D_EALIGN;
   CUtensorMap mq, mo;
   TP3D_TRY(tile_map(&mq, A.qkv, qkv));
   TP3D_TRY(tile_map(&mo, A.o, dO));
