@@ -173,16 +173,29 @@ __global__ void __launch_bounds__(kThreads) ln_bwd_kernel(const Grid g, const bf
   }
 }
 
-// LayerNorm forward with the whole row in registers: C = NV * 256, lane l holds
-// columns 8 (l + 32 i) .. +7 for i < NV.  Every load of a row is issued
-// before the first use, so a warp spends one memory round trip per row, and
-// the statistics are taken from registers (two passes over them, no reload).
+// LayerNorm forward with the whole row staged in shared memory: C = NV * 256,
+// lane l holds columns 8 (l + 32 i) .. +7 for i < NV.  Every load of a row is
+// an asynchronous 16-byte copy into the warp's slice of shared memory, all
+// issued before the first use, so a warp spends one memory round trip per
+// row while holding no registers for the row; the statistics take two passes
+// over the staged row.  gamma and beta are staged once per CTA.  A CTA takes
+// (8 + 2) NV KiB / 2 of shared memory and few registers, so a grid of one row
+// per warp is resident at once (a row held in registers needs more than 64 of
+// them per thread, and the grid then runs in two rounds).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 template <int NV>
 __device__ __forceinline__ int64_t row_vec_off(const Grid& g, int64_t br, int64_t rr, int lane, int i) {
   const int32_t col = (lane + 32 * i) * 8;
   const int32_t bc = col / (int32_t)g.bw;
   return g.block_base((int32_t)br, bc) + rr * g.bw + (col - (int64_t)bc * g.bw);
 }
+
+template <int NV>
+constexpr int ln_row_smem() { return (kWarps + 2) * NV * 32 * 16; }  // the CTA's rows, then gamma and beta
 
 template <int NV>
 __global__ void __launch_bounds__(kThreads) ln_fwd_row_kernel(const Grid g, const bf16* __restrict__ x,
@@ -192,38 +205,54 @@ __global__ void __launch_bounds__(kThreads) ln_fwd_row_kernel(const Grid g, cons
                                                               float* __restrict__ mean, float* __restrict__ rstd,
                                                               float eps) {
   constexpr float invC = 1.0f / (float)(NV * 256);
+  extern __shared__ uint4 ln_rows[];
+  const uint4* sg = ln_rows + kWarps * NV * 32;
+  const uint4* sb = sg + NV * 32;
+  for (int i = threadIdx.x; i < NV * 32; i += kThreads) {
+    ln_rows[kWarps * NV * 32 + i] = __ldg(reinterpret_cast<const uint4*>(gamma) + i);
+    ln_rows[(kWarps + 1) * NV * 32 + i] = __ldg(reinterpret_cast<const uint4*>(beta) + i);
+  }
+  __syncthreads();
   const int lane = threadIdx.x & 31;
+  const uint4* row = ln_rows + (threadIdx.x >> 5) * NV * 32;  // this warp's row
+  const uint32_t row_s = smem_u32(row);
   const int64_t nwarps = (int64_t)gridDim.x * kWarps;
   for (int64_t r = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); r < g.R; r += nwarps) {
     const int64_t br = r / g.bh, rr = r - br * g.bh;
-    uint4 xv[NV];
+    // each lane copies, and later reads back, only its own 16-byte pieces
 #pragma unroll
-    for (int i = 0; i < NV; ++i) xv[i] = __ldg(reinterpret_cast<const uint4*>(x + row_vec_off<NV>(g, br, rr, lane, i)));
+    for (int i = 0; i < NV; ++i)
+      cp_async16(row_s + (uint32_t)(lane + 32 * i) * 16u, x + row_vec_off<NV>(g, br, rr, lane, i));
+    cp_async_wait_all();
     float s1 = 0.0f;
-#pragma unroll
+#pragma unroll 2
     for (int i = 0; i < NV; ++i) {
       float f[8];
-      unpack8(xv[i], f);
+      unpack8(row[lane + 32 * i], f);
 #pragma unroll
       for (int e = 0; e < 8; ++e) s1 += f[e];
     }
     const float mu = warp_sum(s1) * invC;
+    // each pass reads the row (and gamma, beta) from shared memory again, two
+    // vectors at a time: values kept from a pass before, or all of a pass's
+    // reads hoisted ahead, would cost a register per column
+    asm volatile("" ::: "memory");
     float s2 = 0.0f;
-#pragma unroll
+#pragma unroll 2
     for (int i = 0; i < NV; ++i) {
       float f[8];
-      unpack8(xv[i], f);
+      unpack8(row[lane + 32 * i], f);
 #pragma unroll
       for (int e = 0; e < 8; ++e) s2 += (f[e] - mu) * (f[e] - mu);
     }
     const float rs = rsqrtf(warp_sum(s2) * invC + eps);
-#pragma unroll
+    asm volatile("" ::: "memory");
+#pragma unroll 2
     for (int i = 0; i < NV; ++i) {
-      const int32_t col = (lane + 32 * i) * 8;
       float f[8], gg[8], bb[8], o[8];
-      unpack8(xv[i], f);
-      unpack8(__ldg(reinterpret_cast<const uint4*>(gamma + col)), gg);
-      unpack8(__ldg(reinterpret_cast<const uint4*>(beta + col)), bb);
+      unpack8(row[lane + 32 * i], f);
+      unpack8(sg[lane + 32 * i], gg);
+      unpack8(sb[lane + 32 * i], bb);
 #pragma unroll
       for (int e = 0; e < 8; ++e) o[e] = (f[e] - mu) * rs * gg[e] + bb[e];
       const int64_t off = row_vec_off<NV>(g, br, rr, lane, i);
@@ -705,6 +734,14 @@ tp3d_status last_error() { return cudaGetLastError() == cudaSuccess ? TP3D_OK : 
 
 }  // namespace
 
+template <int NV>
+void ln_fwd_row(unsigned grid, cudaStream_t s, const Grid& g, const bf16* x, const bf16* gamma, const bf16* beta,
+                bf16* y, __half* y16, int* err, float* mean, float* rstd, float eps) {
+  if (ln_row_smem<NV>() > 48 * 1024)
+    (void)cudaFuncSetAttribute(ln_fwd_row_kernel<NV>, cudaFuncAttributeMaxDynamicSharedMemorySize, ln_row_smem<NV>());
+  ln_fwd_row_kernel<NV><<<grid, kThreads, ln_row_smem<NV>(), s>>>(g, x, gamma, beta, y, y16, err, mean, rstd, eps);
+}
+
 tp3d_status launch_ln_fwd(const tp3d_ctx* ctx, const Grid& g, const void* x, const void* gamma, const void* beta,
                           void* y, void* y16, float* mean, float* rstd, float eps, cudaStream_t s) {
   const unsigned grid = grid_for_rows(ctx, g.R, 16);
@@ -713,11 +750,11 @@ tp3d_status launch_ln_fwd(const tp3d_ctx* ctx, const Grid& g, const void* x, con
   bf16* yb = static_cast<bf16*>(y);
   __half* yh = static_cast<__half*>(y16);
   int* err = ctx->d_err;
-  switch (g.C % 256 == 0 ? g.C / 256 : 0) {  // whole rows in registers where C = 256 NV
-    case 2: ln_fwd_row_kernel<2><<<grid, kThreads, 0, s>>>(g, xb, gb, bb, yb, yh, err, mean, rstd, eps); break;
-    case 4: ln_fwd_row_kernel<4><<<grid, kThreads, 0, s>>>(g, xb, gb, bb, yb, yh, err, mean, rstd, eps); break;
-    case 8: ln_fwd_row_kernel<8><<<grid, kThreads, 0, s>>>(g, xb, gb, bb, yb, yh, err, mean, rstd, eps); break;
-    case 16: ln_fwd_row_kernel<16><<<grid, kThreads, 0, s>>>(g, xb, gb, bb, yb, yh, err, mean, rstd, eps); break;
+  switch (g.C % 256 == 0 ? g.C / 256 : 0) {  // whole rows staged in shared memory where C = 256 NV
+    case 2: ln_fwd_row<2>(grid, s, g, xb, gb, bb, yb, yh, err, mean, rstd, eps); break;
+    case 4: ln_fwd_row<4>(grid, s, g, xb, gb, bb, yb, yh, err, mean, rstd, eps); break;
+    case 8: ln_fwd_row<8>(grid, s, g, xb, gb, bb, yb, yh, err, mean, rstd, eps); break;
+    case 16: ln_fwd_row<16>(grid, s, g, xb, gb, bb, yb, yh, err, mean, rstd, eps); break;
     default: ln_fwd_kernel<<<grid, kThreads, 0, s>>>(g, xb, gb, bb, yb, yh, err, mean, rstd, eps);
   }
   return last_error();
