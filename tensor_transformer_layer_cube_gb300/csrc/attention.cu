@@ -838,12 +838,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int it = 0; it < niter; ++it, ++n) {
           const uint32_t ks = n % 3, vs = n & 1;
           const int64_t row_k = b * A.s + (int64_t)it * TR;
-          if (!(ok = mbar_wait(k_empty(ks), ((n / 3) & 1) ^ 1, c.abort_flag, A.err))) break;
-          mbar_arrive_expect_tx(k_full(ks), dbytes);
-          load_tile(&mqkv, A.qkv, row_k, A.h + t * A.d, nch, sK(ks), k_full(ks));
+          // V first: its slot frees when dP(j-2) completes, K's only when dQ(j-3) does
           if (!(ok = mbar_wait(v_empty(vs), ((n >> 1) & 1) ^ 1, c.abort_flag, A.err))) break;
           mbar_arrive_expect_tx(v_full(vs), dbytes);
           load_tile(&mqkv, A.qkv, row_k, 2 * A.h + t * A.d, nch, sV(vs), v_full(vs));
+          if (!(ok = mbar_wait(k_empty(ks), ((n / 3) & 1) ^ 1, c.abort_flag, A.err))) break;
+          mbar_arrive_expect_tx(k_full(ks), dbytes);
+          load_tile(&mqkv, A.qkv, row_k, A.h + t * A.d, nch, sK(ks), k_full(ks));
         }
       }
     }
@@ -969,42 +970,47 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // delta[z*s + r] = sum over the head's d columns of dO * O.  One warp per
-// token row: 16-byte loads, 256 columns (every head in them) per step, eight
+// token row: 16-byte loads, 256 columns (every head in them) per step, four
 // steps in flight; the G = d/8 lanes that hold one head reduce with shuffles.
+// 64 registers let four CTAs share an SM, so a grid of one row per warp is
+// resident at once.  Index arithmetic in 32 bits (the launcher checks that
+// the extents fit).
 // The same pass takes dmax0 = max over rows and heads of |dO_r|^2 for the
 // bound that scales the score gradients (ds_sigma): each warp keeps a
 // running maximum, the CTA combines its warps' in shared memory and takes
 // one atomic max (non-negative floats order as their bits; zero on entry).
 template <int G>
-__global__ void __launch_bounds__(256) attn_delta_kernel(const AttnProblem A, const bf16* __restrict__ O,
-                                                         const bf16* __restrict__ dO, float* __restrict__ delta,
-                                                         unsigned* __restrict__ dmax0) {
-  constexpr int U = 8;
+__global__ void __launch_bounds__(256, 4) attn_delta_kernel(const AttnProblem A, const bf16* __restrict__ O,
+                                                            const bf16* __restrict__ dO, float* __restrict__ delta,
+                                                            unsigned* __restrict__ dmax0) {
+  constexpr int U = 4;
   __shared__ float red[8];
   const int lane = threadIdx.x & 31;
-  const int64_t M = A.Z / A.H * A.s;  // token rows
-  const int64_t nw = (int64_t)gridDim.x * 8;
+  const uint32_t M = (uint32_t)(A.Z / A.H * A.s);  // token rows
+  const uint32_t s_len = (uint32_t)A.s, bh = (uint32_t)A.o.bh, bw = (uint32_t)A.o.bw, h = (uint32_t)A.h;
+  const uint32_t nw = gridDim.x * 8u;
   float mdo = 0.0f;
-  for (int64_t tok = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); tok < M; tok += nw) {
-    const int64_t b = tok / A.s, rr = tok - b * A.s;
-    const int64_t br = tok / A.o.bh, rin = tok - br * A.o.bh;
-    for (int64_t c0 = 0; c0 < A.h; c0 += 256 * U) {
+  for (uint32_t tok = blockIdx.x * 8u + (threadIdx.x >> 5); tok < M; tok += nw) {
+    const uint32_t b = tok / s_len, rr = tok - b * s_len;
+    const uint32_t br = tok / bh, rin = tok - br * bh;
+#pragma unroll 1
+    for (uint32_t c0 = 0; c0 < h; c0 += 256u * U) {
       uint4 a[U], g[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int64_t col = c0 + u * 256 + lane * 8;
-        if (col < A.h) {
-          const int64_t bc = col / A.o.bw;
-          const int64_t off = A.o.block_base((int32_t)br, (int32_t)bc) + rin * A.o.bw + (col - bc * A.o.bw);
+        const uint32_t col = c0 + u * 256u + lane * 8u;
+        if (col < h) {
+          const uint32_t bc = col / bw;
+          const int64_t off = A.o.block_base((int32_t)br, (int32_t)bc) + (int64_t)rin * bw + (col - bc * bw);
           a[u] = __ldg(reinterpret_cast<const uint4*>(O + off));
           g[u] = __ldg(reinterpret_cast<const uint4*>(dO + off));
         }
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int64_t col = c0 + u * 256 + lane * 8;
+        const uint32_t col = c0 + u * 256u + lane * 8u;
         float acc = 0.0f, sg = 0.0f;
-        if (col < A.h) {
+        if (col < h) {
           const __nv_bfloat162* ah = reinterpret_cast<const __nv_bfloat162*>(&a[u]);
           const __nv_bfloat162* gh = reinterpret_cast<const __nv_bfloat162*>(&g[u]);
 #pragma unroll
@@ -1019,7 +1025,8 @@ __global__ void __launch_bounds__(256) attn_delta_kernel(const AttnProblem A, co
           acc += __shfl_xor_sync(0xffffffffu, acc, o);
           sg += __shfl_xor_sync(0xffffffffu, sg, o);
         }
-        if ((lane & (G - 1)) == 0 && col < A.h) delta[(b * A.H + col / A.d) * A.s + rr] = acc;
+        if ((lane & (G - 1)) == 0 && col < h)
+          delta[((int64_t)b * A.H + col / (uint32_t)A.d) * s_len + rr] = acc;
         mdo = fmaxf(mdo, sg);
       }
     }
