@@ -305,13 +305,40 @@ __device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr
 // H16: the problem has fp16 output columns or a device-resident scale
 // (instantiated apart, so the plain epilogue's code is left as it is: its
 // speed answers to code layout).
+// The TMA load of the auxiliary input's first chunk for this warp (the
+// coordinates epilogue_tile computes for it), issued before the tile's
+// accumulator is ready so that its latency hides behind the contraction.
+// Returns whether it was issued: the problem has an auxiliary input and the
+// chunk takes the fast path.  The staging half it fills is free: the warp
+// read the previous tile's last chunk from it before leaving that tile.
+template <int BN>
+__device__ __forceinline__ bool aux_prefetch(const GemmProblem& P, const TileInfo& T, int warp, int lane,
+                                             uint8_t* stg, const CUtensorMap* mapX, uint32_t aux_bar) {
+  const void* aux = P.epi.resid ? P.epi.resid : P.epi.gin;
+  if (aux == nullptr || P.epi.zsave != nullptr || P.epi.out_f32) return false;
+  constexpr int CH = BN / 64;
+  const int quarter = warp & 3, half = (warp - 2) >> 2;
+  const int64_t n = T.n0 + (int64_t)(half * CH) * 32;
+  if (!(T.m0 + quarter * 32 + 31 < T.m_end && n + 32 <= T.n_end)) return false;
+  const Grid& cg = P.c.g;
+  const int64_t gm = T.m0 + quarter * 32 + lane + op_off(P.c.hi1, P.c.lo1, P.c.base1, T.z, P.Hz);
+  const int64_t gn0 = T.n0 + op_off(P.c.hi2, P.c.lo2, P.c.base2, T.z, P.Hz);
+  const int64_t cbr = (uint32_t)(gm - lane) / (uint32_t)cg.bh, cbc = (uint32_t)gn0 / (uint32_t)cg.bw;
+  if (lane == 0) {
+    mbar_arrive_expect_tx(aux_bar, 2048u);
+    tma_load_3d(smem_u32(stg) + 2048u, mapX, aux_bar, (int)(gn0 + (n - T.n0) - cbc * cg.bw),
+                (int)(gm - lane - cbr * cg.bh), cg.shard((int32_t)cbr, (int32_t)cbc));
+  }
+  return true;
+}
+
 template <int BN, bool H16>
 __device__ __forceinline__ void epilogue_tile(const GemmProblem& P, const TileInfo& T, bool any_k, int buf,
                                               uint32_t tmem_base, int warp, int lane, uint8_t* stg,
                                               const CUtensorMap* mapC, const CUtensorMap* mapZ,
                                               const CUtensorMap* mapX, uint32_t aux_bar, uint32_t& aux_phase,
                                               volatile int* abort_flag, uint32_t tempty, bool tempty_remote,
-                                              uint32_t& stores, float& cmax) {
+                                              uint32_t& stores, float& cmax, bool aux0_issued = false) {
   const void* aux = P.epi.resid ? P.epi.resid : P.epi.gin;
   const bool aux_ok = aux != nullptr && P.epi.zsave == nullptr && !P.epi.out_f32;
   const int quarter = warp & 3;
@@ -344,7 +371,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmProblem& P, const TileIn
       tma_load_3d(stg_z, mapX, aux_bar, chunk_c0(cc), c1, c2);
     }
   };
-  if (aux_ok && fast(0)) aux_issue(0);
+  if (aux_ok && fast(0) && !aux0_issued) aux_issue(0);  // else issued before the accumulator wait
   const __nv_bfloat16* bias = static_cast<const __nv_bfloat16*>(P.epi.bias);
   const float alpha = H16 && P.epi.alpha_dev ? P.epi.alpha * *P.epi.alpha_dev : P.epi.alpha;
   const bool scaled = alpha != 1.0f;
@@ -777,14 +804,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool any_k = tile_has_k(P, klo, khi, nsegK, tpsK);
       const int buf = (int)(tc & 1u);
       const uint32_t tph = (tc >> 1) & 1u;
+      const bool aux0 = aux_prefetch<BN>(P, T, warp, lane, stg, &mapX, aux_bar(warp - 2));
       // one lane waits and the warp follows it, so the warp stays converged
       // for the .sync.aligned tensor-memory loads
       bool ok = lane == 0 ? mbar_wait(tfull_bar(buf), tph, abort_flag, P.err) : false;
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (!ok) break;
+      if (!ok) {
+        if (aux0 && lane == 0) mbar_wait_drain(aux_bar(warp - 2), aux_phase & 1u);  // let the load land
+        __syncwarp();
+        break;
+      }
       tc_fence_after();
       epilogue_tile<BN, H16>(P, T, any_k, buf, tmem_base, warp, lane, stg, &mapC, &mapZ, &mapX, aux_bar(warp - 2),
-                             aux_phase, abort_flag, tempty_bar(buf), false, stores, cmax);
+                             aux_phase, abort_flag, tempty_bar(buf), false, stores, cmax, aux0);
       ++tc;
     }
     if (lane == 0) bulk_wait_all();
@@ -1147,12 +1179,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       decode_pair_tile(P, t, rank, T);
       const int buf = (int)(tc & 1u);
       const uint32_t tph = (tc >> 1) & 1u;
+      const bool aux0 = aux_prefetch<BN>(P, T, warp, lane, stg, &mapX, aux_bar(warp - 2));
       bool ok = lane == 0 ? mbar_wait(tfull_bar(buf), tph, abort_flag, P.err) : false;
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (!ok) break;
+      if (!ok) {
+        if (aux0 && lane == 0) mbar_wait_drain(aux_bar(warp - 2), aux_phase & 1u);  // let the load land
+        __syncwarp();
+        break;
+      }
       tc_fence_after();
       epilogue_tile<BN, H16>(P, T, true, buf, tmem_base, warp, lane, stg, &mapC, &mapZ, &mapX, aux_bar(warp - 2),
-                             aux_phase, abort_flag, map_to_cta(tempty_bar(buf), 0), true, stores, cmax);
+                             aux_phase, abort_flag, map_to_cta(tempty_bar(buf), 0), true, stores, cmax, aux0);
       ++tc;
     }
     if (lane == 0) bulk_wait_all();
