@@ -200,10 +200,11 @@ __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) {
 // tile's scores are read from TMEM, the row maximum updated, and
 // P = 2^(S log2e / sqrt d - m) (bf16, unnormalised) written back into tensor
 // memory over the tile's own scores, together with the running row sum l.
-// From a row's second key tile on this is one optimistic pass against the
-// current base m (P held in registers until the tile's maximum is known to
-// stay within m + 8); the first tile, and any tile that breaks that bound,
-// takes the two passes (maximum, then P).
+// Each tile takes two passes over its scores in TMEM (the maximum, then P),
+// with the 32-column chunk loops rolled: an unrolled one-pass form (P held in
+// registers against the current base) was faster per tile once warm, but its
+// larger code cost each CTA more in instruction fetches on its first tiles
+// than it saved.
 // The exponent base m only moves when the row maximum exceeds it by more than
 // 8 (2^8: P and l stay far from overflow); then l and the row of O already
 // accumulated in TMEM are scaled by 2^(m_old - m_new) before the next product
@@ -397,58 +398,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         float ps[8];  // eight partial row sums
 #pragma unroll
         for (int i = 0; i < 8; ++i) ps[i] = 0.0f;
-        // From the second key tile on, one optimistic pass: P against the
-        // current base m while the tile's maximum is tracked, P held in
-        // registers.  If no row's maximum passed m + 8, P is stored and the
-        // tile is done; otherwise (rare once the first tiles have set m) the
-        // two passes below run on the scores, still intact in TMEM.
-        bool two_pass = j == 0;
-        if (!two_pass) {
-          uint32_t pk[64];
-          float mx[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
-#pragma unroll
-          for (int cc = 0; cc < TR / 32; cc += 2) {
-            uint32_t v[2][32];
-            tmem_ld_32x32b_x32(tmem_row(tmem, quarter, s_col + (uint32_t)(cc * 32)), v[0]);
-            tmem_ld_32x32b_x32(tmem_row(tmem, quarter, s_col + (uint32_t)(cc * 32 + 32)), v[1]);
-            tmem_ld_wait();
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-#pragma unroll
-              for (int e2 = 0; e2 < 16; ++e2) {
-                const int col = (cc + h) * 32 + 2 * e2;
-                const bool k0 = !diag || col <= r, k1 = !diag || col + 1 <= r;
-                const float x0 = __uint_as_float(v[h][2 * e2]), x1 = __uint_as_float(v[h][2 * e2 + 1]);
-                if (k0) mx[(2 * e2) & 7] = fmaxf(mx[(2 * e2) & 7], x0);
-                if (k1) mx[(2 * e2 + 1) & 7] = fmaxf(mx[(2 * e2 + 1) & 7], x1);
-                const float f0 = k0 ? ex2_approx(fmaf(x0, sl2, -m)) : 0.0f;
-                const float f1 = k1 ? ex2_approx(fmaf(x1, sl2, -m)) : 0.0f;
-                ps[(2 * e2) & 7] += f0;
-                ps[(2 * e2 + 1) & 7] += f1;
-                const __nv_bfloat162 hh = __floats2bfloat162_rn(f0, f1);
-                pk[(cc + h) * 16 + e2] = *reinterpret_cast<const uint32_t*>(&hh);
-              }
-            }
-          }
-          const float mt = sl2 * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-          if (__any_sync(0xffffffffu, mt > m + kRescaleLog2)) {
-            two_pass = true;  // P above 2^8 somewhere in the warp: start over
-#pragma unroll
-            for (int i = 0; i < 8; ++i) ps[i] = 0.0f;
-          } else {
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              uint32_t w16[16];
-#pragma unroll
-              for (int i = 0; i < 16; ++i) w16[i] = pk[q4 * 16 + i];
-              tmem_st_32x32b_x16(tmem_row(tmem, quarter, p_col + (uint32_t)(q4 * 16)), w16);
-            }
-          }
-        }
-        if (two_pass) {
+        {
           // the row maximum: the four 32-column chunks in two pairs of loads
           float mx[8];
 #pragma unroll
