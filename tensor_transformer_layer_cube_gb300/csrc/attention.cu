@@ -399,21 +399,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
         for (int i = 0; i < 8; ++i) ps[i] = 0.0f;
         {
-          // the row maximum: the four 32-column chunks in two pairs of loads
+          // the row maximum, one 32-column chunk at a time (the smallest code)
           float mx[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
 #pragma unroll 1
-          for (int cc = 0; cc < TR / 32; cc += 2) {
-            uint32_t v[2][32];
-            tmem_ld_32x32b_x32(tmem_row(tmem, quarter, s_col + (uint32_t)(cc * 32)), v[0]);
-            tmem_ld_32x32b_x32(tmem_row(tmem, quarter, s_col + (uint32_t)(cc * 32 + 32)), v[1]);
+          for (int cc = 0; cc < TR / 32; ++cc) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tmem_row(tmem, quarter, s_col + (uint32_t)(cc * 32)), v);
             tmem_ld_wait();
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-              for (int e = 0; e < 32; ++e)
-                if (!diag || (cc + h) * 32 + e <= r) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(v[h][e]));
+            for (int e = 0; e < 32; ++e)
+              if (!diag || cc * 32 + e <= r) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(v[e]));
           }
           float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
           mt *= sl2;
