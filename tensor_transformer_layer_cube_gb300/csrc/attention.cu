@@ -45,8 +45,8 @@ namespace {
 
 constexpr int TR = 128;              // rows of a tile (queries or keys)
 constexpr int kComputeWarps = 4;     // forward: row warps per query tile (one per TMEM lane quarter)
-// backward: warp 0 producer, warp 1 MMA issuer, warps 2-9 element-wise work,
-// two per TMEM lane quarter, each on half of a tile row's 128 columns
+// backward: warp 0 producer, warp 1 MMA issuer, warps 2-17 element-wise work,
+// four per TMEM lane quarter, each on a quarter of a tile row's 128 columns
 constexpr int kBwdComputeWarps = 16;  // backward: element-wise warps, kBwdWpq per TMEM lane quarter
 constexpr int kBwdWpq = kBwdComputeWarps / 4;
 constexpr int kBwdCpw = 4 / kBwdWpq;    // 32-column chunks of a 128-key (or 128-query) row per warp
